@@ -1,0 +1,385 @@
+#!/usr/bin/env python
+"""Throughput benchmark of the chunked gated delta rule forward on one GB300 per rank.
+
+Workload (one "step"): the long-context bf16 case -- one packed sequence of T = 65536
+tokens, 16 key heads shared by 32 value heads, K = V = 128, C = 64, fp32 state, h0 = 0,
+synthetic seeded inputs -- run through all three phases (segment summaries, prefix scan,
+re-emit) with P segments.  Metric: tokens/s (whole job, all ranks).  Inputs plus output are
+about 0.8 GB, far larger than the 129 MB L2, so no flush is needed between steps.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead on a
+bounded sample of the same workload.  Multi-GPU (torchrun): every rank runs its own
+independent sequence (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+T_FULL, HK, HV, KD, VD, C = 65536, 16, 32, 128, 128, 64
+METRIC = "GDN fwd tokens/s at T=65536, Hv=32, K=V=128; % of roofline (tensor pipe)"
+# Algorithmic work per token (independent of P): 2*[C(3K+2V) + 3KV + C^2/6] FLOP per value
+# head, and q + k + v + out (bf16) + g + beta (fp32) bytes.
+FLOP_PER_TOKEN = 2 * (C * (3 * KD + 2 * VD) + 3 * KD * VD + C * C / 6) * HV
+BYTES_PER_TOKEN = HK * KD * 2 * 2 + HV * VD * 2 * 2 + HV * 4 * 2
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(
+            d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def make_inputs(T, device, seed):
+    from gated_delta_rule_07_gb300 import inputs
+    inp = inputs.make(inputs.long_bf16(T=T, seed=seed))
+    return inp
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for name in ("gdn_tc.cu", "gdn_common.cuh"):
+        with open(os.path.join(ROOT, "gated_delta_rule_07_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel):
+    """DRAM bytes per token of `kernel` from the committed ncu summary, if the kernel source
+    has not changed since it was captured (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            d = json.load(f)
+        e = d[kernel]
+        if e.get("source_sha") != source_hash():
+            return None
+        return float(e["dram_bytes_per_token"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------------------ our arm
+
+def run_ours(args, ws, rank, local):
+    import torch
+    from gated_delta_rule_07_gb300 import build
+    build.build()
+    from gated_delta_rule_07_gb300 import gdn
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    T = args.T
+    inp = make_inputs(T, dev, seed=rank)
+    d = {n: getattr(inp, n).to(dev).contiguous() for n in ("q", "k", "v", "g", "beta")}
+    out = torch.empty_like(d["v"])
+    hf = torch.empty(1, HV, KD, VD, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def timed_forward(P, steps, warmup):
+        p = gdn.problem_for(d["q"], d["v"], None, P=P)
+        wsb = gdn.workspace_for(p, dev)
+        for _ in range(warmup):
+            gdn.gdn_forward(p, d["q"], d["k"], d["v"], d["g"], d["beta"], None, None, out, hf,
+                            wsb)
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            gdn.gdn_forward(p, d["q"], d["k"], d["v"], d["g"], d["beta"], None, None, out, hf,
+                            wsb)
+        e1.record(stream)
+        barrier()
+        st = gdn.gdn_device_status(wsb)
+        if st != 0:
+            raise gdn.GdnError(st, "device status")
+        return e0.elapsed_time(e1) / steps
+
+    # P sweep (short), then the timed run at the chosen P
+    sweep = {}
+    Ps = [args.P] if args.P else [4, 16, 64, 1]
+    for P in Ps:
+        ms = timed_forward(P, steps=3 if len(Ps) > 1 else 1, warmup=1)
+        sweep[P] = ms
+    P_best = args.P or min(sweep, key=sweep.get)
+
+    with Clocks(local) as clk:
+        ms = timed_forward(P_best, args.steps, args.warmup)
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # per-phase events over the same launches (phase entry points = what gdn_forward enqueues)
+    p = gdn.problem_for(d["q"], d["v"], None, P=P_best)
+    S = P_best * HV
+    M = torch.empty(S, KD, KD, dtype=torch.float32, device=dev)
+    U = torch.empty(S, KD, VD, dtype=torch.float32, device=dev)
+    h_in = torch.empty(S, KD, VD, dtype=torch.float32, device=dev)
+    phase_ms = {"summary": [], "scan": [], "emit": []}
+    for it in range(args.warmup + args.steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        ev[0].record(stream)
+        if P_best > 1:
+            gdn.gdn_segment_summary_fused(p, d["k"], d["v"], d["g"], d["beta"], None, M, U,
+                                          skip_last=True)
+        ev[1].record(stream)
+        if P_best > 1:
+            gdn.gdn_state_prefix_scan(p, M, U, None, h_in, None)
+        ev[2].record(stream)
+        gdn.gdn_chunk_emit_fused(p, d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                 h_in if P_best > 1 else None, None, out, hf)
+        ev[3].record(stream)
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            phase_ms["summary"].append(ev[0].elapsed_time(ev[1]))
+            phase_ms["scan"].append(ev[1].elapsed_time(ev[2]))
+            phase_ms["emit"].append(ev[2].elapsed_time(ev[3]))
+    ph = {k: statistics.mean(v) for k, v in phase_ms.items()}
+
+    # end to end through the C ABI with host buffers: H2D inputs, forward, D2H outputs
+    host = {n: d[n].cpu().pin_memory() for n in d}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    hf_h = torch.empty(hf.shape, dtype=hf.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + hf_h.numel() * hf_h.element_size()
+    pe = gdn.problem_for(d["q"], d["v"], None, P=P_best)
+    wse = gdn.workspace_for(pe, dev)
+    dd = {n: torch.empty_like(d[n]) for n in d}
+
+    def e2e_step():
+        for n in dd:
+            dd[n].copy_(host[n], non_blocking=True)
+        gdn.gdn_forward(pe, dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], None, None, out, hf,
+                        wse)
+        out_h.copy_(out, non_blocking=True)
+        hf_h.copy_(hf, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+
+    if rank != 0:
+        return None
+    hbm, tf, tf_sus, src = peaks()
+    tokens = T * ws
+    emit_bytes = BYTES_PER_TOKEN * T + (P_best * HV + HV) * KD * VD * 4
+    emit_flops = FLOP_PER_TOKEN * T
+    emit_s = ph["emit"] / 1e3
+    achieved_gbs = emit_bytes / emit_s / 1e9
+    tr = stored_traffic("emit")
+    t_bound = max(BYTES_PER_TOKEN * T / (hbm * 1e9), FLOP_PER_TOKEN * T / (tf * 1e12))
+    launches_per_step = 4 if P_best > 1 else 1  # summary (M and U halves), scan, emit
+    res = {
+        "metric": METRIC,
+        "value": tokens / (ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), g=-softplus(N)*0.1, "
+                "beta=sigmoid(N), h0=0)",
+        "config": {"workload": f"long-context bf16 T={T} Hk={HK} Hv={HV} K=V={KD} C={C}",
+                   "segments_per_seq": P_best, "batch": 1, "seq_len": T,
+                   "parallelism": f"replicas x{ws} (independent sequences)",
+                   "l2": "inputs+output 0.8 GB > 129 MB L2; no flush",
+                   "kernel_family": "tensor-core (mma.sync bf16, fp32 state)"},
+        "sweep_ms_per_step": {f"P={k}": round(v, 4) for k, v in sweep.items()},
+        "phase_ms": {k: round(v, 4) for k, v in ph.items()},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {
+            "kernel": "tc_chunk_kernel<emit> (phase 3: prepare + chain + output)",
+            "bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
+            "frac": achieved_gbs / hbm, "peak_source": src,
+            "traffic": None if tr is None else tr * T,
+            "algorithmic_bytes_per_launch": emit_bytes,
+            "tensor_tflops": emit_flops / emit_s / 1e12, "tensor_peak": tf,
+            "tensor_frac": emit_flops / emit_s / 1e12 / tf},
+        "path_roofline": {"bound_us": t_bound * 1e6, "step_us": ms * 1e3,
+                          "frac": t_bound / (ms / 1e3),
+                          "note": "max(FLOP/bf16 peak, bytes/HBM) over the whole step, of "
+                                  + src},
+        "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args.cpu_seconds, inp=inp)
+    return res
+
+
+# ------------------------------------------------------------------------ oracle arm
+
+def cpu_baseline(seconds=12.0, T=None, inp=None):
+    """Times the fp64 oracle (as it stands) on a bounded sample of the workload: the first
+    Ts tokens, all 32 value heads, sized from a short calibration to ~`seconds` of work."""
+    import oracle
+    if inp is None:
+        inp = make_inputs(T_FULL if T is None else T, "cpu", seed=0)
+    threads = os.cpu_count() or 1
+
+    def run(n):
+        sl = {nm: getattr(inp, nm)[:n] for nm in ("q", "k", "v", "g", "beta")}
+        t0 = time.perf_counter()
+        oracle.token(**sl, nthreads=threads)
+        return time.perf_counter() - t0
+
+    cal = 256
+    dt = run(cal)
+    Ts = int(min(inp.q.shape[0], max(cal, cal * seconds / max(dt, 1e-6))))
+    Ts = max(64, Ts // 64 * 64)
+    dt = run(Ts)
+    return {"value": Ts / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {Ts} tokens of the T=65536 stream, all 32 value heads, fp64 "
+                      f"per-token recurrence ({dt:.1f} s)"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return None
+    import oracle
+    inp = make_inputs(T_FULL, "cpu", seed=0)
+    threads = os.cpu_count() or 1
+    Ts = args.ref_tokens
+    sl = {nm: getattr(inp, nm)[:Ts] for nm in ("q", "k", "v", "g", "beta")}
+    for _ in range(args.warmup):
+        oracle.token(**sl, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.token(**sl, nthreads=threads)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = Ts / dt
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (same recipe and seed as our arm)",
+            "config": {"workload": f"long-context bf16 T={T_FULL} Hk={HK} Hv={HV} K=V={KD} "
+                                   f"C={C}", "sample_tokens": Ts},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"first {Ts} tokens, all 32 value heads, per step"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--P", type=int, default=0, help="segments per sequence (0 = sweep)")
+    ap.add_argument("--T", type=int, default=T_FULL)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-tokens", type=int, default=2048)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, ws, rank)
+    else:
+        res = run_ours(args, ws, rank, local)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,316 @@
+// gdn_api.cu -- the C ABI of libgdn: host-side validation, workspace carving and the
+// order of kernel launches for each entry point declared in include/gdn.h.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+using gdn::Args;
+
+constexpr size_t kAlign = 256;
+constexpr size_t kStatusBytes = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t io_bytes(const gdn_problem* p) { return p->io_dtype == GDN_BF16 ? 2 : 4; }
+
+// Resolved kernel family for a problem.
+bool use_tensor_path(const gdn_problem* p) {
+  const bool covers = p->io_dtype == GDN_BF16 && p->k_dim == 128 && p->v_dim == 128;
+  if (p->path == GDN_PATH_SIMT) return false;
+  if (p->path == GDN_PATH_TENSOR) return covers;
+  return covers;
+}
+
+gdn_status check_problem(const gdn_problem* p) {
+  if (!p) return GDN_ERR_INVALID_ARGUMENT;
+  if (p->total_tokens < 0 || p->total_tokens > (int64_t)INT32_MAX || p->num_seqs < 1 ||
+      p->hk < 1 || p->hv < 1 || p->k_dim < 1 || p->v_dim < 1 || p->chunk < 1 ||
+      p->segments_per_seq < 1)
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (p->hv % p->hk != 0) return GDN_ERR_INVALID_ARGUMENT;
+  if (p->io_dtype != GDN_BF16 && p->io_dtype != GDN_F32) return GDN_ERR_UNSUPPORTED;
+  if (p->path < GDN_PATH_AUTO || p->path > GDN_PATH_TENSOR) return GDN_ERR_INVALID_ARGUMENT;
+  if (p->chunk != 64) return GDN_ERR_UNSUPPORTED;
+  if ((p->k_dim != 64 && p->k_dim != 128) || (p->v_dim != 64 && p->v_dim != 128))
+    return GDN_ERR_UNSUPPORTED;
+  if (p->path == GDN_PATH_TENSOR &&
+      !(p->io_dtype == GDN_BF16 && p->k_dim == 128 && p->v_dim == 128))
+    return GDN_ERR_UNSUPPORTED;
+  if (p->hv > 65535) return GDN_ERR_UNSUPPORTED;  // grid.y
+  // grid.x of the per-segment kernels and element offsets in 64 bits
+  if ((int64_t)p->num_seqs * p->segments_per_seq > (int64_t)INT32_MAX)
+    return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+
+Args base_args(const gdn_problem* p) {
+  Args a;
+  memset(&a, 0, sizeof(a));
+  a.T = p->total_tokens;
+  a.N = p->num_seqs;
+  a.hk = p->hk;
+  a.hv = p->hv;
+  a.K = p->k_dim;
+  a.V = p->v_dim;
+  a.P = p->segments_per_seq;
+  a.bf16 = p->io_dtype == GDN_BF16;
+  return a;
+}
+
+// cu_seqlens may be null only for a single sequence.
+bool cu_ok(const gdn_problem* p, const int32_t* cu) { return cu != nullptr || p->num_seqs == 1; }
+
+gdn_status to_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+
+#define GDN_TRY(expr)                              \
+  do {                                             \
+    cudaError_t _e = (expr);                       \
+    if (_e != cudaSuccess) return GDN_ERR_CUDA;    \
+  } while (0)
+
+struct Layout {
+  size_t status, M, U, h_in, w, u, gcum, total;
+};
+
+// Workspace: [status word | M | U | h_in | w | u | gcum], each piece 256-byte aligned.  The
+// summaries and incoming states exist only for P > 1; the materialised chunk factors only on
+// the SIMT path (the tensor-core kernels recompute them on chip).
+Layout layout(const gdn_problem* p) {
+  Layout L;
+  const size_t S = (size_t)p->num_seqs * p->segments_per_seq * p->hv;
+  const size_t K = p->k_dim, V = p->v_dim, T = (size_t)p->total_tokens;
+  const bool seg = p->segments_per_seq > 1;
+  const bool mat = !use_tensor_path(p);
+  size_t off = 0;
+  L.status = off;
+  off += kStatusBytes;
+  L.M = off;
+  off += seg ? align_up(S * K * K * 4) : 0;
+  L.U = off;
+  off += seg ? align_up(S * K * V * 4) : 0;
+  L.h_in = off;
+  off += seg ? align_up(S * K * V * 4) : 0;
+  L.w = off;
+  off += mat ? align_up(T * p->hv * K * io_bytes(p)) : 0;
+  L.u = off;
+  off += mat ? align_up(T * p->hv * V * io_bytes(p)) : 0;
+  L.gcum = off;
+  off += mat ? align_up(T * p->hv * 4) : 0;
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gdn_status_string(gdn_status s) {
+  switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARGUMENT: return "GDN_ERR_INVALID_ARGUMENT: bad pointer, size or alignment";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: dtype/K/V/chunk outside the built set";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing or too small";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA launch or runtime call failed";
+    case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT: a bounded device wait expired";
+    case GDN_ERR_DEVICE_INPUT: return "GDN_ERR_DEVICE_INPUT: cu_seqlens inconsistent on the device";
+  }
+  return "GDN_UNKNOWN_STATUS";
+}
+
+int gdn_version(void) { return 100; }
+
+gdn_status gdn_check_problem(const gdn_problem* p) { return check_problem(p); }
+
+size_t gdn_workspace_size(const gdn_problem* p) {
+  if (check_problem(p) != GDN_OK) return 0;
+  return layout(p).total;
+}
+
+gdn_status gdn_chunk_prepare(const gdn_problem* p, const void* k, const void* v, const float* g,
+                             const float* beta, const int32_t* cu_seqlens, void* w, void* u,
+                             float* gcum, int32_t* dev_status, cudaStream_t stream) {
+  gdn_status st = check_problem(p);
+  if (st != GDN_OK) return st;
+  if (p->total_tokens > 0 && (!k || !v || !g || !beta || !w || !u || !gcum))
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (!cu_ok(p, cu_seqlens)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(w) || !aligned16(u))
+    return GDN_ERR_INVALID_ARGUMENT;
+  Args a = base_args(p);
+  a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu = cu_seqlens;
+  a.w_out = w; a.u_out = u; a.gcum_out = gcum; a.status = dev_status;
+  if (a.T == 0) return GDN_OK;
+  GDN_TRY(gdn::launch_validate_cu(a, stream));
+  return to_status(use_tensor_path(p) ? gdn::tc_prepare(a, stream) : gdn::simt_prepare(a, stream));
+}
+
+gdn_status gdn_segment_summary(const gdn_problem* p, const void* k, const void* w, const void* u,
+                               const float* gcum, const int32_t* cu_seqlens, float* M, float* U,
+                               int32_t* dev_status, cudaStream_t stream) {
+  gdn_status st = check_problem(p);
+  if (st != GDN_OK) return st;
+  if (!M || !U) return GDN_ERR_INVALID_ARGUMENT;
+  if (p->total_tokens > 0 && (!k || !w || !u || !gcum)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!cu_ok(p, cu_seqlens)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned16(k) || !aligned16(w) || !aligned16(u) || !aligned16(M) || !aligned16(U))
+    return GDN_ERR_INVALID_ARGUMENT;
+  Args a = base_args(p);
+  a.k = k; a.w = w; a.u = u; a.gcum = gcum; a.cu = cu_seqlens;
+  a.M_out = M; a.U_out = U; a.status = dev_status;
+  GDN_TRY(gdn::launch_validate_cu(a, stream));
+  return to_status(use_tensor_path(p) ? gdn::tc_summary(a, false, stream)
+                                      : gdn::simt_summary(a, stream));
+}
+
+gdn_status gdn_state_prefix_scan(const gdn_problem* p, const float* M, const float* U,
+                                 const float* h0, float* h_in, float* h_final,
+                                 cudaStream_t stream) {
+  gdn_status st = check_problem(p);
+  if (st != GDN_OK) return st;
+  if (!M || !U || !h_in) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned16(M) || !aligned16(U) || !aligned16(h_in) || !aligned16(h0) || !aligned16(h_final))
+    return GDN_ERR_INVALID_ARGUMENT;
+  Args a = base_args(p);
+  a.M = M; a.U = U; a.h0 = h0; a.h_in_out = h_in; a.h_final = h_final;
+  return to_status(use_tensor_path(p) ? gdn::tc_scan(a, stream) : gdn::simt_scan(a, stream));
+}
+
+gdn_status gdn_chunk_emit(const gdn_problem* p, const void* q, const void* k, const void* w,
+                          const void* u, const float* gcum, const float* h_in,
+                          const int32_t* cu_seqlens, void* out, float* h_final,
+                          int32_t* dev_status, cudaStream_t stream) {
+  gdn_status st = check_problem(p);
+  if (st != GDN_OK) return st;
+  if (p->total_tokens > 0 && (!q || !k || !w || !u || !gcum || !out))
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (!cu_ok(p, cu_seqlens)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(w) || !aligned16(u) || !aligned16(out) ||
+      !aligned16(h_in) || !aligned16(h_final))
+    return GDN_ERR_INVALID_ARGUMENT;
+  Args a = base_args(p);
+  a.q = q; a.k = k; a.w = w; a.u = u; a.gcum = gcum; a.h_in = h_in; a.cu = cu_seqlens;
+  a.out = out; a.h_final = h_final; a.status = dev_status;
+  GDN_TRY(gdn::launch_validate_cu(a, stream));
+  return to_status(use_tensor_path(p) ? gdn::tc_emit(a, false, stream)
+                                      : gdn::simt_emit(a, stream));
+}
+
+gdn_status gdn_forward(const gdn_problem* p, const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const float* h0,
+                       const int32_t* cu_seqlens, void* out, float* h_final, void* workspace,
+                       size_t ws_bytes, cudaStream_t stream) {
+  gdn_status st = check_problem(p);
+  if (st != GDN_OK) return st;
+  if (p->total_tokens > 0 && (!q || !k || !v || !g || !beta || !out))
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (!cu_ok(p, cu_seqlens)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(h0) ||
+      !aligned16(h_final))
+    return GDN_ERR_INVALID_ARGUMENT;
+  const Layout L = layout(p);
+  if (!workspace || ws_bytes < L.total || !aligned16(workspace)) return GDN_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+  GDN_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), stream));
+
+  Args a = base_args(p);
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.cu = cu_seqlens;
+  a.out = out; a.h_final = h_final; a.status = status;
+  const bool seg = p->segments_per_seq > 1;
+  if (seg) {
+    a.M_out = reinterpret_cast<float*>(ws + L.M);
+    a.U_out = reinterpret_cast<float*>(ws + L.U);
+    a.M = a.M_out;
+    a.U = a.U_out;
+    a.h_in_out = reinterpret_cast<float*>(ws + L.h_in);
+  }
+  // With P = 1 the incoming state of the only segment is h0 itself.
+  a.h_in = seg ? a.h_in_out : h0;
+  GDN_TRY(gdn::launch_validate_cu(a, stream));
+
+  if (use_tensor_path(p)) {
+    if (seg) {
+      Args ma = a;
+      ma.skip_last_summary = true;
+      GDN_TRY(gdn::tc_summary(ma, true, stream));
+      Args sa = a;
+      sa.h_final = nullptr;  // the last segment's emit writes the final state
+      GDN_TRY(gdn::tc_scan(sa, stream));
+    }
+    return to_status(gdn::tc_emit(a, true, stream));
+  }
+  a.w_out = ws + L.w;
+  a.u_out = ws + L.u;
+  a.gcum_out = reinterpret_cast<float*>(ws + L.gcum);
+  a.w = a.w_out;
+  a.u = a.u_out;
+  a.gcum = a.gcum_out;
+  if (a.T > 0) GDN_TRY(gdn::simt_prepare(a, stream));
+  if (seg) {
+    GDN_TRY(gdn::simt_summary(a, stream));  // (the SIMT summary computes every segment)
+    Args sa = a;
+    sa.h_final = nullptr;
+    GDN_TRY(gdn::simt_scan(sa, stream));
+  }
+  return to_status(gdn::simt_emit(a, stream));
+}
+
+gdn_status gdn_segment_summary_fused(const gdn_problem* p, const void* k, const void* v,
+                                     const float* g, const float* beta,
+                                     const int32_t* cu_seqlens, float* M, float* U,
+                                     int skip_last, int32_t* dev_status, cudaStream_t stream) {
+  gdn_status st = check_problem(p);
+  if (st != GDN_OK) return st;
+  if (!use_tensor_path(p)) return GDN_ERR_UNSUPPORTED;
+  if (!M || !U) return GDN_ERR_INVALID_ARGUMENT;
+  if (p->total_tokens > 0 && (!k || !v || !g || !beta)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!cu_ok(p, cu_seqlens)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(M) || !aligned16(U))
+    return GDN_ERR_INVALID_ARGUMENT;
+  Args a = base_args(p);
+  a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu = cu_seqlens;
+  a.M_out = M; a.U_out = U; a.status = dev_status; a.skip_last_summary = skip_last != 0;
+  GDN_TRY(gdn::launch_validate_cu(a, stream));
+  return to_status(gdn::tc_summary(a, true, stream));
+}
+
+gdn_status gdn_chunk_emit_fused(const gdn_problem* p, const void* q, const void* k,
+                                const void* v, const float* g, const float* beta,
+                                const float* h_in, const int32_t* cu_seqlens, void* out,
+                                float* h_final, int32_t* dev_status, cudaStream_t stream) {
+  gdn_status st = check_problem(p);
+  if (st != GDN_OK) return st;
+  if (!use_tensor_path(p)) return GDN_ERR_UNSUPPORTED;
+  if (p->total_tokens > 0 && (!q || !k || !v || !g || !beta || !out))
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (!cu_ok(p, cu_seqlens)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(h_in) ||
+      !aligned16(h_final))
+    return GDN_ERR_INVALID_ARGUMENT;
+  Args a = base_args(p);
+  a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h_in = h_in; a.cu = cu_seqlens;
+  a.out = out; a.h_final = h_final; a.status = dev_status;
+  GDN_TRY(gdn::launch_validate_cu(a, stream));
+  return to_status(gdn::tc_emit(a, true, stream));
+}
+
+gdn_status gdn_device_status(const void* status_word, int reset, cudaStream_t stream) {
+  if (!status_word) return GDN_ERR_INVALID_ARGUMENT;
+  int32_t host = 0;
+  int32_t* dev = const_cast<int32_t*>(static_cast<const int32_t*>(status_word));
+  if (cudaMemcpyAsync(&host, dev, sizeof(int32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (reset && cudaMemsetAsync(dev, 0, sizeof(int32_t), stream) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return GDN_ERR_CUDA;
+  return static_cast<gdn_status>(host);
+}
+
+}  // extern "C"

@@ -1,0 +1,49 @@
+// gdn_internal.h -- launcher interface between the C ABI layer and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+// Everything a kernel needs to know about one call.  Pointers are device pointers; the
+// ones a given stage does not use are null.
+struct Args {
+  int64_t T;
+  int N, hk, hv, K, V, P;
+  bool bf16;
+  const void *q, *k, *v;
+  const float *g, *beta;
+  const void *w, *u;
+  const float* gcum;
+  const float *h0, *h_in;
+  const float *M, *U;
+  const int32_t* cu;
+  void* out;
+  void *w_out, *u_out;
+  float* gcum_out;
+  float *M_out, *U_out, *h_in_out, *h_final;
+  int32_t* status;
+  bool skip_last_summary;  // the fused forward never reads the last segment's summary
+};
+
+// Device-side check of cu_seqlens (cu[0] = 0, non-decreasing, cu[N] = T); records
+// GDN_ERR_DEVICE_INPUT in the status word on failure.
+cudaError_t launch_validate_cu(const Args& a, cudaStream_t s);
+
+// SIMT kernels (fp32 arithmetic; any supported dtype/K/V).
+cudaError_t simt_prepare(const Args& a, cudaStream_t s);
+cudaError_t simt_summary(const Args& a, cudaStream_t s);
+cudaError_t simt_scan(const Args& a, cudaStream_t s);
+cudaError_t simt_emit(const Args& a, cudaStream_t s);
+
+// Tensor-core kernels (bf16 operands, fp32 accumulate and state; K = V = 128).
+bool tc_supported(const Args& a);
+cudaError_t tc_prepare(const Args& a, cudaStream_t s);
+cudaError_t tc_summary(const Args& a, bool fused_prepare, cudaStream_t s);
+cudaError_t tc_scan(const Args& a, cudaStream_t s);
+cudaError_t tc_emit(const Args& a, bool fused_prepare, cudaStream_t s);
+
+}  // namespace gdn

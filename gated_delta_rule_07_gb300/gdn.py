@@ -1,0 +1,203 @@
+"""ctypes binding of libgdn.so (the C ABI declared in include/gdn.h).
+
+Argument marshalling only: every step of the computation runs in the library's CUDA
+kernels.  Functions named after the C entry points take torch CUDA tensors, pass their
+data pointers and the current torch stream, and raise ``GdnError`` on a non-OK status.
+``forward()`` is the convenience call that allocates the outputs and the workspace.
+
+Importing this module loads the library and raises ImportError when it has not been built
+(``python -m gated_delta_rule_07_gb300.build``); there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+LIB_PATH = _build.LIB
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libgdn.so is not built ({LIB_PATH}); run "
+                      "`python -m gated_delta_rule_07_gb300.build` (needs nvcc)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+GDN_OK = 0
+STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPORTED",
+                3: "GDN_ERR_WORKSPACE", 4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_TIMEOUT",
+                6: "GDN_ERR_DEVICE_INPUT"}
+GDN_BF16, GDN_F32 = 0, 1
+PATH_AUTO, PATH_SIMT, PATH_TENSOR = 0, 1, 2
+EXPORTED = ("gdn_status_string", "gdn_check_problem", "gdn_workspace_size", "gdn_forward",
+            "gdn_chunk_prepare", "gdn_segment_summary", "gdn_state_prefix_scan",
+            "gdn_chunk_emit", "gdn_device_status", "gdn_version",
+            "gdn_segment_summary_fused", "gdn_chunk_emit_fused")
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("total_tokens", ctypes.c_int64), ("num_seqs", ctypes.c_int32),
+                ("hk", ctypes.c_int32), ("hv", ctypes.c_int32), ("k_dim", ctypes.c_int32),
+                ("v_dim", ctypes.c_int32), ("chunk", ctypes.c_int32),
+                ("segments_per_seq", ctypes.c_int32), ("io_dtype", ctypes.c_int32),
+                ("path", ctypes.c_int32)]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {gdn_status_string(status)}")
+
+
+_vp, _fp, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+_pp = ctypes.POINTER(Problem)
+_lib.gdn_status_string.restype = ctypes.c_char_p
+_lib.gdn_status_string.argtypes = [ctypes.c_int]
+_lib.gdn_check_problem.argtypes = [_pp]
+_lib.gdn_workspace_size.restype = ctypes.c_size_t
+_lib.gdn_workspace_size.argtypes = [_pp]
+_lib.gdn_forward.argtypes = [_pp, _vp, _vp, _vp, _fp, _fp, _fp, _ip, _vp, _fp, _vp,
+                             ctypes.c_size_t, _vp]
+_lib.gdn_chunk_prepare.argtypes = [_pp, _vp, _vp, _fp, _fp, _ip, _vp, _vp, _fp, _ip, _vp]
+_lib.gdn_segment_summary.argtypes = [_pp, _vp, _vp, _vp, _fp, _ip, _fp, _fp, _ip, _vp]
+_lib.gdn_state_prefix_scan.argtypes = [_pp, _fp, _fp, _fp, _fp, _fp, _vp]
+_lib.gdn_chunk_emit.argtypes = [_pp, _vp, _vp, _vp, _vp, _fp, _fp, _ip, _vp, _fp, _ip, _vp]
+_lib.gdn_device_status.argtypes = [_vp, ctypes.c_int, _vp]
+_lib.gdn_segment_summary_fused.argtypes = [_pp, _vp, _vp, _fp, _fp, _ip, _fp, _fp, ctypes.c_int,
+                                           _ip, _vp]
+_lib.gdn_chunk_emit_fused.argtypes = [_pp, _vp, _vp, _vp, _fp, _fp, _fp, _ip, _vp, _fp, _ip, _vp]
+for _n in EXPORTED:
+    if _n not in ("gdn_status_string", "gdn_workspace_size"):
+        getattr(_lib, _n).restype = ctypes.c_int
+
+
+def gdn_status_string(status: int) -> str:
+    return _lib.gdn_status_string(int(status)).decode()
+
+
+def gdn_version() -> int:
+    return _lib.gdn_version()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(status, where):
+    if status != GDN_OK:
+        raise GdnError(status, where)
+
+
+def make_problem(T, N, hk, hv, K, V, P=1, dtype=torch.bfloat16, chunk=64, path=PATH_AUTO):
+    io = {torch.bfloat16: GDN_BF16, torch.float32: GDN_F32}.get(dtype)
+    if io is None:
+        raise GdnError(2, f"dtype {dtype}")
+    return Problem(int(T), int(N), int(hk), int(hv), int(K), int(V), int(chunk), int(P), io,
+                   int(path))
+
+
+def problem_for(q, v, cu_seqlens=None, P=1, path=PATH_AUTO) -> Problem:
+    T, hk, K = q.shape
+    hv, V = v.shape[1], v.shape[2]
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    return make_problem(T, N, hk, hv, K, V, P, q.dtype, path=path)
+
+
+def gdn_check_problem(p: Problem) -> int:
+    return _lib.gdn_check_problem(ctypes.byref(p))
+
+
+def gdn_workspace_size(p: Problem) -> int:
+    return int(_lib.gdn_workspace_size(ctypes.byref(p)))
+
+
+def gdn_forward(p, q, k, v, g, beta, h0, cu_seqlens, out, h_final, workspace, ws_bytes=None,
+                stream=None):
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
+    _check(_lib.gdn_forward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                            _ptr(h0), _ptr(cu_seqlens), _ptr(out), _ptr(h_final),
+                            _ptr(workspace), int(ws_bytes), _stream(stream)), "gdn_forward")
+
+
+def gdn_chunk_prepare(p, k, v, g, beta, cu_seqlens, w, u, gcum, dev_status=None, stream=None):
+    _check(_lib.gdn_chunk_prepare(ctypes.byref(p), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                  _ptr(cu_seqlens), _ptr(w), _ptr(u), _ptr(gcum),
+                                  _ptr(dev_status), _stream(stream)), "gdn_chunk_prepare")
+
+
+def gdn_segment_summary(p, k, w, u, gcum, cu_seqlens, M, U, dev_status=None, stream=None):
+    _check(_lib.gdn_segment_summary(ctypes.byref(p), _ptr(k), _ptr(w), _ptr(u), _ptr(gcum),
+                                    _ptr(cu_seqlens), _ptr(M), _ptr(U), _ptr(dev_status),
+                                    _stream(stream)), "gdn_segment_summary")
+
+
+def gdn_state_prefix_scan(p, M, U, h0, h_in, h_final, stream=None):
+    _check(_lib.gdn_state_prefix_scan(ctypes.byref(p), _ptr(M), _ptr(U), _ptr(h0), _ptr(h_in),
+                                      _ptr(h_final), _stream(stream)), "gdn_state_prefix_scan")
+
+
+def gdn_chunk_emit(p, q, k, w, u, gcum, h_in, cu_seqlens, out, h_final, dev_status=None,
+                   stream=None):
+    _check(_lib.gdn_chunk_emit(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(w), _ptr(u), _ptr(gcum),
+                               _ptr(h_in), _ptr(cu_seqlens), _ptr(out), _ptr(h_final),
+                               _ptr(dev_status), _stream(stream)), "gdn_chunk_emit")
+
+
+def gdn_segment_summary_fused(p, k, v, g, beta, cu_seqlens, M, U, skip_last=False,
+                              dev_status=None, stream=None):
+    _check(_lib.gdn_segment_summary_fused(ctypes.byref(p), _ptr(k), _ptr(v), _ptr(g),
+                                          _ptr(beta), _ptr(cu_seqlens), _ptr(M), _ptr(U),
+                                          int(bool(skip_last)), _ptr(dev_status),
+                                          _stream(stream)), "gdn_segment_summary_fused")
+
+
+def gdn_chunk_emit_fused(p, q, k, v, g, beta, h_in, cu_seqlens, out, h_final, dev_status=None,
+                         stream=None):
+    _check(_lib.gdn_chunk_emit_fused(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                     _ptr(beta), _ptr(h_in), _ptr(cu_seqlens), _ptr(out),
+                                     _ptr(h_final), _ptr(dev_status), _stream(stream)),
+           "gdn_chunk_emit_fused")
+
+
+def gdn_device_status(status_word, reset=True, stream=None) -> int:
+    """Synchronous read of a device status word (a dev_status tensor or a workspace)."""
+    return _lib.gdn_device_status(_ptr(status_word), int(bool(reset)), _stream(stream))
+
+
+# ------------------------------------------------------------------ convenience API
+
+def workspace_for(p: Problem, device="cuda") -> torch.Tensor:
+    return torch.empty(max(gdn_workspace_size(p), 256), dtype=torch.uint8, device=device)
+
+
+def forward(q, k, v, g, beta, h0=None, cu_seqlens=None, P=1, path=PATH_AUTO, out=None,
+            h_final=None, workspace=None, want_final=True, check_status=False, stream=None):
+    """out, h_final = forward(...) on CUDA tensors (layouts of include/gdn.h).
+
+    ``cu_seqlens`` is an int32 CUDA tensor [N+1] or None (one sequence).  With
+    ``check_status`` the device status word is read back (a synchronisation)."""
+    p = problem_for(q, v, cu_seqlens, P, path)
+    N = p.num_seqs
+    if out is None:
+        out = torch.empty_like(v)
+    if h_final is None and want_final:
+        h_final = torch.empty(N, p.hv, p.k_dim, p.v_dim, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = workspace_for(p, q.device)
+    gdn_forward(p, q, k, v, g, beta, h0, cu_seqlens, out, h_final, workspace, stream=stream)
+    if check_status:
+        st = gdn_device_status(workspace, True, stream)
+        _check(st, "gdn_forward (device status)")
+    return out, h_final

@@ -1,0 +1,185 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) chunked gated delta rule forward library (libgdn.so).
+ *
+ * The operation (per value head, h a K x V state):
+ *     h_t = exp(g_t) (I - beta_t k_t k_t^T) h_{t-1} + beta_t k_t v_t^T,     o_t = h_t^T q_t.
+ * It is computed chunk by chunk (C tokens) through the affine chunk map of the page
+ * "Add context parallelism to the Gated Delta Net (Qwen3-Next / Qwen3.5)" (MaxText PR #5040),
+ * section "Why":
+ *     h_out = (gamma I - k_tilde^T w) h + k_tilde^T u = M h + U,
+ *     o     = (q_g - attn_i w) h + attn_i u,
+ * and long sequences are split into segments that run in parallel on the GPU's SMs by the
+ * three phases of its section "Implementation": (1) a zero-state pass per segment carrying
+ * M_r in low-rank form, (2) an exclusive prefix scan over (M_r, U_r), (3) a re-emit pass from
+ * the true incoming state.  Chunk factors (derived from the recurrence; the page names them
+ * without defining them):
+ *     G_t = inclusive within-chunk cumulative sum of g;   gamma = exp(G_last)
+ *     A[t][j] = beta_t exp(G_t - G_j) (k_t . k_j), j < t;  T = (I + A)^-1
+ *     w = T diag(beta exp(G)) K,   u = T diag(beta) V,   k_tilde_j = exp(G_last - G_j) k_j,
+ *     q_g_t = exp(G_t) q_t,   attn_i[t][j] = exp(G_t - G_j) (q_t . k_j), j <= t.
+ *
+ * CONVENTIONS (every entry point)
+ *   Ownership   the caller allocates every buffer; the library allocates nothing, keeps no
+ *               state between calls and never frees caller memory.
+ *   Pointers    all tensor arguments are DEVICE pointers of the current CUDA device; the
+ *               problem struct is a HOST pointer read before the call returns.
+ *   Execution   asynchronous on `stream` (0 = legacy default stream).  Buffers must stay
+ *               valid until the stream reaches the work.
+ *   Layouts     row-major, contiguous, no padding between rows:
+ *                 q, k      [T, hk, K]      io dtype
+ *                 v, out    [T, hv, V]      io dtype
+ *                 g, beta   [T, hv]         fp32 (g = natural-log decay, beta = write strength)
+ *                 h0, h_final [N, hv, K, V] fp32 (the state layout [Hv, K, V] f32 of the page
+ *                           "RFC(qwen35): TP Phase2", section "Partition Contract", per sequence)
+ *                 cu_seqlens int32 [N+1]    cu[0] = 0, non-decreasing, cu[N] = T
+ *                 w [T, hv, K], u [T, hv, V] io dtype;  gcum [T, hv] fp32 (token aligned)
+ *                 M [N*P, hv, K, K], U and h_in [N*P, hv, K, V] fp32; segment (n, r) -> n*P + r
+ *               Value head j reads key head j / (hv / hk) (grouped order).
+ *   Segments    each sequence's Nc = ceil(L / C) chunks are split into P contiguous,
+ *               in-order segments; the first (Nc mod P) segments get one extra chunk; a
+ *               segment past Nc is empty (identity map).  A reordered (load-balanced) split
+ *               cannot be expressed: the section "Limitation: load balancing must be off"
+ *               requires contiguous, in-order pieces.
+ *   Tails       a sequence whose length is not a multiple of C ends in a short chunk; it is
+ *               computed as if padded with g = 0, q = k = v = 0 (the padding bullet of
+ *               "Implementation"), and nothing is written past the sequence.
+ *   Validation  host-side checks run before any launch; on failure nothing is enqueued and
+ *               GDN_ERR_INVALID_ARGUMENT or GDN_ERR_UNSUPPORTED is returned.  cu_seqlens is
+ *               checked ON THE DEVICE (the host never reads it): a bad table leaves the
+ *               outputs of the affected sequences unwritten and records
+ *               GDN_ERR_DEVICE_INPUT in the status word, read by gdn_device_status().
+ *   Supported   io dtype bf16 or fp32; K, V in {64, 128}; C = 64; hv % hk == 0; P >= 1;
+ *               16-byte aligned tensor pointers.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, misaligned pointer          */
+    GDN_ERR_UNSUPPORTED = 2,      /* valid but not built: dtype, K, V, C outside the set  */
+    GDN_ERR_WORKSPACE = 3,        /* workspace null or smaller than gdn_workspace_size()  */
+    GDN_ERR_CUDA = 4,             /* a CUDA launch or runtime call failed                 */
+    GDN_ERR_DEVICE_TIMEOUT = 5,   /* a bounded device-side wait expired                   */
+    GDN_ERR_DEVICE_INPUT = 6      /* the device found cu_seqlens inconsistent             */
+} gdn_status;
+
+typedef enum gdn_dtype { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
+
+/* Kernel family selection (gdn_problem.path).  AUTO picks the tensor-core kernels when they
+ * cover the shape (bf16, K = V = 128) and the SIMT kernels otherwise; the two are
+ * independent implementations of the same steps. */
+typedef enum gdn_path { GDN_PATH_AUTO = 0, GDN_PATH_SIMT = 1, GDN_PATH_TENSOR = 2 } gdn_path;
+
+typedef struct gdn_problem {
+    int64_t total_tokens;     /* T >= 0: tokens of the packed stream                     */
+    int32_t num_seqs;         /* N >= 1                                                  */
+    int32_t hk, hv;           /* key heads, value heads (hv % hk == 0)                   */
+    int32_t k_dim, v_dim;     /* K, V                                                    */
+    int32_t chunk;            /* C (64)                                                  */
+    int32_t segments_per_seq; /* P >= 1                                                  */
+    int32_t io_dtype;         /* gdn_dtype of q, k, v, out, w, u                         */
+    int32_t path;             /* gdn_path                                                */
+} gdn_problem;
+
+/* Status text (static storage; never NULL). */
+const char* gdn_status_string(gdn_status s);
+
+/* Checks a problem description on the host (no device work). */
+gdn_status gdn_check_problem(const gdn_problem* p);
+
+/* Bytes of device workspace gdn_forward needs for problem p (0 when p is invalid).  The
+ * workspace holds the status word, the segment summaries (M_r, U_r), the incoming states
+ * h_in and, on the SIMT path, the materialised chunk factors. */
+size_t gdn_workspace_size(const gdn_problem* p);
+
+/* Whole forward pass ("Implementation": the three phases; with P = 1 the single-pass form,
+ * "the single-device path is the same computation, just reassembled").
+ *   q, k, v, g, beta   inputs (layouts above)
+ *   h0                 initial states [N, hv, K, V] fp32, or NULL for zeros
+ *   cu_seqlens         device int32 [N+1]; may be NULL only when N == 1 (then [0, T])
+ *   out                [T, hv, V] io dtype
+ *   h_final            [N, hv, K, V] fp32, or NULL to skip
+ *   workspace          device buffer of ws_bytes >= gdn_workspace_size(p), 16-byte aligned;
+ *                      its first 4 bytes are the status word (reset by this call)
+ * Returns GDN_OK once the work is enqueued. */
+gdn_status gdn_forward(const gdn_problem* p, const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const float* h0,
+                       const int32_t* cu_seqlens, void* out, float* h_final, void* workspace,
+                       size_t ws_bytes, cudaStream_t stream);
+
+/* Phase "prepare": the WY/UT factors of every chunk ("Implementation": the WY factors that
+ * phase 3 reuses; "Why": w and u of the chunk map).  Writes w [T, hv, K], u [T, hv, V]
+ * (io dtype) and gcum [T, hv] (fp32, inclusive within-chunk cumulative log-decay; a chunk's
+ * gamma is exp of its last row).  dev_status: device int32 status word or NULL. */
+gdn_status gdn_chunk_prepare(const gdn_problem* p, const void* k, const void* v, const float* g,
+                             const float* beta, const int32_t* cu_seqlens, void* w, void* u,
+                             float* gcum, int32_t* dev_status, cudaStream_t stream);
+
+/* Phase 1: zero-state pass per segment carrying the composed transition ("Implementation",
+ * phase 1 and the low-rank composition M_new = gamma M - k_tilde^T (w M)).  From M = I, U = 0,
+ * per chunk: U <- gamma U + k_tilde^T (u - w U), M <- gamma M - k_tilde^T (w M).
+ * Reads k, w, u, gcum (as written by gdn_chunk_prepare); writes M [N*P, hv, K, K] and
+ * U [N*P, hv, K, V] (fp32) for every segment, empty ones as (I, 0). */
+gdn_status gdn_segment_summary(const gdn_problem* p, const void* k, const void* w, const void* u,
+                               const float* gcum, const int32_t* cu_seqlens, float* M, float* U,
+                               int32_t* dev_status, cudaStream_t stream);
+
+/* Phase 2: exclusive prefix scan over the segment summaries ("Implementation", phase 2;
+ * "Why": affine maps compose associatively).  h_in[n*P] = h0[n] (zeros when h0 is NULL),
+ * h_in[n*P + r + 1] = M[n*P + r] h_in[n*P + r] + U[n*P + r]; h_final[n] is the map of the
+ * last segment applied once more (NULL to skip).  Pure fp32; needs no cu_seqlens. */
+gdn_status gdn_state_prefix_scan(const gdn_problem* p, const float* M, const float* U,
+                                 const float* h0, float* h_in, float* h_final,
+                                 cudaStream_t stream);
+
+/* Phase 3: re-emit from the true incoming states, reusing the chunk factors
+ * ("Implementation", phase 3; "Why": o = (q_g - attn_i w) h + attn_i u).  Per chunk:
+ * delta = u - w h, o = q_g h + attn_i delta, h <- gamma h + k_tilde^T delta.
+ * h_in [N*P, hv, K, V] fp32 (NULL = zeros); writes out and, from each sequence's last
+ * segment, h_final (NULL to skip). */
+gdn_status gdn_chunk_emit(const gdn_problem* p, const void* q, const void* k, const void* w,
+                          const void* u, const float* gcum, const float* h_in,
+                          const int32_t* cu_seqlens, void* out, float* h_final,
+                          int32_t* dev_status, cudaStream_t stream);
+
+/* Phase 1 with the chunk factors recomputed on chip (no materialised w, u): the same M_r,
+ * U_r as gdn_chunk_prepare followed by gdn_segment_summary, read straight from k, v, g, beta.
+ * With skip_last != 0 the last segment of each sequence is not summarised (the forward pass
+ * never reads it).  Tensor-core family only (bf16, K = V = 128); GDN_ERR_UNSUPPORTED
+ * otherwise. */
+gdn_status gdn_segment_summary_fused(const gdn_problem* p, const void* k, const void* v,
+                                     const float* g, const float* beta,
+                                     const int32_t* cu_seqlens, float* M, float* U,
+                                     int skip_last, int32_t* dev_status, cudaStream_t stream);
+
+/* Phase 3 with the chunk factors recomputed on chip: the same out and h_final as
+ * gdn_chunk_prepare followed by gdn_chunk_emit.  h_in [N*P, hv, K, V] fp32 or NULL (zeros).
+ * Tensor-core family only (bf16, K = V = 128); GDN_ERR_UNSUPPORTED otherwise. */
+gdn_status gdn_chunk_emit_fused(const gdn_problem* p, const void* q, const void* k,
+                                const void* v, const float* g, const float* beta,
+                                const float* h_in, const int32_t* cu_seqlens, void* out,
+                                float* h_final, int32_t* dev_status, cudaStream_t stream);
+
+/* Reads (synchronously: it waits for `stream`) the status word at `status_word` -- a
+ * dev_status pointer or a gdn_forward workspace -- and clears it when `reset` != 0.
+ * Returns the recorded status (GDN_OK when none), or GDN_ERR_CUDA if the read failed. */
+gdn_status gdn_device_status(const void* status_word, int reset, cudaStream_t stream);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

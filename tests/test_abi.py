@@ -1,0 +1,118 @@
+"""The C-ABI library loads, exports every symbol include/gdn.h declares, and validates its
+arguments on the host (these calls fail before any CUDA work, so they run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    from gated_delta_rule_07_gb300 import build
+    build.build()
+    from gated_delta_rule_07_gb300 import gdn as mod
+    return mod
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "gdn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(gdn):
+    names = declared_functions()
+    assert "gdn_forward" in names and len(names) >= 9
+    lib = ctypes.CDLL(gdn.LIB_PATH)
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(gdn.EXPORTED) == set(names)
+
+
+def test_status_strings(gdn):
+    for code, name in gdn.STATUS_NAMES.items():
+        assert gdn.gdn_status_string(code).startswith(name)
+    assert gdn.gdn_status_string(99) == "GDN_UNKNOWN_STATUS"
+    assert gdn.gdn_version() >= 100
+
+
+def prob(gdn, **kw):
+    base = dict(T=4096, N=1, hk=16, hv=32, K=128, V=128, P=1)
+    base.update(kw)
+    return gdn.make_problem(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(), 0), (dict(P=64, T=65536), 0), (dict(N=8, P=4), 0),
+    (dict(hk=3), 1), (dict(hv=0), 1), (dict(P=0), 1), (dict(N=0), 1), (dict(T=-1), 1),
+    (dict(K=96), 2), (dict(V=256), 2), (dict(chunk=32), 2), (dict(K=64, V=64), 0),
+    (dict(path=2, K=64), 2), (dict(path=7), 1),
+])
+def test_check_problem(gdn, kw, status):
+    p = prob(gdn, **kw)
+    assert gdn.gdn_check_problem(p) == status
+    assert (gdn.gdn_workspace_size(p) > 0) == (status == 0)
+
+
+def test_workspace_size_accounts_for_segments(gdn):
+    p1 = prob(gdn, T=65536, P=1)
+    p16 = prob(gdn, T=65536, P=16)
+    per_seg = 32 * 128 * 128 * 4 * 3  # M, U, h_in
+    assert gdn.gdn_workspace_size(p16) - gdn.gdn_workspace_size(p1) >= 16 * per_seg
+    simt = prob(gdn, T=65536, P=1, path=1)
+    # the SIMT path materialises w, u (bf16) and gcum (fp32)
+    assert gdn.gdn_workspace_size(simt) >= 65536 * 32 * (256 * 2 + 4)
+
+
+def test_entry_points_reject_bad_arguments_before_any_launch(gdn):
+    p = prob(gdn)
+    fake = 1 << 20  # never dereferenced: validation fails first
+    L = gdn._lib
+    by = ctypes.byref
+    # null required pointers
+    assert L.gdn_forward(by(p), None, fake, fake, fake, fake, None, None, fake, None, fake,
+                         1 << 40, None) == 1
+    # misaligned q
+    assert L.gdn_forward(by(p), fake + 2, fake, fake, fake, fake, None, None, fake, None, fake,
+                         1 << 40, None) == 1
+    # workspace too small / missing
+    assert L.gdn_forward(by(p), fake, fake, fake, fake, fake, None, None, fake, None, fake,
+                         16, None) == 3
+    assert L.gdn_forward(by(p), fake, fake, fake, fake, fake, None, None, fake, None, None,
+                         1 << 40, None) == 3
+    # several sequences need cu_seqlens
+    p8 = prob(gdn, N=8)
+    assert L.gdn_forward(by(p8), fake, fake, fake, fake, fake, None, None, fake, None, fake,
+                         1 << 40, None) == 1
+    # unsupported shape
+    assert L.gdn_forward(by(prob(gdn, K=96)), fake, fake, fake, fake, fake, None, None, fake,
+                         None, fake, 1 << 40, None) == 2
+    assert L.gdn_chunk_prepare(by(p), None, fake, fake, fake, None, fake, fake, fake, None,
+                               None) == 1
+    assert L.gdn_segment_summary(by(p), fake, fake, fake, fake, None, None, fake, None,
+                                 None) == 1
+    assert L.gdn_state_prefix_scan(by(p), fake, fake, None, None, None, None) == 1
+    assert L.gdn_chunk_emit(by(p), fake, fake, fake, fake, fake, None, None, None, None, None,
+                            None) == 1
+    assert L.gdn_device_status(None, 0, None) == 1
+    assert L.gdn_forward(None, fake, fake, fake, fake, fake, None, None, fake, None, fake,
+                         1 << 40, None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    """The binding refuses to import when libgdn.so is absent (no silent fallback)."""
+    import importlib
+    import sys
+    from gated_delta_rule_07_gb300 import build
+    monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
+    saved = sys.modules.pop("gated_delta_rule_07_gb300.gdn", None)
+    try:
+        with pytest.raises(ImportError):
+            importlib.import_module("gated_delta_rule_07_gb300.gdn")
+    finally:
+        sys.modules.pop("gated_delta_rule_07_gb300.gdn", None)
+        if saved is not None:
+            sys.modules["gated_delta_rule_07_gb300.gdn"] = saved

@@ -1,0 +1,215 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle.
+
+Tolerances: fp32 I/O max |gpu - oracle| <= 2e-3; bf16 I/O max |gpu - oracle| / rms(oracle)
+<= 2e-2 for `out` and for each sequence's final state.  Both kernel families (SIMT and
+tensor-core) are checked where they apply.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_07_gb300 import inputs
+from gdn_testutil import (BF16_TOL, F32_TOL, check_bf16, key_group, max_abs, rel_to_rms,
+                          to_device, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    from gated_delta_rule_07_gb300 import build
+    build.build()
+    from gated_delta_rule_07_gb300 import gdn as mod
+    assert torch.cuda.is_available()
+    return mod
+
+
+def run_gpu(gdn, inp, P=1, path=0, check_status=True):
+    d = to_device(inp)
+    cu = d["cu_seqlens"] if len(inp.lengths) > 1 else None
+    out, hf = gdn.forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], cu, P=P,
+                          path=path, check_status=check_status)
+    torch.cuda.synchronize()
+    return to_np(out), to_np(hf)
+
+
+def run_oracle(inp, C=64, P=1):
+    return oracle.token(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.h0, inp.cu_seqlens)
+
+
+# ------------------------------------------------------------------ tiny fp32 (SIMT)
+
+def test_tiny_fp32_matches_oracle(gdn):
+    inp = inputs.make(inputs.tiny_fp32())
+    ref_o, ref_h = run_oracle(inp)
+    for P in (1, 2, 3):
+        o, h = run_gpu(gdn, inp, P=P)
+        assert max_abs(o, ref_o) <= F32_TOL, P
+        assert max_abs(h, ref_h) <= F32_TOL, P
+
+
+# ------------------------------------------------------------------ small bf16, both paths
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("T,P,lengths", [
+    (64, 1, None), (64 * 5 + 17, 1, None), (64 * 5 + 17, 2, None), (64 * 7, 3, None),
+    (64 * 3, 5, None), (None, 2, (100, 1, 0, 64, 257))])
+def test_small_bf16_matches_oracle(gdn, path, T, P, lengths):
+    if lengths is not None:
+        inp = inputs.custom(sum(lengths), 2, 4, 128, 128, torch.bfloat16, h0_std=0.02,
+                            lengths=lengths, chunk=1, seed=3)
+    else:
+        inp = inputs.custom(T, 2, 4, 128, 128, torch.bfloat16, h0_std=0.02, seed=1)
+    ref_o, ref_h = run_oracle(inp)
+    o, h = run_gpu(gdn, inp, P=P, path=path)
+    check_bf16(o, h, ref_o, ref_h)
+
+
+@pytest.mark.parametrize("KV", [(64, 64), (64, 128), (128, 64)])
+def test_other_head_dims_simt(gdn, KV):
+    K, V = KV
+    inp = inputs.custom(64 * 3 + 5, 1, 2, K, V, torch.float32, g_kind="log_uniform",
+                        h0_std=0.02, seed=4)
+    ref_o, ref_h = run_oracle(inp)
+    o, h = run_gpu(gdn, inp, P=2)
+    assert max_abs(o, ref_o) <= F32_TOL and max_abs(h, ref_h) <= F32_TOL
+
+
+# ------------------------------------------------------------------ stage entry points
+
+def test_stage_entry_points_match_oracle_stages(gdn):
+    inp = inputs.custom(64 * 4 + 9, 1, 2, 64, 64, torch.float32, g_kind="log_uniform",
+                        h0_std=0.05, seed=5, lengths=(120, 153))
+    P = 2
+    d = to_device(inp)
+    p = gdn.problem_for(d["q"], d["v"], d["cu_seqlens"], P=P)
+    T, hv = inp.v.shape[0], inp.v.shape[1]
+    dev = "cuda"
+    w = torch.empty(T, hv, 64, device=dev)
+    u = torch.empty(T, hv, 64, device=dev)
+    gcum = torch.empty(T, hv, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    gdn.gdn_chunk_prepare(p, d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], w, u, gcum, st)
+    rw, ru, rg = oracle.prepare(inp.k, inp.v, inp.g, inp.beta, inp.cu_seqlens, C=64)
+    torch.cuda.synchronize()
+    assert max_abs(to_np(w), rw) < 1e-4 and max_abs(to_np(u), ru) < 1e-4
+    assert max_abs(to_np(gcum), rg) < 1e-5
+    S = 2 * P
+    M = torch.empty(S, hv, 64, 64, device=dev)
+    U = torch.empty(S, hv, 64, 64, device=dev)
+    gdn.gdn_segment_summary(p, d["k"], w, u, gcum, d["cu_seqlens"], M, U, st)
+    rM, rU = oracle.summary(inp.k, inp.v, inp.g, inp.beta, inp.cu_seqlens, C=64, P=P)
+    torch.cuda.synchronize()
+    assert max_abs(to_np(M), rM) < 1e-4 and max_abs(to_np(U), rU) < 1e-4
+    h_in = torch.empty(S, hv, 64, 64, device=dev)
+    hf = torch.empty(2, hv, 64, 64, device=dev)
+    gdn.gdn_state_prefix_scan(p, M, U, d["h0"], h_in, hf)
+    rh_in, rhf = oracle.scan(rM, rU, inp.h0, N=2, P=P)
+    torch.cuda.synchronize()
+    assert max_abs(to_np(h_in), rh_in) < 1e-4 and max_abs(to_np(hf), rhf) < 1e-4
+    out = torch.empty_like(d["v"])
+    hf2 = torch.empty_like(hf)
+    gdn.gdn_chunk_emit(p, d["q"], d["k"], w, u, gcum, h_in, d["cu_seqlens"], out, hf2, st)
+    ro = oracle.emit(inp.q, inp.k, inp.v, inp.g, inp.beta, rh_in, inp.cu_seqlens, C=64, P=P)
+    torch.cuda.synchronize()
+    assert max_abs(to_np(out), ro) < F32_TOL and max_abs(to_np(hf2), rhf) < F32_TOL
+    assert gdn.gdn_device_status(st) == 0
+
+
+# ------------------------------------------------------------------ workload configs
+
+def test_prefill_bf16_4096(gdn):
+    inp = inputs.make(inputs.prefill_bf16())
+    ref_o, ref_h = run_oracle(inp)
+    for path in (2, 1):
+        o, h = run_gpu(gdn, inp, P=1, path=path)
+        check_bf16(o, h, ref_o, ref_h)
+
+
+def test_segment_bf16_16384_P8_equals_P1(gdn):
+    inp = inputs.make(inputs.segment_bf16())
+    ref_o, ref_h = run_oracle(inp)
+    o8, h8 = run_gpu(gdn, inp, P=8)
+    o1, h1 = run_gpu(gdn, inp, P=1)
+    check_bf16(o8, h8, ref_o, ref_h)
+    check_bf16(o1, h1, ref_o, ref_h)
+    # the segment count changes only rounding: P=8 against P=1 on the GPU
+    assert rel_to_rms(o8, o1) <= BF16_TOL and rel_to_rms(h8, h1) <= BF16_TOL
+
+
+def test_varlen_bf16(gdn):
+    inp = inputs.make(inputs.varlen_bf16())
+    valid = inp.valid.numpy()
+    for P in (1, 4):
+        o, h = run_gpu(gdn, inp, P=P)
+        # padded positions read zeros exactly (q = 0 there)
+        assert np.all(o[~valid] == 0.0)
+        for kh in (0, 9, 15):
+            sub = key_group(inp, kh, 2)
+            ref_o, ref_h = oracle.token(**sub, cu_seqlens=inp.cu_seqlens)
+            check_bf16(o[:, 2 * kh:2 * kh + 2], h[:, 2 * kh:2 * kh + 2], ref_o, ref_h,
+                       valid=valid)
+
+
+@pytest.mark.slow
+def test_long_bf16_65536_sampled_heads(gdn):
+    """Full-size launch (the benchmark's configuration); outputs of sampled key-head groups
+    are checked against the oracle, the rest through segment-count agreement."""
+    inp = inputs.make(inputs.long_bf16())
+    refs = {kh: oracle.token(**key_group(inp, kh, 2)) for kh in (0, 15)}
+    base = None
+    for P in (16, 64, 4, 1):
+        o, h = run_gpu(gdn, inp, P=P)
+        for kh, (ref_o, ref_h) in refs.items():
+            check_bf16(o[:, 2 * kh:2 * kh + 2], h[:, 2 * kh:2 * kh + 2], ref_o, ref_h)
+        if base is None:
+            base = (o, h)
+        else:
+            assert rel_to_rms(o, base[0]) <= BF16_TOL and rel_to_rms(h, base[1]) <= BF16_TOL
+
+
+# ------------------------------------------------------------------ edge cases
+
+def test_empty_stream_returns_h0(gdn):
+    h0 = torch.randn(1, 4, 128, 128, device="cuda")
+    q = torch.zeros(0, 2, 128, dtype=torch.bfloat16, device="cuda")
+    v = torch.zeros(0, 4, 128, dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros(0, 4, device="cuda")
+    for path in (1, 2):
+        out, hf = gdn.forward(q, q, v, g, g, h0, None, P=3, path=path, check_status=True)
+        assert out.numel() == 0 and torch.equal(hf, h0)
+
+
+def test_bad_cu_seqlens_is_reported_not_faulted(gdn):
+    inp = inputs.custom(256, 2, 4, 128, 128, torch.bfloat16, lengths=(128, 128), seed=6)
+    d = to_device(inp)
+    bad = torch.tensor([0, 300, 256], dtype=torch.int32, device="cuda")
+    with pytest.raises(gdn.GdnError) as ei:
+        gdn.forward(d["q"], d["k"], d["v"], d["g"], d["beta"], None, bad, P=2,
+                    check_status=True)
+    assert ei.value.status == 6
+
+
+def test_split_call_resume(gdn):
+    inp = inputs.custom(64 * 6 + 11, 2, 4, 128, 128, torch.bfloat16, h0_std=0.02, seed=7)
+    d = to_device(inp)
+    T1 = 64 * 2 + 30
+    o_full, h_full = gdn.forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], None, P=2)
+    sl = lambda x, a, b: x[a:b].contiguous()
+    oa, ha = gdn.forward(*(sl(d[n], 0, T1) for n in ("q", "k", "v", "g", "beta")), d["h0"], None)
+    ob, hb = gdn.forward(*(sl(d[n], T1, None) for n in ("q", "k", "v", "g", "beta")), ha, None)
+    o2 = torch.cat([oa, ob])
+    assert rel_to_rms(to_np(o2), to_np(o_full)) <= BF16_TOL
+    assert rel_to_rms(to_np(hb), to_np(h_full)) <= BF16_TOL
+
+
+def test_negative_control_tiled_gqa_fails(gdn):
+    """Feeding the key heads in tiled order must break parity (the check has teeth)."""
+    inp = inputs.custom(192, 2, 4, 128, 128, torch.bfloat16, seed=8)
+    ref_o, _ = run_oracle(inp)
+    d = to_device(inp)
+    k_tiled = d["k"][:, [1, 0]].contiguous()
+    q_tiled = d["q"][:, [1, 0]].contiguous()
+    out, _ = gdn.forward(q_tiled, k_tiled, d["v"], d["g"], d["beta"], None, None)
+    assert rel_to_rms(to_np(out), ref_o) > BF16_TOL
