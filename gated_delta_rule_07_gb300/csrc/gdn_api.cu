@@ -18,8 +18,6 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-size_t io_bytes(const gdn_problem* p) { return p->io_dtype == GDN_BF16 ? 2 : 4; }
-
 // Resolved kernel family for a problem.
 bool use_tensor_path(const gdn_problem* p) {
   const bool covers = p->io_dtype == GDN_BF16 && p->k_dim == 128 && p->v_dim == 128;
@@ -98,9 +96,9 @@ Layout layout(const gdn_problem* p) {
   L.h_in = off;
   off += seg ? align_up(S * K * V * 4) : 0;
   L.w = off;
-  off += mat ? align_up(T * p->hv * K * io_bytes(p)) : 0;
+  off += mat ? align_up(T * p->hv * K * 4) : 0;
   L.u = off;
-  off += mat ? align_up(T * p->hv * V * io_bytes(p)) : 0;
+  off += mat ? align_up(T * p->hv * V * 4) : 0;
   L.gcum = off;
   off += mat ? align_up(T * p->hv * 4) : 0;
   L.total = off;
@@ -120,6 +118,7 @@ const char* gdn_status_string(gdn_status s) {
     case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA launch or runtime call failed";
     case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT: a bounded device wait expired";
     case GDN_ERR_DEVICE_INPUT: return "GDN_ERR_DEVICE_INPUT: cu_seqlens inconsistent on the device";
+    case GDN_ERR_DEVICE_RANGE: return "GDN_ERR_DEVICE_RANGE: a tensor-core operand exceeded the fp16 range";
   }
   return "GDN_UNKNOWN_STATUS";
 }

@@ -102,21 +102,21 @@ __global__ void __launch_bounds__(kThreads) simt_prepare_kernel(Args a) {
     }
   }
   __syncthreads();
-  TIO* w = static_cast<TIO*>(a.w_out);
-  TIO* u = static_cast<TIO*>(a.u_out);
+  float* w = static_cast<float*>(a.w_out);
+  float* u = static_cast<float*>(a.u_out);
   for (int e = tid; e < C * KD; e += kThreads) {
     const int t = e / KD, i = e % KD;
     if (t >= L) continue;
     float x = 0.f;
     for (int s = 0; s <= t; ++s) x += Tm[t * CP + s] * bw[s] * ks[s * KP + i];
-    w[((t0 + t) * a.hv + j) * KD + i] = from_f32<TIO>(x);
+    w[((t0 + t) * a.hv + j) * KD + i] = x;
   }
   for (int e = tid; e < C * VD; e += kThreads) {
     const int t = e / VD, c = e % VD;
     if (t >= L) continue;
     float x = 0.f;
     for (int s = 0; s <= t; ++s) x += Tm[t * CP + s] * bs[s] * vs[s * VP + c];
-    u[((t0 + t) * a.hv + j) * VD + c] = from_f32<TIO>(x);
+    u[((t0 + t) * a.hv + j) * VD + c] = x;
   }
   if (tid < L) a.gcum_out[(t0 + tid) * a.hv + j] = G[tid];
 }
@@ -149,8 +149,8 @@ __global__ void __launch_bounds__(kThreads) simt_summary_kernel(Args a) {
   int64_t c0, c1;
   segment_chunks(se - sb, a.P, r, c0, c1);
   const TIO* k = static_cast<const TIO*>(a.k);
-  const TIO* w = static_cast<const TIO*>(a.w);
-  const TIO* u = static_cast<const TIO*>(a.u);
+  const float* w = static_cast<const float*>(a.w);
+  const float* u = static_cast<const float*>(a.u);
 
   for (int e = tid; e < KD * kColBlock; e += kThreads) {
     const int i = e / kColBlock, c = e % kColBlock;
@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kThreads) simt_summary_kernel(Args a) {
       const int t = e / KD, i = e % KD;
       float wv = 0.f, kv = 0.f;
       if (t < L) {
-        wv = to_f32(w[((t0 + t) * a.hv + j) * KD + i]);
+        wv = w[((t0 + t) * a.hv + j) * KD + i];
         kv = to_f32(k[((t0 + t) * a.hk + kh) * KD + i]) * __expf(GL - G[t]);
       }
       ws[t * KP + i] = wv;
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) simt_summary_kernel(Args a) {
     if (is_u)
       for (int e = tid; e < C * kColBlock; e += kThreads) {
         const int t = e / kColBlock, c = e % kColBlock;
-        us[t * XP + c] = t < L ? to_f32(u[((t0 + t) * a.hv + j) * VD + ucol0 + c]) : 0.f;
+        us[t * XP + c] = t < L ? u[((t0 + t) * a.hv + j) * VD + ucol0 + c] : 0.f;
       }
     __syncthreads();
     for (int e = tid; e < C * kColBlock; e += kThreads) {
@@ -284,8 +284,8 @@ __global__ void __launch_bounds__(kThreads) simt_emit_kernel(Args a) {
   segment_chunks(se - sb, a.P, r, c0, c1);
   const TIO* q = static_cast<const TIO*>(a.q);
   const TIO* k = static_cast<const TIO*>(a.k);
-  const TIO* w = static_cast<const TIO*>(a.w);
-  const TIO* u = static_cast<const TIO*>(a.u);
+  const float* w = static_cast<const float*>(a.w);
+  const float* u = static_cast<const float*>(a.u);
   TIO* out = static_cast<TIO*>(a.out);
 
   for (int e = tid; e < KD * kColBlock; e += kThreads) {
@@ -302,11 +302,11 @@ __global__ void __launch_bounds__(kThreads) simt_emit_kernel(Args a) {
       const bool ok = t < L;
       qs[t * KP + i] = ok ? to_f32(q[((t0 + t) * a.hk + kh) * KD + i]) : 0.f;
       ks[t * KP + i] = ok ? to_f32(k[((t0 + t) * a.hk + kh) * KD + i]) : 0.f;
-      ws[t * KP + i] = ok ? to_f32(w[((t0 + t) * a.hv + j) * KD + i]) : 0.f;
+      ws[t * KP + i] = ok ? w[((t0 + t) * a.hv + j) * KD + i] : 0.f;
     }
     for (int e = tid; e < C * kColBlock; e += kThreads) {
       const int t = e / kColBlock, c = e % kColBlock;
-      us[t * XP + c] = t < L ? to_f32(u[((t0 + t) * a.hv + j) * VD + col0 + c]) : 0.f;
+      us[t * XP + c] = t < L ? u[((t0 + t) * a.hv + j) * VD + col0 + c] : 0.f;
     }
     __syncthreads();
     const float GL = G[L - 1];

@@ -13,7 +13,15 @@
 //   phase 1  the same chain on X = [M | U] from [I | 0] (u = 0 for the M half), which is the
 //            low-rank composition M <- gamma M - k_tilde^T (w M).
 // Every decay factor is applied elementwise with a non-positive exponent.
+//
+// MMA operands are fp16 (11-bit significand): the bf16 inputs are converted in shared memory
+// (exact for |x| >= 2^-14, and below that the absolute error is < 2^-25), and the computed
+// operands (T, w, the state copy, delta, attn_i) keep 8x the precision bf16 would.  The bf16
+// output rounding alone costs up to 2^-9 max|o|, so the inner operands must be finer than
+// bf16 to keep max|err| / rms(o) inside 2e-2.  A value outside the fp16 range is reported
+// as GDN_ERR_DEVICE_RANGE.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -50,11 +58,11 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
                : "r"(addr));
 }
 
-// D = A * B + D, m16n8k16, A row-major, B column-major, bf16 in, fp32 accumulate.
+// D = A * B + D, m16n8k16, A row-major, B column-major, fp16 in, fp32 accumulate.
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -68,14 +76,32 @@ __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_all;\n" ::: "memory");
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+constexpr float kHalfMax = 65504.f;
+
+// Converts, in place, the 16-byte chunk at p from 8 bf16 to 8 fp16; returns false when a
+// value does not fit the fp16 range.
+__device__ __forceinline__ bool bf16_chunk_to_f16(char* p) {
+  uint4 x = *reinterpret_cast<uint4*>(p);
+  uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[i]));
+    ok = ok && fabsf(f.x) <= kHalfMax && fabsf(f.y) <= kHalfMax;
+    w[i] = pack_h2(f.x, f.y);
+  }
+  *reinterpret_cast<uint4*>(p) = x;
+  return ok;
 }
 
 // ------------------------------------------------------------ swizzled bf16 tiles
 //
-// A tile is `rows` x RL bf16, row-major, with the 16-byte chunks of each row XOR-permuted by
+// A tile is `rows` x RL 16-bit values (fp16), row-major, with the 16-byte chunks of each row XOR-permuted by
 // (row & 7) so that the eight row addresses of an ldmatrix hit eight different bank groups.
 
 template <int RL>
@@ -112,30 +138,32 @@ __device__ __forceinline__ void load_b_nk(uint32_t base, int k0, int n0, uint32_
   ldsm_x4(base + tile_off<RL>(n0 + rr + ((mi >> 1) << 3), k0 + ((mi & 1) << 3)), b);
 }
 
-// Stores the accumulator of an m16n8 tile at (m0, n0) as bf16, rows scaled by sc[0] (row g)
-// and sc[1] (row g + 8).
+// Stores the accumulator of an m16n8 tile at (m0, n0) as fp16, row g scaled by s0 and row
+// g + 8 by s1.  Returns false when a stored value overflows the fp16 range.
 template <int RL>
-__device__ __forceinline__ void store_acc_bf16(char* base, int m0, int n0, const float (&d)[4],
-                                               float s0, float s1) {
+__device__ __forceinline__ bool store_acc_h(char* base, int m0, int n0, const float (&d)[4],
+                                            float s0, float s1) {
   const int l = threadIdx.x & 31, g = l >> 2, q = l & 3;
   const int r0 = m0 + g, r1 = m0 + g + 8;
-  *reinterpret_cast<uint32_t*>(base + tile_off<RL>(r0, n0) + 4 * q) = pack_bf16(d[0] * s0, d[1] * s0);
-  *reinterpret_cast<uint32_t*>(base + tile_off<RL>(r1, n0) + 4 * q) = pack_bf16(d[2] * s1, d[3] * s1);
+  const float a = d[0] * s0, b = d[1] * s0, c = d[2] * s1, e = d[3] * s1;
+  *reinterpret_cast<uint32_t*>(base + tile_off<RL>(r0, n0) + 4 * q) = pack_h2(a, b);
+  *reinterpret_cast<uint32_t*>(base + tile_off<RL>(r1, n0) + 4 * q) = pack_h2(c, e);
+  return fmaxf(fmaxf(fabsf(a), fabsf(b)), fmaxf(fabsf(c), fabsf(e))) <= kHalfMax;
 }
 
 // ------------------------------------------------------------ shared memory plan
 
 struct Smem {
-  __nv_bfloat16 q[C * KD];    // [t][i]
-  __nv_bfloat16 k[C * KD];    // [t][i]
-  __nv_bfloat16 v[C * VD];    // [t][c]
-  __nv_bfloat16 nw[C * KD];   // -w  [t][i]
-  __nv_bfloat16 h[KD * VD];   // state as an operand [i][c]
-  __nv_bfloat16 d[C * VD];    // delta [t][c]
-  __nv_bfloat16 dp[C * VD];   // diag(e^{G_last - G_t}) delta [t][c]
-  __nv_bfloat16 att[C * C];   // attn_i [t][s]
-  __nv_bfloat16 tw[C * C];    // T diag(beta e^G) [t][s]
-  __nv_bfloat16 tu[C * C];    // T diag(beta) [t][s]
+  __half q[C * KD];    // [t][i]
+  __half k[C * KD];    // [t][i]
+  __half v[C * VD];    // [t][c]
+  __half nw[C * KD];   // -w  [t][i]
+  __half h[KD * VD];   // state as an operand [i][c]
+  __half d[C * VD];    // delta [t][c]
+  __half dp[C * VD];   // diag(e^{G_last - G_t}) delta [t][c]
+  __half att[C * C];   // attn_i [t][s]
+  __half tw[C * C];    // T diag(beta e^G) [t][s]
+  __half tu[C * C];    // T diag(beta) [t][s]
   float A[C * FP];            // masked gram, fp32
   float Ti[C * FP];           // (I + A)^-1, fp32
   float X[C * FP];            // solve scratch
@@ -170,6 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chunk_kernel(Args a) {
   const uint32_t sdp = smem_addr(S.dp), satt = smem_addr(S.att);
   const uint32_t stw = smem_addr(S.tw), stu = smem_addr(S.tu);
 
+  bool range_ok = true;  // every fp16 operand stayed finite
+
   // ---- the state: rows [16 warp, +16), all 128 columns, as 16 m16n8 accumulators
   float hacc[16][4];
   {
@@ -192,7 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chunk_kernel(Args a) {
     // ---- (0) publish the state as a bf16 operand; stage q, k, v, g, beta
     __syncthreads();  // previous chunk finished reading every buffer
     for (int nt = 0; nt < 16; ++nt)
-      store_acc_bf16<VD>(reinterpret_cast<char*>(S.h), warp * 16, nt * 8, hacc[nt], 1.f, 1.f);
+      range_ok &= store_acc_h<VD>(reinterpret_cast<char*>(S.h), warp * 16, nt * 8, hacc[nt], 1.f,
+                                  1.f);
     for (int e = tid; e < C * 16; e += kThreads) {
       const int t = e >> 4, cc = (e & 15) << 3;
       const bool ok = t < L;
@@ -217,6 +248,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chunk_kernel(Args a) {
       S.beta[lane + 32] = lane + 32 < L ? a.beta[(t0 + lane + 32) * a.hv + j] : 0.f;
     }
     cp_async_wait_all();
+    // bf16 -> fp16 in place, each thread on the chunks it copied
+    for (int e = tid; e < C * 16; e += kThreads) {
+      const int t = e >> 4, cc = (e & 15) << 3;
+      range_ok &= bf16_chunk_to_f16(reinterpret_cast<char*>(S.k) + tile_off<KD>(t, cc));
+      if (MODE == kEmit)
+        range_ok &= bf16_chunk_to_f16(reinterpret_cast<char*>(S.q) + tile_off<KD>(t, cc));
+      if (MODE != kSumM)
+        range_ok &= bf16_chunk_to_f16(reinterpret_cast<char*>(S.v) + tile_off<VD>(t, cc));
+    }
     __syncthreads();
     const float GL = S.G[L - 1];
     const float gamma = __expf(GL);
@@ -257,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chunk_kernel(Args a) {
           S.A[t * FP + s + 1] = x[1];
           if (MODE == kEmit)
             *reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(S.att) + tile_off<C>(t, s) +
-                                         (s & 7) * 2) = pack_bf16(y[0], y[1]);
+                                         (s & 7) * 2) = pack_h2(y[0], y[1]);
         }
     }
     __syncthreads();
@@ -310,9 +350,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chunk_kernel(Args a) {
       const float b0 = S.beta[s], b1 = S.beta[s + 1];
       const uint32_t off = tile_off<C>(t, s & ~7) + (s & 7) * 2;
       *reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(S.tw) + off) =
-          pack_bf16(t0v * b0 * __expf(S.G[s]), t1v * b1 * __expf(S.G[s + 1]));
+          pack_h2(t0v * b0 * __expf(S.G[s]), t1v * b1 * __expf(S.G[s + 1]));
       *reinterpret_cast<uint32_t*>(reinterpret_cast<char*>(S.tu) + off) =
-          pack_bf16(t0v * b0, t1v * b1);
+          pack_h2(t0v * b0, t1v * b1);
     }
     __syncthreads();
 
@@ -345,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chunk_kernel(Args a) {
         }
       }
       for (int nt = 0; nt < 8; ++nt)
-        store_acc_bf16<KD>(reinterpret_cast<char*>(S.nw), m0, n0 + nt * 8, wacc[nt], -1.f, -1.f);
+        range_ok &= store_acc_h<KD>(reinterpret_cast<char*>(S.nw), m0, n0 + nt * 8, wacc[nt], -1.f,
+                                    -1.f);
     }
     __syncthreads();
 
@@ -376,8 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chunk_kernel(Args a) {
       const float s0 = __expf(GL - S.G[t0r]), s1 = __expf(GL - S.G[t1r]);
       for (int nt = 0; nt < 8; ++nt) {
         if (MODE == kEmit)
-          store_acc_bf16<VD>(reinterpret_cast<char*>(S.d), m0, n0 + nt * 8, dacc[nt], 1.f, 1.f);
-        store_acc_bf16<VD>(reinterpret_cast<char*>(S.dp), m0, n0 + nt * 8, dacc[nt], s0, s1);
+          range_ok &= store_acc_h<VD>(reinterpret_cast<char*>(S.d), m0, n0 + nt * 8, dacc[nt], 1.f,
+                                      1.f);
+        range_ok &= store_acc_h<VD>(reinterpret_cast<char*>(S.dp), m0, n0 + nt * 8, dacc[nt], s0,
+                                    s1);
       }
     }
     __syncthreads();
@@ -430,6 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_chunk_kernel(Args a) {
       }
     }
   }
+
+  if (!range_ok) set_status(a.status, GDN_ERR_DEVICE_RANGE);
 
   // ---- write the state out
   float* dst = nullptr;

@@ -28,7 +28,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 GDN_OK = 0
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPORTED",
                 3: "GDN_ERR_WORKSPACE", 4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_TIMEOUT",
-                6: "GDN_ERR_DEVICE_INPUT"}
+                6: "GDN_ERR_DEVICE_INPUT", 7: "GDN_ERR_DEVICE_RANGE"}
 GDN_BF16, GDN_F32 = 0, 1
 PATH_AUTO, PATH_SIMT, PATH_TENSOR = 0, 1, 2
 EXPORTED = ("gdn_status_string", "gdn_check_problem", "gdn_workspace_size", "gdn_forward",

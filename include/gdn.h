@@ -32,7 +32,7 @@
  *                 h0, h_final [N, hv, K, V] fp32 (the state layout [Hv, K, V] f32 of the page
  *                           "RFC(qwen35): TP Phase2", section "Partition Contract", per sequence)
  *                 cu_seqlens int32 [N+1]    cu[0] = 0, non-decreasing, cu[N] = T
- *                 w [T, hv, K], u [T, hv, V] io dtype;  gcum [T, hv] fp32 (token aligned)
+ *                 w [T, hv, K], u [T, hv, V], gcum [T, hv] fp32 (token aligned)
  *                 M [N*P, hv, K, K], U and h_in [N*P, hv, K, V] fp32; segment (n, r) -> n*P + r
  *               Value head j reads key head j / (hv / hk) (grouped order).
  *   Segments    each sequence's Nc = ceil(L / C) chunks are split into P contiguous,
@@ -50,6 +50,10 @@
  *               GDN_ERR_DEVICE_INPUT in the status word, read by gdn_device_status().
  *   Supported   io dtype bf16 or fp32; K, V in {64, 128}; C = 64; hv % hk == 0; P >= 1;
  *               16-byte aligned tensor pointers.
+ *   Precision   fp32 I/O runs on fp32 CUDA-core kernels.  bf16 I/O with K = V = 128 runs on the
+ *               tensor cores with fp16 operands (inputs converted exactly in range), fp32
+ *               accumulation and an fp32 state: q, k, v and the state must stay below 65504 in
+ *               magnitude; a value that does not is reported as GDN_ERR_DEVICE_RANGE.
  */
 #ifndef GDN_H_
 #define GDN_H_
@@ -70,7 +74,8 @@ typedef enum gdn_status {
     GDN_ERR_WORKSPACE = 3,        /* workspace null or smaller than gdn_workspace_size()  */
     GDN_ERR_CUDA = 4,             /* a CUDA launch or runtime call failed                 */
     GDN_ERR_DEVICE_TIMEOUT = 5,   /* a bounded device-side wait expired                   */
-    GDN_ERR_DEVICE_INPUT = 6      /* the device found cu_seqlens inconsistent             */
+    GDN_ERR_DEVICE_INPUT = 6,     /* the device found cu_seqlens inconsistent             */
+    GDN_ERR_DEVICE_RANGE = 7      /* a tensor-core operand left the fp16 range (|x| > 65504) */
 } gdn_status;
 
 typedef enum gdn_dtype { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
@@ -87,7 +92,7 @@ typedef struct gdn_problem {
     int32_t k_dim, v_dim;     /* K, V                                                    */
     int32_t chunk;            /* C (64)                                                  */
     int32_t segments_per_seq; /* P >= 1                                                  */
-    int32_t io_dtype;         /* gdn_dtype of q, k, v, out, w, u                         */
+    int32_t io_dtype;         /* gdn_dtype of q, k, v and out                            */
     int32_t path;             /* gdn_path                                                */
 } gdn_problem;
 
@@ -119,7 +124,7 @@ gdn_status gdn_forward(const gdn_problem* p, const void* q, const void* k, const
 
 /* Phase "prepare": the WY/UT factors of every chunk ("Implementation": the WY factors that
  * phase 3 reuses; "Why": w and u of the chunk map).  Writes w [T, hv, K], u [T, hv, V]
- * (io dtype) and gcum [T, hv] (fp32, inclusive within-chunk cumulative log-decay; a chunk's
+ * (fp32) and gcum [T, hv] (fp32, inclusive within-chunk cumulative log-decay; a chunk's
  * gamma is exp of its last row).  dev_status: device int32 status word or NULL. */
 gdn_status gdn_chunk_prepare(const gdn_problem* p, const void* k, const void* v, const float* g,
                              const float* beta, const int32_t* cu_seqlens, void* w, void* u,

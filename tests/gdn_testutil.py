@@ -1,9 +1,13 @@
 """Shared helpers of the test suite: tolerance metrics and oracle/GPU runners.
 
 Tolerances (written in the tests that use them):
-  * fp32 I/O:  max |gpu - oracle| <= 2e-3;
-  * bf16 I/O:  max |gpu - oracle| / rms(oracle) <= 2e-2, applied to `out` and to each
-    sequence's final state separately.
+  * fp32 I/O:  max |gpu - oracle| <= 2e-3 (outputs and final states);
+  * bf16 I/O ("2e-2 relative-to-RMS", fp32 accumulate):
+      - final states (fp32): max |gpu - oracle| / rms(oracle) <= 2e-2 per sequence;
+      - outputs (bf16):      rms(gpu - oracle) / rms(oracle) <= 2e-2, and elementwise
+        |gpu - oracle| <= 2^-8 |o| + 2e-2 rms(oracle), where 2^-8 |o| bounds the rounding of
+        the output itself to bf16.  The plain max form cannot hold for bf16 outputs: the
+        exact result rounded to bf16 already exceeds it (tests/test_tolerance_reading.py).
 """
 import numpy as np
 import torch
@@ -46,17 +50,46 @@ def to_device(inp, device="cuda"):
     return d
 
 
+BF16_HALF_ULP = 2.0 ** -8   # |bf16(x) - x| <= 2^-8 |x| (8 significant bits, nearest)
+
+
+def rms_rel(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
+    err = float(np.sqrt(np.mean((got - ref) ** 2))) if ref.size else 0.0
+    return err / rms if rms > 0 else err
+
+
+def excess_over_rounding(got, ref):
+    """max over elements of (|got - ref| - 2^-8 max(|got|, |ref|)) / rms(ref)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if not ref.size:
+        return 0.0
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    ex = np.abs(got - ref) - BF16_HALF_ULP * np.maximum(np.abs(got), np.abs(ref))
+    return float(np.max(ex)) / rms if rms > 0 else float(np.max(ex))
+
+
+def check_bf16_out(out_gpu, out_ref, tol=BF16_TOL):
+    e_rms = rms_rel(out_gpu, out_ref)
+    e_max = excess_over_rounding(out_gpu, out_ref)
+    assert e_rms <= tol, f"out rms-relative error {e_rms:.3e} > {tol}"
+    assert e_max <= tol, f"out error beyond bf16 rounding {e_max:.3e} rms > {tol}"
+    return e_rms, e_max
+
+
 def check_bf16(out_gpu, hf_gpu, out_ref, hf_ref, valid=None, tol=BF16_TOL):
-    """Returns (out_err, [final-state err per sequence]) and asserts the tolerance."""
+    """Asserts the bf16 tolerances; returns ((out rms-rel, out excess), [state errors])."""
     og = np.asarray(out_gpu)
     orf = np.asarray(out_ref)
     if valid is not None:
         og, orf = og[valid], orf[valid]
-    e_out = rel_to_rms(og, orf)
+    e_out = check_bf16_out(og, orf, tol)
     e_h = [rel_to_rms(hf_gpu[n], hf_ref[n]) for n in range(len(hf_ref))]
-    assert e_out <= tol, f"out rel-to-rms error {e_out:.3e} > {tol}"
     for n, e in enumerate(e_h):
-        assert e <= tol, f"h_final[{n}] rel-to-rms error {e:.3e} > {tol}"
+        assert e <= tol, f"h_final[{n}] max-abs / rms error {e:.3e} > {tol}"
     return e_out, e_h
 
 
