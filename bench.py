@@ -113,7 +113,7 @@ def make_inputs(T, device, seed):
 
 def source_hash():
     h = hashlib.sha256()
-    for name in ("gdn_tc.cu", "gdn_common.cuh"):
+    for name in ("gdn_tc5.cu", "gdn_sm100.cuh", "gdn_common.cuh"):
         with open(os.path.join(ROOT, "gated_delta_rule_07_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -161,7 +161,7 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
 
     def timed_forward(P, steps, warmup):
-        p = gdn.problem_for(d["q"], d["v"], None, P=P)
+        p = gdn.problem_for(d["q"], d["v"], None, P=P, path=args.path)
         wsb = gdn.workspace_for(p, dev)
         for _ in range(warmup):
             gdn.gdn_forward(p, d["q"], d["k"], d["v"], d["g"], d["beta"], None, None, out, hf,
@@ -181,7 +181,7 @@ def run_ours(args, ws, rank, local):
 
     # P sweep (short), then the timed run at the chosen P
     sweep = {}
-    Ps = [args.P] if args.P else [4, 16, 64, 1]
+    Ps = [args.P] if args.P else [8, 16, 19, 32, 38, 64, 4, 1]
     for P in Ps:
         ms = timed_forward(P, steps=3 if len(Ps) > 1 else 1, warmup=1)
         sweep[P] = ms
@@ -196,7 +196,7 @@ def run_ours(args, ws, rank, local):
         ms = float(t.item())
 
     # per-phase events over the same launches (phase entry points = what gdn_forward enqueues)
-    p = gdn.problem_for(d["q"], d["v"], None, P=P_best)
+    p = gdn.problem_for(d["q"], d["v"], None, P=P_best, path=args.path)
     S = P_best * HV
     M = torch.empty(S, KD, KD, dtype=torch.float32, device=dev)
     U = torch.empty(S, KD, VD, dtype=torch.float32, device=dev)
@@ -228,7 +228,7 @@ def run_ours(args, ws, rank, local):
     hf_h = torch.empty(hf.shape, dtype=hf.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size() + hf_h.numel() * hf_h.element_size()
-    pe = gdn.problem_for(d["q"], d["v"], None, P=P_best)
+    pe = gdn.problem_for(d["q"], d["v"], None, P=P_best, path=args.path)
     wse = gdn.workspace_for(pe, dev)
     dd = {n: torch.empty_like(d[n]) for n in d}
 
@@ -280,12 +280,12 @@ def run_ours(args, ws, rank, local):
                    "segments_per_seq": P_best, "batch": 1, "seq_len": T,
                    "parallelism": f"replicas x{ws} (independent sequences)",
                    "l2": "inputs+output 0.8 GB > 129 MB L2; no flush",
-                   "kernel_family": "tensor-core (mma.sync bf16, fp32 state)"},
+                   "kernel_family": args.family},
         "sweep_ms_per_step": {f"P={k}": round(v, 4) for k, v in sweep.items()},
         "phase_ms": {k: round(v, 4) for k, v in ph.items()},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {
-            "kernel": "tc_chunk_kernel<emit> (phase 3: prepare + chain + output)",
+            "kernel": "chunk kernel <emit> (phase 3: prepare + chain + output)",
             "bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
             "frac": achieved_gbs / hbm, "peak_source": src,
             "traffic": None if tr is None else tr * T,
@@ -369,7 +369,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=2048)
+    ap.add_argument("--path", type=int, default=0,
+                    help="kernel family: 0 auto (tcgen05), 3 mma.sync baseline")
     args = ap.parse_args()
+    args.family = {0: "tcgen05 (TMEM accumulators, fp16 operands, fp32 state)",
+                   2: "tcgen05 (TMEM accumulators, fp16 operands, fp32 state)",
+                   3: "mma.sync (fp16 operands, fp32 state)"}.get(args.path, str(args.path))
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_env()

@@ -22,8 +22,18 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool use_tensor_path(const gdn_problem* p) {
   const bool covers = p->io_dtype == GDN_BF16 && p->k_dim == 128 && p->v_dim == 128;
   if (p->path == GDN_PATH_SIMT) return false;
-  if (p->path == GDN_PATH_TENSOR) return covers;
   return covers;
+}
+
+bool use_mma_sync(const gdn_problem* p) { return p->path == GDN_PATH_MMA_SYNC; }
+
+// Phase 1 and phase 3 with the factors recomputed on chip, on the selected tensor-core
+// generation.
+cudaError_t fused_summary(const gdn_problem* p, const Args& a, cudaStream_t s) {
+  return use_mma_sync(p) ? gdn::tc_summary(a, true, s) : gdn::tc5_summary(a, s);
+}
+cudaError_t fused_emit(const gdn_problem* p, const Args& a, cudaStream_t s) {
+  return use_mma_sync(p) ? gdn::tc_emit(a, true, s) : gdn::tc5_emit(a, s);
 }
 
 gdn_status check_problem(const gdn_problem* p) {
@@ -34,11 +44,11 @@ gdn_status check_problem(const gdn_problem* p) {
     return GDN_ERR_INVALID_ARGUMENT;
   if (p->hv % p->hk != 0) return GDN_ERR_INVALID_ARGUMENT;
   if (p->io_dtype != GDN_BF16 && p->io_dtype != GDN_F32) return GDN_ERR_UNSUPPORTED;
-  if (p->path < GDN_PATH_AUTO || p->path > GDN_PATH_TENSOR) return GDN_ERR_INVALID_ARGUMENT;
+  if (p->path < GDN_PATH_AUTO || p->path > GDN_PATH_MMA_SYNC) return GDN_ERR_INVALID_ARGUMENT;
   if (p->chunk != 64) return GDN_ERR_UNSUPPORTED;
   if ((p->k_dim != 64 && p->k_dim != 128) || (p->v_dim != 64 && p->v_dim != 128))
     return GDN_ERR_UNSUPPORTED;
-  if (p->path == GDN_PATH_TENSOR &&
+  if ((p->path == GDN_PATH_TENSOR || p->path == GDN_PATH_MMA_SYNC) &&
       !(p->io_dtype == GDN_BF16 && p->k_dim == 128 && p->v_dim == 128))
     return GDN_ERR_UNSUPPORTED;
   if (p->hv > 65535) return GDN_ERR_UNSUPPORTED;  // grid.y
@@ -238,12 +248,12 @@ gdn_status gdn_forward(const gdn_problem* p, const void* q, const void* k, const
     if (seg) {
       Args ma = a;
       ma.skip_last_summary = true;
-      GDN_TRY(gdn::tc_summary(ma, true, stream));
+      GDN_TRY(fused_summary(p, ma, stream));
       Args sa = a;
       sa.h_final = nullptr;  // the last segment's emit writes the final state
       GDN_TRY(gdn::tc_scan(sa, stream));
     }
-    return to_status(gdn::tc_emit(a, true, stream));
+    return to_status(fused_emit(p, a, stream));
   }
   a.w_out = ws + L.w;
   a.u_out = ws + L.u;
@@ -277,7 +287,7 @@ gdn_status gdn_segment_summary_fused(const gdn_problem* p, const void* k, const 
   a.k = k; a.v = v; a.g = g; a.beta = beta; a.cu = cu_seqlens;
   a.M_out = M; a.U_out = U; a.status = dev_status; a.skip_last_summary = skip_last != 0;
   GDN_TRY(gdn::launch_validate_cu(a, stream));
-  return to_status(gdn::tc_summary(a, true, stream));
+  return to_status(fused_summary(p, a, stream));
 }
 
 gdn_status gdn_chunk_emit_fused(const gdn_problem* p, const void* q, const void* k,
@@ -297,7 +307,7 @@ gdn_status gdn_chunk_emit_fused(const gdn_problem* p, const void* q, const void*
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h_in = h_in; a.cu = cu_seqlens;
   a.out = out; a.h_final = h_final; a.status = dev_status;
   GDN_TRY(gdn::launch_validate_cu(a, stream));
-  return to_status(gdn::tc_emit(a, true, stream));
+  return to_status(fused_emit(p, a, stream));
 }
 
 gdn_status gdn_device_status(const void* status_word, int reset, cudaStream_t stream) {

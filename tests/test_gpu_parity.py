@@ -52,7 +52,7 @@ def test_tiny_fp32_matches_oracle(gdn):
 
 # ------------------------------------------------------------------ small bf16, both paths
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 @pytest.mark.parametrize("T,P,lengths", [
     (64, 1, None), (64 * 5 + 17, 1, None), (64 * 5 + 17, 2, None), (64 * 7, 3, None),
     (64 * 3, 5, None), (None, 2, (100, 1, 0, 64, 257))])
@@ -123,7 +123,7 @@ def test_stage_entry_points_match_oracle_stages(gdn):
 def test_prefill_bf16_4096(gdn):
     inp = inputs.make(inputs.prefill_bf16())
     ref_o, ref_h = run_oracle(inp)
-    for path in (2, 1):
+    for path in (2, 3, 1):
         o, h = run_gpu(gdn, inp, P=1, path=path)
         check_bf16(o, h, ref_o, ref_h)
 
@@ -177,7 +177,7 @@ def test_empty_stream_returns_h0(gdn):
     q = torch.zeros(0, 2, 128, dtype=torch.bfloat16, device="cuda")
     v = torch.zeros(0, 4, 128, dtype=torch.bfloat16, device="cuda")
     g = torch.zeros(0, 4, device="cuda")
-    for path in (1, 2):
+    for path in (1, 2, 3):
         out, hf = gdn.forward(q, q, v, g, g, h0, None, P=3, path=path, check_status=True)
         assert out.numel() == 0 and torch.equal(hf, h0)
 
