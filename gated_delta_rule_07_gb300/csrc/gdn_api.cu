@@ -75,12 +75,20 @@ Args base_args(const gdn_problem* p) {
 // cu_seqlens may be null only for a single sequence.
 bool cu_ok(const gdn_problem* p, const int32_t* cu) { return cu != nullptr || p->num_seqs == 1; }
 
-gdn_status to_status(cudaError_t e) { return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA; }
+// The last CUDA error an entry point met on this host thread (reported by
+// gdn_last_error_string).
+thread_local cudaError_t t_last_error = cudaSuccess;
+
+gdn_status to_status(cudaError_t e) {
+  if (e == cudaSuccess) return GDN_OK;
+  t_last_error = e;
+  return GDN_ERR_CUDA;
+}
 
 #define GDN_TRY(expr)                              \
   do {                                             \
     cudaError_t _e = (expr);                       \
-    if (_e != cudaSuccess) return GDN_ERR_CUDA;    \
+    if (_e != cudaSuccess) return to_status(_e);   \
   } while (0)
 
 struct Layout {
@@ -134,6 +142,10 @@ const char* gdn_status_string(gdn_status s) {
 }
 
 int gdn_version(void) { return 100; }
+
+const char* gdn_last_error_string(void) {
+  return t_last_error == cudaSuccess ? "no CUDA error" : cudaGetErrorString(t_last_error);
+}
 
 gdn_status gdn_check_problem(const gdn_problem* p) { return check_problem(p); }
 
@@ -314,11 +326,9 @@ gdn_status gdn_device_status(const void* status_word, int reset, cudaStream_t st
   if (!status_word) return GDN_ERR_INVALID_ARGUMENT;
   int32_t host = 0;
   int32_t* dev = const_cast<int32_t*>(static_cast<const int32_t*>(status_word));
-  if (cudaMemcpyAsync(&host, dev, sizeof(int32_t), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-    return GDN_ERR_CUDA;
-  if (reset && cudaMemsetAsync(dev, 0, sizeof(int32_t), stream) != cudaSuccess)
-    return GDN_ERR_CUDA;
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return GDN_ERR_CUDA;
+  GDN_TRY(cudaMemcpyAsync(&host, dev, sizeof(int32_t), cudaMemcpyDeviceToHost, stream));
+  if (reset) GDN_TRY(cudaMemsetAsync(dev, 0, sizeof(int32_t), stream));
+  GDN_TRY(cudaStreamSynchronize(stream));
   return static_cast<gdn_status>(host);
 }
 

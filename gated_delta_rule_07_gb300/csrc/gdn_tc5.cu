@@ -145,7 +145,7 @@ __device__ __forceinline__ bool to_half_chunk(uint8_t* p) {
 // ------------------------------------------------------------------ the kernel
 
 template <int MODE>
-__global__ void __maxnreg__(152) tc5_chunk_kernel(Args a) {
+__global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = saddr(smem_raw);
   Smem& S = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (raw & 1023u)) & 1023u));
@@ -197,15 +197,15 @@ __global__ void __maxnreg__(152) tc5_chunk_kernel(Args a) {
     }
     auto publish_h = [&]() {  // fp16 h^T into TMEM (the A operand of delta and O1)
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t p[16];
+      for (int piece = 0; piece < 4; ++piece) {
+        uint32_t p[8];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float x0 = h[32 * half + 2 * q], x1 = h[32 * half + 2 * q + 1];
+        for (int q = 0; q < 8; ++q) {
+          const float x0 = h[16 * piece + 2 * q], x1 = h[16 * piece + 2 * q + 1];
           range_ok = range_ok && fits_half(x0) && fits_half(x1);
           p[q] = pack_h2(x0, x1);
         }
-        tmem_st16(tm + lane_bits + TM_H + 64 * hf + 16 * half, p);
+        tmem_st8(tm + lane_bits + TM_H + 64 * hf + 8 * piece, p);
       }
     };
     if (nch > 0) {
@@ -223,19 +223,32 @@ __global__ void __maxnreg__(152) tc5_chunk_kernel(Args a) {
       if (!group_wait(S, B_D, ci & 1, 2, kChainThreads)) break;
       fence_after_sync();
       {
-        float d[32];
-        tmem_ld32(tm + lane_bits + TM_U + 32 * hf, d);
-        uint32_t pd[16], pp[16];
+        // read both 16-column pieces before writing: the packed results overwrite them
+        float d0[16], d1[16];
+        tmem_ld16(tm + lane_bits + TM_U + 32 * hf, d0);
+        tmem_ld16(tm + lane_bits + TM_U + 32 * hf + 16, d1);
+        {
+          uint32_t pd[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const int t = 32 * hf + 2 * q;
-          const float e0 = S.eGLG[gb][t], e1 = S.eGLG[gb][t + 1];
-          range_ok = range_ok && fits_half(d[2 * q]) && fits_half(d[2 * q + 1]);
-          pd[q] = pack_h2(d[2 * q], d[2 * q + 1]);
-          pp[q] = pack_h2(d[2 * q] * e0, d[2 * q + 1] * e1);
+          for (int q = 0; q < 8; ++q) {
+            range_ok = range_ok && fits_half(d0[2 * q]) && fits_half(d0[2 * q + 1]) &&
+                       fits_half(d1[2 * q]) && fits_half(d1[2 * q + 1]);
+            pd[q] = pack_h2(d0[2 * q], d0[2 * q + 1]);
+            pd[q + 8] = pack_h2(d1[2 * q], d1[2 * q + 1]);
+          }
+          tmem_st16(tm + lane_bits + TM_U + 32 * hf, pd);
         }
-        tmem_st16(tm + lane_bits + TM_U + 32 * hf, pd);
-        tmem_st16(tm + lane_bits + TM_U + 32 * hf + 16, pp);
+        {
+          uint32_t pp[16];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int t = 32 * hf + 2 * q;
+            pp[q] = pack_h2(d0[2 * q] * S.eGLG[gb][t], d0[2 * q + 1] * S.eGLG[gb][t + 1]);
+            pp[q + 8] =
+                pack_h2(d1[2 * q] * S.eGLG[gb][t + 16], d1[2 * q + 1] * S.eGLG[gb][t + 17]);
+          }
+          tmem_st16(tm + lane_bits + TM_U + 32 * hf + 16, pp);
+        }
       }
       fence_before_sync();
       named_bar(2, kChainThreads);
@@ -244,25 +257,28 @@ __global__ void __maxnreg__(152) tc5_chunk_kernel(Args a) {
       if (!group_wait(S, B_H, ci & 1, 2, kChainThreads)) break;
       fence_after_sync();
       if (MODE == kEmit) {
-        float o1[32], o2[32];
-        tmem_ld32(tm + lane_bits + TM_O1 + 32 * hf, o1);
-        tmem_ld32(tm + lane_bits + TM_O2 + 32 * hf, o2);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const int t = 32 * hf + q;
-          if (t < L)
-            out[((t0 + t) * a.hv + j) * VD + c] =
-                __float2bfloat16_rn(S.eG[gb][t] * o1[q] + o2[q]);
+        for (int piece = 0; piece < 2; ++piece) {
+          float o1[16], o2[16];
+          tmem_ld16(tm + lane_bits + TM_O1 + 32 * hf + 16 * piece, o1);
+          tmem_ld16(tm + lane_bits + TM_O2 + 32 * hf + 16 * piece, o2);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const int t = 32 * hf + 16 * piece + q;
+            if (t < L)
+              out[((t0 + t) * a.hv + j) * VD + c] =
+                  __float2bfloat16_rn(S.eG[gb][t] * o1[q] + o2[q]);
+          }
         }
       }
       {
         const float gam = S.gamma[gb];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float dh[32];
-          tmem_ld32(tm + lane_bits + TM_H + 64 * hf + 32 * half, dh);
+        for (int piece = 0; piece < 4; ++piece) {
+          float dh[16];
+          tmem_ld16(tm + lane_bits + TM_H + 64 * hf + 16 * piece, dh);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) h[32 * half + q] = gam * h[32 * half + q] + dh[q];
+          for (int q = 0; q < 16; ++q) h[16 * piece + q] = gam * h[16 * piece + q] + dh[q];
         }
       }
       if (ci + 1 < nch) {
@@ -363,32 +379,34 @@ __global__ void __maxnreg__(152) tc5_chunk_kernel(Args a) {
       if (!group_wait(S, B_SQ, ci & 1, 1, kPrepThreads)) break;
       fence_after_sync();
       {
-        float sv[64];
-        tmem_ld32(tm + lane_bits + TM_SQ, *reinterpret_cast<float(*)[32]>(&sv[0]));
-        tmem_ld32(tm + lane_bits + TM_SQ + 32, *reinterpret_cast<float(*)[32]>(&sv[32]));
         const bool is_s = pt < 64;
         const int t = pt & 63;
         const float bt = S.beta[gb][t];
         float d = 1.f;  // e^{G_t - G_s} as s walks down from t (products of alpha <= 1)
-        float row[64];
 #pragma unroll
-        for (int s = 63; s >= 0; --s) {
-          if (s < t) d *= S.alpha[gb][s + 1];
-          row[s] = is_s ? (s < t ? bt * d * sv[s] : 0.f) : (s <= t ? d * sv[s] : 0.f);
-        }
-        if (is_s) {
+        for (int hb = 1; hb >= 0; --hb) {  // columns [32 hb, 32 hb + 32), walked downwards
+          float sv[32];
+          tmem_ld32(tm + lane_bits + TM_SQ + 32 * hb, sv);
 #pragma unroll
-          for (int s = 0; s < 64; ++s) S.A[t * FP + s] = row[s];
-        } else if (MODE == kEmit) {
-          uint8_t* att = S.att[ci & 1];
+          for (int q = 31; q >= 0; --q) {
+            const int s = 32 * hb + q;
+            if (s < t) d *= S.alpha[gb][s + 1];
+            sv[q] = is_s ? (s < t ? bt * d * sv[q] : 0.f) : (s <= t ? d * sv[q] : 0.f);
+          }
+          if (is_s) {
 #pragma unroll
-          for (int ch = 0; ch < 8; ++ch) {
-            uint4 pk;
-            pk.x = pack_h2(row[8 * ch + 0], row[8 * ch + 1]);
-            pk.y = pack_h2(row[8 * ch + 2], row[8 * ch + 3]);
-            pk.z = pack_h2(row[8 * ch + 4], row[8 * ch + 5]);
-            pk.w = pack_h2(row[8 * ch + 6], row[8 * ch + 7]);
-            *reinterpret_cast<uint4*>(att + sw128_offset(64, t, 8 * ch)) = pk;
+            for (int q = 0; q < 32; ++q) S.A[t * FP + 32 * hb + q] = sv[q];
+          } else if (MODE == kEmit) {
+            uint8_t* att = S.att[ci & 1];
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+              uint4 pk;
+              pk.x = pack_h2(sv[8 * ch + 0], sv[8 * ch + 1]);
+              pk.y = pack_h2(sv[8 * ch + 2], sv[8 * ch + 3]);
+              pk.z = pack_h2(sv[8 * ch + 4], sv[8 * ch + 5]);
+              pk.w = pack_h2(sv[8 * ch + 6], sv[8 * ch + 7]);
+              *reinterpret_cast<uint4*>(att + sw128_offset(64, t, 32 * hb + 8 * ch)) = pk;
+            }
           }
         }
       }
@@ -465,20 +483,22 @@ __global__ void __maxnreg__(152) tc5_chunk_kernel(Args a) {
       if (!group_wait(S, B_WU, ci & 1, 1, kPrepThreads)) break;
       fence_after_sync();
       {
-        float wv[64];
-        tmem_ld32(tm + lane_bits + TM_W, *reinterpret_cast<float(*)[32]>(&wv[0]));
-        tmem_ld32(tm + lane_bits + TM_W + 32, *reinterpret_cast<float(*)[32]>(&wv[32]));
         const int i = pt;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          uint4 pk;
-          pk.x = pack_h2(-wv[8 * ch + 0], -wv[8 * ch + 1]);
-          pk.y = pack_h2(-wv[8 * ch + 2], -wv[8 * ch + 3]);
-          pk.z = pack_h2(-wv[8 * ch + 4], -wv[8 * ch + 5]);
-          pk.w = pack_h2(-wv[8 * ch + 6], -wv[8 * ch + 7]);
+        for (int hb = 0; hb < 2; ++hb) {
+          float wv[32];
+          tmem_ld32(tm + lane_bits + TM_W + 32 * hb, wv);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) range_ok = range_ok && fits_half(wv[8 * ch + q]);
-          *reinterpret_cast<uint4*>(S.nw + sw128_offset(128, i, 8 * ch)) = pk;
+          for (int ch = 0; ch < 4; ++ch) {
+            uint4 pk;
+            pk.x = pack_h2(-wv[8 * ch + 0], -wv[8 * ch + 1]);
+            pk.y = pack_h2(-wv[8 * ch + 2], -wv[8 * ch + 3]);
+            pk.z = pack_h2(-wv[8 * ch + 4], -wv[8 * ch + 5]);
+            pk.w = pack_h2(-wv[8 * ch + 6], -wv[8 * ch + 7]);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) range_ok = range_ok && fits_half(wv[8 * ch + q]);
+            *reinterpret_cast<uint4*>(S.nw + sw128_offset(128, i, 32 * hb + 8 * ch)) = pk;
+          }
         }
       }
       fence_async_smem();

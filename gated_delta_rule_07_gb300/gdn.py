@@ -34,7 +34,7 @@ PATH_AUTO, PATH_SIMT, PATH_TENSOR, PATH_MMA_SYNC = 0, 1, 2, 3
 EXPORTED = ("gdn_status_string", "gdn_check_problem", "gdn_workspace_size", "gdn_forward",
             "gdn_chunk_prepare", "gdn_segment_summary", "gdn_state_prefix_scan",
             "gdn_chunk_emit", "gdn_device_status", "gdn_version",
-            "gdn_segment_summary_fused", "gdn_chunk_emit_fused")
+            "gdn_segment_summary_fused", "gdn_chunk_emit_fused", "gdn_last_error_string")
 
 
 class Problem(ctypes.Structure):
@@ -48,13 +48,18 @@ class Problem(ctypes.Structure):
 class GdnError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {gdn_status_string(status)}")
+        msg = f"{where}: {gdn_status_string(status)}"
+        if status == 4:
+            msg += f" ({_lib.gdn_last_error_string().decode()})"
+        super().__init__(msg)
 
 
 _vp, _fp, _ip = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
 _pp = ctypes.POINTER(Problem)
 _lib.gdn_status_string.restype = ctypes.c_char_p
 _lib.gdn_status_string.argtypes = [ctypes.c_int]
+_lib.gdn_last_error_string.restype = ctypes.c_char_p
+_lib.gdn_last_error_string.argtypes = []
 _lib.gdn_check_problem.argtypes = [_pp]
 _lib.gdn_workspace_size.restype = ctypes.c_size_t
 _lib.gdn_workspace_size.argtypes = [_pp]
@@ -69,7 +74,7 @@ _lib.gdn_segment_summary_fused.argtypes = [_pp, _vp, _vp, _fp, _fp, _ip, _fp, _f
                                            _ip, _vp]
 _lib.gdn_chunk_emit_fused.argtypes = [_pp, _vp, _vp, _vp, _fp, _fp, _fp, _ip, _vp, _fp, _ip, _vp]
 for _n in EXPORTED:
-    if _n not in ("gdn_status_string", "gdn_workspace_size"):
+    if _n not in ("gdn_status_string", "gdn_workspace_size", "gdn_last_error_string"):
         getattr(_lib, _n).restype = ctypes.c_int
 
 

@@ -186,6 +186,10 @@ gdn_status gdn_chunk_emit_fused(const gdn_problem* p, const void* q, const void*
  * Returns the recorded status (GDN_OK when none), or GDN_ERR_CUDA if the read failed. */
 gdn_status gdn_device_status(const void* status_word, int reset, cudaStream_t stream);
 
+/* Text of the last CUDA error that made an entry point return GDN_ERR_CUDA on the calling
+ * host thread ("no CUDA error" when there was none).  Static storage. */
+const char* gdn_last_error_string(void);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int gdn_version(void);
 
