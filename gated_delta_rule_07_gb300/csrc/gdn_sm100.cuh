@@ -181,7 +181,7 @@ __device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, uint32_t limit) {
   for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_test(addr, parity)) return true;
-    if (i > 64) __nanosleep(64);
+    if (i > (1u << 14)) __nanosleep(128);
   }
   return false;
 }

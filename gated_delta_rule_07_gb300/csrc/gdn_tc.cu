@@ -27,9 +27,12 @@
 
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_warp_mma.cuh"
 
 namespace gdn {
 namespace {
+
+using namespace warp_mma;
 
 constexpr int C = kChunk;  // 64
 constexpr int KD = 128;
@@ -44,28 +47,6 @@ enum Mode { kEmit = 0, kSumM = 1, kSumU = 2 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-// D = A * B + D, m16n8k16, A row-major, B column-major, fp16 in, fp32 accumulate.
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
@@ -103,40 +84,6 @@ __device__ __forceinline__ bool bf16_chunk_to_f16(char* p) {
 //
 // A tile is `rows` x RL 16-bit values (fp16), row-major, with the 16-byte chunks of each row XOR-permuted by
 // (row & 7) so that the eight row addresses of an ldmatrix hit eight different bank groups.
-
-template <int RL>
-__device__ __forceinline__ uint32_t tile_off(int r, int c) {  // c: multiple of 8
-  return (uint32_t)(r * RL * 2) + ((((uint32_t)c >> 3) ^ ((uint32_t)r & 7u)) << 4);
-}
-
-// A fragment (16 x 16 at m0, k0) from a tile stored [m][k].
-template <int RL>
-__device__ __forceinline__ void load_a(uint32_t base, int m0, int k0, uint32_t (&a)[4]) {
-  const int l = threadIdx.x & 31;
-  ldsm_x4(base + tile_off<RL>(m0 + (l & 15), k0 + ((l >> 4) << 3)), a);
-}
-
-// A fragment (16 x 16 at m0, k0) from a tile stored [k][m] (the transpose).
-template <int RL>
-__device__ __forceinline__ void load_a_t(uint32_t base, int m0, int k0, uint32_t (&a)[4]) {
-  const int l = threadIdx.x & 31, mi = l >> 3, rr = l & 7;
-  ldsm_x4_t(base + tile_off<RL>(k0 + rr + ((mi >> 1) << 3), m0 + ((mi & 1) << 3)), a);
-}
-
-// B fragments of two n8 tiles (k0..k0+15, n0..n0+15) from a tile stored [k][n]:
-// b[0], b[1] for columns n0..n0+7 and b[2], b[3] for n0+8..n0+15.
-template <int RL>
-__device__ __forceinline__ void load_b_kn(uint32_t base, int k0, int n0, uint32_t (&b)[4]) {
-  const int l = threadIdx.x & 31, mi = l >> 3, rr = l & 7;
-  ldsm_x4_t(base + tile_off<RL>(k0 + rr + ((mi & 1) << 3), n0 + ((mi >> 1) << 3)), b);
-}
-
-// Same from a tile stored [n][k].
-template <int RL>
-__device__ __forceinline__ void load_b_nk(uint32_t base, int k0, int n0, uint32_t (&b)[4]) {
-  const int l = threadIdx.x & 31, mi = l >> 3, rr = l & 7;
-  ldsm_x4(base + tile_off<RL>(n0 + rr + ((mi >> 1) << 3), k0 + ((mi & 1) << 3)), b);
-}
 
 // Stores the accumulator of an m16n8 tile at (m0, n0) as fp16, row g scaled by s0 and row
 // g + 8 by s1.  Returns false when a stored value overflows the fp16 range.

@@ -13,14 +13,17 @@
 //   O1^T      = h^T Q^T                           (128 x 64, K = 128)
 //   O2^T      = delta^T attn_i^T                  (128 x 64, K = 64; delta^T from TMEM)
 //   Dh^T      = (diag(e^{G_last - G}) delta)^T K  (128 x 128, K = 64)
-// and o = e^{G_t} O1 + O2, h <- gamma h + Dh.  The state h^T lives in registers (fp32) of
-// the chain warps; its fp16 copy, delta and delta' are written back into TMEM as the A
-// operands of the next products.  T = (I + A)^-1 is a blocked fp32 forward substitution.
+// with Q pre-scaled to q_g = diag(e^G) Q after [S ; QK], so o = O1 + O2 accumulates in one
+// (double-buffered) TMEM region, and h <- gamma h + Dh.  The state h^T lives in registers
+// (fp32) of the chain warps; its fp16 copy, delta and delta' are written back into TMEM as the
+// A operands of the next products.  T = (I + A)^-1 is blocked by 16 x 16: the diagonal
+// inverses by fp32 forward substitution in registers, the off-diagonal blocks
+// T_ab = -T_aa sum_m A_am T_mb with warp-level mma.sync (fp16 operands, fp32 accumulation).
 //
 // Warp roles (416 threads):
 //   warps 0-7  chain:   TMEM lane = state row c; warps w and w + 4 split the columns
-//   warps 8-11 prepare: chunk loads (cp.async, bf16 -> fp16), decay tables, masked gram and
-//                       attn_i, the triangular solve, -w
+//   warps 8-11 prepare: chunk loads (cp.async, bf16 -> fp16), decay tables, masked gram,
+//                       attn_i and q_g, the triangular solve, -w
 //   warp 12    MMA:     one thread issues every tcgen05.mma and commit in program order
 // Hand-offs use mbarriers; every wait is bounded and a wait that gives up records
 // GDN_ERR_DEVICE_TIMEOUT, and all roles leave their loops (group decisions are made uniform
@@ -33,17 +36,18 @@
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
 #include "gdn_sm100.cuh"
+#include "gdn_warp_mma.cuh"
 
 namespace gdn {
 namespace {
 
 using namespace sm100;
+using namespace warp_mma;
 
 constexpr int C = kChunk;  // 64
 constexpr int KD = 128, VD = 128;
 constexpr int kChainThreads = 256, kPrepThreads = 128;
 constexpr int kThreads = kChainThreads + kPrepThreads + 32;
-constexpr int FP = C + 1;
 constexpr uint32_t kWaitLimit = 1u << 21;
 constexpr float kHalfMax = 65504.f;
 
@@ -53,8 +57,7 @@ enum Mode { kEmit = 0, kSumM = 1, kSumU = 2 };
 constexpr uint32_t TM_SQ = 0;    // [S ; QK]          64 fp32
 constexpr uint32_t TM_W = 64;    // w^T               64 fp32
 constexpr uint32_t TM_U = 128;   // u^T -> delta^T    64 fp32, then fp16 delta / delta'
-constexpr uint32_t TM_O1 = 192;  // O1^T              64 fp32
-constexpr uint32_t TM_O2 = 256;  // O2^T              64 fp32
+constexpr uint32_t TM_O = 192;   // o^T, two buffers  2 x 64 fp32 (chunk parity)
 constexpr uint32_t TM_H = 384;   // Dh^T              128 fp32, then fp16 h^T
 
 // mbarriers
@@ -67,10 +70,12 @@ struct Smem {
   uint8_t tw[64 * 128];          // T diag(beta e^G) [t][s], K-major B
   uint8_t tu[64 * 128];          // T diag(beta) [t][s], K-major B
   uint8_t nw[128 * 128];         // -w [i][t], MN-major B
-  float A[C * FP];               // masked gram (fp32)
-  float Ti[C * FP];              // (I + A)^-1 (fp32)
-  float X[C * FP];               // solve scratch
-  float G[3][C], alpha[3][C], eG[3][C], eGLG[3][C], beta[3][C], gamma[3];
+  uint8_t ah[64 * 128];          // masked gram A [t][s], fp16
+  uint8_t th[64 * 128];          // blocks of (I + A)^-1 [t][s], fp16 operands
+  uint8_t xs[4][16 * 48];        // per-warp 16 x 16 fp16 scratch, 48-byte rows
+  float adiag[C][16];            // the diagonal 16 x 16 blocks of A, fp32
+  float gst[2][2][C];            // g and beta of a staged chunk
+  float G[3][C], eG[3][C], eGLG[3][C], beta[3][C], gamma[3];
   uint64_t bars[kNumBars];
   uint32_t tmem_base;
   int abort_flag;
@@ -125,6 +130,13 @@ __device__ __forceinline__ bool fits_half(float x) { return fabsf(x) <= kHalfMax
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   const int n = valid ? 16 : 0;
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
+  const int n = valid ? 4 : 0;
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(n));
+}
+__device__ __forceinline__ void st_half(uint8_t* tile, int r, int c, float x) {
+  *reinterpret_cast<__half*>(tile + sw128_offset(64, r, c)) = __float2half_rn(x);
 }
 
 // In-place bf16 -> fp16 of one 16-byte chunk; false when a value leaves the fp16 range.
@@ -253,24 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
       fence_before_sync();
       named_bar(2, kChainThreads);
       if (tid == 0) mbar_arrive(saddr(&S.bars[B_DR]));
-      // ---- outputs and the state update
+      // ---- the state update first (it gates the next chunk), the outputs after it
       if (!group_wait(S, B_H, ci & 1, 2, kChainThreads)) break;
       fence_after_sync();
-      if (MODE == kEmit) {
-#pragma unroll
-        for (int piece = 0; piece < 2; ++piece) {
-          float o1[16], o2[16];
-          tmem_ld16(tm + lane_bits + TM_O1 + 32 * hf + 16 * piece, o1);
-          tmem_ld16(tm + lane_bits + TM_O2 + 32 * hf + 16 * piece, o2);
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const int t = 32 * hf + 16 * piece + q;
-            if (t < L)
-              out[((t0 + t) * a.hv + j) * VD + c] =
-                  __float2bfloat16_rn(S.eG[gb][t] * o1[q] + o2[q]);
-          }
-        }
-      }
       {
         const float gam = S.gamma[gb];
 #pragma unroll
@@ -281,11 +278,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
           for (int q = 0; q < 16; ++q) h[16 * piece + q] = gam * h[16 * piece + q] + dh[q];
         }
       }
-      if (ci + 1 < nch) {
-        publish_h();
-        fence_before_sync();
-        named_bar(2, kChainThreads);
-        if (tid == 0) mbar_arrive(saddr(&S.bars[B_HR]));
+      if (ci + 1 < nch) publish_h();
+      fence_before_sync();
+      named_bar(2, kChainThreads);
+      if (tid == 0 && ci + 1 < nch) mbar_arrive(saddr(&S.bars[B_HR]));
+      if (MODE == kEmit) {
+        // o^T buffer ci & 1 is rewritten only after the next chunk's state hand-off
+#pragma unroll
+        for (int piece = 0; piece < 2; ++piece) {
+          float o[16];
+          tmem_ld16(tm + lane_bits + TM_O + 64 * (ci & 1) + 32 * hf + 16 * piece, o);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const int t = 32 * hf + 16 * piece + q;
+            if (t < L) out[((t0 + t) * a.hv + j) * VD + c] = __float2bfloat16_rn(o[q]);
+          }
+        }
       }
     }
     if (!range_ok) S.range_bad = 1;
@@ -305,11 +313,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
   } else if (warp < 12) {
     // =============================================================== prepare (128 threads)
     const int pt = tid - kChainThreads;       // 0..127 = TMEM lane of this thread
+    const int wb = warp - 8;                  // 0..3: this warp's 16-row block of T
     const uint32_t lane_bits = (uint32_t)((warp & 3) * 32) << 16;
+    const int g8 = lane >> 2, q4 = lane & 3;
     bool range_ok = true;
     const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(a.q);
     const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(a.k);
     const __nv_bfloat16* gv = static_cast<const __nv_bfloat16*>(a.v);
+    const uint32_t ah_s = saddr(S.ah), th_s = saddr(S.th), xs_s = saddr(S.xs[wb]);
+
+    // the strictly upper blocks of T diag(.) are zero for every chunk
+    for (int e = pt; e < 64 * 128 / 16; e += kPrepThreads) {
+      reinterpret_cast<uint4*>(S.tw)[e] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(S.tu)[e] = make_uint4(0u, 0u, 0u, 0u);
+    }
 
     auto issue_loads = [&](int ci) {
       const int s = ci & 1;
@@ -326,9 +343,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
         if (MODE != kSumM)
           cp_async16(vv + sw128_offset(64, t, col), gv + (tt * a.hv + j) * VD + col, ok);
       }
+      {  // g (threads 0-63) and beta (threads 64-127) of the chunk's rows
+        const int t = pt & 63;
+        const bool ok = t < L;
+        const int64_t tt = ok ? t0 + t : sb;
+        cp_async4(saddr(&S.gst[s][pt >> 6][t]), (pt < 64 ? a.g : a.beta) + tt * a.hv + j, ok);
+      }
       asm volatile("cp.async.commit_group;\n" ::: "memory");
     };
-    auto finish_data = [&](int ci) {  // convert chunk ci to fp16, decay tables, arrive X
+    auto finish_data = [&](int ci) {  // chunk ci to fp16, decay tables, then arrive X
       const int s = ci & 1, gb = ci % 3;
       const int64_t t0 = sb + (c0 + ci) * C;
       const int L = (int)((se - t0) < C ? (se - t0) : C);
@@ -339,9 +362,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
         if (MODE == kEmit) range_ok &= to_half_chunk(S.kq[s] + sw128_offset(128, 64 + t, col));
         if (MODE != kSumM) range_ok &= to_half_chunk(S.v[s] + sw128_offset(64, t, col));
       }
+      named_bar(1, kPrepThreads);  // the staged g, beta are visible
       if (pt < 32) {  // within-chunk inclusive scan of g; rows >= L decay by nothing
-        float g0 = pt < L ? a.g[(t0 + pt) * a.hv + j] : 0.f;
-        float g1 = pt + 32 < L ? a.g[(t0 + pt + 32) * a.hv + j] : 0.f;
+        const float g0 = S.gst[s][0][pt], g1 = S.gst[s][0][pt + 32];
         float x0 = g0, x1 = g1;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -354,19 +377,62 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
                                     : __shfl_sync(0xffffffffu, x1, (L - 1) & 31);
         S.G[gb][pt] = x0;
         S.G[gb][pt + 32] = x1;
-        S.alpha[gb][pt] = __expf(g0);
-        S.alpha[gb][pt + 32] = __expf(g1);
         S.eG[gb][pt] = __expf(x0);
         S.eG[gb][pt + 32] = __expf(x1);
         S.eGLG[gb][pt] = __expf(GL - x0);
         S.eGLG[gb][pt + 32] = __expf(GL - x1);
-        S.beta[gb][pt] = pt < L ? a.beta[(t0 + pt) * a.hv + j] : 0.f;
-        S.beta[gb][pt + 32] = pt + 32 < L ? a.beta[(t0 + pt + 32) * a.hv + j] : 0.f;
+        S.beta[gb][pt] = S.gst[s][1][pt];
+        S.beta[gb][pt + 32] = S.gst[s][1][pt + 32];
         if (pt == 0) S.gamma[gb] = __expf(GL);
       }
       fence_async_smem();
       named_bar(1, kPrepThreads);
       if (pt == 0) mbar_arrive(saddr(&S.bars[B_X0 + s]));
+    };
+
+    // T_ab = -T_aa sum_{m=b}^{a-1} A_am T_mb for one 16 x 16 block, by one warp: the sum on
+    // mma.sync from the fp16 tiles, then the product with T_aa through the warp's scratch.
+    auto off_diag_block = [&](int ab, int bb, int gb) {
+      float x[2][4] = {};
+      for (int m = bb; m < ab; ++m) {
+        uint32_t af[4], bf[4];
+        load_a<64>(ah_s, 16 * ab, 16 * m, af);
+        load_b_kn<64>(th_s, 16 * m, 16 * bb, bf);
+        mma16816(x[0], af, bf[0], bf[1]);
+        mma16816(x[1], af, bf[2], bf[3]);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        *reinterpret_cast<uint32_t*>(S.xs[wb] + g8 * 48 + (8 * nt + 2 * q4) * 2) =
+            pack_h2(x[nt][0], x[nt][1]);
+        *reinterpret_cast<uint32_t*>(S.xs[wb] + (g8 + 8) * 48 + (8 * nt + 2 * q4) * 2) =
+            pack_h2(x[nt][2], x[nt][3]);
+      }
+      __syncwarp();
+      float y[2][4] = {};
+      {
+        uint32_t af[4], bf[4];
+        load_a<64>(th_s, 16 * ab, 16 * ab, af);
+        const int mi = lane >> 3, rr = lane & 7;
+        ldsm_x4_t(xs_s + (rr + ((mi & 1) << 3)) * 48 + ((mi >> 1) << 3) * 2, bf);
+        mma16816(y[0], af, bf[0], bf[1]);
+        mma16816(y[1], af, bf[2], bf[3]);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int row = 16 * ab + g8 + 8 * hr, col = 16 * bb + 8 * nt + 2 * q4;
+          const float v0 = -y[nt][2 * hr], v1 = -y[nt][2 * hr + 1];
+          const float u0 = S.beta[gb][col], u1 = S.beta[gb][col + 1];
+          const float w0 = u0 * S.eG[gb][col], w1 = u1 * S.eG[gb][col + 1];
+          const uint32_t off = sw128_offset(64, row, col);
+          *reinterpret_cast<uint32_t*>(S.th + off) = pack_h2(v0, v1);
+          *reinterpret_cast<uint32_t*>(S.tw + off) = pack_h2(v0 * w0, v1 * w1);
+          *reinterpret_cast<uint32_t*>(S.tu + off) = pack_h2(v0 * u0, v1 * u1);
+          range_ok = range_ok && fits_half(v0) && fits_half(v1);
+        }
     };
 
     if (nch > 0) {
@@ -375,29 +441,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
     }
     for (int ci = 0; ci < nch; ++ci) {
       const int gb = ci % 3;
-      // ---- masked gram A (fp32) and attn_i (fp16) from [S ; QK]
+      // ---- masked gram A and attn_i from [S ; QK]; q -> q_g = e^{G_t} q
       if (!group_wait(S, B_SQ, ci & 1, 1, kPrepThreads)) break;
       fence_after_sync();
       {
         const bool is_s = pt < 64;
         const int t = pt & 63;
-        const float bt = S.beta[gb][t];
-        float d = 1.f;  // e^{G_t - G_s} as s walks down from t (products of alpha <= 1)
+        const float Gt = S.G[gb][t], bt = S.beta[gb][t];
 #pragma unroll
-        for (int hb = 1; hb >= 0; --hb) {  // columns [32 hb, 32 hb + 32), walked downwards
+        for (int hb = 0; hb < 2; ++hb) {
           float sv[32];
           tmem_ld32(tm + lane_bits + TM_SQ + 32 * hb, sv);
 #pragma unroll
-          for (int q = 31; q >= 0; --q) {
-            const int s = 32 * hb + q;
-            if (s < t) d *= S.alpha[gb][s + 1];
-            sv[q] = is_s ? (s < t ? bt * d * sv[q] : 0.f) : (s <= t ? d * sv[q] : 0.f);
+          for (int q = 0; q < 32; ++q) {
+            const int s2 = 32 * hb + q;
+            const float dec = __expf(fminf(Gt - S.G[gb][s2], 0.f));  // exponent <= 0
+            sv[q] = is_s ? (s2 < t ? bt * dec * sv[q] : 0.f) : (s2 <= t ? dec * sv[q] : 0.f);
           }
           if (is_s) {
 #pragma unroll
-            for (int q = 0; q < 32; ++q) S.A[t * FP + 32 * hb + q] = sv[q];
-          } else if (MODE == kEmit) {
-            uint8_t* att = S.att[ci & 1];
+            for (int q = 0; q < 32; ++q)
+              if (((32 * hb + q) >> 4) == (t >> 4)) S.adiag[t][q & 15] = sv[q];
+          }
+          if (is_s || MODE == kEmit) {
+            uint8_t* dst = is_s ? S.ah : S.att[ci & 1];
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
               uint4 pk;
@@ -405,9 +472,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
               pk.y = pack_h2(sv[8 * ch + 2], sv[8 * ch + 3]);
               pk.z = pack_h2(sv[8 * ch + 4], sv[8 * ch + 5]);
               pk.w = pack_h2(sv[8 * ch + 6], sv[8 * ch + 7]);
-              *reinterpret_cast<uint4*>(att + sw128_offset(64, t, 32 * hb + 8 * ch)) = pk;
+              *reinterpret_cast<uint4*>(dst + sw128_offset(64, t, 32 * hb + 8 * ch)) = pk;
             }
           }
+        }
+        if (MODE == kEmit && !is_s) {  // row t of Q, both column blocks, scaled by e^{G_t}
+          const float sc = S.eG[gb][t];
+#pragma unroll
+          for (int ch = 0; ch < 16; ++ch) {
+            uint4* p = reinterpret_cast<uint4*>(S.kq[ci & 1] +
+                                                sw128_offset(128, 64 + t, 8 * ch));
+            uint4 x = *p;
+            uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = __half22float2(*reinterpret_cast<__half2*>(&w[i]));
+              w[i] = pack_h2(f.x * sc, f.y * sc);
+            }
+            *p = x;
+          }
+          fence_async_smem();
         }
       }
       fence_before_sync();
@@ -417,65 +501,62 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
         if (ci >= 1 && !group_wait(S, B_H, (ci - 1) & 1, 1, kPrepThreads)) break;
         issue_loads(ci + 1);
       }
-      // ---- T = (I + A)^-1: diagonal 16 x 16 blocks, one warp each, two lanes per column
+      // ---- T = (I + A)^-1.  Diagonal block wb by forward substitution in registers:
+      // lane (c, rh) holds rows 8 rh .. 8 rh + 7 of column c of the block inverse.
       {
-        const int b = (warp - 8) * 16, cc = lane & 15, half = lane >> 4;
-        for (int t = 0; t < 16; ++t) S.Ti[(b + t) * FP + b + cc] = (t == cc) ? 1.f : 0.f;
-        __syncwarp();
-        for (int t = 1; t < 16; ++t) {
-          float x = 0.f;
-          for (int s = half; s < t; s += 2) x += S.A[(b + t) * FP + b + s] * S.Ti[(b + s) * FP + b + cc];
-          x += __shfl_xor_sync(0xffffffffu, x, 16);
-          if (half == 0 && t > cc) S.Ti[(b + t) * FP + b + cc] = -x;
-          __syncwarp();
+        const int c = lane & 15, rh = lane >> 4;
+        const float* Ab = &S.adiag[16 * wb][0];
+        float tc[8];
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2) tc[k2] = (8 * rh + k2 == c) ? 1.f : 0.f;
+        if (rh == 0) {
+#pragma unroll
+          for (int rr = 1; rr < 8; ++rr) {
+            float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 < rr; ++s2) {
+              if (s2 & 1) x1 += Ab[rr * 16 + s2] * tc[s2];
+              else x0 += Ab[rr * 16 + s2] * tc[s2];
+            }
+            if (rr > c) tc[rr] = -(x0 + x1);
+          }
+        }
+        float y[8];
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2) y[k2] = __shfl_sync(0xffffffffu, tc[k2], c);
+        if (rh == 1) {
+#pragma unroll
+          for (int rr = 8; rr < 16; ++rr) {
+            float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+            for (int s2 = 0; s2 < 8; ++s2) {
+              if (s2 & 1) x1 += Ab[rr * 16 + s2] * y[s2];
+              else x0 += Ab[rr * 16 + s2] * y[s2];
+            }
+#pragma unroll
+            for (int s2 = 8; s2 < rr; ++s2) {
+              if (s2 & 1) x1 += Ab[rr * 16 + s2] * tc[s2 - 8];
+              else x0 += Ab[rr * 16 + s2] * tc[s2 - 8];
+            }
+            if (rr > c) tc[rr - 8] = -(x0 + x1);
+          }
+        }
+        const int col = 16 * wb + c;
+        const float u = S.beta[gb][col], w = u * S.eG[gb][col];
+#pragma unroll
+        for (int k2 = 0; k2 < 8; ++k2) {
+          const int row = 16 * wb + 8 * rh + k2;
+          st_half(S.th, row, col, tc[k2]);
+          st_half(S.tw, row, col, tc[k2] * w);
+          st_half(S.tu, row, col, tc[k2] * u);
         }
       }
       named_bar(1, kPrepThreads);
-      // off-diagonal blocks by sub-diagonal: T_ab = -T_aa sum_{m=b}^{a-1} A_am T_mb
-      for (int dist = 1; dist < 4; ++dist) {
-        const int nblk = 4 - dist;
-        for (int e = pt; e < nblk * 256; e += kPrepThreads) {
-          const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-          const int bb = blk, aa = blk + dist;
-          float x = 0.f;
-          for (int m = bb; m < aa; ++m)
-#pragma unroll
-            for (int s = 0; s < 16; ++s)
-              x += S.A[(aa * 16 + rr) * FP + m * 16 + s] * S.Ti[(m * 16 + s) * FP + bb * 16 + cc];
-          S.X[(aa * 16 + rr) * FP + bb * 16 + cc] = x;
-        }
-        named_bar(1, kPrepThreads);
-        for (int e = pt; e < nblk * 256; e += kPrepThreads) {
-          const int blk = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-          const int bb = blk, aa = blk + dist;
-          float x = 0.f;
-          for (int s = 0; s <= rr; ++s)
-            x += S.Ti[(aa * 16 + rr) * FP + aa * 16 + s] * S.X[(aa * 16 + s) * FP + bb * 16 + cc];
-          S.Ti[(aa * 16 + rr) * FP + bb * 16 + cc] = -x;
-        }
-        named_bar(1, kPrepThreads);
-      }
-      // T diag(beta e^G) and T diag(beta) as fp16 K-major tiles [t][s]
-      for (int e = pt; e < C * 8; e += kPrepThreads) {
-        const int t = e >> 3, ch = e & 7;
-        uint32_t pw[4], pu[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int s = 8 * ch + 2 * q;
-          const float v0 = s <= t ? S.Ti[t * FP + s] : 0.f;
-          const float v1 = s + 1 <= t ? S.Ti[t * FP + s + 1] : 0.f;
-          const float b0 = S.beta[gb][s], b1 = S.beta[gb][s + 1];
-          const float w0 = v0 * b0 * S.eG[gb][s], w1 = v1 * b1 * S.eG[gb][s + 1];
-          range_ok = range_ok && fits_half(w0) && fits_half(w1) && fits_half(v0 * b0) &&
-                     fits_half(v1 * b1);
-          pw[q] = pack_h2(w0, w1);
-          pu[q] = pack_h2(v0 * b0, v1 * b1);
-        }
-        *reinterpret_cast<uint4*>(S.tw + sw128_offset(64, t, 8 * ch)) =
-            make_uint4(pw[0], pw[1], pw[2], pw[3]);
-        *reinterpret_cast<uint4*>(S.tu + sw128_offset(64, t, 8 * ch)) =
-            make_uint4(pu[0], pu[1], pu[2], pu[3]);
-      }
+      if (wb < 3) off_diag_block(wb + 1, wb, gb);
+      named_bar(1, kPrepThreads);
+      if (wb < 2) off_diag_block(wb + 2, wb, gb);
+      named_bar(1, kPrepThreads);
+      if (wb == 0) off_diag_block(3, 0, gb);
       fence_async_smem();
       named_bar(1, kPrepThreads);
       if (pt == 0) mbar_arrive(saddr(&S.bars[B_T]));
@@ -548,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
       if (ok) wu(0);
       for (int ci = 0; ok && ci < nch; ++ci) {
         const uint32_t kq = saddr(S.kq[ci & 1]);
-        // delta^T (+)= h^T (-w)^T ;  O1^T = h^T Q^T
+        // delta^T (+)= h^T (-w)^T ;  o^T = h^T q_g^T
         ok = single_wait(S, B_WR, ci & 1) && single_wait(S, B_HR, ci & 1);
         if (!ok) break;
         fence_after_sync();
@@ -559,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
           mma_ts(tm + TM_U, ah, sdesc(nw + ks * 2048, 16384, 1024), ID_D,
                  (MODE != kSumM) || ks > 0);
           if (MODE == kEmit)
-            mma_ts(tm + TM_O1, ah,
+            mma_ts(tm + TM_O + 64 * (ci & 1), ah,
                    sdesc(kq + (ks >> 2) * 16384 + 64 * 128 + (ks & 3) * 32, 16, 1024), ID_O,
                    ks > 0);
         }
@@ -569,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
           if (!ok) break;
           sq(ci + 1);
         }
-        // O2^T = delta^T attn_i^T ;  Dh^T = delta'^T K
+        // o^T += delta^T attn_i^T ;  Dh^T = delta'^T K
         ok = single_wait(S, B_DR, ci & 1);
         if (!ok) break;
         fence_after_sync();
@@ -578,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
         for (int ks = 0; ks < 4; ++ks) {
           const uint32_t col = TM_U + 32 * (ks >> 1) + 8 * (ks & 1);
           if (MODE == kEmit)
-            mma_ts(tm + TM_O2, tm + col, sdesc(att + ks * 32, 16, 1024), ID_O, ks > 0);
+            mma_ts(tm + TM_O + 64 * (ci & 1), tm + col, sdesc(att + ks * 32, 16, 1024), ID_O, 1);
           mma_ts(tm + TM_H, tm + col + 16, sdesc(kq + ks * 2048, 16384, 1024), ID_DH, ks > 0);
         }
         mma_commit(saddr(&S.bars[B_H]));
