@@ -22,12 +22,13 @@
 //
 // Warp roles (416 threads):
 //   warps 0-7  chain:   TMEM lane = state row c; warps w and w + 4 split the columns
-//   warps 8-11 prepare: chunk loads (cp.async, bf16 -> fp16), decay tables, masked gram,
+//   warps 8-11 prepare: chunk loads (TMA, then bf16 -> fp16), decay tables, masked gram,
 //                       attn_i and q_g, the triangular solve, -w
 //   warp 12    MMA:     one thread issues every tcgen05.mma and commit in program order
 // Hand-offs use mbarriers; every wait is bounded and a wait that gives up records
 // GDN_ERR_DEVICE_TIMEOUT, and all roles leave their loops (group decisions are made uniform
 // with barrier reductions) so the CTA always reaches its TMEM release.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -61,7 +62,7 @@ constexpr uint32_t TM_O = 192;   // o^T, two buffers  2 x 64 fp32 (chunk parity)
 constexpr uint32_t TM_H = 384;   // Dh^T              128 fp32, then fp16 h^T
 
 // mbarriers
-enum Bar { B_X0 = 0, B_X1, B_SQ, B_T, B_WU, B_WR, B_HR, B_D, B_DR, B_H, kNumBars };
+enum Bar { B_X0 = 0, B_X1, B_SQ, B_T, B_WU, B_WR, B_HR, B_D, B_DR, B_H, B_L0, B_L1, kNumBars };
 
 struct Smem {
   uint8_t kq[2][2 * 128 * 128];  // per stage: [kblk][128 rows: K 0-63, Q 64-127][128 B]
@@ -76,6 +77,8 @@ struct Smem {
   float adiag[C][16];            // the diagonal 16 x 16 blocks of A, fp32
   float gst[2][2][C];            // g and beta of a staged chunk
   float G[3][C], eG[3][C], eGLG[3][C], beta[3][C], gamma[3];
+  float rowf[3][C];              // e^{G_t - G_{16 floor(t/16)}}: decay to the row's block start
+  float colf[3][4][C];           // colf[a][s] = e^{G_{16a} - G_s} for s < 16a
   uint64_t bars[kNumBars];
   uint32_t tmem_base;
   int abort_flag;
@@ -135,6 +138,24 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool va
   const int n = valid ? 4 : 0;
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(n));
 }
+// One 64 x 64 box of a [T, heads, 128] bf16 tensor (128-byte swizzle) into shared memory;
+// completion is counted in bytes on the mbarrier.
+__device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, int x, int head,
+                                        int t0, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(head), "r"(t0), "r"(mbar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
+  asm volatile(
+      "{\n.reg .b64 st;\nmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(
+          mbar),
+      "r"(bytes)
+      : "memory");
+}
+
 __device__ __forceinline__ void st_half(uint8_t* tile, int r, int c, float x) {
   *reinterpret_cast<__half*>(tile + sw128_offset(64, r, c)) = __float2half_rn(x);
 }
@@ -157,7 +178,9 @@ __device__ __forceinline__ bool to_half_chunk(uint8_t* p) {
 // ------------------------------------------------------------------ the kernel
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    tc5_chunk_kernel(Args a, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = saddr(smem_raw);
   Smem& S = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (raw & 1023u)) & 1023u));
@@ -332,18 +355,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
       const int s = ci & 1;
       const int64_t t0 = sb + (c0 + ci) * C;
       const int L = (int)((se - t0) < C ? (se - t0) : C);
-      const uint32_t kq = saddr(S.kq[s]), vv = saddr(S.v[s]);
-      for (int e = pt; e < C * 16; e += kPrepThreads) {
-        const int t = e >> 4, col = (e & 15) << 3;
-        const bool ok = t < L;
-        const int64_t tt = ok ? t0 + t : sb;
-        cp_async16(kq + sw128_offset(128, t, col), gk + (tt * a.hk + kh) * KD + col, ok);
-        if (MODE == kEmit)
-          cp_async16(kq + sw128_offset(128, 64 + t, col), gq + (tt * a.hk + kh) * KD + col, ok);
-        if (MODE != kSumM)
-          cp_async16(vv + sw128_offset(64, t, col), gv + (tt * a.hv + j) * VD + col, ok);
+      if (pt == 0) {  // rows past T read zeros; rows in [L, 64) belong to no computation here
+        const uint32_t bar = saddr(&S.bars[B_L0 + s]);
+        const uint32_t kq = saddr(S.kq[s]), vv = saddr(S.v[s]);
+        const uint32_t bytes = (MODE == kEmit ? 4u : 2u) * 8192u + (MODE != kSumM ? 2u : 0u) * 8192u;
+        mbar_expect_tx(bar, bytes);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          tma_box(kq + kb * 16384, &tm_k, 64 * kb, kh, (int)t0, bar);
+          if (MODE == kEmit) tma_box(kq + kb * 16384 + 8192, &tm_q, 64 * kb, kh, (int)t0, bar);
+          if (MODE != kSumM) tma_box(vv + kb * 8192, &tm_v, 64 * kb, j, (int)t0, bar);
+        }
       }
-      {  // g (threads 0-63) and beta (threads 64-127) of the chunk's rows
+      {  // g (threads 0-63) and beta (threads 64-127) of the chunk's rows; zero past L
         const int t = pt & 63;
         const bool ok = t < L;
         const int64_t tt = ok ? t0 + t : sb;
@@ -351,16 +375,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
       }
       asm volatile("cp.async.commit_group;\n" ::: "memory");
     };
-    auto finish_data = [&](int ci) {  // chunk ci to fp16, decay tables, then arrive X
+    // chunk ci to fp16, decay tables, then arrive X; false when the load wait gave up
+    auto finish_data = [&](int ci) -> bool {
       const int s = ci & 1, gb = ci % 3;
       const int64_t t0 = sb + (c0 + ci) * C;
       const int L = (int)((se - t0) < C ? (se - t0) : C);
       asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-      for (int e = pt; e < C * 16; e += kPrepThreads) {
-        const int t = e >> 4, col = (e & 15) << 3;
-        range_ok &= to_half_chunk(S.kq[s] + sw128_offset(128, t, col));
-        if (MODE == kEmit) range_ok &= to_half_chunk(S.kq[s] + sw128_offset(128, 64 + t, col));
-        if (MODE != kSumM) range_ok &= to_half_chunk(S.v[s] + sw128_offset(64, t, col));
+      if (!group_wait(S, B_L0 + s, (ci >> 1) & 1, 1, kPrepThreads)) return false;
+      // bf16 -> fp16 of K, Q and V; four independent chunks in flight per thread
+      {
+        constexpr int kPer = (MODE == kEmit ? 2 : 1) + (MODE != kSumM ? 1 : 0);
+        const int nchunks = C * 16 * kPer;  // 16-byte chunks
+#pragma unroll 4
+        for (int e = pt; e < nchunks; e += kPrepThreads) {
+          const int which = e / (C * 16), rem = e % (C * 16);
+          const int t = rem >> 4, col = (rem & 15) << 3;
+          uint8_t* p;
+          if (which == 0) p = S.kq[s] + sw128_offset(128, t, col);
+          else if (which == 1 && MODE == kEmit) p = S.kq[s] + sw128_offset(128, 64 + t, col);
+          else p = S.v[s] + sw128_offset(64, t, col);
+          range_ok &= to_half_chunk(p);
+        }
       }
       named_bar(1, kPrepThreads);  // the staged g, beta are visible
       if (pt < 32) {  // within-chunk inclusive scan of g; rows >= L decay by nothing
@@ -375,12 +410,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
         x1 += __shfl_sync(0xffffffffu, x0, 31);
         const float GL = L - 1 < 32 ? __shfl_sync(0xffffffffu, x0, (L - 1) & 31)
                                     : __shfl_sync(0xffffffffu, x1, (L - 1) & 31);
+        // block starts G_0, G_16, G_32, G_48
+        const float B1 = __shfl_sync(0xffffffffu, x0, 16);
+        const float B0 = __shfl_sync(0xffffffffu, x0, 0);
+        const float B2 = __shfl_sync(0xffffffffu, x1, 0);
+        const float B3 = __shfl_sync(0xffffffffu, x1, 16);
         S.G[gb][pt] = x0;
         S.G[gb][pt + 32] = x1;
         S.eG[gb][pt] = __expf(x0);
         S.eG[gb][pt + 32] = __expf(x1);
         S.eGLG[gb][pt] = __expf(GL - x0);
         S.eGLG[gb][pt + 32] = __expf(GL - x1);
+        S.rowf[gb][pt] = __expf(x0 - (pt < 16 ? B0 : B1));
+        S.rowf[gb][pt + 32] = __expf(x1 - (pt < 16 ? B2 : B3));
+        // colf[a][s] = e^{G_{16a} - G_s} for s < 16a (exponent <= 0)
+        S.colf[gb][1][pt] = pt < 16 ? __expf(B1 - x0) : 0.f;
+        S.colf[gb][2][pt] = __expf(B2 - x0);
+        S.colf[gb][3][pt] = __expf(B3 - x0);
+        S.colf[gb][3][pt + 32] = pt < 16 ? __expf(B3 - x1) : 0.f;
         S.beta[gb][pt] = S.gst[s][1][pt];
         S.beta[gb][pt + 32] = S.gst[s][1][pt + 32];
         if (pt == 0) S.gamma[gb] = __expf(GL);
@@ -388,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
       fence_async_smem();
       named_bar(1, kPrepThreads);
       if (pt == 0) mbar_arrive(saddr(&S.bars[B_X0 + s]));
+      return true;
     };
 
     // T_ab = -T_aa sum_{m=b}^{a-1} A_am T_mb for one 16 x 16 block, by one warp: the sum on
@@ -435,33 +483,51 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
         }
     };
 
-    if (nch > 0) {
+    bool go = nch > 0;
+    if (go) {
       issue_loads(0);
-      finish_data(0);
+      go = finish_data(0);
     }
-    for (int ci = 0; ci < nch; ++ci) {
+    for (int ci = 0; go && ci < nch; ++ci) {
       const int gb = ci % 3;
       // ---- masked gram A and attn_i from [S ; QK]; q -> q_g = e^{G_t} q
       if (!group_wait(S, B_SQ, ci & 1, 1, kPrepThreads)) break;
       fence_after_sync();
       {
         const bool is_s = pt < 64;
-        const int t = pt & 63;
-        const float Gt = S.G[gb][t], bt = S.beta[gb][t];
+        const int t = pt & 63, ab = t >> 4;
+        const float Gt = S.G[gb][t];
+        // row factor: beta_t (for A) times the decay from the row's block start
+        const float rf = S.rowf[gb][t] * (is_s ? S.beta[gb][t] : 1.f);
+        const float dscale = is_s ? S.beta[gb][t] : 1.f;
+        const float* cf = &S.colf[gb][ab][0];
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
           float sv[32];
           tmem_ld32(tm + lane_bits + TM_SQ + 32 * hb, sv);
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int s2 = 32 * hb + q;
-            const float dec = __expf(fminf(Gt - S.G[gb][s2], 0.f));  // exponent <= 0
-            sv[q] = is_s ? (s2 < t ? bt * dec * sv[q] : 0.f) : (s2 <= t ? dec * sv[q] : 0.f);
+          for (int cbl = 0; cbl < 2; ++cbl) {
+            const int cb = 2 * hb + cbl;  // column block of these 16 values
+            if (cb < ab) {         // below the diagonal block: e^{G_t - G_s} factorised
+#pragma unroll
+              for (int q = 0; q < 16; ++q) sv[16 * cbl + q] *= rf * cf[16 * cb + q];
+            } else if (cb == ab) {  // the diagonal block: direct, exponent <= 0
+#pragma unroll
+              for (int q = 0; q < 16; ++q) {
+                const int s2 = 16 * cb + q;
+                const bool keep = is_s ? (s2 < t) : (s2 <= t);
+                const float dec = __expf(fminf(Gt - S.G[gb][s2], 0.f));
+                sv[16 * cbl + q] = keep ? dscale * dec * sv[16 * cbl + q] : 0.f;
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < 16; ++q) sv[16 * cbl + q] = 0.f;
+            }
           }
           if (is_s) {
 #pragma unroll
             for (int q = 0; q < 32; ++q)
-              if (((32 * hb + q) >> 4) == (t >> 4)) S.adiag[t][q & 15] = sv[q];
+              if (((32 * hb + q) >> 4) == ab) S.adiag[t][q & 15] = sv[q];
           }
           if (is_s || MODE == kEmit) {
             uint8_t* dst = is_s ? S.ah : S.att[ci & 1];
@@ -479,17 +545,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
         if (MODE == kEmit && !is_s) {  // row t of Q, both column blocks, scaled by e^{G_t}
           const float sc = S.eG[gb][t];
 #pragma unroll
-          for (int ch = 0; ch < 16; ++ch) {
-            uint4* p = reinterpret_cast<uint4*>(S.kq[ci & 1] +
-                                                sw128_offset(128, 64 + t, 8 * ch));
-            uint4 x = *p;
-            uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+          for (int c4 = 0; c4 < 16; c4 += 4) {
+            uint4* p[4];
+            uint4 x[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 f = __half22float2(*reinterpret_cast<__half2*>(&w[i]));
-              w[i] = pack_h2(f.x * sc, f.y * sc);
+            for (int u = 0; u < 4; ++u) {
+              p[u] = reinterpret_cast<uint4*>(S.kq[ci & 1] +
+                                              sw128_offset(128, 64 + t, 8 * (c4 + u)));
+              x[u] = *p[u];
             }
-            *p = x;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              uint32_t* w = reinterpret_cast<uint32_t*>(&x[u]);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(*reinterpret_cast<__half2*>(&w[i]));
+                w[i] = pack_h2(f.x * sc, f.y * sc);
+              }
+              *p[u] = x[u];
+            }
           }
           fence_async_smem();
         }
@@ -587,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
       named_bar(1, kPrepThreads);
       if (pt == 0) mbar_arrive(saddr(&S.bars[B_WR]));
       // ---- the next chunk's data
-      if (ci + 1 < nch) finish_data(ci + 1);
+      if (ci + 1 < nch && !finish_data(ci + 1)) break;
     }
     asm volatile("cp.async.wait_group 0;\n" ::: "memory");
     if (!range_ok) S.range_bad = 1;
@@ -685,6 +759,42 @@ __global__ void __launch_bounds__(kThreads, 1) tc5_chunk_kernel(Args a) {
   }
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link against libcuda).
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn() {
+  static EncodeTiled fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiled>(p);
+  }();
+  return fn;
+}
+
+// [T, heads, 128] bf16 tensor read as 64 (features) x 1 (head) x 64 (tokens) boxes with the
+// 128-byte swizzle; tokens past T read as zeros.
+cudaError_t make_map(CUtensorMap* m, const void* base, int64_t T, int heads) {
+  EncodeTiled fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {128, (cuuint64_t)heads, (cuuint64_t)(T > 0 ? T : 1)};
+  const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)heads * 128 * 2};
+  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  static const uint16_t dummy[64] __attribute__((aligned(16))) = {};
+  void* addr = const_cast<void*>(base ? base : static_cast<const void*>(dummy));
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, addr, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int MODE>
 cudaError_t launch5(const Args& a, cudaStream_t s) {
   const dim3 grid((unsigned)(a.N * a.P), a.hv, 1);
@@ -693,7 +803,14 @@ cudaError_t launch5(const Args& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(tc5_chunk_kernel<MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  tc5_chunk_kernel<MODE><<<grid, kThreads, smem, s>>>(a);
+  CUtensorMap mk, mq, mv;
+  const bool empty = a.T == 0;
+  if ((e = make_map(&mk, empty ? nullptr : a.k, a.T, a.hk)) != cudaSuccess) return e;
+  if ((e = make_map(&mq, empty || MODE != kEmit ? nullptr : a.q, a.T, a.hk)) != cudaSuccess)
+    return e;
+  if ((e = make_map(&mv, empty || MODE == kSumM ? nullptr : a.v, a.T, a.hv)) != cudaSuccess)
+    return e;
+  tc5_chunk_kernel<MODE><<<grid, kThreads, smem, s>>>(a, mk, mq, mv);
   return cudaGetLastError();
 }
 
