@@ -49,7 +49,7 @@ constexpr int C = kChunk;  // 64
 constexpr int KD = 128, VD = 128;
 constexpr int kChainThreads = 256, kPrepThreads = 128;
 constexpr int kThreads = kChainThreads + kPrepThreads + 32;
-constexpr uint32_t kWaitLimit = 1u << 21;
+constexpr uint32_t kWaitLimit = 1u << 16;  // x 20 us: ~1.3 s
 constexpr float kHalfMax = 65504.f;
 
 enum Mode { kEmit = 0, kSumM = 1, kSumU = 2 };
@@ -77,8 +77,7 @@ struct Smem {
   float adiag[C][16];            // the diagonal 16 x 16 blocks of A, fp32
   float gst[2][2][C];            // g and beta of a staged chunk
   float G[3][C], eG[3][C], eGLG[3][C], beta[3][C], gamma[3];
-  float rowf[3][C];              // e^{G_t - G_{16 floor(t/16)}}: decay to the row's block start
-  float colf[3][4][C];           // colf[a][s] = e^{G_{16a} - G_s} for s < 16a
+  float dec[C * C];              // e^{G_t - G_s} for s <= t, else 0; 16-byte chunks swizzled
   uint64_t bars[kNumBars];
   uint32_t tmem_base;
   int abort_flag;
@@ -156,6 +155,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
       : "memory");
 }
 
+// Position of element (t, s) of the 64 x 64 fp32 decay matrix: 16-byte chunks of a row are
+// XOR-permuted by (t & 15) so that a warp reading 32 rows at one column is conflict-free.
+__device__ __forceinline__ int dec_idx(int t, int s) {
+  return t * 64 + ((((s >> 2) ^ (t & 15))) << 2) + (s & 3);
+}
+
 __device__ __forceinline__ void st_half(uint8_t* tile, int r, int c, float x) {
   *reinterpret_cast<__half*>(tile + sw128_offset(64, r, c)) = __float2half_rn(x);
 }
@@ -205,6 +210,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 12) {
     tmem_alloc(saddr(&S.tmem_base), 512);
     tmem_relinquish();
+  }
+  if (tid == kChainThreads) {
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+    if (MODE == kEmit)
+      asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
+    if (MODE != kSumM)
+      asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
   }
   fence_before_sync();
   __syncthreads();
@@ -410,27 +422,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         x1 += __shfl_sync(0xffffffffu, x0, 31);
         const float GL = L - 1 < 32 ? __shfl_sync(0xffffffffu, x0, (L - 1) & 31)
                                     : __shfl_sync(0xffffffffu, x1, (L - 1) & 31);
-        // block starts G_0, G_16, G_32, G_48
-        const float B1 = __shfl_sync(0xffffffffu, x0, 16);
-        const float B0 = __shfl_sync(0xffffffffu, x0, 0);
-        const float B2 = __shfl_sync(0xffffffffu, x1, 0);
-        const float B3 = __shfl_sync(0xffffffffu, x1, 16);
         S.G[gb][pt] = x0;
         S.G[gb][pt + 32] = x1;
         S.eG[gb][pt] = __expf(x0);
         S.eG[gb][pt + 32] = __expf(x1);
         S.eGLG[gb][pt] = __expf(GL - x0);
         S.eGLG[gb][pt + 32] = __expf(GL - x1);
-        S.rowf[gb][pt] = __expf(x0 - (pt < 16 ? B0 : B1));
-        S.rowf[gb][pt + 32] = __expf(x1 - (pt < 16 ? B2 : B3));
-        // colf[a][s] = e^{G_{16a} - G_s} for s < 16a (exponent <= 0)
-        S.colf[gb][1][pt] = pt < 16 ? __expf(B1 - x0) : 0.f;
-        S.colf[gb][2][pt] = __expf(B2 - x0);
-        S.colf[gb][3][pt] = __expf(B3 - x0);
-        S.colf[gb][3][pt + 32] = pt < 16 ? __expf(B3 - x1) : 0.f;
         S.beta[gb][pt] = S.gst[s][1][pt];
         S.beta[gb][pt + 32] = S.gst[s][1][pt + 32];
         if (pt == 0) S.gamma[gb] = __expf(GL);
+      }
+      named_bar(1, kPrepThreads);
+      {  // the decay matrix of this chunk: row t, columns 32 (pt >> 6) .. + 31
+        const int t = pt & 63, s0 = 32 * (pt >> 6);
+        const float Gt = S.G[gb][t];
+#pragma unroll
+        for (int c4 = 0; c4 < 32; c4 += 4) {
+          float4 d;
+          const int s1 = s0 + c4;
+          d.x = s1 <= t ? __expf(Gt - S.G[gb][s1]) : 0.f;
+          d.y = s1 + 1 <= t ? __expf(Gt - S.G[gb][s1 + 1]) : 0.f;
+          d.z = s1 + 2 <= t ? __expf(Gt - S.G[gb][s1 + 2]) : 0.f;
+          d.w = s1 + 3 <= t ? __expf(Gt - S.G[gb][s1 + 3]) : 0.f;
+          *reinterpret_cast<float4*>(&S.dec[dec_idx(t, s1)]) = d;
+        }
       }
       fence_async_smem();
       named_bar(1, kPrepThreads);
@@ -496,33 +511,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         const bool is_s = pt < 64;
         const int t = pt & 63, ab = t >> 4;
-        const float Gt = S.G[gb][t];
-        // row factor: beta_t (for A) times the decay from the row's block start
-        const float rf = S.rowf[gb][t] * (is_s ? S.beta[gb][t] : 1.f);
-        const float dscale = is_s ? S.beta[gb][t] : 1.f;
-        const float* cf = &S.colf[gb][ab][0];
+        const float bt = is_s ? S.beta[gb][t] : 1.f;
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
           float sv[32];
           tmem_ld32(tm + lane_bits + TM_SQ + 32 * hb, sv);
 #pragma unroll
-          for (int cbl = 0; cbl < 2; ++cbl) {
-            const int cb = 2 * hb + cbl;  // column block of these 16 values
-            if (cb < ab) {         // below the diagonal block: e^{G_t - G_s} factorised
-#pragma unroll
-              for (int q = 0; q < 16; ++q) sv[16 * cbl + q] *= rf * cf[16 * cb + q];
-            } else if (cb == ab) {  // the diagonal block: direct, exponent <= 0
-#pragma unroll
-              for (int q = 0; q < 16; ++q) {
-                const int s2 = 16 * cb + q;
-                const bool keep = is_s ? (s2 < t) : (s2 <= t);
-                const float dec = __expf(fminf(Gt - S.G[gb][s2], 0.f));
-                sv[16 * cbl + q] = keep ? dscale * dec * sv[16 * cbl + q] : 0.f;
-              }
-            } else {
-#pragma unroll
-              for (int q = 0; q < 16; ++q) sv[16 * cbl + q] = 0.f;
-            }
+          for (int c4 = 0; c4 < 32; c4 += 4) {
+            const int s1 = 32 * hb + c4;
+            const float4 d = *reinterpret_cast<const float4*>(&S.dec[dec_idx(t, s1)]);
+            // A keeps s < t (times beta_t); attn_i keeps s <= t (the matrix is 0 above)
+            sv[c4 + 0] *= bt * (is_s && s1 + 0 == t ? 0.f : d.x);
+            sv[c4 + 1] *= bt * (is_s && s1 + 1 == t ? 0.f : d.y);
+            sv[c4 + 2] *= bt * (is_s && s1 + 2 == t ? 0.f : d.z);
+            sv[c4 + 3] *= bt * (is_s && s1 + 3 == t ? 0.f : d.w);
           }
           if (is_s) {
 #pragma unroll
