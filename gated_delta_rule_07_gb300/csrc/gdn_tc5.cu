@@ -32,6 +32,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "gdn_common.cuh"
@@ -77,12 +78,21 @@ struct Smem {
   float adiag[C][16];            // the diagonal 16 x 16 blocks of A, fp32
   float gst[2][2][C];            // g and beta of a staged chunk
   float G[3][C], eG[3][C], eGLG[3][C], beta[3][C], gamma[3];
-  float dec[C * C];              // e^{G_t - G_s} for s <= t, else 0; 16-byte chunks swizzled
+  alignas(16) float dec[C * C];  // e^{G_t - G_s} for s <= t, else 0; 16-byte chunks swizzled
   uint64_t bars[kNumBars];
   uint32_t tmem_base;
   int abort_flag;
   int range_bad;
 };
+
+// Members read or written with 16-byte vector accesses, ldmatrix or the tensor core must sit on
+// 16-byte (swizzled tiles: 1024-byte) boundaries of the 1024-aligned base.
+static_assert(offsetof(Smem, kq) % 1024 == 0 && offsetof(Smem, v) % 1024 == 0, "tile alignment");
+static_assert(offsetof(Smem, att) % 1024 == 0 && offsetof(Smem, tw) % 1024 == 0, "tile alignment");
+static_assert(offsetof(Smem, tu) % 1024 == 0 && offsetof(Smem, nw) % 1024 == 0, "tile alignment");
+static_assert(offsetof(Smem, ah) % 1024 == 0 && offsetof(Smem, th) % 1024 == 0, "tile alignment");
+static_assert(offsetof(Smem, xs) % 16 == 0 && offsetof(Smem, dec) % 16 == 0, "vector alignment");
+static_assert(offsetof(Smem, bars) % 8 == 0, "mbarrier alignment");
 
 // ------------------------------------------------------------------ small helpers
 
