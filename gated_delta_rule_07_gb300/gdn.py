@@ -34,7 +34,8 @@ PATH_AUTO, PATH_SIMT, PATH_TENSOR, PATH_MMA_SYNC = 0, 1, 2, 3
 EXPORTED = ("gdn_status_string", "gdn_check_problem", "gdn_workspace_size", "gdn_forward",
             "gdn_chunk_prepare", "gdn_segment_summary", "gdn_state_prefix_scan",
             "gdn_chunk_emit", "gdn_device_status", "gdn_version",
-            "gdn_segment_summary_fused", "gdn_chunk_emit_fused", "gdn_last_error_string")
+            "gdn_segment_summary_fused", "gdn_chunk_emit_fused", "gdn_last_error_string",
+            "gdn_forward_static_scratch")
 
 
 class Problem(ctypes.Structure):
@@ -73,6 +74,7 @@ _lib.gdn_device_status.argtypes = [_vp, ctypes.c_int, _vp]
 _lib.gdn_segment_summary_fused.argtypes = [_pp, _vp, _vp, _fp, _fp, _ip, _fp, _fp, ctypes.c_int,
                                            _ip, _vp]
 _lib.gdn_chunk_emit_fused.argtypes = [_pp, _vp, _vp, _vp, _fp, _fp, _fp, _ip, _vp, _fp, _ip, _vp]
+_lib.gdn_forward_static_scratch.argtypes = [_pp, _vp, _vp, _vp, _fp, _fp, _fp, _ip, _vp, _fp, _vp]
 for _n in EXPORTED:
     if _n not in ("gdn_status_string", "gdn_workspace_size", "gdn_last_error_string"):
         getattr(_lib, _n).restype = ctypes.c_int
@@ -134,6 +136,15 @@ def gdn_forward(p, q, k, v, g, beta, h0, cu_seqlens, out, h_final, workspace, ws
     _check(_lib.gdn_forward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                             _ptr(h0), _ptr(cu_seqlens), _ptr(out), _ptr(h_final),
                             _ptr(workspace), int(ws_bytes), _stream(stream)), "gdn_forward")
+
+
+def gdn_forward_static_scratch(p, q, k, v, g, beta, h0, cu_seqlens, out, h_final, stream=None):
+    """gdn_forward without a workspace: for callers that cannot allocate device memory.  Its
+    scratch is the library's own 64 MiB device array (see include/gdn.h for the limits)."""
+    _check(_lib.gdn_forward_static_scratch(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                           _ptr(beta), _ptr(h0), _ptr(cu_seqlens), _ptr(out),
+                                           _ptr(h_final), _stream(stream)),
+           "gdn_forward_static_scratch")
 
 
 def gdn_chunk_prepare(p, k, v, g, beta, cu_seqlens, w, u, gcum, dev_status=None, stream=None):

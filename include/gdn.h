@@ -186,6 +186,28 @@ gdn_status gdn_chunk_emit_fused(const gdn_problem* p, const void* q, const void*
  * Returns the recorded status (GDN_OK when none), or GDN_ERR_CUDA if the read failed. */
 gdn_status gdn_device_status(const void* status_word, int reset, cudaStream_t stream);
 
+/* gdn_forward for callers that cannot allocate device memory (for example a plug-in whose host
+ * framework owns all device memory, or a serving loop with a fixed memory plan that forbids
+ * allocations after start-up).  It takes no workspace: its scratch is a 64 MiB array in the
+ * library's own device memory, which every GPU that loads the library holds until the process
+ * exits.  There is no counterpart on the source pages; this is a deployment convenience.
+ *   - Same arguments, results and errors as gdn_forward, minus the workspace.  A problem whose
+ *     gdn_workspace_size() exceeds 64 MiB is rejected with GDN_ERR_WORKSPACE before anything is
+ *     enqueued.
+ *   - It allocates nothing (no cudaMalloc, no allocating library call).
+ *   - All calls on a device share the one array, which keeps the last call's contents (each
+ *     call clears the status word; nothing else needs to start at zero).  Calls whose work
+ *     overlaps on the GPU (different streams without ordering, or concurrent host threads)
+ *     race on it: order them on one stream.
+ *   - The first call on a device looks up the array's device address with that device current
+ *     and caches it; make that first call before any stream capture.
+ *   - The status word is the array's first word; it is not exposed, so read a device-side
+ *     error by repeating the call through gdn_forward with a workspace if one is reported. */
+gdn_status gdn_forward_static_scratch(const gdn_problem* p, const void* q, const void* k,
+                                      const void* v, const float* g, const float* beta,
+                                      const float* h0, const int32_t* cu_seqlens, void* out,
+                                      float* h_final, cudaStream_t stream);
+
 /* Text of the last CUDA error that made an entry point return GDN_ERR_CUDA on the calling
  * host thread ("no CUDA error" when there was none).  Static storage. */
 const char* gdn_last_error_string(void);
