@@ -20,11 +20,13 @@
 // inverses by fp32 forward substitution in registers, the off-diagonal blocks
 // T_ab = -T_aa sum_m A_am T_mb with warp-level mma.sync (fp16 operands, fp32 accumulation).
 //
-// Warp roles (416 threads):
-//   warps 0-7  chain:   TMEM lane = state row c; warps w and w + 4 split the columns
-//   warps 8-11 prepare: chunk loads (TMA, then bf16 -> fp16), decay tables, masked gram,
-//                       attn_i and q_g, the triangular solve, -w
+// Warp roles (448 threads):
+//   warps 0-7  chain:   TMEM lane = state row c; warps w and w + 4 split the columns.  Besides
+//                       delta and the state update they convert the next chunk to fp16 and
+//                       scale its q to q_g, work that would otherwise sit on the prepare path
+//   warps 8-11 prepare: decay tables, masked gram and attn_i, the triangular solve, -w
 //   warp 12    MMA:     one thread issues every tcgen05.mma and commit in program order
+//   warp 13    loader:  TMA boxes of K, Q, V and cp.async of g, beta into the free stage
 // Hand-offs use mbarriers; every wait is bounded and a wait that gives up records
 // GDN_ERR_DEVICE_TIMEOUT, and all roles leave their loops (group decisions are made uniform
 // with barrier reductions) so the CTA always reaches its TMEM release.
@@ -49,7 +51,7 @@ using namespace warp_mma;
 constexpr int C = kChunk;  // 64
 constexpr int KD = 128, VD = 128;
 constexpr int kChainThreads = 256, kPrepThreads = 128;
-constexpr int kThreads = kChainThreads + kPrepThreads + 32;
+constexpr int kThreads = kChainThreads + kPrepThreads + 64;  // + MMA warp + loader warp
 constexpr uint32_t kWaitLimit = 1u << 16;  // x 20 us: ~1.3 s
 constexpr float kHalfMax = 65504.f;
 
@@ -63,7 +65,7 @@ constexpr uint32_t TM_O = 192;   // o^T, two buffers  2 x 64 fp32 (chunk parity)
 constexpr uint32_t TM_H = 384;   // Dh^T              128 fp32, then fp16 h^T
 
 // mbarriers
-enum Bar { B_X0 = 0, B_X1, B_SQ, B_T, B_WU, B_WR, B_HR, B_D, B_DR, B_H, B_L0, B_L1, kNumBars };
+enum Bar { B_X0 = 0, B_X1, B_SQ, B_T, B_WU, B_WR, B_HR, B_D, B_DR, B_H, B_L0, B_L1, B_QS, kNumBars };
 
 struct Smem {
   uint8_t kq[2][2 * 128 * 128];  // per stage: [kblk][128 rows: K 0-63, Q 64-127][128 B]
@@ -78,7 +80,8 @@ struct Smem {
   float adiag[C][16];            // the diagonal 16 x 16 blocks of A, fp32
   float gst[2][2][C];            // g and beta of a staged chunk
   float G[3][C], eG[3][C], eGLG[3][C], beta[3][C], gamma[3];
-  alignas(16) float dec[C * C];  // e^{G_t - G_s} for s <= t, else 0; 16-byte chunks swizzled
+  alignas(16) float dec[C * C];
+  float qsc[C];                  // e^{G_t} of the chunk whose q the chain warps scale  // e^{G_t - G_s} for s <= t, else 0; 16-byte chunks swizzled
   uint64_t bars[kNumBars];
   uint32_t tmem_base;
   int abort_flag;
@@ -212,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- setup: mbarriers, TMEM
   if (tid == 0) {
-    for (int b = 0; b < kNumBars; ++b) mbar_init(saddr(&S.bars[b]), 1);
+    for (int b = 0; b < kNumBars; ++b)  // loads: the byte count plus 32 cp.async arrivals
+      mbar_init(saddr(&S.bars[b]), (b == B_L0 || b == B_L1) ? 33 : 1);
     S.abort_flag = 0;
     S.range_bad = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -265,14 +269,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st8(tm + lane_bits + TM_H + 64 * hf + 8 * piece, p);
       }
     };
-    if (nch > 0) {
+    // chunk ci (landed by the loader) to fp16 in place, then hand it to the MMA warp
+    auto convert = [&](int ci) -> bool {
+      const int sg = ci & 1;
+      if (!group_wait(S, B_L0 + sg, (ci >> 1) & 1, 2, kChainThreads)) return false;
+      constexpr int kPer = (MODE == kEmit ? 2 : 1) + (MODE != kSumM ? 1 : 0);
+#pragma unroll 4
+      for (int e = tid; e < C * 16 * kPer; e += kChainThreads) {
+        const int which = e / (C * 16), rem = e % (C * 16);
+        const int t = rem >> 4, col = (rem & 15) << 3;
+        uint8_t* ptr;
+        if (which == 0) ptr = S.kq[sg] + sw128_offset(128, t, col);
+        else if (which == 1 && MODE == kEmit) ptr = S.kq[sg] + sw128_offset(128, 64 + t, col);
+        else ptr = S.v[sg] + sw128_offset(64, t, col);
+        range_ok &= to_half_chunk(ptr);
+      }
+      fence_async_smem();
+      named_bar(2, kChainThreads);
+      if (tid == 0) mbar_arrive(saddr(&S.bars[B_X0 + sg]));
+      return true;
+    };
+    // q -> q_g = e^{G_t} q of chunk ci, after [S ; QK] has read the unscaled q
+    auto scale_q = [&](int ci) -> bool {
+      const int sg = ci & 1;
+      if (!group_wait(S, B_SQ, ci & 1, 2, kChainThreads)) return false;
+      if (warp == 0) {  // within-chunk inclusive scan of g (rows past the sequence are 0)
+        float x0 = S.gst[sg][0][lane], x1 = S.gst[sg][0][lane + 32];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
+          const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
+          if (lane >= o) { x0 += y0; x1 += y1; }
+        }
+        x1 += __shfl_sync(0xffffffffu, x0, 31);
+        S.qsc[lane] = __expf(x0);
+        S.qsc[lane + 32] = __expf(x1);
+      }
+      named_bar(2, kChainThreads);
+      {
+        const int t = tid >> 2, c0q = 4 * (tid & 3);  // row t, four 16-byte chunks
+        const float sc = S.qsc[t];
+        uint4* pq[4];
+        uint4 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          pq[u] = reinterpret_cast<uint4*>(S.kq[sg] + sw128_offset(128, 64 + t, 8 * (c0q + u)));
+          x[u] = *pq[u];
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint32_t* w = reinterpret_cast<uint32_t*>(&x[u]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<__half2*>(&w[i]));
+            w[i] = pack_h2(f.x * sc, f.y * sc);
+          }
+          *pq[u] = x[u];
+        }
+      }
+      fence_async_smem();
+      named_bar(2, kChainThreads);
+      if (tid == 0) mbar_arrive(saddr(&S.bars[B_QS]));
+      return true;
+    };
+    bool go = nch > 0;
+    if (go) go = convert(0);
+    if (go && MODE == kEmit) go = scale_q(0);
+    if (go) {
       publish_h();
       fence_before_sync();
       named_bar(2, kChainThreads);
       if (tid == 0) mbar_arrive(saddr(&S.bars[B_HR]));
     }
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-    for (int ci = 0; ci < nch; ++ci) {
+    for (int ci = 0; go && ci < nch; ++ci) {
       const int gb = ci % 3;
       const int64_t t0 = sb + (c0 + ci) * C;
       const int L = (int)((se - t0) < C ? (se - t0) : C);
@@ -310,6 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_before_sync();
       named_bar(2, kChainThreads);
       if (tid == 0) mbar_arrive(saddr(&S.bars[B_DR]));
+      // ---- while O2 and Dh run: the next chunk to fp16
+      if (ci + 1 < nch && !convert(ci + 1)) break;
       // ---- the state update first (it gates the next chunk), the outputs after it
       if (!group_wait(S, B_H, ci & 1, 2, kChainThreads)) break;
       fence_after_sync();
@@ -340,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (MODE == kEmit && ci + 1 < nch && !scale_q(ci + 1)) break;
     }
     if (!range_ok) S.range_bad = 1;
     // ---- the final state: h^T[c][i] = h[i][c]
@@ -373,56 +446,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       reinterpret_cast<uint4*>(S.tu)[e] = make_uint4(0u, 0u, 0u, 0u);
     }
 
-    auto issue_loads = [&](int ci) {
-      const int s = ci & 1;
+    // decay tables and the decay matrix of chunk ci (g, beta staged by the loader)
+    auto tables = [&](int ci) -> bool {
+      const int sg = ci & 1, gb = ci % 3;
       const int64_t t0 = sb + (c0 + ci) * C;
       const int L = (int)((se - t0) < C ? (se - t0) : C);
-      if (pt == 0) {  // rows past T read zeros; rows in [L, 64) belong to no computation here
-        const uint32_t bar = saddr(&S.bars[B_L0 + s]);
-        const uint32_t kq = saddr(S.kq[s]), vv = saddr(S.v[s]);
-        const uint32_t bytes = (MODE == kEmit ? 4u : 2u) * 8192u + (MODE != kSumM ? 2u : 0u) * 8192u;
-        mbar_expect_tx(bar, bytes);
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-          tma_box(kq + kb * 16384, &tm_k, 64 * kb, kh, (int)t0, bar);
-          if (MODE == kEmit) tma_box(kq + kb * 16384 + 8192, &tm_q, 64 * kb, kh, (int)t0, bar);
-          if (MODE != kSumM) tma_box(vv + kb * 8192, &tm_v, 64 * kb, j, (int)t0, bar);
-        }
-      }
-      {  // g (threads 0-63) and beta (threads 64-127) of the chunk's rows; zero past L
-        const int t = pt & 63;
-        const bool ok = t < L;
-        const int64_t tt = ok ? t0 + t : sb;
-        cp_async4(saddr(&S.gst[s][pt >> 6][t]), (pt < 64 ? a.g : a.beta) + tt * a.hv + j, ok);
-      }
-      asm volatile("cp.async.commit_group;\n" ::: "memory");
-    };
-    // chunk ci to fp16, decay tables, then arrive X; false when the load wait gave up
-    auto finish_data = [&](int ci) -> bool {
-      const int s = ci & 1, gb = ci % 3;
-      const int64_t t0 = sb + (c0 + ci) * C;
-      const int L = (int)((se - t0) < C ? (se - t0) : C);
-      asm volatile("cp.async.wait_group 0;\n" ::: "memory");
-      if (!group_wait(S, B_L0 + s, (ci >> 1) & 1, 1, kPrepThreads)) return false;
-      // bf16 -> fp16 of K, Q and V; four independent chunks in flight per thread
-      {
-        constexpr int kPer = (MODE == kEmit ? 2 : 1) + (MODE != kSumM ? 1 : 0);
-        const int nchunks = C * 16 * kPer;  // 16-byte chunks
-#pragma unroll 4
-        for (int e = pt; e < nchunks; e += kPrepThreads) {
-          const int which = e / (C * 16), rem = e % (C * 16);
-          const int t = rem >> 4, col = (rem & 15) << 3;
-          uint8_t* p;
-          if (which == 0) p = S.kq[s] + sw128_offset(128, t, col);
-          else if (which == 1 && MODE == kEmit) p = S.kq[s] + sw128_offset(128, 64 + t, col);
-          else p = S.v[s] + sw128_offset(64, t, col);
-          range_ok &= to_half_chunk(p);
-        }
-      }
-      named_bar(1, kPrepThreads);  // the staged g, beta are visible
+      if (!group_wait(S, B_L0 + sg, (ci >> 1) & 1, 1, kPrepThreads)) return false;
       if (pt < 32) {  // within-chunk inclusive scan of g; rows >= L decay by nothing
-        const float g0 = S.gst[s][0][pt], g1 = S.gst[s][0][pt + 32];
-        float x0 = g0, x1 = g1;
+        float x0 = S.gst[sg][0][pt], x1 = S.gst[sg][0][pt + 32];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
@@ -438,12 +469,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         S.eG[gb][pt + 32] = __expf(x1);
         S.eGLG[gb][pt] = __expf(GL - x0);
         S.eGLG[gb][pt + 32] = __expf(GL - x1);
-        S.beta[gb][pt] = S.gst[s][1][pt];
-        S.beta[gb][pt + 32] = S.gst[s][1][pt + 32];
+        S.beta[gb][pt] = S.gst[sg][1][pt];
+        S.beta[gb][pt + 32] = S.gst[sg][1][pt + 32];
         if (pt == 0) S.gamma[gb] = __expf(GL);
       }
       named_bar(1, kPrepThreads);
-      {  // the decay matrix of this chunk: row t, columns 32 (pt >> 6) .. + 31
+      {  // the decay matrix: row t, columns 32 (pt >> 6) .. + 31
         const int t = pt & 63, s0 = 32 * (pt >> 6);
         const float Gt = S.G[gb][t];
 #pragma unroll
@@ -457,9 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float4*>(&S.dec[dec_idx(t, s1)]) = d;
         }
       }
-      fence_async_smem();
       named_bar(1, kPrepThreads);
-      if (pt == 0) mbar_arrive(saddr(&S.bars[B_X0 + s]));
       return true;
     };
 
@@ -508,14 +537,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     };
 
-    bool go = nch > 0;
-    if (go) {
-      issue_loads(0);
-      go = finish_data(0);
-    }
-    for (int ci = 0; go && ci < nch; ++ci) {
+    for (int ci = 0; ci < nch; ++ci) {
       const int gb = ci % 3;
-      // ---- masked gram A and attn_i from [S ; QK]; q -> q_g = e^{G_t} q
+      if (!tables(ci)) break;
+      // ---- masked gram A and attn_i from [S ; QK]
       if (!group_wait(S, B_SQ, ci & 1, 1, kPrepThreads)) break;
       fence_after_sync();
       {
@@ -554,39 +579,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (MODE == kEmit && !is_s) {  // row t of Q, both column blocks, scaled by e^{G_t}
-          const float sc = S.eG[gb][t];
-#pragma unroll
-          for (int c4 = 0; c4 < 16; c4 += 4) {
-            uint4* p[4];
-            uint4 x[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              p[u] = reinterpret_cast<uint4*>(S.kq[ci & 1] +
-                                              sw128_offset(128, 64 + t, 8 * (c4 + u)));
-              x[u] = *p[u];
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              uint32_t* w = reinterpret_cast<uint32_t*>(&x[u]);
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const float2 f = __half22float2(*reinterpret_cast<__half2*>(&w[i]));
-                w[i] = pack_h2(f.x * sc, f.y * sc);
-              }
-              *p[u] = x[u];
-            }
-          }
-          fence_async_smem();
-        }
+        if (MODE == kEmit && !is_s) fence_async_smem();  // attn_i feeds the tensor core
       }
       fence_before_sync();
       named_bar(1, kPrepThreads);
-      // ---- next chunk's loads into the stage chunk ci - 1 used (its MMAs are done)
-      if (ci + 1 < nch) {
-        if (ci >= 1 && !group_wait(S, B_H, (ci - 1) & 1, 1, kPrepThreads)) break;
-        issue_loads(ci + 1);
-      }
       // ---- T = (I + A)^-1.  Diagonal block wb by forward substitution in registers:
       // lane (c, rh) holds rows 8 rh .. 8 rh + 7 of column c of the block inverse.
       {
@@ -672,11 +668,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_before_sync();
       named_bar(1, kPrepThreads);
       if (pt == 0) mbar_arrive(saddr(&S.bars[B_WR]));
-      // ---- the next chunk's data
-      if (ci + 1 < nch && !finish_data(ci + 1)) break;
     }
-    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
     if (!range_ok) S.range_bad = 1;
+  } else if (warp == 13) {
+    // =============================================================== loader (1 warp)
+    for (int ci = 0; ci < nch; ++ci) {
+      const int sg = ci & 1;
+      if (ci >= 2) {  // the stage was last used by chunk ci - 2: wait for its last MMA
+        bool ok = true;
+        if (lane == 0) ok = single_wait(S, B_H, (ci - 2) & 1);
+        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+      }
+      const int64_t t0 = sb + (c0 + ci) * C;
+      const int L = (int)((se - t0) < C ? (se - t0) : C);
+      const uint32_t bar = saddr(&S.bars[B_L0 + sg]);
+      if (lane == 0) {  // rows past T read zeros; rows in [L, 64) only meet zero weights
+        const uint32_t kq = saddr(S.kq[sg]), vv = saddr(S.v[sg]);
+        const uint32_t bytes =
+            (MODE == kEmit ? 4u : 2u) * 8192u + (MODE != kSumM ? 2u : 0u) * 8192u;
+        mbar_expect_tx(bar, bytes);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          tma_box(kq + kb * 16384, &tm_k, 64 * kb, kh, (int)t0, bar);
+          if (MODE == kEmit) tma_box(kq + kb * 16384 + 8192, &tm_q, 64 * kb, kh, (int)t0, bar);
+          if (MODE != kSumM) tma_box(vv + kb * 8192, &tm_v, 64 * kb, j, (int)t0, bar);
+        }
+      }
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {  // g and beta, zero past the sequence's end
+        const int t = lane + 32 * h2;
+        const bool ok = t < L;
+        const int64_t tt = ok ? t0 + t : sb;
+        cp_async4(saddr(&S.gst[sg][0][t]), a.g + tt * a.hv + j, ok);
+        cp_async4(saddr(&S.gst[sg][1][t]), a.beta + tt * a.hv + j, ok);
+      }
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar)
+                   : "memory");
+    }
+    asm volatile("cp.async.wait_all;\n" ::: "memory");
   } else if (lane == 0) {
     // =============================================================== MMA issue (1 thread)
     const uint32_t ID_SQ = idesc_f16(128, 64, 0, 0);
@@ -716,7 +745,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ci = 0; ok && ci < nch; ++ci) {
         const uint32_t kq = saddr(S.kq[ci & 1]);
         // delta^T (+)= h^T (-w)^T ;  o^T = h^T q_g^T
-        ok = single_wait(S, B_WR, ci & 1) && single_wait(S, B_HR, ci & 1);
+        ok = single_wait(S, B_WR, ci & 1) && single_wait(S, B_HR, ci & 1) &&
+             (MODE != kEmit || single_wait(S, B_QS, ci & 1));
         if (!ok) break;
         fence_after_sync();
         const uint32_t nw = saddr(S.nw);
@@ -731,11 +761,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                    ks > 0);
         }
         mma_commit(saddr(&S.bars[B_D]));
-        if (ci + 1 < nch) {
-          ok = single_wait(S, B_X0 + ((ci + 1) & 1), ((ci + 1) >> 1) & 1);
-          if (!ok) break;
-          sq(ci + 1);
-        }
         // o^T += delta^T attn_i^T ;  Dh^T = delta'^T K
         ok = single_wait(S, B_DR, ci & 1);
         if (!ok) break;
@@ -749,7 +774,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tm + TM_H, tm + col + 16, sdesc(kq + ks * 2048, 16384, 1024), ID_DH, ks > 0);
         }
         mma_commit(saddr(&S.bars[B_H]));
+        // the next chunk's [S ; QK] and w, u
         if (ci + 1 < nch) {
+          ok = single_wait(S, B_X0 + ((ci + 1) & 1), ((ci + 1) >> 1) & 1);
+          if (!ok) break;
+          sq(ci + 1);
           ok = single_wait(S, B_T, (ci + 1) & 1);
           if (!ok) break;
           wu(ci + 1);
