@@ -39,11 +39,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes,
   return d;
 }
 
-// Instruction descriptor for kind::f16 with fp16 A and B and an fp32 accumulator.
-// a_mn / b_mn: 1 when that operand is MN-major (its M or N index is the contiguous one).
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
-  return (1u << 4)                       // D format: f32
-         | (0u << 7) | (0u << 10)        // A, B format: f16
+// Instruction descriptor for kind::f16 with an fp32 accumulator; A and B are both fp16
+// (bf16 = 0) or both bf16 (bf16 = 1).  a_mn / b_mn: 1 when that operand is MN-major (its M or
+// N index is the contiguous one).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn, int bf16 = 0) {
+  return (1u << 4)                                            // D format: f32
+         | ((uint32_t)bf16 << 7) | ((uint32_t)bf16 << 10)     // A, B format
          | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16)
          | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }

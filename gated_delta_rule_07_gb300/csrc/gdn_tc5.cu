@@ -9,6 +9,8 @@
 //   [S ; QK]  = [K ; Q] K^T                       (128 x 64, K = 128)
 //   w^T       = K^T (T diag(beta e^G))^T          (128 x 64, K = 64)
 //   u^T       = V^T (T diag(beta))^T              (128 x 64, K = 64)
+//   (K, Q, V stay bf16 as loaded; where they meet a computed operand, that operand is split
+//   into bf16 hi + lo parts, x = hi + lo to 2^-16, and the two products accumulate)
 //   delta^T   = u^T + h^T (-w)^T                  (128 x 64, K = 128; h^T read from TMEM)
 //   O1^T      = h^T Q^T                           (128 x 64, K = 128)
 //   O2^T      = delta^T attn_i^T                  (128 x 64, K = 64; delta^T from TMEM)
@@ -22,10 +24,9 @@
 //
 // Warp roles (448 threads):
 //   warps 0-7  chain:   TMEM lane = state row c; warps w and w + 4 split the columns.  Besides
-//                       delta and the state update they convert the next chunk to fp16 and
-//                       scale its q to q_g, work that would otherwise sit on the prepare path
+//                       delta and the state update they turn the next chunk's q into fp16 q_g
 //   warps 8-11 prepare: decay tables, masked gram and attn_i, the triangular solve, -w
-//   warp 12    MMA:     one thread issues every tcgen05.mma and commit in program order
+//   warp 12    MMA:     the whole warp waits, one thread issues every tcgen05.mma and commit
 //   warp 13    loader:  TMA boxes of K, Q, V and cp.async of g, beta into the free stage
 // Hand-offs use mbarriers; every wait is bounded and a wait that gives up records
 // GDN_ERR_DEVICE_TIMEOUT, and all roles leave their loops (group decisions are made uniform
@@ -62,17 +63,20 @@ constexpr uint32_t TM_SQ = 0;    // [S ; QK]          64 fp32
 constexpr uint32_t TM_W = 64;    // w^T               64 fp32
 constexpr uint32_t TM_U = 128;   // u^T -> delta^T    64 fp32, then fp16 delta / delta'
 constexpr uint32_t TM_O = 192;   // o^T, two buffers  2 x 64 fp32 (chunk parity)
+constexpr uint32_t TM_DL = 320;  // lo part of delta'  32 bf16 pairs
 constexpr uint32_t TM_H = 384;   // Dh^T              128 fp32, then fp16 h^T
 
 // mbarriers
-enum Bar { B_X0 = 0, B_X1, B_SQ, B_T, B_WU, B_WR, B_HR, B_D, B_DR, B_H, B_L0, B_L1, B_QS, kNumBars };
+enum Bar { B_SQ = 0, B_T, B_WU, B_WR, B_HR, B_D, B_DR, B_H, B_L0, B_L1, B_QS, kNumBars };
 
 struct Smem {
   uint8_t kq[2][2 * 128 * 128];  // per stage: [kblk][128 rows: K 0-63, Q 64-127][128 B]
   uint8_t v[2][2 * 64 * 128];    // per stage: [kblk][64 rows][128 B]
   uint8_t att[2][64 * 128];      // attn_i [t][s], K-major B
-  uint8_t tw[64 * 128];          // T diag(beta e^G) [t][s], K-major B
-  uint8_t tu[64 * 128];          // T diag(beta) [t][s], K-major B
+  uint8_t twh[64 * 128];         // T diag(beta e^G) [t][s], K-major B, bf16 hi part
+  uint8_t twl[64 * 128];         //   ... and lo part
+  uint8_t tuh[64 * 128];         // T diag(beta) [t][s], K-major B, bf16 hi part
+  uint8_t tul[64 * 128];         //   ... and lo part
   uint8_t nw[128 * 128];         // -w [i][t], MN-major B
   uint8_t ah[64 * 128];          // masked gram A [t][s], fp16
   uint8_t th[64 * 128];          // blocks of (I + A)^-1 [t][s], fp16 operands
@@ -91,11 +95,13 @@ struct Smem {
 // Members read or written with 16-byte vector accesses, ldmatrix or the tensor core must sit on
 // 16-byte (swizzled tiles: 1024-byte) boundaries of the 1024-aligned base.
 static_assert(offsetof(Smem, kq) % 1024 == 0 && offsetof(Smem, v) % 1024 == 0, "tile alignment");
-static_assert(offsetof(Smem, att) % 1024 == 0 && offsetof(Smem, tw) % 1024 == 0, "tile alignment");
-static_assert(offsetof(Smem, tu) % 1024 == 0 && offsetof(Smem, nw) % 1024 == 0, "tile alignment");
+static_assert(offsetof(Smem, att) % 1024 == 0 && offsetof(Smem, twh) % 1024 == 0, "tile alignment");
+static_assert(offsetof(Smem, twl) % 1024 == 0 && offsetof(Smem, tuh) % 1024 == 0, "tile alignment");
+static_assert(offsetof(Smem, tul) % 1024 == 0 && offsetof(Smem, nw) % 1024 == 0, "tile alignment");
 static_assert(offsetof(Smem, ah) % 1024 == 0 && offsetof(Smem, th) % 1024 == 0, "tile alignment");
 static_assert(offsetof(Smem, xs) % 16 == 0 && offsetof(Smem, dec) % 16 == 0, "vector alignment");
 static_assert(offsetof(Smem, bars) % 8 == 0, "mbarrier alignment");
+static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory per block");
 
 // ------------------------------------------------------------------ small helpers
 
@@ -129,11 +135,12 @@ __device__ __forceinline__ bool group_wait(Smem& S, int bar, uint32_t parity, in
   if (!ok) set_abort(S);
   return ok;
 }
-__device__ __forceinline__ bool single_wait(Smem& S, int bar, uint32_t parity) {
-  if (aborted(S)) return false;
-  if (mbar_wait(saddr(&S.bars[bar]), parity, kWaitLimit)) return true;
-  set_abort(S);
-  return false;
+// Warp-uniform bounded wait (every lane waits: a lone waiting lane wakes late).
+__device__ __forceinline__ bool warp_wait(Smem& S, int bar, uint32_t parity) {
+  bool ok = !aborted(S) && mbar_wait(saddr(&S.bars[bar]), parity, kWaitLimit);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) set_abort(S);
+  return ok;
 }
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
@@ -141,6 +148,22 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 __device__ __forceinline__ bool fits_half(float x) { return fabsf(x) <= kHalfMax; }
+
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): products with a bf16 operand keep ~16 bits.
+__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+__device__ __forceinline__ void st_hilo(uint8_t* hi_tile, uint8_t* lo_tile, int r, int c,
+                                        float x) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  const uint32_t off = sw128_offset(64, r, c);
+  *reinterpret_cast<__nv_bfloat16*>(hi_tile + off) = h;
+  *reinterpret_cast<__nv_bfloat16*>(lo_tile + off) = __float2bfloat16_rn(x - __bfloat162float(h));
+}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   const int n = valid ? 16 : 0;
@@ -269,27 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st8(tm + lane_bits + TM_H + 64 * hf + 8 * piece, p);
       }
     };
-    // chunk ci (landed by the loader) to fp16 in place, then hand it to the MMA warp
-    auto convert = [&](int ci) -> bool {
-      const int sg = ci & 1;
-      if (!group_wait(S, B_L0 + sg, (ci >> 1) & 1, 2, kChainThreads)) return false;
-      constexpr int kPer = (MODE == kEmit ? 2 : 1) + (MODE != kSumM ? 1 : 0);
-#pragma unroll 4
-      for (int e = tid; e < C * 16 * kPer; e += kChainThreads) {
-        const int which = e / (C * 16), rem = e % (C * 16);
-        const int t = rem >> 4, col = (rem & 15) << 3;
-        uint8_t* ptr;
-        if (which == 0) ptr = S.kq[sg] + sw128_offset(128, t, col);
-        else if (which == 1 && MODE == kEmit) ptr = S.kq[sg] + sw128_offset(128, 64 + t, col);
-        else ptr = S.v[sg] + sw128_offset(64, t, col);
-        range_ok &= to_half_chunk(ptr);
-      }
-      fence_async_smem();
-      named_bar(2, kChainThreads);
-      if (tid == 0) mbar_arrive(saddr(&S.bars[B_X0 + sg]));
-      return true;
-    };
-    // q -> q_g = e^{G_t} q of chunk ci, after [S ; QK] has read the unscaled q
+    // q (bf16) -> q_g = e^{G_t} q (fp16) of chunk ci, in place, after [S ; QK] has read q
     auto scale_q = [&](int ci) -> bool {
       const int sg = ci & 1;
       if (!group_wait(S, B_SQ, ci & 1, 2, kChainThreads)) return false;
@@ -321,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t* w = reinterpret_cast<uint32_t*>(&x[u]);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const float2 f = __half22float2(*reinterpret_cast<__half2*>(&w[i]));
+            const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[i]));
+            range_ok = range_ok && fits_half(f.x * sc) && fits_half(f.y * sc);
             w[i] = pack_h2(f.x * sc, f.y * sc);
           }
           *pq[u] = x[u];
@@ -333,7 +337,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     bool go = nch > 0;
-    if (go) go = convert(0);
     if (go && MODE == kEmit) go = scale_q(0);
     if (go) {
       publish_h();
@@ -365,23 +368,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st16(tm + lane_bits + TM_U + 32 * hf, pd);
         }
-        {
-          uint32_t pp[16];
+        {  // delta' = e^{G_last - G_t} delta as bf16 hi + lo (it meets bf16 K)
+          uint32_t ph[16], pl[16];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const int t = 32 * hf + 2 * q;
-            pp[q] = pack_h2(d0[2 * q] * S.eGLG[gb][t], d0[2 * q + 1] * S.eGLG[gb][t + 1]);
-            pp[q + 8] =
-                pack_h2(d1[2 * q] * S.eGLG[gb][t + 16], d1[2 * q + 1] * S.eGLG[gb][t + 17]);
+            split_bf16(d0[2 * q] * S.eGLG[gb][t], d0[2 * q + 1] * S.eGLG[gb][t + 1], ph[q], pl[q]);
+            split_bf16(d1[2 * q] * S.eGLG[gb][t + 16], d1[2 * q + 1] * S.eGLG[gb][t + 17],
+                       ph[q + 8], pl[q + 8]);
           }
-          tmem_st16(tm + lane_bits + TM_U + 32 * hf + 16, pp);
+          tmem_st16(tm + lane_bits + TM_U + 32 * hf + 16, ph);
+          tmem_st16(tm + lane_bits + TM_DL + 16 * hf, pl);
         }
       }
       fence_before_sync();
       named_bar(2, kChainThreads);
       if (tid == 0) mbar_arrive(saddr(&S.bars[B_DR]));
-      // ---- while O2 and Dh run: the next chunk to fp16
-      if (ci + 1 < nch && !convert(ci + 1)) break;
+
       // ---- the state update first (it gates the next chunk), the outputs after it
       if (!group_wait(S, B_H, ci & 1, 2, kChainThreads)) break;
       fence_after_sync();
@@ -442,8 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // the strictly upper blocks of T diag(.) are zero for every chunk
     for (int e = pt; e < 64 * 128 / 16; e += kPrepThreads) {
-      reinterpret_cast<uint4*>(S.tw)[e] = make_uint4(0u, 0u, 0u, 0u);
-      reinterpret_cast<uint4*>(S.tu)[e] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(S.twh)[e] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(S.twl)[e] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(S.tuh)[e] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(S.tul)[e] = make_uint4(0u, 0u, 0u, 0u);
     }
 
     // decay tables and the decay matrix of chunk ci (g, beta staged by the loader)
@@ -531,8 +536,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float w0 = u0 * S.eG[gb][col], w1 = u1 * S.eG[gb][col + 1];
           const uint32_t off = sw128_offset(64, row, col);
           *reinterpret_cast<uint32_t*>(S.th + off) = pack_h2(v0, v1);
-          *reinterpret_cast<uint32_t*>(S.tw + off) = pack_h2(v0 * w0, v1 * w1);
-          *reinterpret_cast<uint32_t*>(S.tu + off) = pack_h2(v0 * u0, v1 * u1);
+          uint32_t hi, lo;
+          split_bf16(v0 * w0, v1 * w1, hi, lo);
+          *reinterpret_cast<uint32_t*>(S.twh + off) = hi;
+          *reinterpret_cast<uint32_t*>(S.twl + off) = lo;
+          split_bf16(v0 * u0, v1 * u1, hi, lo);
+          *reinterpret_cast<uint32_t*>(S.tuh + off) = hi;
+          *reinterpret_cast<uint32_t*>(S.tul + off) = lo;
           range_ok = range_ok && fits_half(v0) && fits_half(v1);
         }
     };
@@ -629,8 +639,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k2 = 0; k2 < 8; ++k2) {
           const int row = 16 * wb + 8 * rh + k2;
           st_half(S.th, row, col, tc[k2]);
-          st_half(S.tw, row, col, tc[k2] * w);
-          st_half(S.tu, row, col, tc[k2] * u);
+          st_hilo(S.twh, S.twl, row, col, tc[k2] * w);
+          st_hilo(S.tuh, S.tul, row, col, tc[k2] * u);
         }
       }
       named_bar(1, kPrepThreads);
@@ -674,11 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =============================================================== loader (1 warp)
     for (int ci = 0; ci < nch; ++ci) {
       const int sg = ci & 1;
-      if (ci >= 2) {  // the stage was last used by chunk ci - 2: wait for its last MMA
-        bool ok = true;
-        if (lane == 0) ok = single_wait(S, B_H, (ci - 2) & 1);
-        if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-      }
+      // the stage was last used by chunk ci - 2: wait for its last MMA
+      if (ci >= 2 && !warp_wait(S, B_H, (ci - 2) & 1)) break;
       const int64_t t0 = sb + (c0 + ci) * C;
       const int L = (int)((se - t0) < C ? (se - t0) : C);
       const uint32_t bar = saddr(&S.bars[B_L0 + sg]);
@@ -706,80 +713,104 @@ __global__ void __launch_bounds__(kThreads, 1)
                    : "memory");
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
-  } else if (lane == 0) {
-    // =============================================================== MMA issue (1 thread)
-    const uint32_t ID_SQ = idesc_f16(128, 64, 0, 0);
-    const uint32_t ID_WU = idesc_f16(128, 64, 1, 0);
-    const uint32_t ID_D = idesc_f16(128, 64, 0, 1);
-    const uint32_t ID_O = idesc_f16(128, 64, 0, 0);
-    const uint32_t ID_DH = idesc_f16(128, 128, 0, 1);
+  } else {
+    // =============================================================== MMA (warp 12)
+    // every lane waits; lane 0 issues the MMAs and commits
+    const bool leader = lane == 0;
+    const uint32_t ID_SQ = idesc_f16(128, 64, 0, 0, 1);     // bf16 [K ; Q] K^T
+    const uint32_t ID_WU = idesc_f16(128, 64, 1, 0, 1);     // bf16 K^T, V^T x T parts
+    const uint32_t ID_D = idesc_f16(128, 64, 0, 1);         // fp16 h^T (-w)^T
+    const uint32_t ID_O = idesc_f16(128, 64, 0, 0);         // fp16 h^T q_g^T, delta^T attn^T
+    const uint32_t ID_DH = idesc_f16(128, 128, 0, 1, 1);    // bf16 delta'^T K
     auto sq = [&](int ci) {
-      const uint32_t kq = saddr(S.kq[ci & 1]);
+      if (leader) {
+        const uint32_t kq = saddr(S.kq[ci & 1]);
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint64_t d = sdesc(kq + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
-        mma_ss(tm + TM_SQ, d, d, ID_SQ, ks > 0);
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t d = sdesc(kq + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024);
+          mma_ss(tm + TM_SQ, d, d, ID_SQ, ks > 0);
+        }
+        mma_commit(saddr(&S.bars[B_SQ]));
       }
-      mma_commit(saddr(&S.bars[B_SQ]));
+      __syncwarp();
     };
     auto wu = [&](int ci) {
-      const uint32_t kq = saddr(S.kq[ci & 1]), vv = saddr(S.v[ci & 1]);
-      const uint32_t tw = saddr(S.tw), tu = saddr(S.tu);
+      if (leader) {
+        const uint32_t kq = saddr(S.kq[ci & 1]), vv = saddr(S.v[ci & 1]);
+        const uint32_t tiles_w[2] = {saddr(S.twh), saddr(S.twl)};
+        const uint32_t tiles_u[2] = {saddr(S.tuh), saddr(S.tul)};
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tm + TM_W, sdesc(kq + ks * 2048, 16384, 1024), sdesc(tw + ks * 32, 16, 1024),
-               ID_WU, ks > 0);
-      if (MODE != kSumM) {
+        for (int part = 0; part < 2; ++part)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ss(tm + TM_U, sdesc(vv + ks * 2048, 8192, 1024), sdesc(tu + ks * 32, 16, 1024),
-                 ID_WU, ks > 0);
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss(tm + TM_W, sdesc(kq + ks * 2048, 16384, 1024),
+                   sdesc(tiles_w[part] + ks * 32, 16, 1024), ID_WU, part > 0 || ks > 0);
+        if (MODE != kSumM) {
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_ss(tm + TM_U, sdesc(vv + ks * 2048, 8192, 1024),
+                     sdesc(tiles_u[part] + ks * 32, 16, 1024), ID_WU, part > 0 || ks > 0);
+        }
+        mma_commit(saddr(&S.bars[B_WU]));
       }
-      mma_commit(saddr(&S.bars[B_WU]));
+      __syncwarp();
     };
     if (nch > 0) {
-      bool ok = single_wait(S, B_X0, 0);
+      bool ok = warp_wait(S, B_L0, 0);
       if (ok) sq(0);
-      ok = ok && single_wait(S, B_T, 0);
+      ok = ok && warp_wait(S, B_T, 0);
       if (ok) wu(0);
       for (int ci = 0; ok && ci < nch; ++ci) {
         const uint32_t kq = saddr(S.kq[ci & 1]);
         // delta^T (+)= h^T (-w)^T ;  o^T = h^T q_g^T
-        ok = single_wait(S, B_WR, ci & 1) && single_wait(S, B_HR, ci & 1) &&
-             (MODE != kEmit || single_wait(S, B_QS, ci & 1));
+        ok = warp_wait(S, B_WR, ci & 1) && warp_wait(S, B_HR, ci & 1) &&
+             (MODE != kEmit || warp_wait(S, B_QS, ci & 1));
         if (!ok) break;
         fence_after_sync();
-        const uint32_t nw = saddr(S.nw);
+        if (leader) {
+          const uint32_t nw = saddr(S.nw);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t ah = tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3);
-          mma_ts(tm + TM_U, ah, sdesc(nw + ks * 2048, 16384, 1024), ID_D,
-                 (MODE != kSumM) || ks > 0);
-          if (MODE == kEmit)
-            mma_ts(tm + TM_O + 64 * (ci & 1), ah,
-                   sdesc(kq + (ks >> 2) * 16384 + 64 * 128 + (ks & 3) * 32, 16, 1024), ID_O,
-                   ks > 0);
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t ah = tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3);
+            mma_ts(tm + TM_U, ah, sdesc(nw + ks * 2048, 16384, 1024), ID_D,
+                   (MODE != kSumM) || ks > 0);
+            if (MODE == kEmit)
+              mma_ts(tm + TM_O + 64 * (ci & 1), ah,
+                     sdesc(kq + (ks >> 2) * 16384 + 64 * 128 + (ks & 3) * 32, 16, 1024), ID_O,
+                     ks > 0);
+          }
+          mma_commit(saddr(&S.bars[B_D]));
         }
-        mma_commit(saddr(&S.bars[B_D]));
-        // o^T += delta^T attn_i^T ;  Dh^T = delta'^T K
-        ok = single_wait(S, B_DR, ci & 1);
-        if (!ok) break;
-        fence_after_sync();
-        const uint32_t att = saddr(S.att[ci & 1]);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t col = TM_U + 32 * (ks >> 1) + 8 * (ks & 1);
-          if (MODE == kEmit)
-            mma_ts(tm + TM_O + 64 * (ci & 1), tm + col, sdesc(att + ks * 32, 16, 1024), ID_O, 1);
-          mma_ts(tm + TM_H, tm + col + 16, sdesc(kq + ks * 2048, 16384, 1024), ID_DH, ks > 0);
-        }
-        mma_commit(saddr(&S.bars[B_H]));
-        // the next chunk's [S ; QK] and w, u
+        __syncwarp();
+        // the next chunk's [S ; QK] as soon as its data is in (R_sq was read before T)
         if (ci + 1 < nch) {
-          ok = single_wait(S, B_X0 + ((ci + 1) & 1), ((ci + 1) >> 1) & 1);
+          ok = warp_wait(S, B_L0 + ((ci + 1) & 1), ((ci + 1) >> 1) & 1);
           if (!ok) break;
           sq(ci + 1);
-          ok = single_wait(S, B_T, (ci + 1) & 1);
+        }
+        // o^T += delta^T attn_i^T ;  Dh^T = delta'^T K  (delta' as hi + lo)
+        ok = warp_wait(S, B_DR, ci & 1);
+        if (!ok) break;
+        fence_after_sync();
+        if (leader) {
+          const uint32_t att = saddr(S.att[ci & 1]);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t col = TM_U + 32 * (ks >> 1) + 8 * (ks & 1);
+            if (MODE == kEmit)
+              mma_ts(tm + TM_O + 64 * (ci & 1), tm + col, sdesc(att + ks * 32, 16, 1024), ID_O,
+                     1);
+            const uint64_t bk = sdesc(kq + ks * 2048, 16384, 1024);
+            mma_ts(tm + TM_H, tm + col + 16, bk, ID_DH, ks > 0);
+            mma_ts(tm + TM_H, tm + TM_DL + 16 * (ks >> 1) + 8 * (ks & 1), bk, ID_DH, 1);
+          }
+          mma_commit(saddr(&S.bars[B_H]));
+        }
+        __syncwarp();
+        if (ci + 1 < nch) {
+          ok = warp_wait(S, B_T, (ci + 1) & 1);
           if (!ok) break;
           wu(ci + 1);
         }
