@@ -166,25 +166,26 @@ __device__ __forceinline__ void mbar_arrive(uint32_t addr) {
       "{\n.reg .b64 st;\nmbarrier.arrive.shared::cta.b64 st, [%0];\n}\n" ::"r"(addr)
       : "memory");
 }
-// Tests the phase with the given parity; a thread whose phase is incomplete is suspended by
-// the hardware until the phase completes or about `suspend_ns` pass, whichever is first.
-__device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity, uint32_t suspend_ns) {
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       "selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(addr), "r"(parity), "r"(suspend_ns)
+      : "r"(addr), "r"(parity)
       : "memory");
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete: `limit` suspended tests of up
-// to 20 us each.  Returns false (the caller records a timeout and stops) when it has not
-// completed by then.
+// Bounded wait for the phase with the given parity: polls with short sleeps in between (a
+// waiter wakes within ~100 cycles, and a sleeping warp takes almost no issue slots).  Returns
+// false (the caller records a timeout and stops) after `limit` polls.
 __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_test(addr, parity, 20000u)) return true;
+  for (uint32_t i = 0; i < limit; ++i) {
+    if (mbar_test(addr, parity)) return true;
+    __nanosleep(32);
+  }
   return false;
 }
 

@@ -24,8 +24,9 @@
 //
 // Warp roles (448 threads):
 //   warps 0-7  chain:   TMEM lane = state row c; warps w and w + 4 split the columns.  Besides
-//                       delta and the state update they turn the next chunk's q into fp16 q_g
-//   warps 8-11 prepare: decay tables, masked gram and attn_i, the triangular solve, -w
+//                       delta and the state update they build the next chunk's decay tables
+//                       and turn its q into fp16 q_g
+//   warps 8-11 prepare: masked gram and attn_i, the triangular solve, -w
 //   warp 12    MMA:     the whole warp waits, one thread issues every tcgen05.mma and commit
 //   warp 13    loader:  TMA boxes of K, Q, V and cp.async of g, beta into the free stage
 // Hand-offs use mbarriers; every wait is bounded and a wait that gives up records
@@ -53,7 +54,7 @@ constexpr int C = kChunk;  // 64
 constexpr int KD = 128, VD = 128;
 constexpr int kChainThreads = 256, kPrepThreads = 128;
 constexpr int kThreads = kChainThreads + kPrepThreads + 64;  // + MMA warp + loader warp
-constexpr uint32_t kWaitLimit = 1u << 16;  // x 20 us: ~1.3 s
+constexpr uint32_t kWaitLimit = 1u << 24;  // polls of ~40-100 ns: a second or more
 constexpr float kHalfMax = 65504.f;
 
 enum Mode { kEmit = 0, kSumM = 1, kSumU = 2 };
@@ -67,7 +68,7 @@ constexpr uint32_t TM_DL = 320;  // lo part of delta'  32 bf16 pairs
 constexpr uint32_t TM_H = 384;   // Dh^T              128 fp32, then fp16 h^T
 
 // mbarriers
-enum Bar { B_SQ = 0, B_T, B_WU, B_WR, B_HR, B_D, B_DR, B_H, B_L0, B_L1, B_QS, kNumBars };
+enum Bar { B_SQ = 0, B_T, B_WU, B_WR, B_HR, B_D, B_DR, B_H, B_L0, B_L1, B_QS, B_TB, kNumBars };
 
 struct Smem {
   uint8_t kq[2][2 * 128 * 128];  // per stage: [kblk][128 rows: K 0-63, Q 64-127][128 B]
@@ -292,26 +293,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st8(tm + lane_bits + TM_H + 64 * hf + 8 * piece, p);
       }
     };
-    // q (bf16) -> q_g = e^{G_t} q (fp16) of chunk ci, in place, after [S ; QK] has read q
-    auto scale_q = [&](int ci) -> bool {
-      const int sg = ci & 1;
-      if (!group_wait(S, B_SQ, ci & 1, 2, kChainThreads)) return false;
-      if (warp == 0) {  // within-chunk inclusive scan of g (rows past the sequence are 0)
-        float x0 = S.gst[sg][0][lane], x1 = S.gst[sg][0][lane + 32];
+    // decay tables and the decay matrix of chunk ci (g, beta staged by the loader), for
+    // the prepare warps (arrives TB)
+    auto tables = [&](int ci) -> bool {
+      const int sg = ci & 1, gb = ci % 3;
+      const int64_t t0 = sb + (c0 + ci) * C;
+      const int L = (int)((se - t0) < C ? (se - t0) : C);
+      if (!group_wait(S, B_L0 + sg, (ci >> 1) & 1, 2, kChainThreads)) return false;
+      if (tid < 32) {  // within-chunk inclusive scan of g; rows >= L decay by nothing
+        float x0 = S.gst[sg][0][tid], x1 = S.gst[sg][0][tid + 32];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
           const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
-          if (lane >= o) { x0 += y0; x1 += y1; }
+          if (tid >= o) { x0 += y0; x1 += y1; }
         }
         x1 += __shfl_sync(0xffffffffu, x0, 31);
-        S.qsc[lane] = __expf(x0);
-        S.qsc[lane + 32] = __expf(x1);
+        const float GL = L - 1 < 32 ? __shfl_sync(0xffffffffu, x0, (L - 1) & 31)
+                                    : __shfl_sync(0xffffffffu, x1, (L - 1) & 31);
+        S.G[gb][tid] = x0;
+        S.G[gb][tid + 32] = x1;
+        S.eG[gb][tid] = __expf(x0);
+        S.eG[gb][tid + 32] = __expf(x1);
+        S.eGLG[gb][tid] = __expf(GL - x0);
+        S.eGLG[gb][tid + 32] = __expf(GL - x1);
+        S.beta[gb][tid] = S.gst[sg][1][tid];
+        S.beta[gb][tid + 32] = S.gst[sg][1][tid + 32];
+        if (tid == 0) S.gamma[gb] = __expf(GL);
       }
       named_bar(2, kChainThreads);
+      {  // the decay matrix: row t, columns 16 (tid >> 6) .. + 15
+        const int t = tid & 63, s0 = 16 * (tid >> 6);
+        const float Gt = S.G[gb][t];
+#pragma unroll
+        for (int c4 = 0; c4 < 16; c4 += 4) {
+          float4 d;
+          const int s1 = s0 + c4;
+          d.x = s1 <= t ? __expf(Gt - S.G[gb][s1]) : 0.f;
+          d.y = s1 + 1 <= t ? __expf(Gt - S.G[gb][s1 + 1]) : 0.f;
+          d.z = s1 + 2 <= t ? __expf(Gt - S.G[gb][s1 + 2]) : 0.f;
+          d.w = s1 + 3 <= t ? __expf(Gt - S.G[gb][s1 + 3]) : 0.f;
+          *reinterpret_cast<float4*>(&S.dec[dec_idx(t, s1)]) = d;
+        }
+      }
+      named_bar(2, kChainThreads);
+      if (tid == 0) mbar_arrive(saddr(&S.bars[B_TB]));
+      return true;
+    };
+
+    // q (bf16) -> q_g = e^{G_t} q (fp16) of chunk ci, in place, after [S ; QK] has read q
+    auto scale_q = [&](int ci) -> bool {
+      const int sg = ci & 1;
+      if (!group_wait(S, B_SQ, ci & 1, 2, kChainThreads)) return false;
       {
         const int t = tid >> 2, c0q = 4 * (tid & 3);  // row t, four 16-byte chunks
-        const float sc = S.qsc[t];
+        const float sc = S.eG[ci % 3][t];              // from this chunk's tables
         uint4* pq[4];
         uint4 x[4];
 #pragma unroll
@@ -337,6 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     bool go = nch > 0;
+    if (go) go = tables(0);
     if (go && MODE == kEmit) go = scale_q(0);
     if (go) {
       publish_h();
@@ -384,6 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_before_sync();
       named_bar(2, kChainThreads);
       if (tid == 0) mbar_arrive(saddr(&S.bars[B_DR]));
+      // ---- while O2 and Dh run: the next chunk's decay tables
+      if (ci + 1 < nch && !tables(ci + 1)) break;
 
       // ---- the state update first (it gates the next chunk), the outputs after it
       if (!group_wait(S, B_H, ci & 1, 2, kChainThreads)) break;
@@ -451,52 +490,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       reinterpret_cast<uint4*>(S.tul)[e] = make_uint4(0u, 0u, 0u, 0u);
     }
 
-    // decay tables and the decay matrix of chunk ci (g, beta staged by the loader)
-    auto tables = [&](int ci) -> bool {
-      const int sg = ci & 1, gb = ci % 3;
-      const int64_t t0 = sb + (c0 + ci) * C;
-      const int L = (int)((se - t0) < C ? (se - t0) : C);
-      if (!group_wait(S, B_L0 + sg, (ci >> 1) & 1, 1, kPrepThreads)) return false;
-      if (pt < 32) {  // within-chunk inclusive scan of g; rows >= L decay by nothing
-        float x0 = S.gst[sg][0][pt], x1 = S.gst[sg][0][pt + 32];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
-          const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
-          if (pt >= o) { x0 += y0; x1 += y1; }
-        }
-        x1 += __shfl_sync(0xffffffffu, x0, 31);
-        const float GL = L - 1 < 32 ? __shfl_sync(0xffffffffu, x0, (L - 1) & 31)
-                                    : __shfl_sync(0xffffffffu, x1, (L - 1) & 31);
-        S.G[gb][pt] = x0;
-        S.G[gb][pt + 32] = x1;
-        S.eG[gb][pt] = __expf(x0);
-        S.eG[gb][pt + 32] = __expf(x1);
-        S.eGLG[gb][pt] = __expf(GL - x0);
-        S.eGLG[gb][pt + 32] = __expf(GL - x1);
-        S.beta[gb][pt] = S.gst[sg][1][pt];
-        S.beta[gb][pt + 32] = S.gst[sg][1][pt + 32];
-        if (pt == 0) S.gamma[gb] = __expf(GL);
-      }
-      named_bar(1, kPrepThreads);
-      {  // the decay matrix: row t, columns 32 (pt >> 6) .. + 31
-        const int t = pt & 63, s0 = 32 * (pt >> 6);
-        const float Gt = S.G[gb][t];
-#pragma unroll
-        for (int c4 = 0; c4 < 32; c4 += 4) {
-          float4 d;
-          const int s1 = s0 + c4;
-          d.x = s1 <= t ? __expf(Gt - S.G[gb][s1]) : 0.f;
-          d.y = s1 + 1 <= t ? __expf(Gt - S.G[gb][s1 + 1]) : 0.f;
-          d.z = s1 + 2 <= t ? __expf(Gt - S.G[gb][s1 + 2]) : 0.f;
-          d.w = s1 + 3 <= t ? __expf(Gt - S.G[gb][s1 + 3]) : 0.f;
-          *reinterpret_cast<float4*>(&S.dec[dec_idx(t, s1)]) = d;
-        }
-      }
-      named_bar(1, kPrepThreads);
-      return true;
-    };
-
     // T_ab = -T_aa sum_{m=b}^{a-1} A_am T_mb for one 16 x 16 block, by one warp: the sum on
     // mma.sync from the fp16 tiles, then the product with T_aa through the warp's scratch.
     auto off_diag_block = [&](int ab, int bb, int gb) {
@@ -549,7 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int ci = 0; ci < nch; ++ci) {
       const int gb = ci % 3;
-      if (!tables(ci)) break;
+      if (!group_wait(S, B_TB, ci & 1, 1, kPrepThreads)) break;
       // ---- masked gram A and attn_i from [S ; QK]
       if (!group_wait(S, B_SQ, ci & 1, 1, kPrepThreads)) break;
       fence_after_sync();

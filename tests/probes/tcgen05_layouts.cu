@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(128) probe_kernel(ProbeCase pc, const __half* 
     }
     mma_commit(mb);
   }
-  const bool ok = mbar_wait(mb, 0, 1u << 22);
+  const bool ok = mbar_wait(mb, 0, 1u << 24);
   fence_after_sync();
   if (!ok) {
     if (tid == 0) atomicExch(status, 5);
