@@ -178,6 +178,14 @@ __device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// Bounded busy wait (no sleeps): for the one warp whose wake-up latency is on the critical
+// path.  Returns false after `limit` polls.
+__device__ __forceinline__ bool mbar_spin(uint32_t addr, uint32_t parity, uint32_t limit) {
+  for (uint32_t i = 0; i < limit; ++i)
+    if (mbar_test(addr, parity)) return true;
+  return false;
+}
+
 // Bounded wait for the phase with the given parity: polls with short sleeps in between (a
 // waiter wakes within ~100 cycles, and a sleeping warp takes almost no issue slots).  Returns
 // false (the caller records a timeout and stops) after `limit` polls.

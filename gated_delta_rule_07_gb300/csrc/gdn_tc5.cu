@@ -68,7 +68,7 @@ constexpr uint32_t TM_DL = 320;  // lo part of delta'  32 bf16 pairs
 constexpr uint32_t TM_H = 384;   // Dh^T              128 fp32, then fp16 h^T
 
 // mbarriers
-enum Bar { B_SQ = 0, B_T, B_WU, B_WR, B_HR, B_D, B_DR, B_H, B_L0, B_L1, B_QS, B_TB, kNumBars };
+enum Bar { B_SQ = 0, B_T, B_WU, B_WR, B_HR, B_D, B_DR, B_H, B_L0, B_L1, B_QS, kNumBars };
 
 struct Smem {
   uint8_t kq[2][2 * 128 * 128];  // per stage: [kblk][128 rows: K 0-63, Q 64-127][128 B]
@@ -85,8 +85,8 @@ struct Smem {
   float adiag[C][16];            // the diagonal 16 x 16 blocks of A, fp32
   float gst[2][2][C];            // g and beta of a staged chunk
   float G[3][C], eG[3][C], eGLG[3][C], beta[3][C], gamma[3];
-  alignas(16) float dec[C * C];
-  float qsc[C];                  // e^{G_t} of the chunk whose q the chain warps scale  // e^{G_t - G_s} for s <= t, else 0; 16-byte chunks swizzled
+  alignas(16) float dec[C * C];  // e^{G_t - G_s} for s <= t, else 0; 16-byte chunks swizzled
+  float qsc[C];                  // e^{G_t} of the chunk whose q the chain warps scale
   uint64_t bars[kNumBars];
   uint32_t tmem_base;
   int abort_flag;
@@ -136,9 +136,11 @@ __device__ __forceinline__ bool group_wait(Smem& S, int bar, uint32_t parity, in
   if (!ok) set_abort(S);
   return ok;
 }
-// Warp-uniform bounded wait (every lane waits: a lone waiting lane wakes late).
-__device__ __forceinline__ bool warp_wait(Smem& S, int bar, uint32_t parity) {
-  bool ok = !aborted(S) && mbar_wait(saddr(&S.bars[bar]), parity, kWaitLimit);
+// Warp-uniform bounded wait; `spin` busy-polls (for the MMA warp, whose wake-up delays every
+// product behind it).
+__device__ __forceinline__ bool warp_wait(Smem& S, int bar, uint32_t parity, bool spin = false) {
+  bool ok = !aborted(S) && (spin ? mbar_spin(saddr(&S.bars[bar]), parity, 1u << 28)
+                                 : mbar_wait(saddr(&S.bars[bar]), parity, kWaitLimit));
   ok = __all_sync(0xffffffffu, ok);
   if (!ok) set_abort(S);
   return ok;
@@ -293,61 +295,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st8(tm + lane_bits + TM_H + 64 * hf + 8 * piece, p);
       }
     };
-    // decay tables and the decay matrix of chunk ci (g, beta staged by the loader), for
-    // the prepare warps (arrives TB)
-    auto tables = [&](int ci) -> bool {
-      const int sg = ci & 1, gb = ci % 3;
-      const int64_t t0 = sb + (c0 + ci) * C;
-      const int L = (int)((se - t0) < C ? (se - t0) : C);
-      if (!group_wait(S, B_L0 + sg, (ci >> 1) & 1, 2, kChainThreads)) return false;
-      if (tid < 32) {  // within-chunk inclusive scan of g; rows >= L decay by nothing
-        float x0 = S.gst[sg][0][tid], x1 = S.gst[sg][0][tid + 32];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
-          const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
-          if (tid >= o) { x0 += y0; x1 += y1; }
-        }
-        x1 += __shfl_sync(0xffffffffu, x0, 31);
-        const float GL = L - 1 < 32 ? __shfl_sync(0xffffffffu, x0, (L - 1) & 31)
-                                    : __shfl_sync(0xffffffffu, x1, (L - 1) & 31);
-        S.G[gb][tid] = x0;
-        S.G[gb][tid + 32] = x1;
-        S.eG[gb][tid] = __expf(x0);
-        S.eG[gb][tid + 32] = __expf(x1);
-        S.eGLG[gb][tid] = __expf(GL - x0);
-        S.eGLG[gb][tid + 32] = __expf(GL - x1);
-        S.beta[gb][tid] = S.gst[sg][1][tid];
-        S.beta[gb][tid + 32] = S.gst[sg][1][tid + 32];
-        if (tid == 0) S.gamma[gb] = __expf(GL);
-      }
-      named_bar(2, kChainThreads);
-      {  // the decay matrix: row t, columns 16 (tid >> 6) .. + 15
-        const int t = tid & 63, s0 = 16 * (tid >> 6);
-        const float Gt = S.G[gb][t];
-#pragma unroll
-        for (int c4 = 0; c4 < 16; c4 += 4) {
-          float4 d;
-          const int s1 = s0 + c4;
-          d.x = s1 <= t ? __expf(Gt - S.G[gb][s1]) : 0.f;
-          d.y = s1 + 1 <= t ? __expf(Gt - S.G[gb][s1 + 1]) : 0.f;
-          d.z = s1 + 2 <= t ? __expf(Gt - S.G[gb][s1 + 2]) : 0.f;
-          d.w = s1 + 3 <= t ? __expf(Gt - S.G[gb][s1 + 3]) : 0.f;
-          *reinterpret_cast<float4*>(&S.dec[dec_idx(t, s1)]) = d;
-        }
-      }
-      named_bar(2, kChainThreads);
-      if (tid == 0) mbar_arrive(saddr(&S.bars[B_TB]));
-      return true;
-    };
-
     // q (bf16) -> q_g = e^{G_t} q (fp16) of chunk ci, in place, after [S ; QK] has read q
     auto scale_q = [&](int ci) -> bool {
       const int sg = ci & 1;
       if (!group_wait(S, B_SQ, ci & 1, 2, kChainThreads)) return false;
+      if (warp == 0) {  // e^{G_t} of chunk ci from its staged g (rows past the end are 0)
+        float x0 = S.gst[sg][0][lane], x1 = S.gst[sg][0][lane + 32];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
+          const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
+          if (lane >= o) { x0 += y0; x1 += y1; }
+        }
+        x1 += __shfl_sync(0xffffffffu, x0, 31);
+        S.qsc[lane] = __expf(x0);
+        S.qsc[lane + 32] = __expf(x1);
+      }
+      named_bar(2, kChainThreads);
       {
         const int t = tid >> 2, c0q = 4 * (tid & 3);  // row t, four 16-byte chunks
-        const float sc = S.eG[ci % 3][t];              // from this chunk's tables
+        const float sc = S.qsc[t];
         uint4* pq[4];
         uint4 x[4];
 #pragma unroll
@@ -373,7 +340,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     bool go = nch > 0;
-    if (go) go = tables(0);
     if (go && MODE == kEmit) go = scale_q(0);
     if (go) {
       publish_h();
@@ -421,8 +387,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_before_sync();
       named_bar(2, kChainThreads);
       if (tid == 0) mbar_arrive(saddr(&S.bars[B_DR]));
-      // ---- while O2 and Dh run: the next chunk's decay tables
-      if (ci + 1 < nch && !tables(ci + 1)) break;
 
       // ---- the state update first (it gates the next chunk), the outputs after it
       if (!group_wait(S, B_H, ci & 1, 2, kChainThreads)) break;
@@ -490,6 +454,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       reinterpret_cast<uint4*>(S.tul)[e] = make_uint4(0u, 0u, 0u, 0u);
     }
 
+    // decay tables and the decay matrix of chunk ci (g, beta staged by the loader)
+    auto tables = [&](int ci) -> bool {
+      const int sg = ci & 1, gb = ci % 3;
+      const int64_t t0 = sb + (c0 + ci) * C;
+      const int L = (int)((se - t0) < C ? (se - t0) : C);
+      if (!group_wait(S, B_L0 + sg, (ci >> 1) & 1, 1, kPrepThreads)) return false;
+      if (pt < 32) {  // within-chunk inclusive scan of g; rows >= L decay by nothing
+        float x0 = S.gst[sg][0][pt], x1 = S.gst[sg][0][pt + 32];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
+          const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
+          if (pt >= o) { x0 += y0; x1 += y1; }
+        }
+        x1 += __shfl_sync(0xffffffffu, x0, 31);
+        const float GL = L - 1 < 32 ? __shfl_sync(0xffffffffu, x0, (L - 1) & 31)
+                                    : __shfl_sync(0xffffffffu, x1, (L - 1) & 31);
+        S.G[gb][pt] = x0;
+        S.G[gb][pt + 32] = x1;
+        S.eG[gb][pt] = __expf(x0);
+        S.eG[gb][pt + 32] = __expf(x1);
+        S.eGLG[gb][pt] = __expf(GL - x0);
+        S.eGLG[gb][pt + 32] = __expf(GL - x1);
+        S.beta[gb][pt] = S.gst[sg][1][pt];
+        S.beta[gb][pt + 32] = S.gst[sg][1][pt + 32];
+        if (pt == 0) S.gamma[gb] = __expf(GL);
+      }
+      named_bar(1, kPrepThreads);
+      {  // the decay matrix: row t, columns 32 (pt >> 6) .. + 31
+        const int t = pt & 63, s0 = 32 * (pt >> 6);
+        const float Gt = S.G[gb][t];
+#pragma unroll
+        for (int c4 = 0; c4 < 32; c4 += 4) {
+          float4 d;
+          const int s1 = s0 + c4;
+          d.x = s1 <= t ? __expf(Gt - S.G[gb][s1]) : 0.f;
+          d.y = s1 + 1 <= t ? __expf(Gt - S.G[gb][s1 + 1]) : 0.f;
+          d.z = s1 + 2 <= t ? __expf(Gt - S.G[gb][s1 + 2]) : 0.f;
+          d.w = s1 + 3 <= t ? __expf(Gt - S.G[gb][s1 + 3]) : 0.f;
+          *reinterpret_cast<float4*>(&S.dec[dec_idx(t, s1)]) = d;
+        }
+      }
+      named_bar(1, kPrepThreads);
+      return true;
+    };
+
     // T_ab = -T_aa sum_{m=b}^{a-1} A_am T_mb for one 16 x 16 block, by one warp: the sum on
     // mma.sync from the fp16 tiles, then the product with T_aa through the warp's scratch.
     auto off_diag_block = [&](int ab, int bb, int gb) {
@@ -542,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int ci = 0; ci < nch; ++ci) {
       const int gb = ci % 3;
-      if (!group_wait(S, B_TB, ci & 1, 1, kPrepThreads)) break;
+      if (ci == 0 && !tables(0)) break;
       // ---- masked gram A and attn_i from [S ; QK]
       if (!group_wait(S, B_SQ, ci & 1, 1, kPrepThreads)) break;
       fence_after_sync();
@@ -645,6 +655,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_async_smem();
       named_bar(1, kPrepThreads);
       if (pt == 0) mbar_arrive(saddr(&S.bars[B_T]));
+      // ---- while w and u are computed: the next chunk's decay tables (E2 of this chunk,
+      // the only reader of the decay matrix, is done)
+      if (ci + 1 < nch && !tables(ci + 1)) break;
       // ---- -w: lane i holds w[t][i] for every t; written as the MN-major tile [i][t]
       if (!group_wait(S, B_WU, ci & 1, 1, kPrepThreads)) break;
       fence_after_sync();
@@ -751,15 +764,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     };
     if (nch > 0) {
-      bool ok = warp_wait(S, B_L0, 0);
+      bool ok = warp_wait(S, B_L0, 0, true);
       if (ok) sq(0);
-      ok = ok && warp_wait(S, B_T, 0);
+      ok = ok && warp_wait(S, B_T, 0, true);
       if (ok) wu(0);
       for (int ci = 0; ok && ci < nch; ++ci) {
         const uint32_t kq = saddr(S.kq[ci & 1]);
         // delta^T (+)= h^T (-w)^T ;  o^T = h^T q_g^T
-        ok = warp_wait(S, B_WR, ci & 1) && warp_wait(S, B_HR, ci & 1) &&
-             (MODE != kEmit || warp_wait(S, B_QS, ci & 1));
+        ok = warp_wait(S, B_WR, ci & 1, true) && warp_wait(S, B_HR, ci & 1, true) &&
+             (MODE != kEmit || warp_wait(S, B_QS, ci & 1, true));
         if (!ok) break;
         fence_after_sync();
         if (leader) {
@@ -779,12 +792,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         // the next chunk's [S ; QK] as soon as its data is in (R_sq was read before T)
         if (ci + 1 < nch) {
-          ok = warp_wait(S, B_L0 + ((ci + 1) & 1), ((ci + 1) >> 1) & 1);
+          ok = warp_wait(S, B_L0 + ((ci + 1) & 1), ((ci + 1) >> 1) & 1, true);
           if (!ok) break;
           sq(ci + 1);
         }
         // o^T += delta^T attn_i^T ;  Dh^T = delta'^T K  (delta' as hi + lo)
-        ok = warp_wait(S, B_DR, ci & 1);
+        ok = warp_wait(S, B_DR, ci & 1, true);
         if (!ok) break;
         fence_after_sync();
         if (leader) {
@@ -803,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (ci + 1 < nch) {
-          ok = warp_wait(S, B_T, (ci + 1) & 1);
+          ok = warp_wait(S, B_T, (ci + 1) & 1, true);
           if (!ok) break;
           wu(ci + 1);
         }
