@@ -178,6 +178,19 @@ __device__ __forceinline__ bool mbar_test(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// One hardware-suspended wait for the phase with the given parity: the thread sleeps until the
+// phase completes or a system-dependent time limit passes (no issue slots are spent meanwhile).
+__device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded busy wait (no sleeps): for the one warp whose wake-up latency is on the critical
 // path.  Returns false after `limit` polls.
 __device__ __forceinline__ bool mbar_spin(uint32_t addr, uint32_t parity, uint32_t limit) {

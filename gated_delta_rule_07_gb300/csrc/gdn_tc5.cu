@@ -6,32 +6,33 @@
 // half of X = [M | U]).  Every contraction is a tcgen05.mma with fp32 accumulation in Tensor
 // Memory; products are taken in transposed form so that M = 128 (a state or feature index)
 // fills the 128 TMEM lanes:
-//   [S ; QK]  = [K ; Q] K^T                       (128 x 64, K = 128)
-//   w^T       = K^T (T diag(beta e^G))^T          (128 x 64, K = 64)
-//   u^T       = V^T (T diag(beta))^T              (128 x 64, K = 64)
-//   (K, Q, V stay bf16 as loaded; where they meet a computed operand, that operand is split
-//   into bf16 hi + lo parts, x = hi + lo to 2^-16, and the two products accumulate)
-//   delta^T   = u^T + h^T (-w)^T                  (128 x 64, K = 128; h^T read from TMEM)
-//   O1^T      = h^T Q^T                           (128 x 64, K = 128)
-//   O2^T      = delta^T attn_i^T                  (128 x 64, K = 64; delta^T from TMEM)
-//   Dh^T      = (diag(e^{G_last - G}) delta)^T K  (128 x 128, K = 64)
-// with Q pre-scaled to q_g = diag(e^G) Q after [S ; QK], so o = O1 + O2 accumulates in one
-// (double-buffered) TMEM region, and h <- gamma h + Dh.  The state h^T lives in registers
+//   [S ; QK]     = [K ; Q] K^T                          (128 x 64, K = 128; bf16 as loaded)
+//   w^T          = K^T (T diag(beta e^G))^T              (128 x 64, K = 64)
+//   u^T          = V^T (T diag(beta))^T                  (128 x 64, K = 64)
+//   [D | O1]^T   = h^T [-w ; q_g]^T                      (128 x 128, K = 128)
+//   O^T         += delta^T attn_i^T                      (128 x 64, K = 64)
+//   Dh^T         = (diag(e^{G_last - G}) delta)^T K      (128 x 128, K = 64)
+// with delta = u + D, q_g = diag(e^G) Q, o = O1 + O2 and h <- gamma h + Dh.  A tcgen05.mma
+// occupies the tensor pipe for about as long at N = 64 as at N = 128, so the two products that
+// share h^T are issued as one N = 128 product.  [S ; QK] reads K and Q as loaded (bf16); the
+// converter warps write K as fp16 (a separate, double-buffered tile), V as fp16 in place and
+// q_g^T as fp16, and every later product has fp16 operands.  The state h^T lives in registers
 // (fp32) of the chain warps; its fp16 copy, delta and delta' are written back into TMEM as the
-// A operands of the next products.  T = (I + A)^-1 is blocked by 16 x 16: the diagonal
-// inverses by fp32 forward substitution in registers, the off-diagonal blocks
-// T_ab = -T_aa sum_m A_am T_mb with warp-level mma.sync (fp16 operands, fp32 accumulation).
+// A operands of the next products.  T = (I + A)^-1 is blocked by 16 x 16: the diagonal inverses
+// by fp32 forward substitution in registers, the off-diagonal blocks
+// T_ab = -T_aa sum_m A_am T_mb with warp-level mma.sync.
 //
-// Warp roles (448 threads):
-//   warps 0-7  chain:   TMEM lane = state row c; warps w and w + 4 split the columns.  Besides
-//                       delta and the state update they build the next chunk's decay tables
-//                       and turn its q into fp16 q_g
-//   warps 8-11 prepare: masked gram and attn_i, the triangular solve, -w
-//   warp 12    MMA:     the whole warp waits, one thread issues every tcgen05.mma and commit
-//   warp 13    loader:  TMA boxes of K, Q, V and cp.async of g, beta into the free stage
-// Hand-offs use mbarriers; every wait is bounded and a wait that gives up records
-// GDN_ERR_DEVICE_TIMEOUT, and all roles leave their loops (group decisions are made uniform
-// with barrier reductions) so the CTA always reaches its TMEM release.
+// Warp roles (512 threads):
+//   warps 0-7   chain:     TMEM lane = state row c; warps w and w + 4 split the columns
+//   warps 8-11  prepare:   masked gram and attn_i, the triangular solve, -w; one chunk ahead
+//   warp 12     MMA:       waits for each product's inputs in a fixed order; lane 0 issues
+//   warp 13     loader:    TMA boxes of K, Q, V and cp.async of g, beta into the free stage
+//   warps 14-15 converter: decay tables, fp16 K and V, q_g^T
+// Hand-offs use mbarriers: a producing group arrives with every thread (the barrier counts the
+// group), a consumer waits with hardware-suspended try_wait (no issue slots spent).  Every wait
+// is bounded; one that gives up records GDN_ERR_DEVICE_TIMEOUT and the thread carries on, and
+// each role checks the record at one group-uniform point per chunk and leaves its loop, so the
+// CTA always reaches its TMEM release.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -52,56 +53,82 @@ using namespace warp_mma;
 
 constexpr int C = kChunk;  // 64
 constexpr int KD = 128, VD = 128;
-constexpr int kChainThreads = 256, kPrepThreads = 128;
-constexpr int kThreads = kChainThreads + kPrepThreads + 64;  // + MMA warp + loader warp
-constexpr uint32_t kWaitLimit = 1u << 24;  // polls of ~40-100 ns: a second or more
+constexpr int kChainThreads = 256, kPrepThreads = 128, kConvThreads = 64;
+constexpr int kThreads = kChainThreads + kPrepThreads + 64 + kConvThreads;
+constexpr long long kWaitCycles = 2000000000LL;  // about a second at GB300 clocks
 constexpr float kHalfMax = 65504.f;
 
 enum Mode { kEmit = 0, kSumM = 1, kSumU = 2 };
 
 // TMEM columns (512 allocated)
-constexpr uint32_t TM_SQ = 0;    // [S ; QK]          64 fp32
-constexpr uint32_t TM_W = 64;    // w^T               64 fp32
-constexpr uint32_t TM_U = 128;   // u^T -> delta^T    64 fp32, then fp16 delta / delta'
-constexpr uint32_t TM_O = 192;   // o^T, two buffers  2 x 64 fp32 (chunk parity)
-constexpr uint32_t TM_DL = 320;  // lo part of delta'  32 bf16 pairs
-constexpr uint32_t TM_H = 384;   // Dh^T              128 fp32, then fp16 h^T
+constexpr uint32_t TM_SQ = 0;    // [S ; QK]               64 fp32
+constexpr uint32_t TM_W = 64;    // w^T                    64 fp32
+constexpr uint32_t TM_U = 128;   // u^T, then fp16 delta'  64 fp32
+constexpr uint32_t TM_DO = 192;  // [D | O]^T: D, then fp16 delta, in 0-63; o^T in 64-127
+constexpr uint32_t TM_H = 320;   // Dh^T                   128 fp32, then fp16 h^T
 
-// mbarriers
-enum Bar { B_SQ = 0, B_T, B_WU, B_WR, B_HR, B_D, B_DR, B_H, B_L0, B_L1, B_QS, kNumBars };
+// mbarriers: who completes them
+enum Bar {
+  B_SQ = 0,    // [S ; QK] of a chunk is in TMEM                      MMA commit
+  B_E2,        // the gram has read it and the decay tables           prepare (128)
+  B_TB,        // decay tables of a chunk are in shared memory        converter (64)
+  B_CV,        // fp16 K, V and q_g^T of a chunk are ready            converter (64)
+  B_T,         // the T tiles are ready                               prepare (128)
+  B_WU,        // w^T, u^T are in TMEM                                MMA commit
+  B_WR,        // -w^T is in shared memory                            prepare (128)
+  B_HR,        // fp16 h^T is in TMEM and the previous o^T was read   chain (256)
+  B_D,         // [D | O1]^T is in TMEM                               MMA commit
+  B_DR,        // fp16 delta, delta' are in TMEM                      chain (256)
+  B_H,         // Dh^T and o^T are complete                           MMA commit
+  B_L0, B_L1,  // stage loaded: byte count plus 32 cp.async arrivals  loader
+  B_F0, B_F1,  // stage free (its chunk's w, u products are done)     MMA commit
+  B_KF0, B_KF1,  // fp16 K tile free (its chunk's Dh is done)         MMA commit
+  B_END,       // every product issued has completed                  MMA commit
+  kNumBars
+};
+__device__ __forceinline__ uint32_t bar_count(int b) {
+  return (b == B_E2 || b == B_T || b == B_WR)  ? (uint32_t)kPrepThreads
+         : (b == B_TB || b == B_CV)            ? (uint32_t)kConvThreads
+         : (b == B_HR || b == B_DR)            ? (uint32_t)kChainThreads
+         : (b == B_L0 || b == B_L1)            ? 33u
+                                               : 1u;
+}
 
 struct Smem {
-  uint8_t kq[2][2 * 128 * 128];  // per stage: [kblk][128 rows: K 0-63, Q 64-127][128 B]
-  uint8_t v[2][2 * 64 * 128];    // per stage: [kblk][64 rows][128 B]
-  uint8_t att[2][64 * 128];      // attn_i [t][s], K-major B
-  uint8_t twh[64 * 128];         // T diag(beta e^G) [t][s], K-major B, bf16 hi part
-  uint8_t twl[64 * 128];         //   ... and lo part
-  uint8_t tuh[64 * 128];         // T diag(beta) [t][s], K-major B, bf16 hi part
-  uint8_t tul[64 * 128];         //   ... and lo part
-  uint8_t nw[128 * 128];         // -w [i][t], MN-major B
+  uint8_t kq[2][2 * 128 * 128];  // per stage: [kblk][K rows 0-63 | Q rows 64-127][128 B], bf16
+  uint8_t v[2][2 * 64 * 128];    // per stage: [kblk][64 rows][128 B]; V -> fp16 in place
+  uint8_t kh[2][2 * 64 * 128];   // fp16 K: [kblk][64 rows][128 B] (chunk parity)
+  uint8_t att[2][64 * 128];      // attn_i [t][s] fp16, K-major B (chunk parity)
+  uint8_t tw[64 * 128];          // T diag(beta e^G) [t][s] fp16, K-major B
+  uint8_t tu[64 * 128];          // T diag(beta) [t][s] fp16, K-major B
+  uint8_t nwq[2][128 * 128];     // MN-major B of [D | O1]: -w^T [i][t], then q_g^T [i][t]
   uint8_t ah[64 * 128];          // masked gram A [t][s], fp16
   uint8_t th[64 * 128];          // blocks of (I + A)^-1 [t][s], fp16 operands
   uint8_t xs[4][16 * 48];        // per-warp 16 x 16 fp16 scratch, 48-byte rows
   float adiag[C][16];            // the diagonal 16 x 16 blocks of A, fp32
   float gst[2][2][C];            // g and beta of a staged chunk
-  float G[3][C], eG[3][C], eGLG[3][C], beta[3][C], gamma[3];
-  alignas(16) float dec[C * C];  // e^{G_t - G_s} for s <= t, else 0; 16-byte chunks swizzled
-  float qsc[C];                  // e^{G_t} of the chunk whose q the chain warps scale
+  float G[3][C], eG[3][C], eGLG[3][C], beta[3][C], gamma[4];
+  // decay e^{G_t - G_s} (s <= t) of the chunk the gram reads next: on the 16-block of t it is
+  // ddiag[t][s & 15]; for s in an earlier block b it is rf[t][b] * cf[s], with
+  // rf = e^{G_t - G_e}, cf = e^{G_e - G_s} and e the last row of block b (both <= 1 for g <= 0)
+  alignas(16) float ddiag[C][16];
+  alignas(16) float rf[C][4];
+  alignas(16) float cf[C];
   uint64_t bars[kNumBars];
   uint32_t tmem_base;
   int abort_flag;
   int range_bad;
 };
 
-// Members read or written with 16-byte vector accesses, ldmatrix or the tensor core must sit on
-// 16-byte (swizzled tiles: 1024-byte) boundaries of the 1024-aligned base.
+// Members read or written with 16-byte vector accesses, ldmatrix / stmatrix or the tensor core
+// must sit on 16-byte (swizzled tiles: 1024-byte) boundaries of the 1024-aligned base.
 static_assert(offsetof(Smem, kq) % 1024 == 0 && offsetof(Smem, v) % 1024 == 0, "tile alignment");
-static_assert(offsetof(Smem, att) % 1024 == 0 && offsetof(Smem, twh) % 1024 == 0, "tile alignment");
-static_assert(offsetof(Smem, twl) % 1024 == 0 && offsetof(Smem, tuh) % 1024 == 0, "tile alignment");
-static_assert(offsetof(Smem, tul) % 1024 == 0 && offsetof(Smem, nw) % 1024 == 0, "tile alignment");
-static_assert(offsetof(Smem, ah) % 1024 == 0 && offsetof(Smem, th) % 1024 == 0, "tile alignment");
-static_assert(offsetof(Smem, xs) % 16 == 0 && offsetof(Smem, dec) % 16 == 0, "vector alignment");
-static_assert(offsetof(Smem, bars) % 8 == 0, "mbarrier alignment");
+static_assert(offsetof(Smem, kh) % 1024 == 0 && offsetof(Smem, att) % 1024 == 0, "tile alignment");
+static_assert(offsetof(Smem, tw) % 1024 == 0 && offsetof(Smem, tu) % 1024 == 0, "tile alignment");
+static_assert(offsetof(Smem, nwq) % 1024 == 0 && offsetof(Smem, ah) % 1024 == 0, "tile alignment");
+static_assert(offsetof(Smem, th) % 1024 == 0 && offsetof(Smem, xs) % 16 == 0, "tile alignment");
+static_assert(offsetof(Smem, ddiag) % 16 == 0 && offsetof(Smem, rf) % 16 == 0, "vector alignment");
+static_assert(offsetof(Smem, cf) % 16 == 0 && offsetof(Smem, bars) % 8 == 0, "alignment");
 static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory per block");
 
 // ------------------------------------------------------------------ small helpers
@@ -123,55 +150,38 @@ __device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
       : "memory");
   return r != 0;
 }
-// Group-uniform bounded wait: every thread polls, then the group agrees.
 __device__ __forceinline__ bool aborted(Smem& S) {
   return *reinterpret_cast<volatile int*>(&S.abort_flag) != 0;
 }
 __device__ __forceinline__ void set_abort(Smem& S) {
   *reinterpret_cast<volatile int*>(&S.abort_flag) = 1;
 }
-__device__ __forceinline__ bool group_wait(Smem& S, int bar, uint32_t parity, int id, int n) {
-  bool ok = !aborted(S) && mbar_wait(saddr(&S.bars[bar]), parity, kWaitLimit);
-  ok = named_bar_and(id, n, ok);
-  if (!ok) set_abort(S);
-  return ok;
+// Bounded wait for the phase with the given parity, suspended in hardware between tries.  On
+// giving up (about a second, or at once when another thread already gave up) it records the
+// abort flag; the caller carries on and leaves at its next group-uniform check.
+__device__ __forceinline__ void wait_bar(Smem& S, int bar, uint32_t parity) {
+  const uint32_t a = saddr(&S.bars[bar]);
+  if (mbar_try(a, parity)) return;
+  const long long t_end = clock64() + kWaitCycles;
+  while (!mbar_try(a, parity)) {
+    if (clock64() > t_end || aborted(S)) {
+      set_abort(S);
+      return;
+    }
+  }
 }
-// Warp-uniform bounded wait; `spin` busy-polls (for the MMA warp, whose wake-up delays every
-// product behind it).
-__device__ __forceinline__ bool warp_wait(Smem& S, int bar, uint32_t parity, bool spin = false) {
-  bool ok = !aborted(S) && (spin ? mbar_spin(saddr(&S.bars[bar]), parity, 1u << 28)
-                                 : mbar_wait(saddr(&S.bars[bar]), parity, kWaitLimit));
-  ok = __all_sync(0xffffffffu, ok);
-  if (!ok) set_abort(S);
-  return ok;
-}
+__device__ __forceinline__ void arrive(Smem& S, int bar) { mbar_arrive(saddr(&S.bars[bar])); }
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
 __device__ __forceinline__ bool fits_half(float x) { return fabsf(x) <= kHalfMax; }
 
-// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): products with a bf16 operand keep ~16 bits.
-__device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-__device__ __forceinline__ void st_hilo(uint8_t* hi_tile, uint8_t* lo_tile, int r, int c,
-                                        float x) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(x);
-  const uint32_t off = sw128_offset(64, r, c);
-  *reinterpret_cast<__nv_bfloat16*>(hi_tile + off) = h;
-  *reinterpret_cast<__nv_bfloat16*>(lo_tile + off) = __float2bfloat16_rn(x - __bfloat162float(h));
-}
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  const int n = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
-}
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
   const int n = valid ? 4 : 0;
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(n));
@@ -193,30 +203,28 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
       "r"(bytes)
       : "memory");
 }
-
-// Position of element (t, s) of the 64 x 64 fp32 decay matrix: 16-byte chunks of a row are
-// XOR-permuted by (t & 15) so that a warp reading 32 rows at one column is conflict-free.
-__device__ __forceinline__ int dec_idx(int t, int s) {
-  return t * 64 + ((((s >> 2) ^ (t & 15))) << 2) + (s & 3);
+__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(addr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
 }
 
 __device__ __forceinline__ void st_half(uint8_t* tile, int r, int c, float x) {
   *reinterpret_cast<__half*>(tile + sw128_offset(64, r, c)) = __float2half_rn(x);
 }
 
-// In-place bf16 -> fp16 of one 16-byte chunk; false when a value leaves the fp16 range.
-__device__ __forceinline__ bool to_half_chunk(uint8_t* p) {
-  uint4 x = *reinterpret_cast<uint4*>(p);
+// bf16 -> fp16 of one 16-byte chunk (src and dst may coincide); returns the largest magnitude.
+__device__ __forceinline__ float to_half_chunk(const uint8_t* src, uint8_t* dst, float m) {
+  uint4 x = *reinterpret_cast<const uint4*>(src);
   uint32_t* w = reinterpret_cast<uint32_t*>(&x);
-  bool ok = true;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[i]));
-    ok = ok && fits_half(f.x) && fits_half(f.y);
+    m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
     w[i] = pack_h2(f.x, f.y);
   }
-  *reinterpret_cast<uint4*>(p) = x;
-  return ok;
+  *reinterpret_cast<uint4*>(dst) = x;
+  return m;
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -241,8 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- setup: mbarriers, TMEM
   if (tid == 0) {
-    for (int b = 0; b < kNumBars; ++b)  // loads: the byte count plus 32 cp.async arrivals
-      mbar_init(saddr(&S.bars[b]), (b == B_L0 || b == B_L1) ? 33 : 1);
+    for (int b = 0; b < kNumBars; ++b) mbar_init(saddr(&S.bars[b]), bar_count(b));
     S.abort_flag = 0;
     S.range_bad = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -282,114 +289,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         h[q] = x;
       }
     }
-    auto publish_h = [&]() {  // fp16 h^T into TMEM (the A operand of delta and O1)
+    // fp16 h^T into TMEM (the A operand of [D | O1]).  Not range-checked: an infinite h^T
+    // makes delta infinite or NaN, and delta is checked.
+    auto publish_h = [&]() {
 #pragma unroll
       for (int piece = 0; piece < 4; ++piece) {
         uint32_t p[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float x0 = h[16 * piece + 2 * q], x1 = h[16 * piece + 2 * q + 1];
-          range_ok = range_ok && fits_half(x0) && fits_half(x1);
-          p[q] = pack_h2(x0, x1);
-        }
+        for (int q = 0; q < 8; ++q) p[q] = pack_h2(h[16 * piece + 2 * q], h[16 * piece + 2 * q + 1]);
         tmem_st8(tm + lane_bits + TM_H + 64 * hf + 8 * piece, p);
       }
     };
-    // q (bf16) -> q_g = e^{G_t} q (fp16) of chunk ci, in place, after [S ; QK] has read q
-    auto scale_q = [&](int ci) -> bool {
-      const int sg = ci & 1;
-      if (!group_wait(S, B_SQ, ci & 1, 2, kChainThreads)) return false;
-      if (warp == 0) {  // e^{G_t} of chunk ci from its staged g (rows past the end are 0)
-        float x0 = S.gst[sg][0][lane], x1 = S.gst[sg][0][lane + 32];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
-          const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
-          if (lane >= o) { x0 += y0; x1 += y1; }
-        }
-        x1 += __shfl_sync(0xffffffffu, x0, 31);
-        S.qsc[lane] = __expf(x0);
-        S.qsc[lane + 32] = __expf(x1);
-      }
-      named_bar(2, kChainThreads);
-      {
-        const int t = tid >> 2, c0q = 4 * (tid & 3);  // row t, four 16-byte chunks
-        const float sc = S.qsc[t];
-        uint4* pq[4];
-        uint4 x[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          pq[u] = reinterpret_cast<uint4*>(S.kq[sg] + sw128_offset(128, 64 + t, 8 * (c0q + u)));
-          x[u] = *pq[u];
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint32_t* w = reinterpret_cast<uint32_t*>(&x[u]);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[i]));
-            range_ok = range_ok && fits_half(f.x * sc) && fits_half(f.y * sc);
-            w[i] = pack_h2(f.x * sc, f.y * sc);
-          }
-          *pq[u] = x[u];
-        }
-      }
-      fence_async_smem();
-      named_bar(2, kChainThreads);
-      if (tid == 0) mbar_arrive(saddr(&S.bars[B_QS]));
-      return true;
-    };
-    bool go = nch > 0;
-    if (go && MODE == kEmit) go = scale_q(0);
-    if (go) {
+    if (nch > 0) {
       publish_h();
       fence_before_sync();
-      named_bar(2, kChainThreads);
-      if (tid == 0) mbar_arrive(saddr(&S.bars[B_HR]));
+      arrive(S, B_HR);
     }
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-    for (int ci = 0; go && ci < nch; ++ci) {
+    for (int ci = 0; ci < nch; ++ci) {
       const int gb = ci % 3;
       const int64_t t0 = sb + (c0 + ci) * C;
       const int L = (int)((se - t0) < C ? (se - t0) : C);
-      // ---- delta: fp32 delta^T -> fp16 delta and delta' (= e^{G_last - G_t} delta)
-      if (!group_wait(S, B_D, ci & 1, 2, kChainThreads)) break;
+      // ---- delta = u + D -> fp16 delta (into D's columns) and delta' (into u's columns)
+      wait_bar(S, B_D, ci & 1);
       fence_after_sync();
-      {
-        // read both 16-column pieces before writing: the packed results overwrite them
-        float d0[16], d1[16];
-        tmem_ld16(tm + lane_bits + TM_U + 32 * hf, d0);
-        tmem_ld16(tm + lane_bits + TM_U + 32 * hf + 16, d1);
-        {
-          uint32_t pd[16];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            range_ok = range_ok && fits_half(d0[2 * q]) && fits_half(d0[2 * q + 1]) &&
-                       fits_half(d1[2 * q]) && fits_half(d1[2 * q + 1]);
-            pd[q] = pack_h2(d0[2 * q], d0[2 * q + 1]);
-            pd[q + 8] = pack_h2(d1[2 * q], d1[2 * q + 1]);
-          }
-          tmem_st16(tm + lane_bits + TM_U + 32 * hf, pd);
-        }
-        {  // delta' = e^{G_last - G_t} delta as bf16 hi + lo (it meets bf16 K)
-          uint32_t ph[16], pl[16];
+      for (int piece = 0; piece < 2; ++piece) {
+        float d[16];
+        tmem_ld16(tm + lane_bits + TM_DO + 32 * hf + 16 * piece, d);
+        if (MODE != kSumM) {
+          float u[16];
+          tmem_ld16(tm + lane_bits + TM_U + 32 * hf + 16 * piece, u);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int t = 32 * hf + 2 * q;
-            split_bf16(d0[2 * q] * S.eGLG[gb][t], d0[2 * q + 1] * S.eGLG[gb][t + 1], ph[q], pl[q]);
-            split_bf16(d1[2 * q] * S.eGLG[gb][t + 16], d1[2 * q + 1] * S.eGLG[gb][t + 17],
-                       ph[q + 8], pl[q + 8]);
-          }
-          tmem_st16(tm + lane_bits + TM_U + 32 * hf + 16, ph);
-          tmem_st16(tm + lane_bits + TM_DL + 16 * hf, pl);
+          for (int q = 0; q < 16; ++q) d[q] += u[q];
         }
+        uint32_t pd[8], pp[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int t = 32 * hf + 16 * piece + 2 * q;
+          range_ok = range_ok && fits_half(d[2 * q]) && fits_half(d[2 * q + 1]);
+          pd[q] = pack_h2(d[2 * q], d[2 * q + 1]);
+          pp[q] = pack_h2(d[2 * q] * S.eGLG[gb][t], d[2 * q + 1] * S.eGLG[gb][t + 1]);
+        }
+        if (MODE == kEmit) tmem_st8(tm + lane_bits + TM_DO + 32 * hf + 8 * piece, pd);
+        tmem_st8(tm + lane_bits + TM_U + 32 * hf + 8 * piece, pp);
       }
       fence_before_sync();
-      named_bar(2, kChainThreads);
-      if (tid == 0) mbar_arrive(saddr(&S.bars[B_DR]));
+      arrive(S, B_DR);
 
-      // ---- the state update first (it gates the next chunk), the outputs after it
-      if (!group_wait(S, B_H, ci & 1, 2, kChainThreads)) break;
+      // ---- the state update; its fp16 copy and the read of o^T before the hand-off
+      wait_bar(S, B_H, ci & 1);
       fence_after_sync();
       {
         const float gam = S.gamma[gb];
@@ -402,23 +351,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (ci + 1 < nch) publish_h();
-      fence_before_sync();
-      named_bar(2, kChainThreads);
-      if (tid == 0 && ci + 1 < nch) mbar_arrive(saddr(&S.bars[B_HR]));
+      uint32_t ob[16];
       if (MODE == kEmit) {
-        // o^T buffer ci & 1 is rewritten only after the next chunk's state hand-off
 #pragma unroll
         for (int piece = 0; piece < 2; ++piece) {
           float o[16];
-          tmem_ld16(tm + lane_bits + TM_O + 64 * (ci & 1) + 32 * hf + 16 * piece, o);
+          tmem_ld16(tm + lane_bits + TM_DO + 64 + 32 * hf + 16 * piece, o);
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const int t = 32 * hf + 16 * piece + q;
-            if (t < L) out[((t0 + t) * a.hv + j) * VD + c] = __float2bfloat16_rn(o[q]);
-          }
+          for (int q = 0; q < 8; ++q) ob[8 * piece + q] = pack_bf2(o[2 * q], o[2 * q + 1]);
         }
       }
-      if (MODE == kEmit && ci + 1 < nch && !scale_q(ci + 1)) break;
+      fence_before_sync();
+      if (ci + 1 < nch) arrive(S, B_HR);
+      if (MODE == kEmit) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int t = 32 * hf + 2 * q;
+          const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&ob[q]);
+          if (t < L) out[((t0 + t) * a.hv + j) * VD + c] = p2.x;
+          if (t + 1 < L) out[((t0 + t + 1) * a.hv + j) * VD + c] = p2.y;
+        }
+      }
+      if (!named_bar_and(2, kChainThreads, !aborted(S))) break;
     }
     if (!range_ok) S.range_bad = 1;
     // ---- the final state: h^T[c][i] = h[i][c]
@@ -440,64 +394,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wb = warp - 8;                  // 0..3: this warp's 16-row block of T
     const uint32_t lane_bits = (uint32_t)((warp & 3) * 32) << 16;
     const int g8 = lane >> 2, q4 = lane & 3;
-    bool range_ok = true;
-    const __nv_bfloat16* gq = static_cast<const __nv_bfloat16*>(a.q);
-    const __nv_bfloat16* gk = static_cast<const __nv_bfloat16*>(a.k);
-    const __nv_bfloat16* gv = static_cast<const __nv_bfloat16*>(a.v);
     const uint32_t ah_s = saddr(S.ah), th_s = saddr(S.th), xs_s = saddr(S.xs[wb]);
 
     // the strictly upper blocks of T diag(.) are zero for every chunk
     for (int e = pt; e < 64 * 128 / 16; e += kPrepThreads) {
-      reinterpret_cast<uint4*>(S.twh)[e] = make_uint4(0u, 0u, 0u, 0u);
-      reinterpret_cast<uint4*>(S.twl)[e] = make_uint4(0u, 0u, 0u, 0u);
-      reinterpret_cast<uint4*>(S.tuh)[e] = make_uint4(0u, 0u, 0u, 0u);
-      reinterpret_cast<uint4*>(S.tul)[e] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(S.tw)[e] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(S.tu)[e] = make_uint4(0u, 0u, 0u, 0u);
     }
 
-    // decay tables and the decay matrix of chunk ci (g, beta staged by the loader)
-    auto tables = [&](int ci) -> bool {
-      const int sg = ci & 1, gb = ci % 3;
-      const int64_t t0 = sb + (c0 + ci) * C;
-      const int L = (int)((se - t0) < C ? (se - t0) : C);
-      if (!group_wait(S, B_L0 + sg, (ci >> 1) & 1, 1, kPrepThreads)) return false;
-      if (pt < 32) {  // within-chunk inclusive scan of g; rows >= L decay by nothing
-        float x0 = S.gst[sg][0][pt], x1 = S.gst[sg][0][pt + 32];
+    // ---- masked gram A (fp16 tile + fp32 diagonal blocks) and attn_i from [S ; QK]
+    auto gram = [&](int ci) {
+      const int gb = ci % 3;
+      wait_bar(S, B_SQ, ci & 1);
+      wait_bar(S, B_TB, ci & 1);
+      fence_after_sync();
+      const bool is_s = pt < 64;
+      const int t = pt & 63, at = t >> 4;
+      const float bt = is_s ? S.beta[gb][t] : 1.f;
+      const float4 rf4 = *reinterpret_cast<const float4*>(&S.rf[t][0]);
+      float dd[16];
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
-          const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
-          if (pt >= o) { x0 += y0; x1 += y1; }
-        }
-        x1 += __shfl_sync(0xffffffffu, x0, 31);
-        const float GL = L - 1 < 32 ? __shfl_sync(0xffffffffu, x0, (L - 1) & 31)
-                                    : __shfl_sync(0xffffffffu, x1, (L - 1) & 31);
-        S.G[gb][pt] = x0;
-        S.G[gb][pt + 32] = x1;
-        S.eG[gb][pt] = __expf(x0);
-        S.eG[gb][pt + 32] = __expf(x1);
-        S.eGLG[gb][pt] = __expf(GL - x0);
-        S.eGLG[gb][pt + 32] = __expf(GL - x1);
-        S.beta[gb][pt] = S.gst[sg][1][pt];
-        S.beta[gb][pt + 32] = S.gst[sg][1][pt + 32];
-        if (pt == 0) S.gamma[gb] = __expf(GL);
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 x = *reinterpret_cast<const float4*>(&S.ddiag[t][4 * k4]);
+        dd[4 * k4] = x.x; dd[4 * k4 + 1] = x.y; dd[4 * k4 + 2] = x.z; dd[4 * k4 + 3] = x.w;
       }
-      named_bar(1, kPrepThreads);
-      {  // the decay matrix: row t, columns 32 (pt >> 6) .. + 31
-        const int t = pt & 63, s0 = 32 * (pt >> 6);
-        const float Gt = S.G[gb][t];
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        float sv[32];
+        tmem_ld32(tm + lane_bits + TM_SQ + 32 * hb, sv);
 #pragma unroll
         for (int c4 = 0; c4 < 32; c4 += 4) {
-          float4 d;
-          const int s1 = s0 + c4;
-          d.x = s1 <= t ? __expf(Gt - S.G[gb][s1]) : 0.f;
-          d.y = s1 + 1 <= t ? __expf(Gt - S.G[gb][s1 + 1]) : 0.f;
-          d.z = s1 + 2 <= t ? __expf(Gt - S.G[gb][s1 + 2]) : 0.f;
-          d.w = s1 + 3 <= t ? __expf(Gt - S.G[gb][s1 + 3]) : 0.f;
-          *reinterpret_cast<float4*>(&S.dec[dec_idx(t, s1)]) = d;
+          const int s1 = 32 * hb + c4, b2 = s1 >> 4, k = s1 & 15;
+          const float4 cf4 = *reinterpret_cast<const float4*>(&S.cf[s1]);
+          const float f = b2 == 0 ? rf4.x : b2 == 1 ? rf4.y : rf4.z;
+          const bool below = b2 < at, diag = b2 == at;
+          const float dx = below ? f * cf4.x : (diag ? dd[k + 0] : 0.f);
+          const float dy = below ? f * cf4.y : (diag ? dd[k + 1] : 0.f);
+          const float dz = below ? f * cf4.z : (diag ? dd[k + 2] : 0.f);
+          const float dw = below ? f * cf4.w : (diag ? dd[k + 3] : 0.f);
+          // A keeps s < t (times beta_t); attn_i keeps s <= t (the decay is 0 above)
+          sv[c4 + 0] *= bt * (is_s && s1 + 0 == t ? 0.f : dx);
+          sv[c4 + 1] *= bt * (is_s && s1 + 1 == t ? 0.f : dy);
+          sv[c4 + 2] *= bt * (is_s && s1 + 2 == t ? 0.f : dz);
+          sv[c4 + 3] *= bt * (is_s && s1 + 3 == t ? 0.f : dw);
+        }
+        if (is_s) {
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            if (((32 * hb + q) >> 4) == at) S.adiag[t][q & 15] = sv[q];
+        }
+        if (is_s || MODE == kEmit) {
+          uint8_t* dst = is_s ? S.ah : S.att[ci & 1];
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint4 pk;
+            pk.x = pack_h2(sv[8 * ch + 0], sv[8 * ch + 1]);
+            pk.y = pack_h2(sv[8 * ch + 2], sv[8 * ch + 3]);
+            pk.z = pack_h2(sv[8 * ch + 4], sv[8 * ch + 5]);
+            pk.w = pack_h2(sv[8 * ch + 6], sv[8 * ch + 7]);
+            *reinterpret_cast<uint4*>(dst + sw128_offset(64, t, 32 * hb + 8 * ch)) = pk;
+          }
         }
       }
-      named_bar(1, kPrepThreads);
-      return true;
+      if (MODE == kEmit && !is_s) fence_async_smem();  // attn_i feeds the tensor core
+      fence_before_sync();
+      arrive(S, B_E2);
     };
 
     // T_ab = -T_aa sum_{m=b}^{a-1} A_am T_mb for one 16 x 16 block, by one warp: the sum on
@@ -539,66 +500,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float w0 = u0 * S.eG[gb][col], w1 = u1 * S.eG[gb][col + 1];
           const uint32_t off = sw128_offset(64, row, col);
           *reinterpret_cast<uint32_t*>(S.th + off) = pack_h2(v0, v1);
-          uint32_t hi, lo;
-          split_bf16(v0 * w0, v1 * w1, hi, lo);
-          *reinterpret_cast<uint32_t*>(S.twh + off) = hi;
-          *reinterpret_cast<uint32_t*>(S.twl + off) = lo;
-          split_bf16(v0 * u0, v1 * u1, hi, lo);
-          *reinterpret_cast<uint32_t*>(S.tuh + off) = hi;
-          *reinterpret_cast<uint32_t*>(S.tul + off) = lo;
-          range_ok = range_ok && fits_half(v0) && fits_half(v1);
+          *reinterpret_cast<uint32_t*>(S.tw + off) = pack_h2(v0 * w0, v1 * w1);
+          *reinterpret_cast<uint32_t*>(S.tu + off) = pack_h2(v0 * u0, v1 * u1);
         }
     };
 
-    for (int ci = 0; ci < nch; ++ci) {
+    // ---- T = (I + A)^-1 and the two scaled copies the w / u products read.  T, w and h^T are
+    // not range-checked: an infinite fp16 value there makes delta infinite or NaN.
+    auto solve = [&](int ci) {
       const int gb = ci % 3;
-      if (ci == 0 && !tables(0)) break;
-      // ---- masked gram A and attn_i from [S ; QK]
-      if (!group_wait(S, B_SQ, ci & 1, 1, kPrepThreads)) break;
-      fence_after_sync();
-      {
-        const bool is_s = pt < 64;
-        const int t = pt & 63, ab = t >> 4;
-        const float bt = is_s ? S.beta[gb][t] : 1.f;
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-          float sv[32];
-          tmem_ld32(tm + lane_bits + TM_SQ + 32 * hb, sv);
-#pragma unroll
-          for (int c4 = 0; c4 < 32; c4 += 4) {
-            const int s1 = 32 * hb + c4;
-            const float4 d = *reinterpret_cast<const float4*>(&S.dec[dec_idx(t, s1)]);
-            // A keeps s < t (times beta_t); attn_i keeps s <= t (the matrix is 0 above)
-            sv[c4 + 0] *= bt * (is_s && s1 + 0 == t ? 0.f : d.x);
-            sv[c4 + 1] *= bt * (is_s && s1 + 1 == t ? 0.f : d.y);
-            sv[c4 + 2] *= bt * (is_s && s1 + 2 == t ? 0.f : d.z);
-            sv[c4 + 3] *= bt * (is_s && s1 + 3 == t ? 0.f : d.w);
-          }
-          if (is_s) {
-#pragma unroll
-            for (int q = 0; q < 32; ++q)
-              if (((32 * hb + q) >> 4) == ab) S.adiag[t][q & 15] = sv[q];
-          }
-          if (is_s || MODE == kEmit) {
-            uint8_t* dst = is_s ? S.ah : S.att[ci & 1];
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-              uint4 pk;
-              pk.x = pack_h2(sv[8 * ch + 0], sv[8 * ch + 1]);
-              pk.y = pack_h2(sv[8 * ch + 2], sv[8 * ch + 3]);
-              pk.z = pack_h2(sv[8 * ch + 4], sv[8 * ch + 5]);
-              pk.w = pack_h2(sv[8 * ch + 6], sv[8 * ch + 7]);
-              *reinterpret_cast<uint4*>(dst + sw128_offset(64, t, 32 * hb + 8 * ch)) = pk;
-            }
-          }
-        }
-        if (MODE == kEmit && !is_s) fence_async_smem();  // attn_i feeds the tensor core
-      }
-      fence_before_sync();
-      named_bar(1, kPrepThreads);
-      // ---- T = (I + A)^-1.  Diagonal block wb by forward substitution in registers:
-      // lane (c, rh) holds rows 8 rh .. 8 rh + 7 of column c of the block inverse.
-      {
+      {  // diagonal block wb by forward substitution in registers: lane (c, rh) holds rows
+         // 8 rh .. 8 rh + 7 of column c of the block inverse
         const int c = lane & 15, rh = lane >> 4;
         const float* Ab = &S.adiag[16 * wb][0];
         float tc[8];
@@ -642,8 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k2 = 0; k2 < 8; ++k2) {
           const int row = 16 * wb + 8 * rh + k2;
           st_half(S.th, row, col, tc[k2]);
-          st_hilo(S.twh, S.twl, row, col, tc[k2] * w);
-          st_hilo(S.tuh, S.tul, row, col, tc[k2] * u);
+          st_half(S.tw, row, col, tc[k2] * w);
+          st_half(S.tu, row, col, tc[k2] * u);
         }
       }
       named_bar(1, kPrepThreads);
@@ -653,45 +565,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar(1, kPrepThreads);
       if (wb == 0) off_diag_block(3, 0, gb);
       fence_async_smem();
-      named_bar(1, kPrepThreads);
-      if (pt == 0) mbar_arrive(saddr(&S.bars[B_T]));
-      // ---- while w and u are computed: the next chunk's decay tables (E2 of this chunk,
-      // the only reader of the decay matrix, is done)
-      if (ci + 1 < nch && !tables(ci + 1)) break;
-      // ---- -w: lane i holds w[t][i] for every t; written as the MN-major tile [i][t]
-      if (!group_wait(S, B_WU, ci & 1, 1, kPrepThreads)) break;
+      arrive(S, B_T);
+      named_bar(1, kPrepThreads);  // the next gram rewrites A
+    };
+
+    // ---- -w: lane i holds w[t][i] for every t; written as the MN-major tile [i][t]
+    auto neg_w = [&](int ci) {
+      wait_bar(S, B_WU, ci & 1);
       fence_after_sync();
-      {
-        const int i = pt;
+      const int i = pt;
 #pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-          float wv[32];
-          tmem_ld32(tm + lane_bits + TM_W + 32 * hb, wv);
+      for (int hb = 0; hb < 2; ++hb) {
+        float wv[32];
+        tmem_ld32(tm + lane_bits + TM_W + 32 * hb, wv);
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint4 pk;
-            pk.x = pack_h2(-wv[8 * ch + 0], -wv[8 * ch + 1]);
-            pk.y = pack_h2(-wv[8 * ch + 2], -wv[8 * ch + 3]);
-            pk.z = pack_h2(-wv[8 * ch + 4], -wv[8 * ch + 5]);
-            pk.w = pack_h2(-wv[8 * ch + 6], -wv[8 * ch + 7]);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) range_ok = range_ok && fits_half(wv[8 * ch + q]);
-            *reinterpret_cast<uint4*>(S.nw + sw128_offset(128, i, 32 * hb + 8 * ch)) = pk;
-          }
+        for (int ch = 0; ch < 4; ++ch) {
+          uint4 pk;
+          pk.x = pack_h2(-wv[8 * ch + 0], -wv[8 * ch + 1]);
+          pk.y = pack_h2(-wv[8 * ch + 2], -wv[8 * ch + 3]);
+          pk.z = pack_h2(-wv[8 * ch + 4], -wv[8 * ch + 5]);
+          pk.w = pack_h2(-wv[8 * ch + 6], -wv[8 * ch + 7]);
+          *reinterpret_cast<uint4*>(S.nwq[0] + sw128_offset(128, i, 32 * hb + 8 * ch)) = pk;
         }
       }
       fence_async_smem();
       fence_before_sync();
-      named_bar(1, kPrepThreads);
-      if (pt == 0) mbar_arrive(saddr(&S.bars[B_WR]));
+      arrive(S, B_WR);
+    };
+
+    // one chunk ahead: the gram of chunk ci + 1 is built while w of chunk ci is computed
+    bool go = nch > 0;
+    if (go) {
+      gram(0);
+      go = named_bar_and(1, kPrepThreads, !aborted(S));
     }
-    if (!range_ok) S.range_bad = 1;
+    for (int ci = 0; go && ci < nch; ++ci) {
+      solve(ci);
+      if (ci + 1 < nch) gram(ci + 1);
+      neg_w(ci);
+      go = named_bar_and(1, kPrepThreads, !aborted(S));  // also: the gram's A is complete
+    }
   } else if (warp == 13) {
     // =============================================================== loader (1 warp)
     for (int ci = 0; ci < nch; ++ci) {
       const int sg = ci & 1;
-      // the stage was last used by chunk ci - 2: wait for its last MMA
-      if (ci >= 2 && !warp_wait(S, B_H, (ci - 2) & 1)) break;
+      // the stage was last used by chunk ci - 2: wait for its w, u products
+      if (ci >= 2) wait_bar(S, B_F0 + sg, ((ci >> 1) + 1) & 1);
+      if (__any_sync(0xffffffffu, aborted(S))) break;
       const int64_t t0 = sb + (c0 + ci) * C;
       const int L = (int)((se - t0) < C ? (se - t0) : C);
       const uint32_t bar = saddr(&S.bars[B_L0 + sg]);
@@ -719,15 +639,129 @@ __global__ void __launch_bounds__(kThreads, 1)
                    : "memory");
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
+  } else if (warp >= 14) {
+    // =============================================================== converter (64 threads)
+    const int p = tid - (kThreads - kConvThreads);  // 0..63
+    float maxabs = 0.f;
+    for (int ci = 0; ci < nch; ++ci) {
+      const int sg = ci & 1, gb = ci % 3;
+      const int64_t t0 = sb + (c0 + ci) * C;
+      const int L = (int)((se - t0) < C ? (se - t0) : C);
+      wait_bar(S, B_L0 + sg, (ci >> 1) & 1);
+      // the decay tables are single: the previous chunk's gram must be done with them
+      if (ci >= 1) wait_bar(S, B_E2, (ci - 1) & 1);
+      if (p < 32) {  // within-chunk inclusive scan of g; rows >= L decay by nothing
+        float x0 = S.gst[sg][0][p], x1 = S.gst[sg][0][p + 32];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y0 = __shfl_up_sync(0xffffffffu, x0, o);
+          const float y1 = __shfl_up_sync(0xffffffffu, x1, o);
+          if (p >= o) { x0 += y0; x1 += y1; }
+        }
+        x1 += __shfl_sync(0xffffffffu, x0, 31);
+        const float GL = L - 1 < 32 ? __shfl_sync(0xffffffffu, x0, (L - 1) & 31)
+                                    : __shfl_sync(0xffffffffu, x1, (L - 1) & 31);
+        // G at the last row of this lane's 16-block: rows p | 15 and (p | 15) + 32
+        const float e0 = __shfl_sync(0xffffffffu, x0, p | 15);
+        const float e1 = __shfl_sync(0xffffffffu, x1, p | 15);
+        S.G[gb][p] = x0;
+        S.G[gb][p + 32] = x1;
+        S.eG[gb][p] = __expf(x0);
+        S.eG[gb][p + 32] = __expf(x1);
+        S.eGLG[gb][p] = __expf(GL - x0);
+        S.eGLG[gb][p + 32] = __expf(GL - x1);
+        S.beta[gb][p] = S.gst[sg][1][p];
+        S.beta[gb][p + 32] = S.gst[sg][1][p + 32];
+        S.cf[p] = __expf(e0 - x0);
+        S.cf[p + 32] = __expf(e1 - x1);
+        if (p == 0) S.gamma[gb] = __expf(GL);
+      }
+      if (!named_bar_and(3, kConvThreads, !aborted(S))) break;
+      {  // row t: its own 16-block directly, the factor to each earlier block's last row
+        const int t = p, at = t >> 4;
+        const float Gt = S.G[gb][t];
+        float dd[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float x = __expf(Gt - S.G[gb][16 * at + k]);
+          dd[k] = k <= (t & 15) ? x : 0.f;
+        }
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4)
+          *reinterpret_cast<float4*>(&S.ddiag[t][4 * k4]) =
+              make_float4(dd[4 * k4], dd[4 * k4 + 1], dd[4 * k4 + 2], dd[4 * k4 + 3]);
+        float4 f;
+        f.x = at > 0 ? __expf(Gt - S.G[gb][15]) : 0.f;
+        f.y = at > 1 ? __expf(Gt - S.G[gb][31]) : 0.f;
+        f.z = at > 2 ? __expf(Gt - S.G[gb][47]) : 0.f;
+        f.w = 0.f;
+        *reinterpret_cast<float4*>(&S.rf[t][0]) = f;
+      }
+      arrive(S, B_TB);
+      if (MODE != kSumM) {  // V -> fp16 in place (read only by the u product)
+        uint8_t* vb = S.v[sg];
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k) {
+          uint8_t* pp = vb + 16 * (p + 64 * k);
+          maxabs = to_half_chunk(pp, pp, maxabs);
+        }
+      }
+      // fp16 K into its tile, once the chunk that last used the tile has finished Dh
+      if (ci >= 2) wait_bar(S, B_KF0 + sg, ((ci >> 1) + 1) & 1);
+      {
+        const uint8_t* kb = S.kq[sg];
+        uint8_t* kd = S.kh[sg];
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k) {
+          const int e = p + 64 * k, off = 16 * (e & 511);
+          maxabs = to_half_chunk(kb + (e >> 9) * 16384 + off, kd + (e >> 9) * 8192 + off, maxabs);
+        }
+      }
+      // the MMA warp has taken the previous chunk's hand-off (and, for q_g^T, its O1 is done)
+      if (ci >= 1) wait_bar(S, MODE == kEmit ? B_D : B_WU, (ci - 1) & 1);
+      if (MODE == kEmit) {
+        // q_g^T = (diag(e^G) Q)^T as fp16: ldmatrix.trans of 8 x 8 blocks of Q, scaling,
+        // stmatrix into [i][t]
+        const int cw = p >> 5;
+        const uint32_t qsrc = saddr(S.kq[sg]) + 8192, qdst = saddr(S.nwq[1]);
+        const int m = lane >> 3, jr = lane & 7;
+#pragma unroll 4
+        for (int it = 0; it < 16; ++it) {
+          const int qi = cw * 16 + it;          // 0..31
+          const int ib = qi >> 1;               // 8-feature block 0..15
+          const int tb0 = 4 * (qi & 1);         // first of four 8-token blocks
+          // source row t = 8 (tb0 + m) + jr, features 8 ib .. 8 ib + 7
+          const int ts = 8 * (tb0 + m) + jr;
+          const uint32_t src = qsrc + (ib >> 3) * 16384 + ts * 128 + ((((ib & 7) ^ (ts & 7))) << 4);
+          uint32_t rg[4];
+          ldsm_x4_t(src, rg);
+#pragma unroll
+          for (int mm = 0; mm < 4; ++mm) {
+            const int t = 8 * (tb0 + mm) + 2 * (lane & 3);
+            const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&rg[mm]));
+            const float y0 = f.x * S.eG[gb][t], y1 = f.y * S.eG[gb][t + 1];
+            maxabs = fmaxf(maxabs, fmaxf(fabsf(y0), fabsf(y1)));
+            rg[mm] = pack_h2(y0, y1);
+          }
+          // destination row i = 8 ib + jr, tokens 8 (tb0 + m) .. + 7
+          const int id = 8 * ib + jr;
+          stsm_x4(qdst + id * 128 + ((((tb0 + m) ^ (id & 7))) << 4), rg);
+        }
+      }
+      fence_async_smem();
+      arrive(S, B_CV);
+    }
+    if (!(maxabs <= kHalfMax)) S.range_bad = 1;
   } else {
     // =============================================================== MMA (warp 12)
-    // every lane waits; lane 0 issues the MMAs and commits
+    // Fixed order per chunk c: w, u (c); [D | O1] (c); O2, Dh (c); [S ; QK] (c + 2).  Every lane
+    // waits, lane 0 issues and commits.
     const bool leader = lane == 0;
-    const uint32_t ID_SQ = idesc_f16(128, 64, 0, 0, 1);     // bf16 [K ; Q] K^T
-    const uint32_t ID_WU = idesc_f16(128, 64, 1, 0, 1);     // bf16 K^T, V^T x T parts
-    const uint32_t ID_D = idesc_f16(128, 64, 0, 1);         // fp16 h^T (-w)^T
-    const uint32_t ID_O = idesc_f16(128, 64, 0, 0);         // fp16 h^T q_g^T, delta^T attn^T
-    const uint32_t ID_DH = idesc_f16(128, 128, 0, 1, 1);    // bf16 delta'^T K
+    const uint32_t ID_SQ = idesc_f16(128, 64, 0, 0, 1);           // bf16 [K ; Q] K^T
+    const uint32_t ID_WU = idesc_f16(128, 64, 1, 0);              // K^T, V^T x T tiles
+    const uint32_t ID_D = idesc_f16(128, MODE == kEmit ? 128 : 64, 0, 1);  // h^T [-w ; q_g]^T
+    const uint32_t ID_O2 = idesc_f16(128, 64, 0, 0);              // delta^T attn_i^T
+    const uint32_t ID_DH = idesc_f16(128, 128, 0, 1);             // delta'^T K
     auto sq = [&](int ci) {
       if (leader) {
         const uint32_t kq = saddr(S.kq[ci & 1]);
@@ -740,88 +774,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
-    auto wu = [&](int ci) {
-      if (leader) {
-        const uint32_t kq = saddr(S.kq[ci & 1]), vv = saddr(S.v[ci & 1]);
-        const uint32_t tiles_w[2] = {saddr(S.twh), saddr(S.twl)};
-        const uint32_t tiles_u[2] = {saddr(S.tuh), saddr(S.tul)};
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_ss(tm + TM_W, sdesc(kq + ks * 2048, 16384, 1024),
-                   sdesc(tiles_w[part] + ks * 32, 16, 1024), ID_WU, part > 0 || ks > 0);
-        if (MODE != kSumM) {
-#pragma unroll
-          for (int part = 0; part < 2; ++part)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_ss(tm + TM_U, sdesc(vv + ks * 2048, 8192, 1024),
-                     sdesc(tiles_u[part] + ks * 32, 16, 1024), ID_WU, part > 0 || ks > 0);
-        }
-        mma_commit(saddr(&S.bars[B_WU]));
-      }
-      __syncwarp();
-    };
     if (nch > 0) {
-      bool ok = warp_wait(S, B_L0, 0, true);
-      if (ok) sq(0);
-      ok = ok && warp_wait(S, B_T, 0, true);
-      if (ok) wu(0);
-      for (int ci = 0; ok && ci < nch; ++ci) {
-        const uint32_t kq = saddr(S.kq[ci & 1]);
-        // delta^T (+)= h^T (-w)^T ;  o^T = h^T q_g^T
-        ok = warp_wait(S, B_WR, ci & 1, true) && warp_wait(S, B_HR, ci & 1, true) &&
-             (MODE != kEmit || warp_wait(S, B_QS, ci & 1, true));
-        if (!ok) break;
-        fence_after_sync();
-        if (leader) {
-          const uint32_t nw = saddr(S.nw);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t ah = tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3);
-            mma_ts(tm + TM_U, ah, sdesc(nw + ks * 2048, 16384, 1024), ID_D,
-                   (MODE != kSumM) || ks > 0);
-            if (MODE == kEmit)
-              mma_ts(tm + TM_O + 64 * (ci & 1), ah,
-                     sdesc(kq + (ks >> 2) * 16384 + 64 * 128 + (ks & 3) * 32, 16, 1024), ID_O,
-                     ks > 0);
-          }
-          mma_commit(saddr(&S.bars[B_D]));
-        }
-        __syncwarp();
-        // the next chunk's [S ; QK] as soon as its data is in (R_sq was read before T)
-        if (ci + 1 < nch) {
-          ok = warp_wait(S, B_L0 + ((ci + 1) & 1), ((ci + 1) >> 1) & 1, true);
-          if (!ok) break;
-          sq(ci + 1);
-        }
-        // o^T += delta^T attn_i^T ;  Dh^T = delta'^T K  (delta' as hi + lo)
-        ok = warp_wait(S, B_DR, ci & 1, true);
-        if (!ok) break;
-        fence_after_sync();
-        if (leader) {
-          const uint32_t att = saddr(S.att[ci & 1]);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t col = TM_U + 32 * (ks >> 1) + 8 * (ks & 1);
-            if (MODE == kEmit)
-              mma_ts(tm + TM_O + 64 * (ci & 1), tm + col, sdesc(att + ks * 32, 16, 1024), ID_O,
-                     1);
-            const uint64_t bk = sdesc(kq + ks * 2048, 16384, 1024);
-            mma_ts(tm + TM_H, tm + col + 16, bk, ID_DH, ks > 0);
-            mma_ts(tm + TM_H, tm + TM_DL + 16 * (ks >> 1) + 8 * (ks & 1), bk, ID_DH, 1);
-          }
-          mma_commit(saddr(&S.bars[B_H]));
-        }
-        __syncwarp();
-        if (ci + 1 < nch) {
-          ok = warp_wait(S, B_T, (ci + 1) & 1, true);
-          if (!ok) break;
-          wu(ci + 1);
-        }
+      wait_bar(S, B_L0, 0);
+      sq(0);
+      if (nch > 1) {  // the SQ columns are reused once the first gram has read them
+        wait_bar(S, B_E2, 0);
+        wait_bar(S, B_L1, 0);
+        sq(1);
       }
     }
+    for (int ci = 0; ci < nch; ++ci) {
+      const uint32_t khs = saddr(S.kh[ci & 1]), vv = saddr(S.v[ci & 1]);
+      // w^T = K^T T_w^T ;  u^T = V^T T_u^T; then the stage is free for the loader
+      wait_bar(S, B_T, ci & 1);
+      wait_bar(S, B_CV, ci & 1);
+      if (leader) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_ss(tm + TM_W, sdesc(khs + ks * 2048, 8192, 1024),
+                 sdesc(saddr(S.tw) + ks * 32, 16, 1024), ID_WU, ks > 0);
+        if (MODE != kSumM) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss(tm + TM_U, sdesc(vv + ks * 2048, 8192, 1024),
+                   sdesc(saddr(S.tu) + ks * 32, 16, 1024), ID_WU, ks > 0);
+        }
+        mma_commit(saddr(&S.bars[B_WU]));
+        mma_commit(saddr(&S.bars[B_F0 + (ci & 1)]));
+      }
+      __syncwarp();
+      // [D | O1]^T = h^T [-w ; q_g]^T
+      wait_bar(S, B_WR, ci & 1);
+      wait_bar(S, B_HR, ci & 1);
+      fence_after_sync();
+      if (leader) {
+        const uint32_t nw = saddr(S.nwq[0]);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ts(tm + TM_DO, tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3),
+                 sdesc(nw + ks * 2048, 16384, 1024), ID_D, ks > 0);
+        mma_commit(saddr(&S.bars[B_D]));
+      }
+      __syncwarp();
+      // o^T += delta^T attn_i^T ;  Dh^T = delta'^T K
+      wait_bar(S, B_DR, ci & 1);
+      fence_after_sync();
+      if (leader) {
+        const uint32_t att = saddr(S.att[ci & 1]);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint32_t col = 32 * (ks >> 1) + 8 * (ks & 1);
+          if (MODE == kEmit)
+            mma_ts(tm + TM_DO + 64, tm + TM_DO + col, sdesc(att + ks * 32, 16, 1024), ID_O2, 1);
+          mma_ts(tm + TM_H, tm + TM_U + col, sdesc(khs + ks * 2048, 8192, 1024), ID_DH, ks > 0);
+        }
+        mma_commit(saddr(&S.bars[B_H]));
+        mma_commit(saddr(&S.bars[B_KF0 + (ci & 1)]));
+      }
+      __syncwarp();
+      // [S ; QK] two chunks ahead, once the gram of the next chunk has read the columns
+      if (ci + 2 < nch) {
+        wait_bar(S, B_E2, (ci + 1) & 1);
+        wait_bar(S, B_L0 + (ci & 1), ((ci + 2) >> 1) & 1);
+        sq(ci + 2);
+      }
+      if (__any_sync(0xffffffffu, aborted(S))) break;
+    }
+    // every product issued has completed before the TMEM is released
+    if (leader) mma_commit(saddr(&S.bars[B_END]));
+    __syncwarp();
+    wait_bar(S, B_END, 0);
   }
 
   // ---- teardown: every role has left its loop
