@@ -181,7 +181,7 @@ def run_ours(args, ws, rank, local):
 
     # P sweep (short), then the timed run at the chosen P
     sweep = {}
-    Ps = [args.P] if args.P else [8, 16, 19, 32, 38, 64, 4, 1]
+    Ps = [args.P] if args.P else [1, 2, 3, 4, 5, 6, 8, 16, 64]
     for P in Ps:
         ms = timed_forward(P, steps=3 if len(Ps) > 1 else 1, warmup=1)
         sweep[P] = ms

@@ -363,13 +363,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_before_sync();
       if (ci + 1 < nch) arrive(S, B_HR);
-      if (MODE == kEmit) {
+      if (MODE == kEmit) {  // o[t][j][c] for t = 32 hf .. 32 hf + 31
+        const int64_t stride = (int64_t)a.hv * VD;
+        __nv_bfloat16* po = out + ((t0 + 32 * hf) * a.hv + j) * VD + c;
+        const int nt = L - 32 * hf;
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-          const int t = 32 * hf + 2 * q;
           const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&ob[q]);
-          if (t < L) out[((t0 + t) * a.hv + j) * VD + c] = p2.x;
-          if (t + 1 < L) out[((t0 + t + 1) * a.hv + j) * VD + c] = p2.y;
+          if (2 * q < nt) po[0] = p2.x;
+          if (2 * q + 1 < nt) po[stride] = p2.y;
+          po += 2 * stride;
         }
       }
       if (!named_bar_and(2, kChainThreads, !aborted(S))) break;
