@@ -12,7 +12,9 @@
 //   [D | O1]^T   = h^T [-w ; q_g]^T                      (128 x 128, K = 128)
 //   O^T         += delta^T attn_i^T                      (128 x 64, K = 64)
 //   Dh^T         = (diag(e^{G_last - G}) delta)^T K      (128 x 128, K = 64)
-// with delta = u + D, q_g = diag(e^G) Q, o = O1 + O2 and h <- gamma h + Dh.  A tcgen05.mma
+// with delta = u + D, q_g = diag(e^G) Q, o = O1 + O2 and h <- gamma h + Dh.  The u product
+// writes u^T into the D half of the [D | O1] accumulator (the chain warps clear the O half after
+// reading o^T), so that product yields delta itself.  A tcgen05.mma
 // occupies the tensor pipe for about as long at N = 64 as at N = 128, so the two products that
 // share h^T are issued as one N = 128 product.  [S ; QK] reads K and Q as loaded (bf16); the
 // converter warps write K as fp16 (a separate, double-buffered tile), V as fp16 in place and
@@ -63,8 +65,8 @@ enum Mode { kEmit = 0, kSumM = 1, kSumU = 2 };
 // TMEM columns (512 allocated)
 constexpr uint32_t TM_SQ = 0;    // [S ; QK]               64 fp32
 constexpr uint32_t TM_W = 64;    // w^T                    64 fp32
-constexpr uint32_t TM_U = 128;   // u^T, then fp16 delta'  64 fp32
-constexpr uint32_t TM_DO = 192;  // [D | O]^T: D, then fp16 delta, in 0-63; o^T in 64-127
+constexpr uint32_t TM_U = 128;   // fp16 delta' (columns 32 hf + 0..15)
+constexpr uint32_t TM_DO = 192;  // [D | O]^T: u^T + D = delta^T, then fp16 delta, in 0-63; o^T in 64-127
 constexpr uint32_t TM_H = 320;   // Dh^T                   128 fp32, then fp16 h^T
 
 // mbarriers: who completes them
@@ -300,7 +302,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st8(tm + lane_bits + TM_H + 64 * hf + 8 * piece, p);
       }
     };
+    auto zero_o = [&]() {  // the O half of [D | O] starts from zeros for the next chunk
+      uint32_t z[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) z[q] = 0u;
+      tmem_st16(tm + lane_bits + TM_DO + 64 + 32 * hf, z);
+      tmem_st16(tm + lane_bits + TM_DO + 64 + 32 * hf + 16, z);
+    };
     if (nch > 0) {
+      if (MODE == kEmit) zero_o();
       publish_h();
       fence_before_sync();
       arrive(S, B_HR);
@@ -317,12 +327,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int piece = 0; piece < 2; ++piece) {
         float d[16];
         tmem_ld16(tm + lane_bits + TM_DO + 32 * hf + 16 * piece, d);
-        if (MODE != kSumM) {
-          float u[16];
-          tmem_ld16(tm + lane_bits + TM_U + 32 * hf + 16 * piece, u);
-#pragma unroll
-          for (int q = 0; q < 16; ++q) d[q] += u[q];
-        }
         uint32_t pd[8], pp[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -360,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 8; ++q) ob[8 * piece + q] = pack_bf2(o[2 * q], o[2 * q + 1]);
         }
+        zero_o();
       }
       fence_before_sync();
       if (ci + 1 < nch) arrive(S, B_HR);
@@ -799,7 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (MODE != kSumM) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_ss(tm + TM_U, sdesc(vv + ks * 2048, 8192, 1024),
+            mma_ss(tm + TM_DO, sdesc(vv + ks * 2048, 8192, 1024),
                    sdesc(saddr(S.tu) + ks * 32, 16, 1024), ID_WU, ks > 0);
         }
         mma_commit(saddr(&S.bars[B_WU]));
@@ -815,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           mma_ts(tm + TM_DO, tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3),
-                 sdesc(nw + ks * 2048, 16384, 1024), ID_D, ks > 0);
+                 sdesc(nw + ks * 2048, 16384, 1024), ID_D, MODE != kSumM || ks > 0);
         mma_commit(saddr(&S.bars[B_D]));
       }
       __syncwarp();
