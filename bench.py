@@ -279,7 +279,7 @@ def run_ours(args, ws, rank, local):
         "config": {"workload": f"long-context bf16 T={T} Hk={HK} Hv={HV} K=V={KD} C={C}",
                    "segments_per_seq": P_best, "batch": 1, "seq_len": T,
                    "parallelism": f"replicas x{ws} (independent sequences)",
-                   "l2": "inputs+output 0.8 GB > 129 MB L2; no flush",
+                   "l2": f"inputs+output {BYTES_PER_TOKEN * T / 1e9:.2f} GB vs 129 MB L2" + ("; no flush" if BYTES_PER_TOKEN * T > 129e6 else "; L2-resident"),
                    "kernel_family": args.family},
         "sweep_ms_per_step": {f"P={k}": round(v, 4) for k, v in sweep.items()},
         "phase_ms": {k: round(v, 4) for k, v in ph.items()},

@@ -113,7 +113,7 @@ struct Smem {
   // decay e^{G_t - G_s} (s <= t) of the chunk the gram reads next: on the 16-block of t it is
   // ddiag[t][s & 15]; for s in an earlier block b it is rf[t][b] * cf[s], with
   // rf = e^{G_t - G_e}, cf = e^{G_e - G_s} and e the last row of block b (both <= 1 for g <= 0)
-  alignas(16) float ddiag[C][16];
+  alignas(16) float ddiag[C][16];  // row t's 16-byte chunk k at position k ^ (t & 3)
   alignas(16) float rf[C][4];
   alignas(16) float cf[C];
   uint64_t bars[kNumBars];
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float dd[16];
 #pragma unroll
       for (int k4 = 0; k4 < 4; ++k4) {
-        const float4 x = *reinterpret_cast<const float4*>(&S.ddiag[t][4 * k4]);
+        const float4 x = *reinterpret_cast<const float4*>(&S.ddiag[t][4 * (k4 ^ (t & 3))]);
         dd[4 * k4] = x.x; dd[4 * k4 + 1] = x.y; dd[4 * k4 + 2] = x.z; dd[4 * k4 + 3] = x.w;
       }
 #pragma unroll
@@ -696,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4)
-          *reinterpret_cast<float4*>(&S.ddiag[t][4 * k4]) =
+          *reinterpret_cast<float4*>(&S.ddiag[t][4 * (k4 ^ (t & 3))]) =
               make_float4(dd[4 * k4], dd[4 * k4 + 1], dd[4 * k4 + 2], dd[4 * k4 + 3]);
         float4 f;
         f.x = at > 0 ? __expf(Gt - S.G[gb][15]) : 0.f;

@@ -51,9 +51,11 @@
  *   Supported   io dtype bf16 or fp32; K, V in {64, 128}; C = 64; hv % hk == 0; P >= 1;
  *               16-byte aligned tensor pointers.
  *   Precision   fp32 I/O runs on fp32 CUDA-core kernels.  bf16 I/O with K = V = 128 runs on the
- *               tensor cores with fp16 operands (inputs converted exactly in range), fp32
- *               accumulation and an fp32 state: q, k, v and the state must stay below 65504 in
- *               magnitude; a value that does not is reported as GDN_ERR_DEVICE_RANGE.
+ *               tensor cores: K K^T and Q K^T on the bf16 inputs as given, every later product
+ *               on fp16 operands (inputs converted exactly in range), fp32 accumulation, an
+ *               fp32 triangular solve and an fp32 state.  q, k, v, the state and the corrected
+ *               values delta must stay below 65504 in magnitude; a value that does not is
+ *               reported as GDN_ERR_DEVICE_RANGE.
  */
 #ifndef GDN_H_
 #define GDN_H_
