@@ -9,16 +9,15 @@
 //   [S ; QK]     = [K ; Q] K^T                          (128 x 64, K = 128; bf16 as loaded)
 //   w^T          = K^T (T diag(beta e^G))^T              (128 x 64, K = 64)
 //   u^T          = V^T (T diag(beta))^T                  (128 x 64, K = 64)
-//   [D | O1]^T   = h^T [-w ; q_g]^T                      (128 x 128, K = 128)
+//   O^T          = h^T q_g^T                            (128 x 64, K = 128)
+//   D^T          = h^T (-w)^T                           (128 x 64, K = 128)
 //   O^T         += delta^T attn_i^T                      (128 x 64, K = 64)
 //   Dh^T         = (diag(e^{G_last - G}) delta)^T K      (128 x 128, K = 64)
-// with delta = u + D, q_g = diag(e^G) Q, o = O1 + O2 and h <- gamma h + Dh.  The u product
-// writes u^T into the D half of the [D | O1] accumulator (the chain warps clear the O half after
-// reading o^T), so that product yields delta itself.  A tcgen05.mma
-// occupies the tensor pipe for about as long at N = 64 as at N = 128, so the two products that
-// share h^T are issued as one N = 128 product.  [S ; QK] reads K and Q as loaded (bf16); the
-// converter warps write K as fp16 (a separate, double-buffered tile), V as fp16 in place and
-// q_g^T as fp16, and every later product has fp16 operands.  The state h^T lives in registers
+// with delta = u + D, q_g = diag(e^G) Q, o = q_g h + attn_i delta and h <- gamma h + Dh.  The
+// u product writes u^T into the D accumulator, so that the D product yields delta itself.
+// [S ; QK] reads K and Q as loaded (bf16); the converter warps then write K as fp16 (a
+// separate, double-buffered tile), and V and q_g as fp16 in place (q_g keeps Q's K-major
+// layout, so it needs no transpose), and every later product has fp16 operands.  The state h^T lives in registers
 // (fp32) of the chain warps; its fp16 copy, delta and delta' are written back into TMEM as the
 // A operands of the next products.  T = (I + A)^-1 is blocked by 16 x 16: the diagonal inverses
 // by fp32 forward substitution in registers, the off-diagonal blocks
@@ -29,7 +28,7 @@
 //   warps 8-11  prepare:   masked gram and attn_i, the triangular solve, -w; one chunk ahead
 //   warp 12     MMA:       waits for each product's inputs in a fixed order; lane 0 issues
 //   warp 13     loader:    TMA boxes of K, Q, V and cp.async of g, beta into the free stage
-//   warps 14-15 converter: decay tables, fp16 K and V, q_g^T
+//   warps 14-15 converter: decay tables, fp16 K, V and q_g
 // Hand-offs use mbarriers: a producing group arrives with every thread (the barrier counts the
 // group), a consumer waits with hardware-suspended try_wait (no issue slots spent).  Every wait
 // is bounded; one that gives up records GDN_ERR_DEVICE_TIMEOUT and the thread carries on, and
@@ -66,7 +65,7 @@ enum Mode { kEmit = 0, kSumM = 1, kSumU = 2 };
 constexpr uint32_t TM_SQ = 0;    // [S ; QK]               64 fp32
 constexpr uint32_t TM_W = 64;    // w^T                    64 fp32
 constexpr uint32_t TM_U = 128;   // fp16 delta' (columns 32 hf + 0..15)
-constexpr uint32_t TM_DO = 192;  // [D | O]^T: u^T + D = delta^T, then fp16 delta, in 0-63; o^T in 64-127
+constexpr uint32_t TM_DO = 192;  // u^T + D = delta^T, then fp16 delta, in 0-63; o^T in 64-127
 constexpr uint32_t TM_H = 320;   // Dh^T                   128 fp32, then fp16 h^T
 
 // mbarriers: who completes them
@@ -74,16 +73,16 @@ enum Bar {
   B_SQ = 0,    // [S ; QK] of a chunk is in TMEM                      MMA commit
   B_E2,        // the gram has read it and the decay tables           prepare (128)
   B_TB,        // decay tables of a chunk are in shared memory        converter (64)
-  B_CV,        // fp16 K, V and q_g^T of a chunk are ready            converter (64)
+  B_CV,        // fp16 K, V and q_g of a chunk are ready              converter (64)
   B_T,         // the T tiles are ready                               prepare (128)
   B_WU,        // w^T, u^T are in TMEM                                MMA commit
   B_WR,        // -w^T is in shared memory                            prepare (128)
   B_HR,        // fp16 h^T is in TMEM and the previous o^T was read   chain (256)
-  B_D,         // [D | O1]^T is in TMEM                               MMA commit
+  B_D,         // delta^T = u^T + D^T is in TMEM                      MMA commit
   B_DR,        // fp16 delta, delta' are in TMEM                      chain (256)
   B_H,         // Dh^T and o^T are complete                           MMA commit
   B_L0, B_L1,  // stage loaded: byte count plus 32 cp.async arrivals  loader
-  B_F0, B_F1,  // stage free (its chunk's w, u products are done)     MMA commit
+  B_F0, B_F1,  // stage free (its chunk's w, u and q_g h products are done)  MMA commit
   B_KF0, B_KF1,  // fp16 K tile free (its chunk's Dh is done)         MMA commit
   B_END,       // every product issued has completed                  MMA commit
   kNumBars
@@ -97,13 +96,14 @@ __device__ __forceinline__ uint32_t bar_count(int b) {
 }
 
 struct Smem {
-  uint8_t kq[2][2 * 128 * 128];  // per stage: [kblk][K rows 0-63 | Q rows 64-127][128 B], bf16
+  uint8_t kq[2][2 * 128 * 128];  // per stage: [kblk][K rows 0-63 | Q rows 64-127][128 B], bf16;
+                                 // Q becomes fp16 q_g in place
   uint8_t v[2][2 * 64 * 128];    // per stage: [kblk][64 rows][128 B]; V -> fp16 in place
   uint8_t kh[2][2 * 64 * 128];   // fp16 K: [kblk][64 rows][128 B] (chunk parity)
   uint8_t att[2][64 * 128];      // attn_i [t][s] fp16, K-major B (chunk parity)
   uint8_t tw[64 * 128];          // T diag(beta e^G) [t][s] fp16, K-major B
   uint8_t tu[64 * 128];          // T diag(beta) [t][s] fp16, K-major B
-  uint8_t nwq[2][128 * 128];     // MN-major B of [D | O1]: -w^T [i][t], then q_g^T [i][t]
+  uint8_t nw[128 * 128];         // -w^T [i][t] fp16, MN-major B of D
   uint8_t ah[64 * 128];          // masked gram A [t][s], fp16
   uint8_t th[64 * 128];          // blocks of (I + A)^-1 [t][s], fp16 operands
   uint8_t xs[4][16 * 48];        // per-warp 16 x 16 fp16 scratch, 48-byte rows
@@ -127,7 +127,7 @@ struct Smem {
 static_assert(offsetof(Smem, kq) % 1024 == 0 && offsetof(Smem, v) % 1024 == 0, "tile alignment");
 static_assert(offsetof(Smem, kh) % 1024 == 0 && offsetof(Smem, att) % 1024 == 0, "tile alignment");
 static_assert(offsetof(Smem, tw) % 1024 == 0 && offsetof(Smem, tu) % 1024 == 0, "tile alignment");
-static_assert(offsetof(Smem, nwq) % 1024 == 0 && offsetof(Smem, ah) % 1024 == 0, "tile alignment");
+static_assert(offsetof(Smem, nw) % 1024 == 0 && offsetof(Smem, ah) % 1024 == 0, "tile alignment");
 static_assert(offsetof(Smem, th) % 1024 == 0 && offsetof(Smem, xs) % 16 == 0, "tile alignment");
 static_assert(offsetof(Smem, ddiag) % 16 == 0 && offsetof(Smem, rf) % 16 == 0, "vector alignment");
 static_assert(offsetof(Smem, cf) % 16 == 0 && offsetof(Smem, bars) % 8 == 0, "alignment");
@@ -205,28 +205,40 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
       "r"(bytes)
       : "memory");
 }
-__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
-  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(addr),
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
-               : "memory");
-}
 
 __device__ __forceinline__ void st_half(uint8_t* tile, int r, int c, float x) {
   *reinterpret_cast<__half*>(tile + sw128_offset(64, r, c)) = __float2half_rn(x);
 }
 
-// bf16 -> fp16 of one 16-byte chunk (src and dst may coincide); returns the largest magnitude.
-__device__ __forceinline__ float to_half_chunk(const uint8_t* src, uint8_t* dst, float m) {
-  uint4 x = *reinterpret_cast<const uint4*>(src);
-  uint32_t* w = reinterpret_cast<uint32_t*>(&x);
+// NB 16-byte chunks of bf16 at src + 1024 k to fp16 at dst + 1024 k; with SCALED the values of
+// chunk k are multiplied by e[8 k] (chunks 1024 bytes apart lie 8 rows apart in a tile of
+// 128-byte rows, and swizzling permutes chunks within a row only).  Returns the largest
+// magnitude written, or m if larger.  All loads are issued before the first store: the compiler
+// cannot tell src and dst apart and would otherwise wait for each store before the next load.
+template <int NB, bool SCALED>
+__device__ __forceinline__ float to_half_chunks(const uint8_t* src, uint8_t* dst, const float* e,
+                                                float m) {
+  uint4 x[NB];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[i]));
-    m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
-    w[i] = pack_h2(f.x, f.y);
+  for (int k = 0; k < NB; ++k) x[k] = *reinterpret_cast<const uint4*>(src + 1024 * k);
+  float mk[2] = {m, 0.f};
+#pragma unroll
+  for (int k = 0; k < NB; ++k) {
+    const float sc = SCALED ? e[8 * k] : 1.f;
+    uint32_t* w = reinterpret_cast<uint32_t*>(&x[k]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[i]));
+      if (SCALED) {
+        f.x *= sc;
+        f.y *= sc;
+      }
+      mk[k & 1] = fmaxf(mk[k & 1], fmaxf(fabsf(f.x), fabsf(f.y)));
+      w[i] = pack_h2(f.x, f.y);
+    }
+    *reinterpret_cast<uint4*>(dst + 1024 * k) = x[k];
   }
-  *reinterpret_cast<uint4*>(dst) = x;
-  return m;
+  return fmaxf(mk[0], mk[1]);
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -291,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         h[q] = x;
       }
     }
-    // fp16 h^T into TMEM (the A operand of [D | O1]).  Not range-checked: an infinite h^T
+    // fp16 h^T into TMEM (the A operand of D and of q_g h).  Not range-checked: an infinite h^T
     // makes delta infinite or NaN, and delta is checked.
     auto publish_h = [&]() {
 #pragma unroll
@@ -302,15 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st8(tm + lane_bits + TM_H + 64 * hf + 8 * piece, p);
       }
     };
-    auto zero_o = [&]() {  // the O half of [D | O] starts from zeros for the next chunk
-      uint32_t z[16];
-#pragma unroll
-      for (int q = 0; q < 16; ++q) z[q] = 0u;
-      tmem_st16(tm + lane_bits + TM_DO + 64 + 32 * hf, z);
-      tmem_st16(tm + lane_bits + TM_DO + 64 + 32 * hf + 16, z);
-    };
     if (nch > 0) {
-      if (MODE == kEmit) zero_o();
       publish_h();
       fence_before_sync();
       arrive(S, B_HR);
@@ -364,7 +368,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 8; ++q) ob[8 * piece + q] = pack_bf2(o[2 * q], o[2 * q + 1]);
         }
-        zero_o();
       }
       fence_before_sync();
       if (ci + 1 < nch) arrive(S, B_HR);
@@ -593,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk.y = pack_h2(-wv[8 * ch + 2], -wv[8 * ch + 3]);
           pk.z = pack_h2(-wv[8 * ch + 4], -wv[8 * ch + 5]);
           pk.w = pack_h2(-wv[8 * ch + 6], -wv[8 * ch + 7]);
-          *reinterpret_cast<uint4*>(S.nwq[0] + sw128_offset(128, i, 32 * hb + 8 * ch)) = pk;
+          *reinterpret_cast<uint4*>(S.nw + sw128_offset(128, i, 32 * hb + 8 * ch)) = pk;
         }
       }
       fence_async_smem();
@@ -617,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =============================================================== loader (1 warp)
     for (int ci = 0; ci < nch; ++ci) {
       const int sg = ci & 1;
-      // the stage was last used by chunk ci - 2: wait for its w, u products
+      // the stage was last used by chunk ci - 2: wait for its w, u (and q_g h) products
       if (ci >= 2) wait_bar(S, B_F0 + sg, ((ci >> 1) + 1) & 1);
       if (__any_sync(0xffffffffu, aborted(S))) break;
       const int64_t t0 = sb + (c0 + ci) * C;
@@ -705,69 +708,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         f.w = 0.f;
         *reinterpret_cast<float4*>(&S.rf[t][0]) = f;
       }
+      if (MODE == kEmit) wait_bar(S, B_SQ, ci & 1);  // [S ; QK] has read the bf16 Q
       arrive(S, B_TB);
       if (MODE != kSumM) {  // V -> fp16 in place (read only by the u product)
-        uint8_t* vb = S.v[sg];
-#pragma unroll 4
-        for (int k = 0; k < 16; ++k) {
-          uint8_t* pp = vb + 16 * (p + 64 * k);
-          maxabs = to_half_chunk(pp, pp, maxabs);
-        }
+        uint8_t* vb = S.v[sg] + 16 * p;
+#pragma unroll 1
+        for (int k0 = 0; k0 < 16; k0 += 4)
+          maxabs = to_half_chunks<4, false>(vb + 1024 * k0, vb + 1024 * k0, nullptr, maxabs);
       }
       // fp16 K into its tile, once the chunk that last used the tile has finished Dh
       if (ci >= 2) wait_bar(S, B_KF0 + sg, ((ci >> 1) + 1) & 1);
       {
-        const uint8_t* kb = S.kq[sg];
-        uint8_t* kd = S.kh[sg];
-#pragma unroll 4
-        for (int k = 0; k < 16; ++k) {
-          const int e = p + 64 * k, off = 16 * (e & 511);
-          maxabs = to_half_chunk(kb + (e >> 9) * 16384 + off, kd + (e >> 9) * 8192 + off, maxabs);
+        const uint8_t* kb = S.kq[sg] + 16 * p;
+        uint8_t* kd = S.kh[sg] + 16 * p;
+#pragma unroll 1
+        for (int k0 = 0; k0 < 16; k0 += 4)
+          maxabs = to_half_chunks<4, false>(kb + (k0 >> 3) * 16384 + 1024 * (k0 & 7),
+                                            kd + (k0 >> 3) * 8192 + 1024 * (k0 & 7), nullptr, maxabs);
+      }
+      if (MODE == kEmit) {  // q_g = diag(e^G) Q as fp16, in place: the K-major B of q_g h
+        uint8_t* qb = S.kq[sg] + 8192 + 16 * p;
+#pragma unroll 1
+        for (int k0 = 0; k0 < 16; k0 += 4) {
+          uint8_t* pq = qb + (k0 >> 3) * 16384 + 1024 * (k0 & 7);
+          maxabs = to_half_chunks<4, true>(pq, pq, &S.eG[gb][(p >> 3) + 8 * (k0 & 7)], maxabs);
         }
       }
-      // the MMA warp has taken the previous chunk's hand-off (and, for q_g^T, its O1 is done)
-      if (ci >= 1) wait_bar(S, MODE == kEmit ? B_D : B_WU, (ci - 1) & 1);
-      if (MODE == kEmit) {
-        // q_g^T = (diag(e^G) Q)^T as fp16: ldmatrix.trans of 8 x 8 blocks of Q, scaling,
-        // stmatrix into [i][t]
-        const int cw = p >> 5;
-        const uint32_t qsrc = saddr(S.kq[sg]) + 8192, qdst = saddr(S.nwq[1]);
-        const int m = lane >> 3, jr = lane & 7;
-#pragma unroll 4
-        for (int it = 0; it < 16; ++it) {
-          const int qi = cw * 16 + it;          // 0..31
-          const int ib = qi >> 1;               // 8-feature block 0..15
-          const int tb0 = 4 * (qi & 1);         // first of four 8-token blocks
-          // source row t = 8 (tb0 + m) + jr, features 8 ib .. 8 ib + 7
-          const int ts = 8 * (tb0 + m) + jr;
-          const uint32_t src = qsrc + (ib >> 3) * 16384 + ts * 128 + ((((ib & 7) ^ (ts & 7))) << 4);
-          uint32_t rg[4];
-          ldsm_x4_t(src, rg);
-#pragma unroll
-          for (int mm = 0; mm < 4; ++mm) {
-            const int t = 8 * (tb0 + mm) + 2 * (lane & 3);
-            const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&rg[mm]));
-            const float y0 = f.x * S.eG[gb][t], y1 = f.y * S.eG[gb][t + 1];
-            maxabs = fmaxf(maxabs, fmaxf(fabsf(y0), fabsf(y1)));
-            rg[mm] = pack_h2(y0, y1);
-          }
-          // destination row i = 8 ib + jr, tokens 8 (tb0 + m) .. + 7
-          const int id = 8 * ib + jr;
-          stsm_x4(qdst + id * 128 + ((((tb0 + m) ^ (id & 7))) << 4), rg);
-        }
-      }
+      // the MMA warp has waited for the previous chunk's hand-off
+      if (ci >= 1) wait_bar(S, B_WU, (ci - 1) & 1);
       fence_async_smem();
       arrive(S, B_CV);
     }
     if (!(maxabs <= kHalfMax)) S.range_bad = 1;
   } else {
     // =============================================================== MMA (warp 12)
-    // Fixed order per chunk c: w, u (c); [D | O1] (c); O2, Dh (c); [S ; QK] (c + 2).  Every lane
+    // Fixed order per chunk c: w, u (c); q_g h (c); D (c); O2, Dh (c); [S ; QK] (c + 2).  Every lane
     // waits, lane 0 issues and commits.
     const bool leader = lane == 0;
     const uint32_t ID_SQ = idesc_f16(128, 64, 0, 0, 1);           // bf16 [K ; Q] K^T
     const uint32_t ID_WU = idesc_f16(128, 64, 1, 0);              // K^T, V^T x T tiles
-    const uint32_t ID_D = idesc_f16(128, MODE == kEmit ? 128 : 64, 0, 1);  // h^T [-w ; q_g]^T
+    const uint32_t ID_D = idesc_f16(128, 64, 0, 1);               // h^T (-w)^T
+    const uint32_t ID_QH = idesc_f16(128, 64, 0, 0);              // h^T q_g^T
     const uint32_t ID_O2 = idesc_f16(128, 64, 0, 0);              // delta^T attn_i^T
     const uint32_t ID_DH = idesc_f16(128, 128, 0, 1);             // delta'^T K
     auto sq = [&](int ci) {
@@ -808,15 +789,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                    sdesc(saddr(S.tu) + ks * 32, 16, 1024), ID_WU, ks > 0);
         }
         mma_commit(saddr(&S.bars[B_WU]));
-        mma_commit(saddr(&S.bars[B_F0 + (ci & 1)]));
+        if (MODE != kEmit) mma_commit(saddr(&S.bars[B_F0 + (ci & 1)]));
       }
       __syncwarp();
-      // [D | O1]^T = h^T [-w ; q_g]^T
+      if (MODE == kEmit) {  // o^T = h^T q_g^T starts the O accumulator; then the stage is free
+        wait_bar(S, B_HR, ci & 1);
+        fence_after_sync();
+        if (leader) {
+          const uint32_t qg = saddr(S.kq[ci & 1]) + 8192;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ts(tm + TM_DO + 64, tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3),
+                   sdesc(qg + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), ID_QH, ks > 0);
+          mma_commit(saddr(&S.bars[B_F0 + (ci & 1)]));
+        }
+        __syncwarp();
+      }
+      // delta^T = u^T + h^T (-w)^T
       wait_bar(S, B_WR, ci & 1);
-      wait_bar(S, B_HR, ci & 1);
+      if (MODE != kEmit) wait_bar(S, B_HR, ci & 1);
       fence_after_sync();
       if (leader) {
-        const uint32_t nw = saddr(S.nwq[0]);
+        const uint32_t nw = saddr(S.nw);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           mma_ts(tm + TM_DO, tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3),
