@@ -106,15 +106,19 @@ struct Smem {
   uint8_t nw[128 * 128];         // -w^T [i][t] fp16, MN-major B of D
   uint8_t ah[64 * 128];          // masked gram A [t][s], fp16
   uint8_t th[64 * 128];          // blocks of (I + A)^-1 [t][s], fp16 operands
-  uint8_t xs[4][16 * 48];        // per-warp 16 x 16 fp16 scratch, 48-byte rows
-  float adiag[C][16];            // the diagonal 16 x 16 blocks of A, fp32
+  uint8_t xs[4][16 * 48];        // 16 x 16 fp16 blocks for mma.sync, 48-byte rows
+  alignas(16) float adiag[C][20];  // the diagonal 16 x 16 blocks of A, fp32 (padded rows)
+  float wd[4][16 * 17];          // per-warp fp32 16 x 16 block of T (padded rows)
   float gst[2][2][C];            // g and beta of a staged chunk
   float G[3][C], eG[3][C], eGLG[3][C], beta[3][C], gamma[4];
   // decay e^{G_t - G_s} (s <= t) of the chunk the gram reads next: on the 16-block of t it is
-  // ddiag[t][s & 15]; for s in an earlier block b it is rf[t][b] * cf[s], with
-  // rf = e^{G_t - G_e}, cf = e^{G_e - G_s} and e the last row of block b (both <= 1 for g <= 0)
-  alignas(16) float ddiag[C][16];  // row t's 16-byte chunk k at position k ^ (t & 3)
-  alignas(16) float rf[C][4];
+  // dd*[t][s & 15]; for s in an earlier block b it is rf*[t][b] * cf[s], with
+  // rf = e^{G_t - G_e}, cf = e^{G_e - G_s} and e the last row of block b (both <= 1 for g <= 0).
+  // The A rows (ddA, rfA) carry beta_t and exclude s = t; attn_i's (ddO, rfO) keep s = t.
+  alignas(16) float ddA[C][20];  // padded rows: conflict-free 16-byte accesses by row
+  alignas(16) float ddO[C][20];
+  alignas(16) float rfA[C][4];
+  alignas(16) float rfO[C][4];
   alignas(16) float cf[C];
   uint64_t bars[kNumBars];
   uint32_t tmem_base;
@@ -129,7 +133,9 @@ static_assert(offsetof(Smem, kh) % 1024 == 0 && offsetof(Smem, att) % 1024 == 0,
 static_assert(offsetof(Smem, tw) % 1024 == 0 && offsetof(Smem, tu) % 1024 == 0, "tile alignment");
 static_assert(offsetof(Smem, nw) % 1024 == 0 && offsetof(Smem, ah) % 1024 == 0, "tile alignment");
 static_assert(offsetof(Smem, th) % 1024 == 0 && offsetof(Smem, xs) % 16 == 0, "tile alignment");
-static_assert(offsetof(Smem, ddiag) % 16 == 0 && offsetof(Smem, rf) % 16 == 0, "vector alignment");
+static_assert(offsetof(Smem, ddA) % 16 == 0 && offsetof(Smem, ddO) % 16 == 0, "vector alignment");
+static_assert(offsetof(Smem, rfA) % 16 == 0 && offsetof(Smem, rfO) % 16 == 0, "vector alignment");
+static_assert(offsetof(Smem, adiag) % 16 == 0, "vector alignment");
 static_assert(offsetof(Smem, cf) % 16 == 0 && offsetof(Smem, bars) % 8 == 0, "alignment");
 static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory per block");
 
@@ -405,102 +411,125 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wb = warp - 8;                  // 0..3: this warp's 16-row block of T
     const uint32_t lane_bits = (uint32_t)((warp & 3) * 32) << 16;
     const int g8 = lane >> 2, q4 = lane & 3;
-    const uint32_t ah_s = saddr(S.ah), th_s = saddr(S.th), xs_s = saddr(S.xs[wb]);
+    const uint32_t ah_s = saddr(S.ah), th_s = saddr(S.th);
 
-    // the strictly upper blocks of T diag(.) are zero for every chunk
+    // the strictly upper blocks of T diag(.), rows 0-31 x columns 32-63 of A and attn_i, and the
+    // upper right 8 x 8 of each warp's fp32 block of T are zero for every chunk
     for (int e = pt; e < 64 * 128 / 16; e += kPrepThreads) {
       reinterpret_cast<uint4*>(S.tw)[e] = make_uint4(0u, 0u, 0u, 0u);
       reinterpret_cast<uint4*>(S.tu)[e] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(S.ah)[e] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(S.att[0])[e] = make_uint4(0u, 0u, 0u, 0u);
+      reinterpret_cast<uint4*>(S.att[1])[e] = make_uint4(0u, 0u, 0u, 0u);
     }
+    for (int e = pt; e < 4 * 16 * 17; e += kPrepThreads) (&S.wd[0][0])[e] = 0.f;
 
-    // ---- masked gram A (fp16 tile + fp32 diagonal blocks) and attn_i from [S ; QK]
+    // 32 fp32 values as fp16 into row t, columns 32 hb .. 32 hb + 31, of a 64-column tile
+    auto put_row32 = [&](uint8_t* dst, int t, int hb, const float (&sv)[32]) {
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint4 pk;
+        pk.x = pack_h2(sv[8 * ch + 0], sv[8 * ch + 1]);
+        pk.y = pack_h2(sv[8 * ch + 2], sv[8 * ch + 3]);
+        pk.z = pack_h2(sv[8 * ch + 4], sv[8 * ch + 5]);
+        pk.w = pack_h2(sv[8 * ch + 6], sv[8 * ch + 7]);
+        *reinterpret_cast<uint4*>(dst + sw128_offset(64, t, 32 * hb + 8 * ch)) = pk;
+      }
+    };
+
+    // ---- masked gram A (fp16 tile + fp32 diagonal blocks) and attn_i from [S ; QK].  Row t
+    // meets 16-blocks below its own (decay rf[t][b] cf[s]), its own block (dd[t][s & 15]) and
+    // blocks above (zero).  Rows 32-63 see only lower blocks in columns 0-31 and rows 0-31 only
+    // upper blocks in columns 32-63 (left zero from the start), so each row computes one plain
+    // half at most and one half holding its own block.
     auto gram = [&](int ci) {
-      const int gb = ci % 3;
       wait_bar(S, B_SQ, ci & 1);
       wait_bar(S, B_TB, ci & 1);
       fence_after_sync();
-      const bool is_s = pt < 64;
-      const int t = pt & 63, at = t >> 4;
-      const float bt = is_s ? S.beta[gb][t] : 1.f;
-      const float4 rf4 = *reinterpret_cast<const float4*>(&S.rf[t][0]);
-      float dd[16];
-#pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
-        const float4 x = *reinterpret_cast<const float4*>(&S.ddiag[t][4 * (k4 ^ (t & 3))]);
-        dd[4 * k4] = x.x; dd[4 * k4 + 1] = x.y; dd[4 * k4 + 2] = x.z; dd[4 * k4 + 3] = x.w;
-      }
-#pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
+      const bool is_s = pt < 64;  // warps 8, 9: rows of A; warps 10, 11: rows of attn_i
+      if (is_s || MODE == kEmit) {
+        const int t = pt & 63, hi = t >> 5, ab = (t >> 4) & 1;  // hi is warp-uniform
+        const float4 rf4 = *reinterpret_cast<const float4*>(is_s ? S.rfA[t] : S.rfO[t]);
+        uint8_t* dst = is_s ? S.ah : S.att[ci & 1];
         float sv[32];
-        tmem_ld32(tm + lane_bits + TM_SQ + 32 * hb, sv);
+        if (hi) {
+          tmem_ld32(tm + lane_bits + TM_SQ, sv);
 #pragma unroll
-        for (int c4 = 0; c4 < 32; c4 += 4) {
-          const int s1 = 32 * hb + c4, b2 = s1 >> 4, k = s1 & 15;
-          const float4 cf4 = *reinterpret_cast<const float4*>(&S.cf[s1]);
-          const float f = b2 == 0 ? rf4.x : b2 == 1 ? rf4.y : rf4.z;
-          const bool below = b2 < at, diag = b2 == at;
-          const float dx = below ? f * cf4.x : (diag ? dd[k + 0] : 0.f);
-          const float dy = below ? f * cf4.y : (diag ? dd[k + 1] : 0.f);
-          const float dz = below ? f * cf4.z : (diag ? dd[k + 2] : 0.f);
-          const float dw = below ? f * cf4.w : (diag ? dd[k + 3] : 0.f);
-          // A keeps s < t (times beta_t); attn_i keeps s <= t (the decay is 0 above)
-          sv[c4 + 0] *= bt * (is_s && s1 + 0 == t ? 0.f : dx);
-          sv[c4 + 1] *= bt * (is_s && s1 + 1 == t ? 0.f : dy);
-          sv[c4 + 2] *= bt * (is_s && s1 + 2 == t ? 0.f : dz);
-          sv[c4 + 3] *= bt * (is_s && s1 + 3 == t ? 0.f : dw);
+          for (int c4 = 0; c4 < 32; c4 += 4) {
+            const float4 cf4 = *reinterpret_cast<const float4*>(&S.cf[c4]);
+            const float f = c4 < 16 ? rf4.x : rf4.y;
+            sv[c4 + 0] *= f * cf4.x;
+            sv[c4 + 1] *= f * cf4.y;
+            sv[c4 + 2] *= f * cf4.z;
+            sv[c4 + 3] *= f * cf4.w;
+          }
+          put_row32(dst, t, 0, sv);
+        }
+        tmem_ld32(tm + lane_bits + TM_SQ + 32 * hi, sv);
+        const float* ddr = is_s ? S.ddA[t] : S.ddO[t];
+        const float fb = hi ? rf4.z : rf4.x;  // to the last row of block 2 hi (when ab = 1)
+#pragma unroll
+        for (int c4 = 0; c4 < 16; c4 += 4) {  // block 2 hi: own block (ab = 0) or below it
+          const float4 cf4 = *reinterpret_cast<const float4*>(&S.cf[32 * hi + c4]);
+          const float4 d4 = *reinterpret_cast<const float4*>(ddr + c4);
+          sv[c4 + 0] *= ab ? fb * cf4.x : d4.x;
+          sv[c4 + 1] *= ab ? fb * cf4.y : d4.y;
+          sv[c4 + 2] *= ab ? fb * cf4.z : d4.z;
+          sv[c4 + 3] *= ab ? fb * cf4.w : d4.w;
+        }
+#pragma unroll
+        for (int c4 = 16; c4 < 32; c4 += 4) {  // block 2 hi + 1: own block (ab = 1) or above
+          const float4 d4 = *reinterpret_cast<const float4*>(ddr + c4 - 16);
+          sv[c4 + 0] *= ab ? d4.x : 0.f;
+          sv[c4 + 1] *= ab ? d4.y : 0.f;
+          sv[c4 + 2] *= ab ? d4.z : 0.f;
+          sv[c4 + 3] *= ab ? d4.w : 0.f;
         }
         if (is_s) {
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
-            if (((32 * hb + q) >> 4) == at) S.adiag[t][q & 15] = sv[q];
+          for (int k4 = 0; k4 < 16; k4 += 4)
+            *reinterpret_cast<float4*>(&S.adiag[t][k4]) =
+                ab ? make_float4(sv[16 + k4], sv[17 + k4], sv[18 + k4], sv[19 + k4])
+                   : make_float4(sv[k4], sv[1 + k4], sv[2 + k4], sv[3 + k4]);
         }
-        if (is_s || MODE == kEmit) {
-          uint8_t* dst = is_s ? S.ah : S.att[ci & 1];
-#pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint4 pk;
-            pk.x = pack_h2(sv[8 * ch + 0], sv[8 * ch + 1]);
-            pk.y = pack_h2(sv[8 * ch + 2], sv[8 * ch + 3]);
-            pk.z = pack_h2(sv[8 * ch + 4], sv[8 * ch + 5]);
-            pk.w = pack_h2(sv[8 * ch + 6], sv[8 * ch + 7]);
-            *reinterpret_cast<uint4*>(dst + sw128_offset(64, t, 32 * hb + 8 * ch)) = pk;
-          }
-        }
+        put_row32(dst, t, hi, sv);
       }
       if (MODE == kEmit && !is_s) fence_async_smem();  // attn_i feeds the tensor core
       fence_before_sync();
       arrive(S, B_E2);
     };
 
-    // T_ab = -T_aa sum_{m=b}^{a-1} A_am T_mb for one 16 x 16 block, by one warp: the sum on
-    // mma.sync from the fp16 tiles, then the product with T_aa through the warp's scratch.
-    auto off_diag_block = [&](int ab, int bb, int gb) {
-      float x[2][4] = {};
-      for (int m = bb; m < ab; ++m) {
-        uint32_t af[4], bf[4];
-        load_a<64>(ah_s, 16 * ab, 16 * m, af);
-        load_b_kn<64>(th_s, 16 * m, 16 * bb, bf);
-        mma16816(x[0], af, bf[0], bf[1]);
-        mma16816(x[1], af, bf[2], bf[3]);
-      }
+    // ---- 16 x 16 blocks on mma.sync (m16n8k16, two n8 tiles per block)
+    // x += A_blk(a_r, a_c) B_blk(b_r, b_c), A from a tile [m][k] and B from a tile [k][n]
+    auto mma_blk = [&](float (&x)[2][4], uint32_t a_base, int a_r, int a_c, uint32_t b_base,
+                       int b_r, int b_c) {
+      uint32_t af[4], bf[4];
+      load_a<64>(a_base, a_r, a_c, af);
+      load_b_kn<64>(b_base, b_r, b_c, bf);
+      mma16816(x[0], af, bf[0], bf[1]);
+      mma16816(x[1], af, bf[2], bf[3]);
+    };
+    // accumulator fragment -> fp16 block xs[tile] ([k][n], 48-byte rows)
+    auto frag_to_xs = [&](const float (&x)[2][4], int tile) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        *reinterpret_cast<uint32_t*>(S.xs[wb] + g8 * 48 + (8 * nt + 2 * q4) * 2) =
+        *reinterpret_cast<uint32_t*>(S.xs[tile] + g8 * 48 + (8 * nt + 2 * q4) * 2) =
             pack_h2(x[nt][0], x[nt][1]);
-        *reinterpret_cast<uint32_t*>(S.xs[wb] + (g8 + 8) * 48 + (8 * nt + 2 * q4) * 2) =
+        *reinterpret_cast<uint32_t*>(S.xs[tile] + (g8 + 8) * 48 + (8 * nt + 2 * q4) * 2) =
             pack_h2(x[nt][2], x[nt][3]);
       }
-      __syncwarp();
-      float y[2][4] = {};
-      {
-        uint32_t af[4], bf[4];
-        load_a<64>(th_s, 16 * ab, 16 * ab, af);
-        const int mi = lane >> 3, rr = lane & 7;
-        ldsm_x4_t(xs_s + (rr + ((mi & 1) << 3)) * 48 + ((mi >> 1) << 3) * 2, bf);
-        mma16816(y[0], af, bf[0], bf[1]);
-        mma16816(y[1], af, bf[2], bf[3]);
-      }
-      __syncwarp();
+    };
+    // y += T_blk(a_r, a_c) xs[tile]
+    auto mma_xs = [&](float (&y)[2][4], int a_r, int a_c, int tile) {
+      uint32_t af[4], bf[4];
+      load_a<64>(th_s, a_r, a_c, af);
+      const int mi = lane >> 3, rr = lane & 7;
+      ldsm_x4_t(saddr(S.xs[tile]) + (rr + ((mi & 1) << 3)) * 48 + ((mi >> 1) << 3) * 2, bf);
+      mma16816(y[0], af, bf[0], bf[1]);
+      mma16816(y[1], af, bf[2], bf[3]);
+    };
+    // T_ab = -y into th and its scaled copies tw, tu
+    auto store_t = [&](const float (&y)[2][4], int ab, int bb, int gb) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -520,61 +549,110 @@ __global__ void __launch_bounds__(kThreads, 1)
     // not range-checked: an infinite fp16 value there makes delta infinite or NaN.
     auto solve = [&](int ci) {
       const int gb = ci % 3;
-      {  // diagonal block wb by forward substitution in registers: lane (c, rh) holds rows
-         // 8 rh .. 8 rh + 7 of column c of the block inverse
-        const int c = lane & 15, rh = lane >> 4;
+      {  // Diagonal block wb = [[P, 0], [R, Q]] (8 x 8 parts): P^-1 and Q^-1 by forward
+         // substitution side by side (lane c < 8: column c of P^-1, 8 <= c < 16: column c - 8
+         // of Q^-1), then the lower left block -Q^-1 (R P^-1) by all lanes, in fp32 in wd.
+        float* W = S.wd[wb];
         const float* Ab = &S.adiag[16 * wb][0];
-        float tc[8];
+        {
+          const int c = lane & 7, rb = lane & 8;
+          const float* Ar = Ab + rb * 21;  // A[rb + r][rb + s] = Ar[20 r + s]
+          float x[8];
 #pragma unroll
-        for (int k2 = 0; k2 < 8; ++k2) tc[k2] = (8 * rh + k2 == c) ? 1.f : 0.f;
-        if (rh == 0) {
+          for (int r = 0; r < 8; ++r) x[r] = r == c ? 1.f : 0.f;
 #pragma unroll
-          for (int rr = 1; rr < 8; ++rr) {
+          for (int r = 1; r < 8; ++r) {
             float x0 = 0.f, x1 = 0.f;
 #pragma unroll
-            for (int s2 = 0; s2 < rr; ++s2) {
-              if (s2 & 1) x1 += Ab[rr * 16 + s2] * tc[s2];
-              else x0 += Ab[rr * 16 + s2] * tc[s2];
+            for (int s2 = 0; s2 < r; ++s2) {
+              if (s2 & 1) x1 += Ar[20 * r + s2] * x[s2];
+              else x0 += Ar[20 * r + s2] * x[s2];
             }
-            if (rr > c) tc[rr] = -(x0 + x1);
+            if (r > c) x[r] = -(x0 + x1);
+          }
+          if (lane < 16) {
+#pragma unroll
+            for (int r = 0; r < 8; ++r) W[(rb + r) * 17 + rb + c] = x[r];
           }
         }
-        float y[8];
+        __syncwarp();
+        const int c = lane & 7, m0 = 2 * (lane >> 3);  // rows m0, m0 + 1 of the lower left block
+        {  // Y = R P^-1 into the lower left block
+          float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-        for (int k2 = 0; k2 < 8; ++k2) y[k2] = __shfl_sync(0xffffffffu, tc[k2], c);
-        if (rh == 1) {
-#pragma unroll
-          for (int rr = 8; rr < 16; ++rr) {
-            float x0 = 0.f, x1 = 0.f;
-#pragma unroll
-            for (int s2 = 0; s2 < 8; ++s2) {
-              if (s2 & 1) x1 += Ab[rr * 16 + s2] * y[s2];
-              else x0 += Ab[rr * 16 + s2] * y[s2];
-            }
-#pragma unroll
-            for (int s2 = 8; s2 < rr; ++s2) {
-              if (s2 & 1) x1 += Ab[rr * 16 + s2] * tc[s2 - 8];
-              else x0 += Ab[rr * 16 + s2] * tc[s2 - 8];
-            }
-            if (rr > c) tc[rr - 8] = -(x0 + x1);
+          for (int k = 0; k < 8; ++k) {
+            const float pk = W[k * 17 + c];
+            y0 += Ab[(8 + m0) * 20 + k] * pk;
+            y1 += Ab[(9 + m0) * 20 + k] * pk;
           }
+          W[(8 + m0) * 17 + c] = y0;
+          W[(9 + m0) * 17 + c] = y1;
         }
-        const int col = 16 * wb + c;
-        const float u = S.beta[gb][col], w = u * S.eG[gb][col];
+        __syncwarp();
+        {  // X = -Q^-1 Y in its place
+          float z0 = 0.f, z1 = 0.f;
 #pragma unroll
-        for (int k2 = 0; k2 < 8; ++k2) {
-          const int row = 16 * wb + 8 * rh + k2;
-          st_half(S.th, row, col, tc[k2]);
-          st_half(S.tw, row, col, tc[k2] * w);
-          st_half(S.tu, row, col, tc[k2] * u);
+          for (int m = 0; m < 8; ++m) {
+            const float ym = W[(8 + m) * 17 + c];
+            z0 += W[(8 + m0) * 17 + 8 + m] * ym;
+            z1 += W[(9 + m0) * 17 + 8 + m] * ym;
+          }
+          __syncwarp();
+          W[(8 + m0) * 17 + c] = -z0;
+          W[(9 + m0) * 17 + c] = -z1;
+        }
+        __syncwarp();
+        {  // row r = lane / 2, columns 8 (lane & 1) .. + 7 of the block into th, tw, tu
+          const int r = lane >> 1, col0 = 16 * wb + 8 * (lane & 1);
+          const float* wr = W + r * 17 + 8 * (lane & 1);
+          uint32_t ph[4], pw[4], pu[4];
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            const float v0 = wr[j], v1 = wr[j + 1];
+            const float u0 = S.beta[gb][col0 + j], u1 = S.beta[gb][col0 + j + 1];
+            const float w0 = u0 * S.eG[gb][col0 + j], w1 = u1 * S.eG[gb][col0 + j + 1];
+            ph[j >> 1] = pack_h2(v0, v1);
+            pw[j >> 1] = pack_h2(v0 * w0, v1 * w1);
+            pu[j >> 1] = pack_h2(v0 * u0, v1 * u1);
+          }
+          const uint32_t off = sw128_offset(64, 16 * wb + r, col0);
+          *reinterpret_cast<uint4*>(S.th + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+          *reinterpret_cast<uint4*>(S.tw + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          *reinterpret_cast<uint4*>(S.tu + off) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
         }
       }
       named_bar(1, kPrepThreads);
-      if (wb < 3) off_diag_block(wb + 1, wb, gb);
+      // The off-diagonal blocks by doubling: T_10 and T_32 join the 16-blocks into 32-blocks
+      // (T_ab = -T_aa A_ab T_bb), then the lower left 32-block is -T_BB X with
+      // X = A_BA T_AA (A = blocks 0-1, B = blocks 2-3), whose products with the diagonal
+      // blocks of T_AA are started meanwhile.
+      float x[2][4] = {}, x2[2][4] = {};
+      const int rw = 2 + (wb >> 1);  // warps 0, 2: row block of X
+      if (wb & 1) {
+        mma_blk(x, ah_s, 16 * wb, 16 * (wb - 1), th_s, 16 * (wb - 1), 16 * (wb - 1));
+        frag_to_xs(x, wb);
+        __syncwarp();
+        float y[2][4] = {};
+        mma_xs(y, 16 * wb, 16 * wb, wb);
+        store_t(y, wb, wb - 1, gb);
+      } else {
+        mma_blk(x, ah_s, 16 * rw, 0, th_s, 0, 0);      // A_r0 T_00
+        mma_blk(x2, ah_s, 16 * rw, 16, th_s, 16, 16);  // X_r1 = A_r1 T_11
+      }
       named_bar(1, kPrepThreads);
-      if (wb < 2) off_diag_block(wb + 2, wb, gb);
+      if (!(wb & 1)) {
+        mma_blk(x, ah_s, 16 * rw, 16, th_s, 16, 0);    // X_r0 = A_r0 T_00 + A_r1 T_10
+        frag_to_xs(x, wb);                              // X_20, X_21, X_30, X_31 -> xs[0..3]
+        frag_to_xs(x2, wb + 1);
+      }
       named_bar(1, kPrepThreads);
-      if (wb == 0) off_diag_block(3, 0, gb);
+      {  // warp wb: T_{r c}, r = 2 + wb / 2, c = wb % 2:  T_2c = -T_22 X_2c,
+         // T_3c = -(T_32 X_2c + T_33 X_3c)
+        float y[2][4] = {};
+        if (rw == 3) mma_xs(y, 48, 32, wb & 1);
+        mma_xs(y, 16 * rw, 16 * rw, wb);
+        store_t(y, rw, wb & 1, gb);
+      }
       fence_async_smem();
       arrive(S, B_T);
       named_bar(1, kPrepThreads);  // the next gram rewrites A
@@ -688,25 +766,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p == 0) S.gamma[gb] = __expf(GL);
       }
       if (!named_bar_and(3, kConvThreads, !aborted(S))) break;
-      {  // row t: its own 16-block directly, the factor to each earlier block's last row
-        const int t = p, at = t >> 4;
-        const float Gt = S.G[gb][t];
-        float dd[16];
+      {  // row t: its own 16-block directly, the factor to each earlier block's last row;
+         // the A rows' copies carry beta_t and leave out s = t
+        const int t = p, at = t >> 4, k0 = t & 15;
+        const float Gt = S.G[gb][t], bt = S.beta[gb][t];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float x = __expf(Gt - S.G[gb][16 * at + k]);
-          dd[k] = k <= (t & 15) ? x : 0.f;
+        for (int k4 = 0; k4 < 16; k4 += 4) {
+          float d[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d[i] = __expf(Gt - S.G[gb][16 * at + k4 + i]);
+          *reinterpret_cast<float4*>(&S.ddO[t][k4]) =
+              make_float4(k4 + 0 <= k0 ? d[0] : 0.f, k4 + 1 <= k0 ? d[1] : 0.f,
+                          k4 + 2 <= k0 ? d[2] : 0.f, k4 + 3 <= k0 ? d[3] : 0.f);
+          *reinterpret_cast<float4*>(&S.ddA[t][k4]) =
+              make_float4(k4 + 0 < k0 ? bt * d[0] : 0.f, k4 + 1 < k0 ? bt * d[1] : 0.f,
+                          k4 + 2 < k0 ? bt * d[2] : 0.f, k4 + 3 < k0 ? bt * d[3] : 0.f);
         }
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4)
-          *reinterpret_cast<float4*>(&S.ddiag[t][4 * (k4 ^ (t & 3))]) =
-              make_float4(dd[4 * k4], dd[4 * k4 + 1], dd[4 * k4 + 2], dd[4 * k4 + 3]);
         float4 f;
         f.x = at > 0 ? __expf(Gt - S.G[gb][15]) : 0.f;
         f.y = at > 1 ? __expf(Gt - S.G[gb][31]) : 0.f;
         f.z = at > 2 ? __expf(Gt - S.G[gb][47]) : 0.f;
         f.w = 0.f;
-        *reinterpret_cast<float4*>(&S.rf[t][0]) = f;
+        *reinterpret_cast<float4*>(&S.rfO[t][0]) = f;
+        *reinterpret_cast<float4*>(&S.rfA[t][0]) = make_float4(bt * f.x, bt * f.y, bt * f.z, 0.f);
       }
       if (MODE == kEmit) wait_bar(S, B_SQ, ci & 1);  // [S ; QK] has read the bf16 Q
       arrive(S, B_TB);
