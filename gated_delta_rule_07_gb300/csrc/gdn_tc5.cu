@@ -167,9 +167,7 @@ __device__ __forceinline__ void set_abort(Smem& S) {
 // Bounded wait for the phase with the given parity, suspended in hardware between tries.  On
 // giving up (about a second, or at once when another thread already gave up) it records the
 // abort flag; the caller carries on and leaves at its next group-uniform check.
-__device__ __forceinline__ void wait_bar(Smem& S, int bar, uint32_t parity) {
-  const uint32_t a = saddr(&S.bars[bar]);
-  if (mbar_try(a, parity)) return;
+__device__ __noinline__ void wait_bar_slow(Smem& S, uint32_t a, uint32_t parity) {
   const long long t_end = clock64() + kWaitCycles;
   while (!mbar_try(a, parity)) {
     if (clock64() > t_end || aborted(S)) {
@@ -177,6 +175,11 @@ __device__ __forceinline__ void wait_bar(Smem& S, int bar, uint32_t parity) {
       return;
     }
   }
+}
+__device__ __forceinline__ void wait_bar(Smem& S, int bar, uint32_t parity) {
+  const uint32_t a = saddr(&S.bars[bar]);
+  if (mbar_try(a, parity)) return;
+  wait_bar_slow(S, a, parity);
 }
 __device__ __forceinline__ void arrive(Smem& S, int bar) { mbar_arrive(saddr(&S.bars[bar])); }
 
