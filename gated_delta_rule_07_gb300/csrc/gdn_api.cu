@@ -92,13 +92,15 @@ gdn_status to_status(cudaError_t e) {
   } while (0)
 
 struct Layout {
-  size_t status, M, U, h_in, w, u, gcum, total;
+  size_t status, M, U, h_in, w, u, gcum, wy, total;
 };
 
-// Workspace: [status word | M | U | h_in | w | u | gcum], each piece 256-byte aligned.  The
-// summaries and incoming states exist only for P > 1; the materialised chunk factors only on
-// the SIMT path (the tensor-core kernels recompute them on chip).
-Layout layout(const gdn_problem* p) {
+// Workspace: [status word | M | U | h_in | w | u | gcum | records], each piece 256-byte
+// aligned.  The summaries and incoming states exist only for P > 1; the materialised chunk
+// factors only on the SIMT path (the tensor-core kernels recompute them on chip); the records
+// (-w^T, fp16 K and the decay of each chunk, 33,280 bytes per chunk and value head) only on
+// the tcgen05 path with P > 1, where the U summary writes them and the M summary reads them.
+Layout layout(const gdn_problem* p, bool records = true) {
   Layout L;
   const size_t S = (size_t)p->num_seqs * p->segments_per_seq * p->hv;
   const size_t K = p->k_dim, V = p->v_dim, T = (size_t)p->total_tokens;
@@ -119,6 +121,10 @@ Layout layout(const gdn_problem* p) {
   off += mat ? align_up(T * p->hv * V * 4) : 0;
   L.gcum = off;
   off += mat ? align_up(T * p->hv * 4) : 0;
+  L.wy = off;  // tcgen05 path: the U summary's per-chunk records for the M summary
+  off += (records && seg && !mat && !use_mma_sync(p))
+             ? align_up(gdn::tc5_records_bytes(p->total_tokens, p->num_seqs, p->hv))
+             : 0;
   L.total = off;
   return L;
 }
@@ -153,6 +159,14 @@ size_t gdn_workspace_size(const gdn_problem* p) {
   if (check_problem(p) != GDN_OK) return 0;
   return layout(p).total;
 }
+
+}  // extern "C"
+
+size_t gdn::workspace_min_bytes(const gdn_problem* p) {
+  return check_problem(p) != GDN_OK ? 0 : layout(p, false).total;
+}
+
+extern "C" {
 
 gdn_status gdn_chunk_prepare(const gdn_problem* p, const void* k, const void* v, const float* g,
                              const float* beta, const int32_t* cu_seqlens, void* w, void* u,
@@ -235,7 +249,8 @@ gdn_status gdn_forward(const gdn_problem* p, const void* q, const void* k, const
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(h0) ||
       !aligned16(h_final))
     return GDN_ERR_INVALID_ARGUMENT;
-  const Layout L = layout(p);
+  // The records are optional: without room for them both summaries compute their factors.
+  const Layout Lr = layout(p, true), L = ws_bytes >= Lr.total ? Lr : layout(p, false);
   if (!workspace || ws_bytes < L.total || !aligned16(workspace)) return GDN_ERR_WORKSPACE;
   char* ws = static_cast<char*>(workspace);
   int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
@@ -251,6 +266,8 @@ gdn_status gdn_forward(const gdn_problem* p, const void* q, const void* k, const
     a.M = a.M_out;
     a.U = a.U_out;
     a.h_in_out = reinterpret_cast<float*>(ws + L.h_in);
+    if (use_tensor_path(p) && !use_mma_sync(p) && L.total == Lr.total && Lr.total > Lr.wy)
+      a.wy = ws + L.wy;
   }
   // With P = 1 the incoming state of the only segment is h0 itself.
   a.h_in = seg ? a.h_in_out : h0;

@@ -23,6 +23,7 @@ struct Args {
   const int32_t* cu;
   void* out;
   void *w_out, *u_out;
+  void* wy;  // tcgen05 summaries: per-chunk factor records written by the U half (nullable)
   float* gcum_out;
   float *M_out, *U_out, *h_in_out, *h_final;
   int32_t* status;
@@ -50,6 +51,10 @@ cudaError_t tc_emit(const Args& a, bool fused_prepare, cudaStream_t s);
 // Tensor-core kernels, tcgen05 generation (TMEM accumulators, fp16 operands, fp32 state;
 // bf16 I/O, K = V = 128).  Factors are always recomputed on chip.
 size_t tc5_smem_bytes();
+// Workspace bytes gdn_forward needs without the optional factor records.
+size_t workspace_min_bytes(const gdn_problem* p);
+// Bytes of the per-chunk factor records the U summary stores for the M summary.
+size_t tc5_records_bytes(int64_t T, int N, int hv);
 cudaError_t tc5_summary(const Args& a, cudaStream_t s);
 cudaError_t tc5_emit(const Args& a, cudaStream_t s);
 

@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "gdn.h"
+#include "gdn_internal.h"
 
 namespace {
 
@@ -66,7 +67,7 @@ gdn_status gdn_forward_static_scratch(const gdn_problem* p, const void* q, const
                                       float* h_final, cudaStream_t stream) {
   const gdn_status st = gdn_check_problem(p);
   if (st != GDN_OK) return st;
-  const size_t need = gdn_workspace_size(p);
+  const size_t need = gdn::workspace_min_bytes(p);  // the factor records are optional
   if (need > kStaticScratchBytes) return GDN_ERR_WORKSPACE;
   void* scratch = nullptr;
   const gdn_status ss = scratch_for_current_device(&scratch);

@@ -59,7 +59,14 @@ constexpr int kThreads = kChainThreads + kPrepThreads + 64 + kConvThreads;
 constexpr long long kWaitCycles = 2000000000LL;  // about a second at GB300 clocks
 constexpr float kHalfMax = 65504.f;
 
-enum Mode { kEmit = 0, kSumM = 1, kSumU = 2 };
+// kSumML is the M half when the U half has stored each chunk's factors (-w^T, fp16 K and the
+// decay of the state update) in the workspace: it only loads them and runs the chain.
+enum Mode { kEmit = 0, kSumM = 1, kSumU = 2, kSumML = 3 };
+
+// Per-chunk factor record in the workspace: the MN-major fp16 tiles -w^T [i][t] and K [t][i]
+// as they sit in shared memory, then e^{G_last - G_t} (64 floats) and gamma.
+constexpr uint32_t kRecNw = 0, kRecKh = 16384, kRecTbl = 32768, kRecTblBytes = 272;
+constexpr size_t kRecBytes = 33280;
 
 // TMEM columns (512 allocated)
 constexpr uint32_t TM_SQ = 0;    // [S ; QK]               64 fp32
@@ -81,17 +88,18 @@ enum Bar {
   B_D,         // delta^T = u^T + D^T is in TMEM                      MMA commit
   B_DR,        // fp16 delta, delta' are in TMEM                      chain (256)
   B_H,         // Dh^T and o^T are complete                           MMA commit
-  B_L0, B_L1,  // stage loaded: byte count plus 32 cp.async arrivals  loader
-  B_F0, B_F1,  // stage free (its chunk's w, u and q_g h products are done)  MMA commit
+  B_L0, B_L1, B_L2,  // stage loaded: byte count (+ 32 cp.async arrivals)  loader
+  B_F0, B_F1, B_F2,  // stage free (its chunk's w, u and q_g h products are done)  MMA commit
   B_KF0, B_KF1,  // fp16 K tile free (its chunk's Dh is done)         MMA commit
   B_END,       // every product issued has completed                  MMA commit
   kNumBars
 };
+template <int MODE>
 __device__ __forceinline__ uint32_t bar_count(int b) {
   return (b == B_E2 || b == B_T || b == B_WR)  ? (uint32_t)kPrepThreads
          : (b == B_TB || b == B_CV)            ? (uint32_t)kConvThreads
          : (b == B_HR || b == B_DR)            ? (uint32_t)kChainThreads
-         : (b == B_L0 || b == B_L1)            ? 33u
+         : (b >= B_L0 && b <= B_L2)            ? (MODE == kSumML ? 1u : 33u)
                                                : 1u;
 }
 
@@ -120,6 +128,7 @@ struct Smem {
   alignas(16) float rfA[C][4];
   alignas(16) float rfO[C][4];
   alignas(16) float cf[C];
+  alignas(16) float tbl[3][68];  // kSumML: e^{G_last - G_t} and gamma of a staged record
   uint64_t bars[kNumBars];
   uint32_t tmem_base;
   int abort_flag;
@@ -250,6 +259,37 @@ __device__ __forceinline__ float to_half_chunks(const uint8_t* src, uint8_t* dst
   return fmaxf(mk[0], mk[1]);
 }
 
+// Bulk copies (no tensor map): global -> shared completing on an mbarrier, and shared ->
+// global in a bulk group.  Sizes are multiples of 16 bytes, addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(mbar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(src), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {  // sources of earlier bulk stores reusable
+  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {  // earlier bulk stores complete
+  asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+}
+// The record of chunk cg (index within sequence n, which starts at token sb) of value head j:
+// slots are the 64-token windows of the packed token axis, plus n so that a sequence's last,
+// partial chunk and the next sequence's first chunk never share one.
+__device__ __forceinline__ char* chunk_record(const Args& a, int n, int64_t sb, int64_t cg,
+                                              int j) {
+  const int64_t slot = ((sb + C * cg) >> 6) + n;
+  return static_cast<char*>(a.wy) + (slot * a.hv + j) * (int64_t)kRecBytes;
+}
+
 // ------------------------------------------------------------------ the kernel
 
 template <int MODE>
@@ -272,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- setup: mbarriers, TMEM
   if (tid == 0) {
-    for (int b = 0; b < kNumBars; ++b) mbar_init(saddr(&S.bars[b]), bar_count(b));
+    for (int b = 0; b < kNumBars; ++b) mbar_init(saddr(&S.bars[b]), bar_count<MODE>(b));
     S.abort_flag = 0;
     S.range_bad = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -281,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(saddr(&S.tmem_base), 512);
     tmem_relinquish();
   }
-  if (tid == kChainThreads) {
+  if (MODE != kSumML && tid == kChainThreads) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
     if (MODE == kEmit)
       asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
@@ -292,6 +332,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   fence_after_sync();
   const uint32_t tm = S.tmem_base;
+  // -w^T of chunk ci; the U half keeps two, the second in the attn_i tiles it has no use for,
+  // so that the copy of one into the chunk's record overlaps the next chunk
+  auto nw_tile = [&](int ci) -> uint8_t* {
+    return (MODE == kSumU && (ci & 1)) ? S.att[0] : S.nw;
+  };
+  // kSumML stages: the -w^T and K tiles of a record, 32 KB each, in the K | Q and V tiles
+  auto rec_stage = [&](int st) -> uint8_t* { return st == 0 ? S.kq[0] : st == 1 ? S.kq[1] : S.v[0]; };
 
   if (warp < 8) {
     // =============================================================== chain (256 threads)
@@ -308,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = 64 * hf + q;
         float x = 0.f;
         if (MODE == kEmit) x = src ? src[i * VD + c] : 0.f;
-        if (MODE == kSumM) x = (i == c) ? 1.f : 0.f;
+        if (MODE == kSumM || MODE == kSumML) x = (i == c) ? 1.f : 0.f;
         h[q] = x;
       }
     }
@@ -333,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int gb = ci % 3;
       const int64_t t0 = sb + (c0 + ci) * C;
       const int L = (int)((se - t0) < C ? (se - t0) : C);
+      const float* eglg = MODE == kSumML ? S.tbl[gb] : S.eGLG[gb];
       // ---- delta = u + D -> fp16 delta (into D's columns) and delta' (into u's columns)
       wait_bar(S, B_D, ci & 1);
       fence_after_sync();
@@ -346,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int t = 32 * hf + 16 * piece + 2 * q;
           range_ok = range_ok && fits_half(d[2 * q]) && fits_half(d[2 * q + 1]);
           pd[q] = pack_h2(d[2 * q], d[2 * q + 1]);
-          pp[q] = pack_h2(d[2 * q] * S.eGLG[gb][t], d[2 * q + 1] * S.eGLG[gb][t + 1]);
+          pp[q] = pack_h2(d[2 * q] * eglg[t], d[2 * q + 1] * eglg[t + 1]);
         }
         if (MODE == kEmit) tmem_st8(tm + lane_bits + TM_DO + 32 * hf + 8 * piece, pd);
         tmem_st8(tm + lane_bits + TM_U + 32 * hf + 8 * piece, pp);
@@ -358,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_bar(S, B_H, ci & 1);
       fence_after_sync();
       {
-        const float gam = S.gamma[gb];
+        const float gam = MODE == kSumML ? S.tbl[gb][64] : S.gamma[gb];
 #pragma unroll
         for (int piece = 0; piece < 4; ++piece) {
           float dh[16];
@@ -399,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* dst = nullptr;
     if (MODE == kEmit) {
       if (a.h_final && r == a.P - 1) dst = a.h_final + ((int64_t)n_seq * a.hv + j) * KD * VD;
-    } else if (MODE == kSumM) {
+    } else if (MODE == kSumM || MODE == kSumML) {
       dst = a.M_out + ((int64_t)seg * a.hv + j) * KD * KD;
     } else {
       dst = a.U_out + ((int64_t)seg * a.hv + j) * KD * VD;
@@ -409,6 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = 0; q < 64; ++q) dst[(64 * hf + q) * VD + c] = h[q];
     }
   } else if (warp < 12) {
+    if (MODE != kSumML) {  // (kSumML loads what the prepare warps compute)
     // =============================================================== prepare (128 threads)
     const int pt = tid - kChainThreads;       // 0..127 = TMEM lane of this thread
     const int wb = warp - 8;                  // 0..3: this warp's 16-row block of T
@@ -677,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pk.y = pack_h2(-wv[8 * ch + 2], -wv[8 * ch + 3]);
           pk.z = pack_h2(-wv[8 * ch + 4], -wv[8 * ch + 5]);
           pk.w = pack_h2(-wv[8 * ch + 6], -wv[8 * ch + 7]);
-          *reinterpret_cast<uint4*>(S.nw + sw128_offset(128, i, 32 * hb + 8 * ch)) = pk;
+          *reinterpret_cast<uint4*>(nw_tile(ci) + sw128_offset(128, i, 32 * hb + 8 * ch)) = pk;
         }
       }
       fence_async_smem();
@@ -695,11 +744,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       solve(ci);
       if (ci + 1 < nch) gram(ci + 1);
       neg_w(ci);
+      // the U half stores -w^T for the M half; the tile is rewritten two chunks later, and
+      // this thread has seen its earlier copy read before the barrier of the chunk between
+      if (MODE == kSumU && a.wy && pt == 0) bulk_wait_read();
       go = named_bar_and(1, kPrepThreads, !aborted(S));  // also: the gram's A is complete
+      if (MODE == kSumU && a.wy && pt == 0 && go)
+        bulk_s2g(chunk_record(a, n_seq, sb, c0 + ci, j) + kRecNw, saddr(nw_tile(ci)), 16384);
+    }
+    if (MODE == kSumU && a.wy && pt == 0) bulk_wait_all();
     }
   } else if (warp == 13) {
     // =============================================================== loader (1 warp)
-    for (int ci = 0; ci < nch; ++ci) {
+    if (MODE == kSumML) {  // the records of the U half, three stages
+      for (int ci = 0; ci < nch; ++ci) {
+        const int st = ci % 3;
+        if (ci >= 3) wait_bar(S, B_F0 + st, ((ci / 3) + 1) & 1);
+        if (__any_sync(0xffffffffu, aborted(S))) break;
+        if (lane == 0) {
+          const char* rec = chunk_record(a, n_seq, sb, c0 + ci, j);
+          const uint32_t bar = saddr(&S.bars[B_L0 + st]);
+          const uint32_t dst = saddr(rec_stage(st));
+          mbar_expect_tx(bar, 32768u + kRecTblBytes);
+          bulk_g2s(dst, rec + kRecNw, 16384u, bar);
+          bulk_g2s(dst + 16384u, rec + kRecKh, 16384u, bar);
+          bulk_g2s(saddr(S.tbl[st]), rec + kRecTbl, kRecTblBytes, bar);
+        }
+        __syncwarp();
+      }
+    }
+    for (int ci = 0; MODE != kSumML && ci < nch; ++ci) {
       const int sg = ci & 1;
       // the stage was last used by chunk ci - 2: wait for its w, u (and q_g h) products
       if (ci >= 2) wait_bar(S, B_F0 + sg, ((ci >> 1) + 1) & 1);
@@ -735,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // =============================================================== converter (64 threads)
     const int p = tid - (kThreads - kConvThreads);  // 0..63
     float maxabs = 0.f;
-    for (int ci = 0; ci < nch; ++ci) {
+    for (int ci = 0; MODE != kSumML && ci < nch; ++ci) {
       const int sg = ci & 1, gb = ci % 3;
       const int64_t t0 = sb + (c0 + ci) * C;
       const int L = (int)((se - t0) < C ? (se - t0) : C);
@@ -767,7 +840,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         S.cf[p] = __expf(e0 - x0);
         S.cf[p + 32] = __expf(e1 - x1);
         if (p == 0) S.gamma[gb] = __expf(GL);
+        if (MODE == kSumU && a.wy) {  // the state update's decay, for the M half
+          float* tb = reinterpret_cast<float*>(chunk_record(a, n_seq, sb, c0 + ci, j) + kRecTbl);
+          tb[p] = S.eGLG[gb][p];
+          tb[p + 32] = S.eGLG[gb][p + 32];
+          if (p == 0) tb[64] = S.gamma[gb];
+        }
       }
+      // the K tile stored two chunks back has been read before it is rewritten
+      if (MODE == kSumU && a.wy && p == 0) bulk_wait_read();
       if (!named_bar_and(3, kConvThreads, !aborted(S))) break;
       {  // row t: its own 16-block directly, the factor to each earlier block's last row;
          // the A rows' copies carry beta_t and leave out s = t
@@ -811,6 +892,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           maxabs = to_half_chunks<4, false>(kb + (k0 >> 3) * 16384 + 1024 * (k0 & 7),
                                             kd + (k0 >> 3) * 8192 + 1024 * (k0 & 7), nullptr, maxabs);
       }
+      if (MODE == kSumU && a.wy) {  // fp16 K into the chunk's record, for the M half
+        fence_async_smem();
+        named_bar(3, kConvThreads);
+        if (p == 0)
+          bulk_s2g(chunk_record(a, n_seq, sb, c0 + ci, j) + kRecKh, saddr(S.kh[sg]), 16384);
+      }
       if (MODE == kEmit) {  // q_g = diag(e^G) Q as fp16, in place: the K-major B of q_g h
         uint8_t* qb = S.kq[sg] + 8192 + 16 * p;
 #pragma unroll 1
@@ -825,6 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       arrive(S, B_CV);
     }
     if (!(maxabs <= kHalfMax)) S.range_bad = 1;
+    if (MODE == kSumU && a.wy && p == 0) bulk_wait_all();
   } else {
     // =============================================================== MMA (warp 12)
     // Fixed order per chunk c: w, u (c); q_g h (c); D (c); O2, Dh (c); [S ; QK] (c + 2).  Every lane
@@ -836,6 +924,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ID_QH = idesc_f16(128, 64, 0, 0);              // h^T q_g^T
     const uint32_t ID_O2 = idesc_f16(128, 64, 0, 0);              // delta^T attn_i^T
     const uint32_t ID_DH = idesc_f16(128, 128, 0, 1);             // delta'^T K
+    if (MODE == kSumML) {  // D and Dh of each loaded record
+      for (int ci = 0; ci < nch; ++ci) {
+        const int st = ci % 3;
+        const uint32_t nw = saddr(rec_stage(st)), khs = nw + 16384u;
+        wait_bar(S, B_L0 + st, (ci / 3) & 1);
+        wait_bar(S, B_HR, ci & 1);
+        fence_after_sync();
+        if (leader) {
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ts(tm + TM_DO, tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3),
+                   sdesc(nw + ks * 2048, 16384, 1024), ID_D, ks > 0);
+          mma_commit(saddr(&S.bars[B_D]));
+        }
+        __syncwarp();
+        wait_bar(S, B_DR, ci & 1);
+        fence_after_sync();
+        if (leader) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ts(tm + TM_H, tm + TM_U + 32 * (ks >> 1) + 8 * (ks & 1),
+                   sdesc(khs + ks * 2048, 8192, 1024), ID_DH, ks > 0);
+          mma_commit(saddr(&S.bars[B_H]));
+          mma_commit(saddr(&S.bars[B_F0 + st]));
+        }
+        __syncwarp();
+        if (__any_sync(0xffffffffu, aborted(S))) break;
+      }
+    }
     auto sq = [&](int ci) {
       if (leader) {
         const uint32_t kq = saddr(S.kq[ci & 1]);
@@ -848,7 +965,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
-    if (nch > 0) {
+    if (MODE != kSumML && nch > 0) {
       wait_bar(S, B_L0, 0);
       sq(0);
       if (nch > 1) {  // the SQ columns are reused once the first gram has read them
@@ -857,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         sq(1);
       }
     }
-    for (int ci = 0; ci < nch; ++ci) {
+    for (int ci = 0; MODE != kSumML && ci < nch; ++ci) {
       const uint32_t khs = saddr(S.kh[ci & 1]), vv = saddr(S.v[ci & 1]);
       // w^T = K^T T_w^T ;  u^T = V^T T_u^T; then the stage is free for the loader
       wait_bar(S, B_T, ci & 1);
@@ -895,7 +1012,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (MODE != kEmit) wait_bar(S, B_HR, ci & 1);
       fence_after_sync();
       if (leader) {
-        const uint32_t nw = saddr(S.nw);
+        const uint32_t nw = saddr(nw_tile(ci));
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           mma_ts(tm + TM_DO, tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3),
@@ -992,10 +1109,12 @@ cudaError_t launch5(const Args& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   CUtensorMap mk, mq, mv;
   const bool empty = a.T == 0;
-  if ((e = make_map(&mk, empty ? nullptr : a.k, a.T, a.hk)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, empty || MODE == kSumML ? nullptr : a.k, a.T, a.hk)) != cudaSuccess)
+    return e;
   if ((e = make_map(&mq, empty || MODE != kEmit ? nullptr : a.q, a.T, a.hk)) != cudaSuccess)
     return e;
-  if ((e = make_map(&mv, empty || MODE == kSumM ? nullptr : a.v, a.T, a.hv)) != cudaSuccess)
+  if ((e = make_map(&mv, empty || MODE == kSumM || MODE == kSumML ? nullptr : a.v, a.T, a.hv)) !=
+      cudaSuccess)
     return e;
   tc5_chunk_kernel<MODE><<<grid, kThreads, smem, s>>>(a, mk, mq, mv);
   return cudaGetLastError();
@@ -1005,7 +1124,19 @@ cudaError_t launch5(const Args& a, cudaStream_t s) {
 
 size_t tc5_smem_bytes() { return sizeof(Smem) + 1024; }
 
+// one record per (64-token window of the packed token axis, plus one per sequence, value head)
+size_t tc5_records_bytes(int64_t T, int N, int hv) {
+  return ((size_t)(T / C) + (size_t)N + 1) * (size_t)hv * kRecBytes;
+}
+
+// With records (a.wy), the U half runs first and stores each chunk's -w^T, fp16 K and decay,
+// and the M half only loads them; without, each half computes its own factors.
 cudaError_t tc5_summary(const Args& a, cudaStream_t s) {
+  if (a.wy) {
+    cudaError_t e = launch5<kSumU>(a, s);
+    if (e != cudaSuccess) return e;
+    return launch5<kSumML>(a, s);
+  }
   cudaError_t e = launch5<kSumM>(a, s);
   if (e != cudaSuccess) return e;
   return launch5<kSumU>(a, s);
