@@ -98,8 +98,9 @@ struct Layout {
 // Workspace: [status word | M | U | h_in | w | u | gcum | records], each piece 256-byte
 // aligned.  The summaries and incoming states exist only for P > 1; the materialised chunk
 // factors only on the SIMT path (the tensor-core kernels recompute them on chip); the records
-// (-w^T, fp16 K and the decay of each chunk, 33,280 bytes per chunk and value head) only on
-// the tcgen05 path with P > 1, where the U summary writes them and the M summary reads them.
+// (-w^T, fp16 K, u^T and the decay of each chunk, 49,664 bytes per chunk and value head) only
+// on the tcgen05 path with P > 1, where the U summary writes them and the M summary and the
+// emit kernel read them.
 Layout layout(const gdn_problem* p, bool records = true) {
   Layout L;
   const size_t S = (size_t)p->num_seqs * p->segments_per_seq * p->hv;

@@ -59,14 +59,17 @@ constexpr int kThreads = kChainThreads + kPrepThreads + 64 + kConvThreads;
 constexpr long long kWaitCycles = 2000000000LL;  // about a second at GB300 clocks
 constexpr float kHalfMax = 65504.f;
 
-// kSumML is the M half when the U half has stored each chunk's factors (-w^T, fp16 K and the
-// decay of the state update) in the workspace: it only loads them and runs the chain.
-enum Mode { kEmit = 0, kSumM = 1, kSumU = 2, kSumML = 3 };
+// With per-chunk factor records in the workspace, the U half stores each chunk's -w^T, fp16 K,
+// u^T and the state update's decay; kSumML (the M half) and kEmitR (phase 3) load them instead
+// of computing them, and run only what depends on the state (kEmitR also forms attn_i and q_g).
+enum Mode { kEmit = 0, kSumM = 1, kSumU = 2, kSumML = 3, kEmitR = 4 };
 
-// Per-chunk factor record in the workspace: the MN-major fp16 tiles -w^T [i][t] and K [t][i]
-// as they sit in shared memory, then e^{G_last - G_t} (64 floats) and gamma.
-constexpr uint32_t kRecNw = 0, kRecKh = 16384, kRecTbl = 32768, kRecTblBytes = 272;
-constexpr size_t kRecBytes = 33280;
+// Record layout: the fp16 tiles -w^T [i][t] (MN-major), K [t][i] (MN-major) and u^T [c][t]
+// (128-byte swizzled rows) as they sit in shared memory, then e^{G_last - G_t} (64 floats) and
+// gamma.
+constexpr uint32_t kRecNw = 0, kRecKh = 16384, kRecU = 32768, kRecTbl = 49152;
+constexpr uint32_t kRecTblBytes = 272;
+constexpr size_t kRecBytes = 49664;
 
 // TMEM columns (512 allocated)
 constexpr uint32_t TM_SQ = 0;    // [S ; QK]               64 fp32
@@ -91,6 +94,8 @@ enum Bar {
   B_L0, B_L1, B_L2,  // stage loaded: byte count (+ 32 cp.async arrivals)  loader
   B_F0, B_F1, B_F2,  // stage free (its chunk's w, u and q_g h products are done)  MMA commit
   B_KF0, B_KF1,  // fp16 K tile free (its chunk's Dh is done)         MMA commit
+  B_RL0, B_RL1,  // kEmitR: a record is staged (byte count)              loader
+  B_RF0, B_RF1,  // kEmitR: its record stage is free (D, O2, Dh done)    MMA commit
   B_END,       // every product issued has completed                  MMA commit
   kNumBars
 };
@@ -100,6 +105,7 @@ __device__ __forceinline__ uint32_t bar_count(int b) {
          : (b == B_TB || b == B_CV)            ? (uint32_t)kConvThreads
          : (b == B_HR || b == B_DR)            ? (uint32_t)kChainThreads
          : (b >= B_L0 && b <= B_L2)            ? (MODE == kSumML ? 1u : 33u)
+         : (b == B_RL0 || b == B_RL1)          ? 1u
                                                : 1u;
 }
 
@@ -302,7 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int seg = blockIdx.x, j = blockIdx.y;
   const int n_seq = seg / a.P, r = seg % a.P;
-  if (MODE != kEmit && r == a.P - 1 && a.skip_last_summary) return;
+  constexpr bool OUT = MODE == kEmit || MODE == kEmitR;  // phase 3: outputs o
+  if (!OUT && r == a.P - 1 && a.skip_last_summary) return;
   const int kh = j / (a.hv / a.hk);
   int64_t sb, se;
   if (!seq_bounds(a.cu, n_seq, a.T, a.status, sb, se)) return;
@@ -323,9 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (MODE != kSumML && tid == kChainThreads) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
-    if (MODE == kEmit)
+    if (OUT)
       asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
-    if (MODE != kSumM)
+    if (MODE != kSumM && MODE != kEmitR)
       asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
   }
   fence_before_sync();
@@ -349,12 +356,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     float h[64];                              // h^T[c][64 hf .. 64 hf + 63]
     {
       const float* src = nullptr;
-      if (MODE == kEmit && a.h_in) src = a.h_in + ((int64_t)seg * a.hv + j) * KD * VD;
+      if (OUT && a.h_in) src = a.h_in + ((int64_t)seg * a.hv + j) * KD * VD;
 #pragma unroll
       for (int q = 0; q < 64; ++q) {
         const int i = 64 * hf + q;
         float x = 0.f;
-        if (MODE == kEmit) x = src ? src[i * VD + c] : 0.f;
+        if (OUT) x = src ? src[i * VD + c] : 0.f;
         if (MODE == kSumM || MODE == kSumML) x = (i == c) ? 1.f : 0.f;
         h[q] = x;
       }
@@ -383,11 +390,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float* eglg = MODE == kSumML ? S.tbl[gb] : S.eGLG[gb];
       // ---- delta = u + D -> fp16 delta (into D's columns) and delta' (into u's columns)
       wait_bar(S, B_D, ci & 1);
+      if (MODE == kEmitR) wait_bar(S, B_RL0 + (ci & 1), (ci >> 1) & 1);  // u^T of the record
       fence_after_sync();
 #pragma unroll
       for (int piece = 0; piece < 2; ++piece) {
         float d[16];
         tmem_ld16(tm + lane_bits + TM_DO + 32 * hf + 16 * piece, d);
+        if (MODE == kEmitR) {  // u^T[c][t], fp16, 128-byte swizzled rows
+          const uint8_t* ur = S.v[ci & 1] + c * 128;
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int ch = 4 * hf + 2 * piece + h2;
+            const uint4 x = *reinterpret_cast<const uint4*>(ur + ((ch ^ (c & 7)) << 4));
+            const uint32_t* xw = reinterpret_cast<const uint32_t*>(&x);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw[i]));
+              d[8 * h2 + 2 * i] += f.x;
+              d[8 * h2 + 2 * i + 1] += f.y;
+            }
+          }
+        }
         uint32_t pd[8], pp[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -396,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           pd[q] = pack_h2(d[2 * q], d[2 * q + 1]);
           pp[q] = pack_h2(d[2 * q] * eglg[t], d[2 * q + 1] * eglg[t + 1]);
         }
-        if (MODE == kEmit) tmem_st8(tm + lane_bits + TM_DO + 32 * hf + 8 * piece, pd);
+        if (OUT) tmem_st8(tm + lane_bits + TM_DO + 32 * hf + 8 * piece, pd);
         tmem_st8(tm + lane_bits + TM_U + 32 * hf + 8 * piece, pp);
       }
       fence_before_sync();
@@ -417,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ci + 1 < nch) publish_h();
       uint32_t ob[16];
-      if (MODE == kEmit) {
+      if (OUT) {
 #pragma unroll
         for (int piece = 0; piece < 2; ++piece) {
           float o[16];
@@ -428,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_before_sync();
       if (ci + 1 < nch) arrive(S, B_HR);
-      if (MODE == kEmit) {  // o[t][j][c] for t = 32 hf .. 32 hf + 31
+      if (OUT) {  // o[t][j][c] for t = 32 hf .. 32 hf + 31
         const int64_t stride = (int64_t)a.hv * VD;
         __nv_bfloat16* po = out + ((t0 + 32 * hf) * a.hv + j) * VD + c;
         const int nt = L - 32 * hf;
@@ -445,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!range_ok) S.range_bad = 1;
     // ---- the final state: h^T[c][i] = h[i][c]
     float* dst = nullptr;
-    if (MODE == kEmit) {
+    if (OUT) {
       if (a.h_final && r == a.P - 1) dst = a.h_final + ((int64_t)n_seq * a.hv + j) * KD * VD;
     } else if (MODE == kSumM || MODE == kSumML) {
       dst = a.M_out + ((int64_t)seg * a.hv + j) * KD * KD;
@@ -468,8 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the strictly upper blocks of T diag(.), rows 0-31 x columns 32-63 of A and attn_i, and the
     // upper right 8 x 8 of each warp's fp32 block of T are zero for every chunk
     for (int e = pt; e < 64 * 128 / 16; e += kPrepThreads) {
-      reinterpret_cast<uint4*>(S.tw)[e] = make_uint4(0u, 0u, 0u, 0u);
-      reinterpret_cast<uint4*>(S.tu)[e] = make_uint4(0u, 0u, 0u, 0u);
+      if (MODE != kEmitR) {  // (kEmitR stages records there)
+        reinterpret_cast<uint4*>(S.tw)[e] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(S.tu)[e] = make_uint4(0u, 0u, 0u, 0u);
+      }
       reinterpret_cast<uint4*>(S.ah)[e] = make_uint4(0u, 0u, 0u, 0u);
       reinterpret_cast<uint4*>(S.att[0])[e] = make_uint4(0u, 0u, 0u, 0u);
       reinterpret_cast<uint4*>(S.att[1])[e] = make_uint4(0u, 0u, 0u, 0u);
@@ -499,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_bar(S, B_TB, ci & 1);
       fence_after_sync();
       const bool is_s = pt < 64;  // warps 8, 9: rows of A; warps 10, 11: rows of attn_i
-      if (is_s || MODE == kEmit) {
+      if (MODE == kEmitR ? !is_s : (is_s || MODE == kEmit)) {  // (kEmitR: attn_i rows only)
         const int t = pt & 63, hi = t >> 5, ab = (t >> 4) & 1;  // hi is warp-uniform
         const float4 rf4 = *reinterpret_cast<const float4*>(is_s ? S.rfA[t] : S.rfO[t]);
         uint8_t* dst = is_s ? S.ah : S.att[ci & 1];
@@ -546,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         put_row32(dst, t, hi, sv);
       }
-      if (MODE == kEmit && !is_s) fence_async_smem();  // attn_i feeds the tensor core
+      if (OUT && !is_s) fence_async_smem();  // attn_i feeds the tensor core
       fence_before_sync();
       arrive(S, B_E2);
     };
@@ -729,13 +754,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(nw_tile(ci) + sw128_offset(128, i, 32 * hb + 8 * ch)) = pk;
         }
       }
+      if (MODE == kSumU && a.wy) {  // u^T [c][t] fp16 for phase 3, in the Q rows it never loads
+        uint8_t* ut = S.kq[ci & 1] + 8192 + (i >> 6) * 16384 + (i & 63) * 128;
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          float uv[32];
+          tmem_ld32(tm + lane_bits + TM_DO + 32 * hb, uv);
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint4 pk;
+            pk.x = pack_h2(uv[8 * ch + 0], uv[8 * ch + 1]);
+            pk.y = pack_h2(uv[8 * ch + 2], uv[8 * ch + 3]);
+            pk.z = pack_h2(uv[8 * ch + 4], uv[8 * ch + 5]);
+            pk.w = pack_h2(uv[8 * ch + 6], uv[8 * ch + 7]);
+            *reinterpret_cast<uint4*>(ut + (((4 * hb + ch) ^ (i & 7)) << 4)) = pk;
+          }
+        }
+      }
       fence_async_smem();
       fence_before_sync();
       arrive(S, B_WR);
     };
 
+    if (MODE == kEmitR) {  // the factors come from the records: attn_i only
+      for (int ci = 0; ci < nch; ++ci) {
+        gram(ci);
+        if (!named_bar_and(1, kPrepThreads, !aborted(S))) break;
+      }
+    }
     // one chunk ahead: the gram of chunk ci + 1 is built while w of chunk ci is computed
-    bool go = nch > 0;
+    bool go = MODE != kEmitR && nch > 0;
     if (go) {
       gram(0);
       go = named_bar_and(1, kPrepThreads, !aborted(S));
@@ -748,8 +796,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // this thread has seen its earlier copy read before the barrier of the chunk between
       if (MODE == kSumU && a.wy && pt == 0) bulk_wait_read();
       go = named_bar_and(1, kPrepThreads, !aborted(S));  // also: the gram's A is complete
-      if (MODE == kSumU && a.wy && pt == 0 && go)
-        bulk_s2g(chunk_record(a, n_seq, sb, c0 + ci, j) + kRecNw, saddr(nw_tile(ci)), 16384);
+      if (MODE == kSumU && a.wy && pt == 0 && go) {
+        char* rec = chunk_record(a, n_seq, sb, c0 + ci, j);
+        bulk_s2g(rec + kRecNw, saddr(nw_tile(ci)), 16384);
+        bulk_s2g(rec + kRecU, saddr(S.kq[ci & 1]) + 8192, 8192);
+        bulk_s2g(rec + kRecU + 8192, saddr(S.kq[ci & 1]) + 16384 + 8192, 8192);
+      }
     }
     if (MODE == kSumU && a.wy && pt == 0) bulk_wait_all();
     }
@@ -783,13 +835,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {  // rows past T read zeros; rows in [L, 64) only meet zero weights
         const uint32_t kq = saddr(S.kq[sg]), vv = saddr(S.v[sg]);
         const uint32_t bytes =
-            (MODE == kEmit ? 4u : 2u) * 8192u + (MODE != kSumM ? 2u : 0u) * 8192u;
+            (OUT ? 4u : 2u) * 8192u + (MODE != kSumM && MODE != kEmitR ? 2u : 0u) * 8192u;
         mbar_expect_tx(bar, bytes);
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
           tma_box(kq + kb * 16384, &tm_k, 64 * kb, kh, (int)t0, bar);
-          if (MODE == kEmit) tma_box(kq + kb * 16384 + 8192, &tm_q, 64 * kb, kh, (int)t0, bar);
-          if (MODE != kSumM) tma_box(vv + kb * 8192, &tm_v, 64 * kb, j, (int)t0, bar);
+          if (OUT) tma_box(kq + kb * 16384 + 8192, &tm_q, 64 * kb, kh, (int)t0, bar);
+          if (MODE != kSumM && MODE != kEmitR) tma_box(vv + kb * 8192, &tm_v, 64 * kb, j, (int)t0, bar);
         }
       }
 #pragma unroll
@@ -802,6 +854,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar)
                    : "memory");
+      if (MODE == kEmitR) {  // the chunk's record (-w^T, fp16 K, u^T) into its own ring
+        if (ci >= 2) wait_bar(S, B_RF0 + sg, ((ci >> 1) + 1) & 1);
+        if (lane == 0) {
+          const char* rec = chunk_record(a, n_seq, sb, c0 + ci, j);
+          const uint32_t rb = saddr(&S.bars[B_RL0 + sg]);
+          mbar_expect_tx(rb, 3u * 16384u);
+          bulk_g2s(saddr(sg ? S.tw : S.nw), rec + kRecNw, 16384u, rb);
+          bulk_g2s(saddr(S.kh[sg]), rec + kRecKh, 16384u, rb);
+          bulk_g2s(saddr(S.v[sg]), rec + kRecU, 16384u, rb);
+        }
+        __syncwarp();
+      }
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
   } else if (warp >= 14) {
@@ -874,17 +938,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float4*>(&S.rfO[t][0]) = f;
         *reinterpret_cast<float4*>(&S.rfA[t][0]) = make_float4(bt * f.x, bt * f.y, bt * f.z, 0.f);
       }
-      if (MODE == kEmit) wait_bar(S, B_SQ, ci & 1);  // [S ; QK] has read the bf16 Q
+      if (OUT) wait_bar(S, B_SQ, ci & 1);  // [S ; QK] has read the bf16 Q
       arrive(S, B_TB);
-      if (MODE != kSumM) {  // V -> fp16 in place (read only by the u product)
+      if (MODE != kSumM && MODE != kEmitR) {  // V -> fp16 in place (read only by the u product)
         uint8_t* vb = S.v[sg] + 16 * p;
 #pragma unroll 1
         for (int k0 = 0; k0 < 16; k0 += 4)
           maxabs = to_half_chunks<4, false>(vb + 1024 * k0, vb + 1024 * k0, nullptr, maxabs);
       }
       // fp16 K into its tile, once the chunk that last used the tile has finished Dh
-      if (ci >= 2) wait_bar(S, B_KF0 + sg, ((ci >> 1) + 1) & 1);
-      {
+      if (MODE != kEmitR && ci >= 2) wait_bar(S, B_KF0 + sg, ((ci >> 1) + 1) & 1);
+      if (MODE != kEmitR) {  // (kEmitR: fp16 K comes with the record)
         const uint8_t* kb = S.kq[sg] + 16 * p;
         uint8_t* kd = S.kh[sg] + 16 * p;
 #pragma unroll 1
@@ -898,7 +962,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p == 0)
           bulk_s2g(chunk_record(a, n_seq, sb, c0 + ci, j) + kRecKh, saddr(S.kh[sg]), 16384);
       }
-      if (MODE == kEmit) {  // q_g = diag(e^G) Q as fp16, in place: the K-major B of q_g h
+      if (OUT) {  // q_g = diag(e^G) Q as fp16, in place: the K-major B of q_g h
         uint8_t* qb = S.kq[sg] + 8192 + 16 * p;
 #pragma unroll 1
         for (int k0 = 0; k0 < 16; k0 += 4) {
@@ -907,7 +971,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // the MMA warp has waited for the previous chunk's hand-off
-      if (ci >= 1) wait_bar(S, B_WU, (ci - 1) & 1);
+      if (ci >= 1) {
+        if (MODE == kEmitR) wait_bar(S, B_F0 + ((ci - 1) & 1), ((ci - 1) >> 1) & 1);  // q_g h
+        else wait_bar(S, B_WU, (ci - 1) & 1);
+      }
       fence_async_smem();
       arrive(S, B_CV);
     }
@@ -974,7 +1041,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         sq(1);
       }
     }
-    for (int ci = 0; MODE != kSumML && ci < nch; ++ci) {
+    // kEmitR, per chunk c: D (c) from the staged record; q_g h (c); O2, Dh (c); [S ; QK] (c + 2)
+    for (int ci = 0; MODE == kEmitR && ci < nch; ++ci) {
+      const int st = ci & 1;
+      wait_bar(S, B_RL0 + st, (ci >> 1) & 1);
+      wait_bar(S, B_HR, ci & 1);
+      fence_after_sync();
+      if (leader) {
+        const uint32_t nw = saddr(st ? S.tw : S.nw);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ts(tm + TM_DO, tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3),
+                 sdesc(nw + ks * 2048, 16384, 1024), ID_D, ks > 0);
+        mma_commit(saddr(&S.bars[B_D]));
+      }
+      __syncwarp();
+      wait_bar(S, B_CV, ci & 1);
+      fence_after_sync();
+      if (leader) {  // o^T = h^T q_g^T starts the O accumulator; then the K | Q stage is free
+        const uint32_t qg = saddr(S.kq[st]) + 8192;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ts(tm + TM_DO + 64, tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3),
+                 sdesc(qg + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), ID_QH, ks > 0);
+        mma_commit(saddr(&S.bars[B_F0 + st]));
+      }
+      __syncwarp();
+      wait_bar(S, B_DR, ci & 1);
+      fence_after_sync();
+      if (leader) {  // then the record stage is free
+        const uint32_t att = saddr(S.att[st]), khs = saddr(S.kh[st]);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint32_t col = 32 * (ks >> 1) + 8 * (ks & 1);
+          mma_ts(tm + TM_DO + 64, tm + TM_DO + col, sdesc(att + ks * 32, 16, 1024), ID_O2, 1);
+          mma_ts(tm + TM_H, tm + TM_U + col, sdesc(khs + ks * 2048, 8192, 1024), ID_DH, ks > 0);
+        }
+        mma_commit(saddr(&S.bars[B_H]));
+        mma_commit(saddr(&S.bars[B_RF0 + st]));
+      }
+      __syncwarp();
+      if (ci + 2 < nch) {
+        wait_bar(S, B_E2, (ci + 1) & 1);
+        wait_bar(S, B_L0 + st, ((ci + 2) >> 1) & 1);
+        sq(ci + 2);
+      }
+      if (__any_sync(0xffffffffu, aborted(S))) break;
+    }
+    for (int ci = 0; MODE != kSumML && MODE != kEmitR && ci < nch; ++ci) {
       const uint32_t khs = saddr(S.kh[ci & 1]), vv = saddr(S.v[ci & 1]);
       // w^T = K^T T_w^T ;  u^T = V^T T_u^T; then the stage is free for the loader
       wait_bar(S, B_T, ci & 1);
@@ -1111,9 +1225,11 @@ cudaError_t launch5(const Args& a, cudaStream_t s) {
   const bool empty = a.T == 0;
   if ((e = make_map(&mk, empty || MODE == kSumML ? nullptr : a.k, a.T, a.hk)) != cudaSuccess)
     return e;
-  if ((e = make_map(&mq, empty || MODE != kEmit ? nullptr : a.q, a.T, a.hk)) != cudaSuccess)
+  if ((e = make_map(&mq, empty || (MODE != kEmit && MODE != kEmitR) ? nullptr : a.q, a.T,
+                    a.hk)) != cudaSuccess)
     return e;
-  if ((e = make_map(&mv, empty || MODE == kSumM || MODE == kSumML ? nullptr : a.v, a.T, a.hv)) !=
+  if ((e = make_map(&mv, empty || MODE == kSumM || MODE == kSumML || MODE == kEmitR ? nullptr : a.v,
+                    a.T, a.hv)) !=
       cudaSuccess)
     return e;
   tc5_chunk_kernel<MODE><<<grid, kThreads, smem, s>>>(a, mk, mq, mv);
@@ -1132,8 +1248,10 @@ size_t tc5_records_bytes(int64_t T, int N, int hv) {
 // With records (a.wy), the U half runs first and stores each chunk's -w^T, fp16 K and decay,
 // and the M half only loads them; without, each half computes its own factors.
 cudaError_t tc5_summary(const Args& a, cudaStream_t s) {
-  if (a.wy) {
-    cudaError_t e = launch5<kSumU>(a, s);
+  if (a.wy) {  // the U half also runs on the last segment: phase 3 reads its records
+    Args ua = a;
+    ua.skip_last_summary = false;
+    cudaError_t e = launch5<kSumU>(ua, s);
     if (e != cudaSuccess) return e;
     return launch5<kSumML>(a, s);
   }
@@ -1142,6 +1260,8 @@ cudaError_t tc5_summary(const Args& a, cudaStream_t s) {
   return launch5<kSumU>(a, s);
 }
 
-cudaError_t tc5_emit(const Args& a, cudaStream_t s) { return launch5<kEmit>(a, s); }
+cudaError_t tc5_emit(const Args& a, cudaStream_t s) {
+  return a.wy ? launch5<kEmitR>(a, s) : launch5<kEmit>(a, s);
+}
 
 }  // namespace gdn

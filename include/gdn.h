@@ -113,11 +113,11 @@ gdn_status gdn_check_problem(const gdn_problem* p);
 /* Bytes of device workspace gdn_forward needs for problem p (0 when p is invalid).  The
  * workspace holds the status word, the segment summaries (M_r, U_r), the incoming states
  * h_in, on the SIMT path the materialised chunk factors, and on the tcgen05 path with P > 1
- * per-chunk factor records (-w^T, fp16 K and the state update's decay, 33,280 bytes per
- * 64-token window and value head) that the U summary writes and the M summary reads, so the
- * M summary skips the preparation ("Implementation": phase 1 carries M with the factors the
+ * per-chunk factor records: -w^T, fp16 K, u^T and the state update's decay, 49,664 bytes per
+ * 64-token window and value head.  The U summary writes them; the M summary and phase 3 read
+ * them and skip the preparation ("Implementation": phase 3 re-emits with the factors the
  * zero-state pass already computed).  A workspace without room for the records is accepted:
- * both summaries then compute their own factors. */
+ * every phase then computes its own factors. */
 size_t gdn_workspace_size(const gdn_problem* p);
 
 /* Whole forward pass ("Implementation": the three phases; with P = 1 the single-pass form,
