@@ -195,31 +195,17 @@ def run_ours(args, ws, rank, local):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
 
-    # per-phase events over the same launches (phase entry points = what gdn_forward enqueues)
+    # per-phase times of the forward itself: CUDA events between its launches
     p = gdn.problem_for(d["q"], d["v"], None, P=P_best, path=args.path)
-    S = P_best * HV
-    M = torch.empty(S, KD, KD, dtype=torch.float32, device=dev)
-    U = torch.empty(S, KD, VD, dtype=torch.float32, device=dev)
-    h_in = torch.empty(S, KD, VD, dtype=torch.float32, device=dev)
+    wsp = gdn.workspace_for(p, dev)
     phase_ms = {"summary": [], "scan": [], "emit": []}
     for it in range(args.warmup + args.steps):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        ev[0].record(stream)
-        if P_best > 1:
-            gdn.gdn_segment_summary_fused(p, d["k"], d["v"], d["g"], d["beta"], None, M, U,
-                                          skip_last=True)
-        ev[1].record(stream)
-        if P_best > 1:
-            gdn.gdn_state_prefix_scan(p, M, U, None, h_in, None)
-        ev[2].record(stream)
-        gdn.gdn_chunk_emit_fused(p, d["q"], d["k"], d["v"], d["g"], d["beta"],
-                                 h_in if P_best > 1 else None, None, out, hf)
-        ev[3].record(stream)
-        torch.cuda.synchronize()
+        sm_, sc_, em_ = gdn.gdn_forward_timed(p, d["q"], d["k"], d["v"], d["g"], d["beta"], None,
+                                              None, out, hf, wsp, stream=stream)
         if it >= args.warmup:
-            phase_ms["summary"].append(ev[0].elapsed_time(ev[1]))
-            phase_ms["scan"].append(ev[1].elapsed_time(ev[2]))
-            phase_ms["emit"].append(ev[2].elapsed_time(ev[3]))
+            phase_ms["summary"].append(sm_)
+            phase_ms["scan"].append(sc_)
+            phase_ms["emit"].append(em_)
     ph = {k: statistics.mean(v) for k, v in phase_ms.items()}
 
     # end to end through the C ABI with host buffers: H2D inputs, forward, D2H outputs
@@ -259,7 +245,7 @@ def run_ours(args, ws, rank, local):
     emit_flops = FLOP_PER_TOKEN * T
     emit_s = ph["emit"] / 1e3
     achieved_gbs = emit_bytes / emit_s / 1e9
-    tr = stored_traffic("emit")
+    tr = stored_traffic("emit_records" if P_best > 1 else "emit")
     t_bound = max(BYTES_PER_TOKEN * T / (hbm * 1e9), FLOP_PER_TOKEN * T / (tf * 1e12))
     launches_per_step = 4 if P_best > 1 else 1  # summary (M and U halves), scan, emit
     res = {
@@ -285,7 +271,8 @@ def run_ours(args, ws, rank, local):
         "phase_ms": {k: round(v, 4) for k, v in ph.items()},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {
-            "kernel": "chunk kernel <emit> (phase 3: prepare + chain + output)",
+            "kernel": ("chunk kernel <emit from records> (phase 3: attn_i + chain + output)"
+                       if P_best > 1 else "chunk kernel <emit> (prepare + chain + output)"),
             "bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
             "frac": achieved_gbs / hbm, "peak_source": src,
             "traffic": None if tr is None else tr * T,

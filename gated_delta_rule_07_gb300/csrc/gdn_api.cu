@@ -238,10 +238,16 @@ gdn_status gdn_chunk_emit(const gdn_problem* p, const void* q, const void* k, co
                                       : gdn::simt_emit(a, stream));
 }
 
-gdn_status gdn_forward(const gdn_problem* p, const void* q, const void* k, const void* v,
-                       const float* g, const float* beta, const float* h0,
-                       const int32_t* cu_seqlens, void* out, float* h_final, void* workspace,
-                       size_t ws_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+// gdn_forward, recording ev[0..3] (when given) before phase 1, after phase 1, after the scan
+// and after phase 3.
+gdn_status forward_impl(const gdn_problem* p, const void* q, const void* k, const void* v,
+                        const float* g, const float* beta, const float* h0,
+                        const int32_t* cu_seqlens, void* out, float* h_final, void* workspace,
+                        size_t ws_bytes, cudaStream_t stream, cudaEvent_t* ev) {
+  auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
   gdn_status st = check_problem(p);
   if (st != GDN_OK) return st;
   if (p->total_tokens > 0 && (!q || !k || !v || !g || !beta || !out))
@@ -274,16 +280,22 @@ gdn_status gdn_forward(const gdn_problem* p, const void* q, const void* k, const
   a.h_in = seg ? a.h_in_out : h0;
   GDN_TRY(gdn::launch_validate_cu(a, stream));
 
+  GDN_TRY(mark(0));
   if (use_tensor_path(p)) {
     if (seg) {
       Args ma = a;
       ma.skip_last_summary = true;
       GDN_TRY(fused_summary(p, ma, stream));
+      GDN_TRY(mark(1));
       Args sa = a;
       sa.h_final = nullptr;  // the last segment's emit writes the final state
       GDN_TRY(gdn::tc_scan(sa, stream));
+    } else {
+      GDN_TRY(mark(1));
     }
-    return to_status(fused_emit(p, a, stream));
+    GDN_TRY(mark(2));
+    GDN_TRY(fused_emit(p, a, stream));
+    return to_status(mark(3));
   }
   a.w_out = ws + L.w;
   a.u_out = ws + L.u;
@@ -294,11 +306,50 @@ gdn_status gdn_forward(const gdn_problem* p, const void* q, const void* k, const
   if (a.T > 0) GDN_TRY(gdn::simt_prepare(a, stream));
   if (seg) {
     GDN_TRY(gdn::simt_summary(a, stream));  // (the SIMT summary computes every segment)
+    GDN_TRY(mark(1));
     Args sa = a;
     sa.h_final = nullptr;
     GDN_TRY(gdn::simt_scan(sa, stream));
+  } else {
+    GDN_TRY(mark(1));
   }
-  return to_status(gdn::simt_emit(a, stream));
+  GDN_TRY(mark(2));
+  GDN_TRY(gdn::simt_emit(a, stream));
+  return to_status(mark(3));
+}
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_forward(const gdn_problem* p, const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const float* h0,
+                       const int32_t* cu_seqlens, void* out, float* h_final, void* workspace,
+                       size_t ws_bytes, cudaStream_t stream) {
+  return forward_impl(p, q, k, v, g, beta, h0, cu_seqlens, out, h_final, workspace, ws_bytes,
+                      stream, nullptr);
+}
+
+gdn_status gdn_forward_timed(const gdn_problem* p, const void* q, const void* k, const void* v,
+                             const float* g, const float* beta, const float* h0,
+                             const int32_t* cu_seqlens, void* out, float* h_final,
+                             void* workspace, size_t ws_bytes, cudaStream_t stream,
+                             float* phase_ms) {
+  if (!phase_ms) return GDN_ERR_INVALID_ARGUMENT;
+  cudaEvent_t ev[4] = {};
+  for (int i = 0; i < 4; ++i)
+    if (cudaEventCreate(&ev[i]) != cudaSuccess) {
+      for (int k2 = 0; k2 < i; ++k2) cudaEventDestroy(ev[k2]);
+      return to_status(cudaGetLastError());
+    }
+  gdn_status st = forward_impl(p, q, k, v, g, beta, h0, cu_seqlens, out, h_final, workspace,
+                               ws_bytes, stream, ev);
+  if (st == GDN_OK) {
+    cudaError_t e = cudaEventSynchronize(ev[3]);
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventElapsedTime(&phase_ms[i], ev[i], ev[i + 1]);
+    if (e != cudaSuccess) st = to_status(e);
+  }
+  for (int i = 0; i < 4; ++i) cudaEventDestroy(ev[i]);
+  return st;
 }
 
 gdn_status gdn_segment_summary_fused(const gdn_problem* p, const void* k, const void* v,
