@@ -31,6 +31,9 @@ METRIC = "GDN fwd tokens/s at T=65536, Hv=32, K=V=128; % of roofline (tensor pip
 # head, and q + k + v + out (bf16) + g + beta (fp32) bytes.
 FLOP_PER_TOKEN = 2 * (C * (3 * KD + 2 * VD) + 3 * KD * VD + C * C / 6) * HV
 BYTES_PER_TOKEN = HK * KD * 2 * 2 + HV * VD * 2 * 2 + HV * 4 * 2
+# what each phase-1 kernel must read per token: k, v, g, beta (U half); k, g, beta (M half)
+SUM_U_BYTES_PER_TOKEN = HK * KD * 2 + HV * VD * 2 + HV * 4 * 2
+SUM_M_BYTES_PER_TOKEN = HK * KD * 2 + HV * 4 * 2
 
 
 def peaks():
@@ -198,14 +201,15 @@ def run_ours(args, ws, rank, local):
     # per-phase times of the forward itself: CUDA events between its launches
     p = gdn.problem_for(d["q"], d["v"], None, P=P_best, path=args.path)
     wsp = gdn.workspace_for(p, dev)
-    phase_ms = {"summary": [], "scan": [], "emit": []}
+    phase_ms = {"summary": [], "scan": [], "emit": [], "summary_first": []}
     for it in range(args.warmup + args.steps):
-        sm_, sc_, em_ = gdn.gdn_forward_timed(p, d["q"], d["k"], d["v"], d["g"], d["beta"], None,
-                                              None, out, hf, wsp, stream=stream)
+        sm_, sc_, em_, s1_ = gdn.gdn_forward_timed(p, d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                                   None, None, out, hf, wsp, stream=stream)
         if it >= args.warmup:
             phase_ms["summary"].append(sm_)
             phase_ms["scan"].append(sc_)
             phase_ms["emit"].append(em_)
+            phase_ms["summary_first"].append(s1_)
     ph = {k: statistics.mean(v) for k, v in phase_ms.items()}
 
     # end to end through the C ABI with host buffers: H2D inputs, forward, D2H outputs
@@ -241,11 +245,30 @@ def run_ours(args, ws, rank, local):
         return None
     hbm, tf, tf_sus, src = peaks()
     tokens = T * ws
-    emit_bytes = BYTES_PER_TOKEN * T + (P_best * HV + HV) * KD * VD * 4
+    # the launches of one forward, their times and what each must move (algorithmic bytes)
+    kern_ms = {"emit": ph["emit"]}
+    if P_best > 1:  # phase 1 = the U half (writes the factor records), then the M half
+        kern_ms["sum_u"] = ph["summary_first"]
+        kern_ms["sum_m"] = ph["summary"] - ph["summary_first"]
+    kern_bytes = {
+        "emit": BYTES_PER_TOKEN * T + (P_best * HV + HV) * KD * VD * 4,
+        "sum_u": SUM_U_BYTES_PER_TOKEN * T + P_best * HV * KD * VD * 4,
+        "sum_m": SUM_M_BYTES_PER_TOKEN * T * (P_best - 1) // P_best + (P_best - 1) * HV * KD * KD * 4,
+    }
+    kern_name = {
+        "emit": ("chunk kernel <emit from records> (phase 3: attn_i + chain + output)"
+                 if P_best > 1 else "chunk kernel <emit> (prepare + chain + output)"),
+        "sum_u": "chunk kernel <U summary> (phase 1: prepare + U chain + factor records)",
+        "sum_m": "chunk kernel <M summary from records> (phase 1: M chain)",
+    }
+    kern_traffic_key = {"emit": "emit_records" if P_best > 1 else "emit",
+                        "sum_u": "sum_u_records", "sum_m": "sum_m_records"}
+    dom = max(kern_ms, key=kern_ms.get)
+    emit_bytes = kern_bytes[dom]
     emit_flops = FLOP_PER_TOKEN * T
-    emit_s = ph["emit"] / 1e3
+    emit_s = kern_ms[dom] / 1e3
     achieved_gbs = emit_bytes / emit_s / 1e9
-    tr = stored_traffic("emit_records" if P_best > 1 else "emit")
+    tr = stored_traffic(kern_traffic_key[dom])
     t_bound = max(BYTES_PER_TOKEN * T / (hbm * 1e9), FLOP_PER_TOKEN * T / (tf * 1e12))
     launches_per_step = 4 if P_best > 1 else 1  # summary (M and U halves), scan, emit
     res = {
@@ -270,15 +293,21 @@ def run_ours(args, ws, rank, local):
         "sweep_ms_per_step": {f"P={k}": round(v, 4) for k, v in sweep.items()},
         "phase_ms": {k: round(v, 4) for k, v in ph.items()},
         "gpu_launches": launches_per_step * args.steps,
+        "kernels_ms": {k: round(v, 4) for k, v in kern_ms.items()},
         "roofline": {
-            "kernel": ("chunk kernel <emit from records> (phase 3: attn_i + chain + output)"
-                       if P_best > 1 else "chunk kernel <emit> (prepare + chain + output)"),
+            "kernel": kern_name[dom] + " -- the longest launch of the step",
             "bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
             "frac": achieved_gbs / hbm, "peak_source": src,
             "traffic": None if tr is None else tr * T,
-            "algorithmic_bytes_per_launch": emit_bytes,
-            "tensor_tflops": emit_flops / emit_s / 1e12, "tensor_peak": tf,
-            "tensor_frac": emit_flops / emit_s / 1e12 / tf},
+            "algorithmic_bytes_per_launch": emit_bytes},
+        "roofline_by_kernel": {
+            k: {"ms": round(kern_ms[k], 4), "algorithmic_bytes": kern_bytes[k],
+                "achieved_gbs": kern_bytes[k] / (kern_ms[k] / 1e3) / 1e9,
+                "frac": kern_bytes[k] / (kern_ms[k] / 1e3) / 1e9 / hbm}
+            for k in kern_ms},
+        "emit_tensor": {"tflops": emit_flops / (ph["emit"] / 1e3) / 1e12, "peak": tf,
+                        "frac": emit_flops / (ph["emit"] / 1e3) / 1e12 / tf,
+                        "note": "the path's FLOPs over the phase-3 kernel's time"},
         "path_roofline": {"bound_us": t_bound * 1e6, "step_us": ms * 1e3,
                           "frac": t_bound / (ms / 1e3),
                           "note": "max(FLOP/bf16 peak, bytes/HBM) over the whole step, of "

@@ -29,8 +29,13 @@ bool use_mma_sync(const gdn_problem* p) { return p->path == GDN_PATH_MMA_SYNC; }
 
 // Phase 1 and phase 3 with the factors recomputed on chip, on the selected tensor-core
 // generation.
-cudaError_t fused_summary(const gdn_problem* p, const Args& a, cudaStream_t s) {
-  return use_mma_sync(p) ? gdn::tc_summary(a, true, s) : gdn::tc5_summary(a, s);
+cudaError_t fused_summary(const gdn_problem* p, const Args& a, cudaStream_t s,
+                          cudaEvent_t mid = nullptr) {
+  if (use_mma_sync(p)) {
+    cudaError_t e = gdn::tc_summary(a, true, s);
+    return (e == cudaSuccess && mid) ? cudaEventRecord(mid, s) : e;
+  }
+  return gdn::tc5_summary(a, s, mid);
 }
 cudaError_t fused_emit(const gdn_problem* p, const Args& a, cudaStream_t s) {
   return use_mma_sync(p) ? gdn::tc_emit(a, true, s) : gdn::tc5_emit(a, s);
@@ -241,8 +246,9 @@ gdn_status gdn_chunk_emit(const gdn_problem* p, const void* q, const void* k, co
 }  // extern "C"
 
 namespace {
-// gdn_forward, recording ev[0..3] (when given) before phase 1, after phase 1, after the scan
-// and after phase 3.
+// gdn_forward, recording ev[0..4] (when given) before phase 1, after phase 1, after the scan,
+// after phase 3, and between the two kernels of phase 1 (after phase 1's only launch on the
+// paths with one).
 gdn_status forward_impl(const gdn_problem* p, const void* q, const void* k, const void* v,
                         const float* g, const float* beta, const float* h0,
                         const int32_t* cu_seqlens, void* out, float* h_final, void* workspace,
@@ -285,13 +291,14 @@ gdn_status forward_impl(const gdn_problem* p, const void* q, const void* k, cons
     if (seg) {
       Args ma = a;
       ma.skip_last_summary = true;
-      GDN_TRY(fused_summary(p, ma, stream));
+      GDN_TRY(fused_summary(p, ma, stream, ev ? ev[4] : nullptr));
       GDN_TRY(mark(1));
       Args sa = a;
       sa.h_final = nullptr;  // the last segment's emit writes the final state
       GDN_TRY(gdn::tc_scan(sa, stream));
     } else {
       GDN_TRY(mark(1));
+      GDN_TRY(mark(4));
     }
     GDN_TRY(mark(2));
     GDN_TRY(fused_emit(p, a, stream));
@@ -306,12 +313,14 @@ gdn_status forward_impl(const gdn_problem* p, const void* q, const void* k, cons
   if (a.T > 0) GDN_TRY(gdn::simt_prepare(a, stream));
   if (seg) {
     GDN_TRY(gdn::simt_summary(a, stream));  // (the SIMT summary computes every segment)
+    GDN_TRY(mark(4));
     GDN_TRY(mark(1));
     Args sa = a;
     sa.h_final = nullptr;
     GDN_TRY(gdn::simt_scan(sa, stream));
   } else {
     GDN_TRY(mark(1));
+    GDN_TRY(mark(4));
   }
   GDN_TRY(mark(2));
   GDN_TRY(gdn::simt_emit(a, stream));
@@ -335,8 +344,8 @@ gdn_status gdn_forward_timed(const gdn_problem* p, const void* q, const void* k,
                              void* workspace, size_t ws_bytes, cudaStream_t stream,
                              float* phase_ms) {
   if (!phase_ms) return GDN_ERR_INVALID_ARGUMENT;
-  cudaEvent_t ev[4] = {};
-  for (int i = 0; i < 4; ++i)
+  cudaEvent_t ev[5] = {};
+  for (int i = 0; i < 5; ++i)
     if (cudaEventCreate(&ev[i]) != cudaSuccess) {
       for (int k2 = 0; k2 < i; ++k2) cudaEventDestroy(ev[k2]);
       return to_status(cudaGetLastError());
@@ -346,9 +355,10 @@ gdn_status gdn_forward_timed(const gdn_problem* p, const void* q, const void* k,
   if (st == GDN_OK) {
     cudaError_t e = cudaEventSynchronize(ev[3]);
     for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventElapsedTime(&phase_ms[i], ev[i], ev[i + 1]);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&phase_ms[3], ev[0], ev[4]);
     if (e != cudaSuccess) st = to_status(e);
   }
-  for (int i = 0; i < 4; ++i) cudaEventDestroy(ev[i]);
+  for (int i = 0; i < 5; ++i) cudaEventDestroy(ev[i]);
   return st;
 }
 

@@ -55,7 +55,8 @@ size_t tc5_smem_bytes();
 size_t workspace_min_bytes(const gdn_problem* p);
 // Bytes of the per-chunk factor records the U summary stores for the M summary.
 size_t tc5_records_bytes(int64_t T, int N, int hv);
-cudaError_t tc5_summary(const Args& a, cudaStream_t s);
+// `mid`, when given, is recorded between the two launches of phase 1.
+cudaError_t tc5_summary(const Args& a, cudaStream_t s, cudaEvent_t mid = nullptr);
 cudaError_t tc5_emit(const Args& a, cudaStream_t s);
 
 }  // namespace gdn

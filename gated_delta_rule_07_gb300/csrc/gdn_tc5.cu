@@ -1247,15 +1247,17 @@ size_t tc5_records_bytes(int64_t T, int N, int hv) {
 
 // With records (a.wy), the U half runs first and stores each chunk's -w^T, fp16 K and decay,
 // and the M half only loads them; without, each half computes its own factors.
-cudaError_t tc5_summary(const Args& a, cudaStream_t s) {
+cudaError_t tc5_summary(const Args& a, cudaStream_t s, cudaEvent_t mid) {
   if (a.wy) {  // the U half also runs on the last segment: phase 3 reads its records
     Args ua = a;
     ua.skip_last_summary = false;
     cudaError_t e = launch5<kSumU>(ua, s);
+    if (e == cudaSuccess && mid) e = cudaEventRecord(mid, s);
     if (e != cudaSuccess) return e;
     return launch5<kSumML>(a, s);
   }
   cudaError_t e = launch5<kSumM>(a, s);
+  if (e == cudaSuccess && mid) e = cudaEventRecord(mid, s);
   if (e != cudaSuccess) return e;
   return launch5<kSumU>(a, s);
 }

@@ -143,14 +143,14 @@ def gdn_forward(p, q, k, v, g, beta, h0, cu_seqlens, out, h_final, workspace, ws
 def gdn_forward_timed(p, q, k, v, g, beta, h0, cu_seqlens, out, h_final, workspace,
                       ws_bytes=None, stream=None):
     """gdn_forward that waits for its own end and returns the milliseconds of (summaries,
-    prefix scan, phase 3) measured with CUDA events on the stream."""
+    prefix scan, phase 3, first summary kernel) measured with CUDA events on the stream."""
     ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
-    ms = (ctypes.c_float * 3)()
+    ms = (ctypes.c_float * 4)()
     _check(_lib.gdn_forward_timed(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                   _ptr(h0), _ptr(cu_seqlens), _ptr(out), _ptr(h_final),
                                   _ptr(workspace), int(ws_bytes), _stream(stream), ms),
            "gdn_forward_timed")
-    return float(ms[0]), float(ms[1]), float(ms[2])
+    return float(ms[0]), float(ms[1]), float(ms[2]), float(ms[3])
 
 
 def gdn_forward_static_scratch(p, q, k, v, g, beta, h0, cu_seqlens, out, h_final, stream=None):

@@ -135,13 +135,14 @@ gdn_status gdn_forward(const gdn_problem* p, const void* q, const void* k, const
                        const int32_t* cu_seqlens, void* out, float* h_final, void* workspace,
                        size_t ws_bytes, cudaStream_t stream);
 
-/* gdn_forward with a per-phase clock: it records CUDA events on `stream` before phase 1, after
- * phase 1 (the segment summaries), after the prefix scan and after phase 3, waits for the
- * last, and writes the three elapsed times in milliseconds to phase_ms[0..2] (a host array;
- * 0 for a phase that does not run, e.g. the summaries and the scan with P = 1).  It runs the
- * same kernels as gdn_forward; the wait makes it synchronous.  For measurement only.  Errors:
- * those of gdn_forward, GDN_ERR_INVALID_ARGUMENT for a NULL phase_ms, GDN_ERR_CUDA if an event
- * call fails. */
+/* gdn_forward with a per-phase clock: it records CUDA events on `stream` around its launches,
+ * waits for the last, and writes four elapsed times in milliseconds to phase_ms[0..3] (a host
+ * array): phase 1 (the segment summaries), the prefix scan, phase 3, and the first of phase 1's
+ * two kernels (the U half when the workspace holds factor records, else the M half).  A phase
+ * that does not run (the summaries and the scan with P = 1) reads 0.  It runs the same kernels
+ * as gdn_forward; the wait makes it synchronous.  For measurement only.  Errors: those of
+ * gdn_forward, GDN_ERR_INVALID_ARGUMENT for a NULL phase_ms, GDN_ERR_CUDA if an event call
+ * fails. */
 gdn_status gdn_forward_timed(const gdn_problem* p, const void* q, const void* k, const void* v,
                              const float* g, const float* beta, const float* h0,
                              const int32_t* cu_seqlens, void* out, float* h_final,
