@@ -17,6 +17,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int C = kChunk;
 constexpr int kColBlock = 32;  // state columns per CTA (columns of h, M, U are independent)
+constexpr int kScanCols = 8;   // the scan: narrower blocks, four times the CTAs, for its latency
 
 // ------------------------------------------------------------------ validation
 
@@ -206,27 +207,27 @@ __global__ void __launch_bounds__(kThreads) simt_summary_kernel(Args a) {
 
 // ------------------------------------------------------------------ phase 2
 
-// One CTA per (sequence, value head, block of 32 state columns); serial over segments:
+// One CTA per (sequence, value head, block of 8 state columns); serial over segments:
 // h_in[r] = h, h <- M_r h + U_r.
 template <int KD, int VD>
 __global__ void __launch_bounds__(kThreads) simt_scan_kernel(Args a) {
-  constexpr int KP = KD + 1, XP = kColBlock + 1;
+  constexpr int KP = KD + 1, XP = kScanCols + 1;
   extern __shared__ float sm[];
   float* Ms = sm;              // [KD][KP]
   float* hs = Ms + KD * KP;    // [KD][XP]
   float* hn = hs + KD * XP;    // [KD][XP]
-  const int n = blockIdx.x, j = blockIdx.y, col0 = blockIdx.z * kColBlock;
+  const int n = blockIdx.x, j = blockIdx.y, col0 = blockIdx.z * kScanCols;
   const int tid = threadIdx.x;
-  for (int e = tid; e < KD * kColBlock; e += kThreads) {
-    const int i = e / kColBlock, c = e % kColBlock;
+  for (int e = tid; e < KD * kScanCols; e += kThreads) {
+    const int i = e / kScanCols, c = e % kScanCols;
     hs[i * XP + c] = a.h0 ? a.h0[(((int64_t)n * a.hv + j) * KD + i) * VD + col0 + c] : 0.f;
   }
   for (int r = 0; r < a.P; ++r) {
     const int64_t seg = (int64_t)n * a.P + r;
     if (r == a.P - 1 && a.h_final == nullptr) {  // the last summary only feeds h_final
       __syncthreads();
-      for (int e = tid; e < KD * kColBlock; e += kThreads) {
-        const int i = e / kColBlock, c = e % kColBlock;
+      for (int e = tid; e < KD * kScanCols; e += kThreads) {
+        const int i = e / kScanCols, c = e % kScanCols;
         a.h_in_out[((seg * a.hv + j) * KD + i) * VD + col0 + c] = hs[i * XP + c];
       }
       return;
@@ -234,25 +235,25 @@ __global__ void __launch_bounds__(kThreads) simt_scan_kernel(Args a) {
     __syncthreads();
     for (int e = tid; e < KD * KD; e += kThreads)
       Ms[(e / KD) * KP + e % KD] = a.M[((seg * a.hv + j) * KD) * KD + e];
-    for (int e = tid; e < KD * kColBlock; e += kThreads) {
-      const int i = e / kColBlock, c = e % kColBlock;
+    for (int e = tid; e < KD * kScanCols; e += kThreads) {
+      const int i = e / kScanCols, c = e % kScanCols;
       if (a.h_in_out) a.h_in_out[((seg * a.hv + j) * KD + i) * VD + col0 + c] = hs[i * XP + c];
     }
     __syncthreads();
-    for (int e = tid; e < KD * kColBlock; e += kThreads) {
-      const int i = e / kColBlock, c = e % kColBlock;
+    for (int e = tid; e < KD * kScanCols; e += kThreads) {
+      const int i = e / kScanCols, c = e % kScanCols;
       float x = a.U[((seg * a.hv + j) * KD + i) * VD + col0 + c];
       for (int b = 0; b < KD; ++b) x += Ms[i * KP + b] * hs[b * XP + c];
       hn[i * XP + c] = x;
     }
     __syncthreads();
-    for (int e = tid; e < KD * kColBlock; e += kThreads) hs[(e / kColBlock) * XP + e % kColBlock] =
-        hn[(e / kColBlock) * XP + e % kColBlock];
+    for (int e = tid; e < KD * kScanCols; e += kThreads) hs[(e / kScanCols) * XP + e % kScanCols] =
+        hn[(e / kScanCols) * XP + e % kScanCols];
   }
   __syncthreads();
   if (a.h_final)
-    for (int e = tid; e < KD * kColBlock; e += kThreads) {
-      const int i = e / kColBlock, c = e % kColBlock;
+    for (int e = tid; e < KD * kScanCols; e += kThreads) {
+      const int i = e / kScanCols, c = e % kScanCols;
       a.h_final[(((int64_t)n * a.hv + j) * KD + i) * VD + col0 + c] = hs[i * XP + c];
     }
 }
@@ -383,8 +384,8 @@ struct Simt {
                   dim3((unsigned)(a.N * a.P), a.hv, (KD + VD) / kColBlock), smem, s, a);
   }
   static cudaError_t scan(const Args& a, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (KD * (KD + 1) + 2 * KD * (kColBlock + 1));
-    return launch(simt_scan_kernel<KD, VD>, dim3((unsigned)a.N, a.hv, VD / kColBlock), smem, s,
+    const size_t smem = sizeof(float) * (KD * (KD + 1) + 2 * KD * (kScanCols + 1));
+    return launch(simt_scan_kernel<KD, VD>, dim3((unsigned)a.N, a.hv, VD / kScanCols), smem, s,
                   a);
   }
   static cudaError_t emit(const Args& a, cudaStream_t s) {
