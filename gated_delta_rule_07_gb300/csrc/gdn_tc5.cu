@@ -94,6 +94,7 @@ enum Bar {
   B_L0, B_L1, B_L2,  // stage loaded: byte count (+ 32 cp.async arrivals)  loader
   B_F0, B_F1, B_F2,  // stage free (its chunk's w, u and q_g h products are done)  MMA commit
   B_KF0, B_KF1,  // fp16 K tile free (its chunk's Dh is done)         MMA commit
+  B_QF0, B_QF1,  // kEmitR: the K | Q stage has been read (q_g copied out)  converter (64)
   B_RL0, B_RL1,  // kEmitR: a record is staged (byte count)              loader
   B_RF0, B_RF1,  // kEmitR: its record stage is free (D, O2, Dh done)    MMA commit
   B_END,       // every product issued has completed                  MMA commit
@@ -102,7 +103,7 @@ enum Bar {
 template <int MODE>
 __device__ __forceinline__ uint32_t bar_count(int b) {
   return (b == B_E2 || b == B_T || b == B_WR)  ? (uint32_t)kPrepThreads
-         : (b == B_TB || b == B_CV)            ? (uint32_t)kConvThreads
+         : (b == B_TB || b == B_CV || b == B_QF0 || b == B_QF1) ? (uint32_t)kConvThreads
          : (b == B_HR || b == B_DR)            ? (uint32_t)kChainThreads
          : (b >= B_L0 && b <= B_L2)            ? (MODE == kSumML ? 1u : 33u)
          : (b == B_RL0 || b == B_RL1)          ? 1u
@@ -495,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         reinterpret_cast<uint4*>(S.tw)[e] = make_uint4(0u, 0u, 0u, 0u);
         reinterpret_cast<uint4*>(S.tu)[e] = make_uint4(0u, 0u, 0u, 0u);
       }
-      reinterpret_cast<uint4*>(S.ah)[e] = make_uint4(0u, 0u, 0u, 0u);
+      if (MODE != kEmitR) reinterpret_cast<uint4*>(S.ah)[e] = make_uint4(0u, 0u, 0u, 0u);
       reinterpret_cast<uint4*>(S.att[0])[e] = make_uint4(0u, 0u, 0u, 0u);
       reinterpret_cast<uint4*>(S.att[1])[e] = make_uint4(0u, 0u, 0u, 0u);
     }
@@ -826,8 +827,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int ci = 0; MODE != kSumML && ci < nch; ++ci) {
       const int sg = ci & 1;
-      // the stage was last used by chunk ci - 2: wait for its w, u (and q_g h) products
-      if (ci >= 2) wait_bar(S, B_F0 + sg, ((ci >> 1) + 1) & 1);
+      // the stage was last used by chunk ci - 2: wait for its w, u (and q_g h) products, or
+      // (kEmitR) for q_g to have been copied out of it
+      if (ci >= 2) wait_bar(S, (MODE == kEmitR ? B_QF0 : B_F0) + sg, ((ci >> 1) + 1) & 1);
       if (__any_sync(0xffffffffu, aborted(S))) break;
       const int64_t t0 = sb + (c0 + ci) * C;
       const int L = (int)((se - t0) < C ? (se - t0) : C);
@@ -962,7 +964,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p == 0)
           bulk_s2g(chunk_record(a, n_seq, sb, c0 + ci, j) + kRecKh, saddr(S.kh[sg]), 16384);
       }
-      if (OUT) {  // q_g = diag(e^G) Q as fp16, in place: the K-major B of q_g h
+      if (MODE == kEmit) {  // q_g = diag(e^G) Q as fp16, in place: the K-major B of q_g h
         uint8_t* qb = S.kq[sg] + 8192 + 16 * p;
 #pragma unroll 1
         for (int k0 = 0; k0 < 16; k0 += 4) {
@@ -970,11 +972,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           maxabs = to_half_chunks<4, true>(pq, pq, &S.eG[gb][(p >> 3) + 8 * (k0 & 7)], maxabs);
         }
       }
-      // the MMA warp has waited for the previous chunk's hand-off
-      if (ci >= 1) {
-        if (MODE == kEmitR) wait_bar(S, B_F0 + ((ci - 1) & 1), ((ci - 1) >> 1) & 1);  // q_g h
-        else wait_bar(S, B_WU, (ci - 1) & 1);
+      if (MODE == kEmitR) {
+        // q_g into its own tile (the A and T tiles, unused here; boxes 8 KB apart), once q_g h
+        // of the previous chunk is done, so the K | Q stage is free for the loader at once
+        if (ci >= 1) wait_bar(S, B_F0 + ((ci - 1) & 1), ((ci - 1) >> 1) & 1);
+        const uint8_t* qb = S.kq[sg] + 8192 + 16 * p;
+        uint8_t* qd = S.ah + 16 * p;
+#pragma unroll 1
+        for (int k0 = 0; k0 < 16; k0 += 4)
+          maxabs = to_half_chunks<4, true>(qb + (k0 >> 3) * 16384 + 1024 * (k0 & 7),
+                                           qd + (k0 >> 3) * 8192 + 1024 * (k0 & 7),
+                                           &S.eG[gb][(p >> 3) + 8 * (k0 & 7)], maxabs);
+        arrive(S, B_QF0 + sg);
       }
+      // the MMA warp has waited for the previous chunk's hand-off
+      if (ci >= 1 && MODE != kEmitR) wait_bar(S, B_WU, (ci - 1) & 1);  // (kEmitR: above)
       fence_async_smem();
       arrive(S, B_CV);
     }
@@ -1059,11 +1071,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_bar(S, B_CV, ci & 1);
       fence_after_sync();
       if (leader) {  // o^T = h^T q_g^T starts the O accumulator; then the K | Q stage is free
-        const uint32_t qg = saddr(S.kq[st]) + 8192;
+        const uint32_t qg = saddr(S.ah);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           mma_ts(tm + TM_DO + 64, tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3),
-                 sdesc(qg + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024), ID_QH, ks > 0);
+                 sdesc(qg + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), ID_QH, ks > 0);
         mma_commit(saddr(&S.bars[B_F0 + st]));
       }
       __syncwarp();
