@@ -23,6 +23,11 @@
 // by fp32 forward substitution in registers, the off-diagonal blocks
 // T_ab = -T_aa sum_m A_am T_mb with warp-level mma.sync.
 //
+// Phase 3 from factor records (kEmitR) loads Q and the chunk's record (-w^T, fp16 K, u^T) and
+// prepares nothing: two prepare warps write Q^T (fp16, MN-major) beside -w^T, so that one
+// N = 128 product gives [D^T | (Q h)^T] = h^T [-w^T | Q^T]; Q K^T takes Q^T and the record's K;
+// attn_i delta goes to its own columns, and the chain forms o = e^{G_t} (Q h)_t + (attn_i delta)_t.
+//
 // Warp roles (512 threads):
 //   warps 0-7   chain:     TMEM lane = state row c; warps w and w + 4 split the columns
 //   warps 8-11  prepare:   masked gram and attn_i, the triangular solve, -w; one chunk ahead
@@ -84,6 +89,7 @@ enum Bar {
   B_E2,        // the gram has read it and the decay tables           prepare (128)
   B_TB,        // decay tables of a chunk are in shared memory        converter (64)
   B_CV,        // fp16 K, V and q_g of a chunk are ready              converter (64)
+               //   (kEmitR: fp16 Q^T is ready                         transposer (64))
   B_T,         // the T tiles are ready                               prepare (128)
   B_WU,        // w^T, u^T are in TMEM                                MMA commit
   B_WR,        // -w^T is in shared memory                            prepare (128)
@@ -94,7 +100,7 @@ enum Bar {
   B_L0, B_L1, B_L2,  // stage loaded: byte count (+ 32 cp.async arrivals)  loader
   B_F0, B_F1, B_F2,  // stage free (its chunk's w, u and q_g h products are done)  MMA commit
   B_KF0, B_KF1,  // fp16 K tile free (its chunk's Dh is done)         MMA commit
-  B_QF0, B_QF1,  // kEmitR: the K | Q stage has been read (q_g copied out)  converter (64)
+  B_QF0, B_QF1,  // kEmitR: the staged bf16 Q, g and beta have been read  transposer + converter
   B_RL0, B_RL1,  // kEmitR: a record is staged (byte count)              loader
   B_RF0, B_RF1,  // kEmitR: its record stage is free (D, O2, Dh done)    MMA commit
   B_END,       // every product issued has completed                  MMA commit
@@ -102,8 +108,10 @@ enum Bar {
 };
 template <int MODE>
 __device__ __forceinline__ uint32_t bar_count(int b) {
-  return (b == B_E2 || b == B_T || b == B_WR)  ? (uint32_t)kPrepThreads
-         : (b == B_TB || b == B_CV || b == B_QF0 || b == B_QF1) ? (uint32_t)kConvThreads
+  return (b == B_E2 && MODE == kEmitR)         ? 64u  // (kEmitR: the two gram warps)
+         : (b == B_QF0 || b == B_QF1)          ? (uint32_t)(64 + kConvThreads)
+         : (b == B_E2 || b == B_T || b == B_WR)  ? (uint32_t)kPrepThreads
+         : (b == B_TB || b == B_CV) ? (uint32_t)kConvThreads
          : (b == B_HR || b == B_DR)            ? (uint32_t)kChainThreads
          : (b >= B_L0 && b <= B_L2)            ? (MODE == kSumML ? 1u : 33u)
          : (b == B_RL0 || b == B_RL1)          ? 1u
@@ -330,7 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_relinquish();
   }
   if (MODE != kSumML && tid == kChainThreads) {
-    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
+    if (MODE != kEmitR)
+      asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
     if (OUT)
       asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
     if (MODE != kSumM && MODE != kEmitR)
@@ -347,6 +356,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // kSumML stages: the -w^T and K tiles of a record, 32 KB each, in the K | Q and V tiles
   auto rec_stage = [&](int st) -> uint8_t* { return st == 0 ? S.kq[0] : st == 1 ? S.kq[1] : S.v[0]; };
+  // kEmitR: the bf16 Q boxes of a stage land in tiles the factors would use (16 KB each); the
+  // stage's K | Q tile holds [-w^T rows 0-63 | Q^T box 0 | -w^T rows 64-127 | Q^T box 1], so
+  // that one MN-major operand with its second 64 columns 8 KB on is [-w^T | Q^T]
+  auto qstage = [&](int sg) -> uint8_t* { return sg ? S.nw : S.tw; };
 
   if (warp < 8) {
     // =============================================================== chain (256 threads)
@@ -446,6 +459,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int piece = 0; piece < 2; ++piece) {
           float o[16];
           tmem_ld16(tm + lane_bits + TM_DO + 64 + 32 * hf + 16 * piece, o);
+          if (MODE == kEmitR) {  // o = e^{G_t} (q h)_t + (attn_i delta)_t
+            float o2[16];
+            tmem_ld16(tm + lane_bits + TM_W + 32 * hf + 16 * piece, o2);
+            const float* eg = &S.eG[gb][32 * hf + 16 * piece];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) o[q] = fmaf(eg[q], o[q], o2[q]);
+          }
 #pragma unroll
           for (int q = 0; q < 8; ++q) ob[8 * piece + q] = pack_bf2(o[2 * q], o[2 * q + 1]);
         }
@@ -488,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_bits = (uint32_t)((warp & 3) * 32) << 16;
     const int g8 = lane >> 2, q4 = lane & 3;
     const uint32_t ah_s = saddr(S.ah), th_s = saddr(S.th);
+    const bool lo_warps = pt < 64;
 
     // the strictly upper blocks of T diag(.), rows 0-31 x columns 32-63 of A and attn_i, and the
     // upper right 8 x 8 of each warp's fp32 block of T are zero for every chunk
@@ -501,6 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       reinterpret_cast<uint4*>(S.att[1])[e] = make_uint4(0u, 0u, 0u, 0u);
     }
     for (int e = pt; e < 4 * 16 * 17; e += kPrepThreads) (&S.wd[0][0])[e] = 0.f;
+    named_bar(1, kPrepThreads);
 
     // 32 fp32 values as fp16 into row t, columns 32 hb .. 32 hb + 31, of a 64-column tile
     auto put_row32 = [&](uint8_t* dst, int t, int hb, const float (&sv)[32]) {
@@ -524,8 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_bar(S, B_SQ, ci & 1);
       wait_bar(S, B_TB, ci & 1);
       fence_after_sync();
-      const bool is_s = pt < 64;  // warps 8, 9: rows of A; warps 10, 11: rows of attn_i
-      if (MODE == kEmitR ? !is_s : (is_s || MODE == kEmit)) {  // (kEmitR: attn_i rows only)
+      // warps 8, 9: rows of A (kEmitR: of attn_i, from Q K^T); warps 10, 11: rows of attn_i
+      const bool lo = pt < 64, is_s = MODE != kEmitR && lo;
+      if (MODE == kEmit || lo) {
         const int t = pt & 63, hi = t >> 5, ab = (t >> 4) & 1;  // hi is warp-uniform
         const float4 rf4 = *reinterpret_cast<const float4*>(is_s ? S.rfA[t] : S.rfO[t]);
         uint8_t* dst = is_s ? S.ah : S.att[ci & 1];
@@ -777,11 +800,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       arrive(S, B_WR);
     };
 
-    if (MODE == kEmitR) {  // the factors come from the records: attn_i only
+    if (MODE == kEmitR && lo_warps) {  // the factors come from the records: attn_i only
       for (int ci = 0; ci < nch; ++ci) {
         gram(ci);
-        if (!named_bar_and(1, kPrepThreads, !aborted(S))) break;
+        if (!named_bar_and(1, 64, !aborted(S))) break;
       }
+    }
+    if (MODE == kEmitR && !lo_warps) {
+      // Q (bf16, rows t) -> Q^T (fp16, rows i), the MN-major operand of Q K^T and of q h.  Warp
+      // 10 + b takes the features of box b, as 8 x 8 blocks (t-block tb, i-block ib): four per
+      // step through ldmatrix.trans, and stmatrix to rows i, column chunk tb.
+      const int box = warp - 10, m = lane >> 3, r = lane & 7;
+      __nv_bfloat162 mx2 = __floats2bfloat162_rn(0.f, 0.f);
+      for (int ci = 0; ci < nch; ++ci) {
+        const int sg = ci & 1;
+        wait_bar(S, B_L0 + sg, (ci >> 1) & 1);
+        // Q K^T of the previous chunk is done, and with it [D | q h] of ci - 2, the last reader of
+        // this stage's Q^T (this also keeps Q^T at most one chunk ahead of the MMA warp's wait)
+        if (ci >= 1) wait_bar(S, B_SQ, (ci - 1) & 1);
+        const uint32_t src = saddr(qstage(sg)) + box * 8192;
+        const uint32_t dst = saddr(S.kq[sg]) + 8192 + box * 16384;
+#pragma unroll 2
+        for (int g = 0; g < 16; ++g) {
+          const int tb = g >> 1, ib = 4 * (g & 1) + m;
+          uint32_t x[4];
+          ldsm_x4_t(src + (8 * tb + r) * 128 + ((ib ^ r) << 4), x);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&x[k]);
+            mx2 = __hmax2(mx2, __habs2(b2));
+            const float2 f = __bfloat1622float2(b2);
+            x[k] = pack_h2(f.x, f.y);
+          }
+          stsm_x4(dst + (8 * ib + r) * 128 + ((tb ^ r) << 4), x);
+        }
+        fence_async_smem();  // Q^T feeds the tensor core
+        fence_before_sync();
+        arrive(S, B_CV);
+        arrive(S, B_QF0 + sg);
+        if (!named_bar_and(4, 64, !aborted(S))) break;
+      }
+      const float2 mx = __bfloat1622float2(mx2);
+      if (!(fmaxf(mx.x, mx.y) <= kHalfMax)) S.range_bad = 1;
     }
     // one chunk ahead: the gram of chunk ci + 1 is built while w of chunk ci is computed
     bool go = MODE != kEmitR && nch > 0;
@@ -828,7 +888,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int ci = 0; MODE != kSumML && ci < nch; ++ci) {
       const int sg = ci & 1;
       // the stage was last used by chunk ci - 2: wait for its w, u (and q_g h) products, or
-      // (kEmitR) for q_g to have been copied out of it
+      // (kEmitR) for its Q, g and beta to have been read
       if (ci >= 2) wait_bar(S, (MODE == kEmitR ? B_QF0 : B_F0) + sg, ((ci >> 1) + 1) & 1);
       if (__any_sync(0xffffffffu, aborted(S))) break;
       const int64_t t0 = sb + (c0 + ci) * C;
@@ -836,14 +896,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t bar = saddr(&S.bars[B_L0 + sg]);
       if (lane == 0) {  // rows past T read zeros; rows in [L, 64) only meet zero weights
         const uint32_t kq = saddr(S.kq[sg]), vv = saddr(S.v[sg]);
-        const uint32_t bytes =
-            (OUT ? 4u : 2u) * 8192u + (MODE != kSumM && MODE != kEmitR ? 2u : 0u) * 8192u;
+        const uint32_t bytes = MODE == kEmitR ? 2u * 8192u
+                                              : (OUT ? 4u : 2u) * 8192u + (MODE != kSumM ? 2u : 0u) * 8192u;
         mbar_expect_tx(bar, bytes);
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
+          if (MODE == kEmitR) {  // Q only: [S ; QK] takes fp16 K from the record
+            tma_box(saddr(qstage(sg)) + kb * 8192, &tm_q, 64 * kb, kh, (int)t0, bar);
+            continue;
+          }
           tma_box(kq + kb * 16384, &tm_k, 64 * kb, kh, (int)t0, bar);
           if (OUT) tma_box(kq + kb * 16384 + 8192, &tm_q, 64 * kb, kh, (int)t0, bar);
-          if (MODE != kSumM && MODE != kEmitR) tma_box(vv + kb * 8192, &tm_v, 64 * kb, j, (int)t0, bar);
+          if (MODE != kSumM) tma_box(vv + kb * 8192, &tm_v, 64 * kb, j, (int)t0, bar);
         }
       }
 #pragma unroll
@@ -856,13 +920,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar)
                    : "memory");
-      if (MODE == kEmitR) {  // the chunk's record (-w^T, fp16 K, u^T) into its own ring
+      if (MODE == kEmitR) {  // the chunk's record (-w^T, fp16 K, u^T), once Dh of ci - 2 is done
         if (ci >= 2) wait_bar(S, B_RF0 + sg, ((ci >> 1) + 1) & 1);
         if (lane == 0) {
           const char* rec = chunk_record(a, n_seq, sb, c0 + ci, j);
           const uint32_t rb = saddr(&S.bars[B_RL0 + sg]);
           mbar_expect_tx(rb, 3u * 16384u);
-          bulk_g2s(saddr(sg ? S.tw : S.nw), rec + kRecNw, 16384u, rb);
+          bulk_g2s(saddr(S.kq[sg]), rec + kRecNw, 8192u, rb);
+          bulk_g2s(saddr(S.kq[sg]) + 16384u, rec + kRecNw + 8192, 8192u, rb);
           bulk_g2s(saddr(S.kh[sg]), rec + kRecKh, 16384u, rb);
           bulk_g2s(saddr(S.v[sg]), rec + kRecU, 16384u, rb);
         }
@@ -916,6 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the K tile stored two chunks back has been read before it is rewritten
       if (MODE == kSumU && a.wy && p == 0) bulk_wait_read();
       if (!named_bar_and(3, kConvThreads, !aborted(S))) break;
+      if (MODE == kEmitR) arrive(S, B_QF0 + sg);  // g and beta of the stage have been read
       {  // row t: its own 16-block directly, the factor to each earlier block's last row;
          // the A rows' copies carry beta_t and leave out s = t
         const int t = p, at = t >> 4, k0 = t & 15;
@@ -940,7 +1006,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float4*>(&S.rfO[t][0]) = f;
         *reinterpret_cast<float4*>(&S.rfA[t][0]) = make_float4(bt * f.x, bt * f.y, bt * f.z, 0.f);
       }
-      if (OUT) wait_bar(S, B_SQ, ci & 1);  // [S ; QK] has read the bf16 Q
+      if (MODE == kEmit) wait_bar(S, B_SQ, ci & 1);  // [S ; QK] has read the bf16 Q
       arrive(S, B_TB);
       if (MODE != kSumM && MODE != kEmitR) {  // V -> fp16 in place (read only by the u product)
         uint8_t* vb = S.v[sg] + 16 * p;
@@ -972,23 +1038,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           maxabs = to_half_chunks<4, true>(pq, pq, &S.eG[gb][(p >> 3) + 8 * (k0 & 7)], maxabs);
         }
       }
-      if (MODE == kEmitR) {
-        // q_g into its own tile (the A and T tiles, unused here; boxes 8 KB apart), once q_g h
-        // of the previous chunk is done, so the K | Q stage is free for the loader at once
-        if (ci >= 1) wait_bar(S, B_F0 + ((ci - 1) & 1), ((ci - 1) >> 1) & 1);
-        const uint8_t* qb = S.kq[sg] + 8192 + 16 * p;
-        uint8_t* qd = S.ah + 16 * p;
-#pragma unroll 1
-        for (int k0 = 0; k0 < 16; k0 += 4)
-          maxabs = to_half_chunks<4, true>(qb + (k0 >> 3) * 16384 + 1024 * (k0 & 7),
-                                           qd + (k0 >> 3) * 8192 + 1024 * (k0 & 7),
-                                           &S.eG[gb][(p >> 3) + 8 * (k0 & 7)], maxabs);
-        arrive(S, B_QF0 + sg);
+      if (MODE != kEmitR) {  // (kEmitR: the transposer hands over Q^T)
+        // the MMA warp has waited for the previous chunk's hand-off
+        if (ci >= 1) wait_bar(S, B_WU, (ci - 1) & 1);
+        fence_async_smem();
+        arrive(S, B_CV);
       }
-      // the MMA warp has waited for the previous chunk's hand-off
-      if (ci >= 1 && MODE != kEmitR) wait_bar(S, B_WU, (ci - 1) & 1);  // (kEmitR: above)
-      fence_async_smem();
-      arrive(S, B_CV);
     }
     if (!(maxabs <= kHalfMax)) S.range_bad = 1;
     if (MODE == kSumU && a.wy && p == 0) bulk_wait_all();
@@ -1044,7 +1099,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     };
-    if (MODE != kSumML && nch > 0) {
+    if (MODE != kSumML && MODE != kEmitR && nch > 0) {
       wait_bar(S, B_L0, 0);
       sq(0);
       if (nch > 1) {  // the SQ columns are reused once the first gram has read them
@@ -1053,51 +1108,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         sq(1);
       }
     }
-    // kEmitR, per chunk c: D (c) from the staged record; q_g h (c); O2, Dh (c); [S ; QK] (c + 2)
-    for (int ci = 0; MODE == kEmitR && ci < nch; ++ci) {
+    // kEmitR, per chunk c: [D | q h] (c); O2, Dh (c); Q K^T (c + 1).  Q K^T takes Q^T (MN-major
+    // A; only its 64 rows t are read out) and the record's fp16 K.
+    const uint32_t ID_SQR = idesc_f16(128, 64, 1, 0);   // Q K^T
+    const uint32_t ID_DQ = idesc_f16(128, 128, 0, 1);   // h^T [-w^T | Q^T]
+    auto sqr = [&](int ci) {
       const int st = ci & 1;
+      wait_bar(S, B_CV, ci & 1);
       wait_bar(S, B_RL0 + st, (ci >> 1) & 1);
-      wait_bar(S, B_HR, ci & 1);
       fence_after_sync();
       if (leader) {
-        const uint32_t nw = saddr(st ? S.tw : S.nw);
+        const uint32_t qt = saddr(S.kq[st]) + 8192, khs = saddr(S.kh[st]);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss(tm + TM_SQ, sdesc(qt + (ks >> 2) * 16384 + (ks & 3) * 2048, 8192, 1024),
+                 sdesc(khs + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), ID_SQR, ks > 0);
+        mma_commit(saddr(&S.bars[B_SQ]));
+      }
+      __syncwarp();
+    };
+    if (MODE == kEmitR && nch > 0) sqr(0);
+    for (int ci = 0; MODE == kEmitR && ci < nch; ++ci) {
+      const int st = ci & 1;
+      wait_bar(S, B_HR, ci & 1);  // (the record and Q^T were waited for by Q K^T)
+      fence_after_sync();
+      if (leader) {  // D^T (delta^T less u^T) and (q h)^T in one product
+        const uint32_t b = saddr(S.kq[st]);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           mma_ts(tm + TM_DO, tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3),
-                 sdesc(nw + ks * 2048, 16384, 1024), ID_D, ks > 0);
+                 sdesc(b + (ks >> 2) * 16384 + (ks & 3) * 2048, 8192, 1024), ID_DQ, ks > 0);
         mma_commit(saddr(&S.bars[B_D]));
       }
       __syncwarp();
-      wait_bar(S, B_CV, ci & 1);
-      fence_after_sync();
-      if (leader) {  // o^T = h^T q_g^T starts the O accumulator; then the K | Q stage is free
-        const uint32_t qg = saddr(S.ah);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ts(tm + TM_DO + 64, tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3),
-                 sdesc(qg + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), ID_QH, ks > 0);
-        mma_commit(saddr(&S.bars[B_F0 + st]));
-      }
-      __syncwarp();
       wait_bar(S, B_DR, ci & 1);
+      wait_bar(S, B_E2, ci & 1);  // attn_i is written and the Q K^T columns are read
       fence_after_sync();
-      if (leader) {  // then the record stage is free
+      if (leader) {  // (attn_i delta)^T into its own columns; then the record stage is free
         const uint32_t att = saddr(S.att[st]), khs = saddr(S.kh[st]);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const uint32_t col = 32 * (ks >> 1) + 8 * (ks & 1);
-          mma_ts(tm + TM_DO + 64, tm + TM_DO + col, sdesc(att + ks * 32, 16, 1024), ID_O2, 1);
+          mma_ts(tm + TM_W, tm + TM_DO + col, sdesc(att + ks * 32, 16, 1024), ID_O2, ks > 0);
           mma_ts(tm + TM_H, tm + TM_U + col, sdesc(khs + ks * 2048, 8192, 1024), ID_DH, ks > 0);
         }
         mma_commit(saddr(&S.bars[B_H]));
         mma_commit(saddr(&S.bars[B_RF0 + st]));
       }
       __syncwarp();
-      if (ci + 2 < nch) {
-        wait_bar(S, B_E2, (ci + 1) & 1);
-        wait_bar(S, B_L0 + st, ((ci + 2) >> 1) & 1);
-        sq(ci + 2);
-      }
+      if (ci + 1 < nch) sqr(ci + 1);
       if (__any_sync(0xffffffffu, aborted(S))) break;
     }
     for (int ci = 0; MODE != kSumML && MODE != kEmitR && ci < nch; ++ci) {
@@ -1235,7 +1294,8 @@ cudaError_t launch5(const Args& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   CUtensorMap mk, mq, mv;
   const bool empty = a.T == 0;
-  if ((e = make_map(&mk, empty || MODE == kSumML ? nullptr : a.k, a.T, a.hk)) != cudaSuccess)
+  if ((e = make_map(&mk, empty || MODE == kSumML || MODE == kEmitR ? nullptr : a.k, a.T, a.hk)) !=
+      cudaSuccess)
     return e;
   if ((e = make_map(&mq, empty || (MODE != kEmit && MODE != kEmitR) ? nullptr : a.q, a.T,
                     a.hk)) != cudaSuccess)

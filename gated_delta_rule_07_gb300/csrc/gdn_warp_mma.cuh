@@ -20,6 +20,15 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
                : "r"(addr));
 }
 
+// Four 8 x 8 matrices of 16-bit values to shared memory; lanes 8m .. 8m + 7 give the row
+// addresses of matrix m, and lane l's register m holds its row l / 4, columns 2 (l % 4) and
+// 2 (l % 4) + 1 (the layout ldmatrix returns).
+__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&r)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(addr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+
 // D = A * B + D, m16n8k16, A row-major, B column-major, fp16 in, fp32 accumulate.
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
