@@ -168,18 +168,26 @@ static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory per block");
 __device__ __forceinline__ uint32_t saddr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// Named barriers over `n` threads (whole warps).  A lane may arrive after divergent work of its
+// own (one lane issuing bulk copies, or waiting for them), so each warp first reconverges and
+// the barrier is the form that does not require a converged warp; the warp leaves converged, as
+// the tcgen05.ld / st that follow require.
 __device__ __forceinline__ void named_bar(int id, int n) {
-  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+  __syncwarp();
+  asm volatile("barrier.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+  __syncwarp();
 }
 // Barrier over `n` threads that also ANDs a predicate across them.
 __device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
   uint32_t r;
+  __syncwarp();
   asm volatile(
-      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, %2, %3, p;\n"
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbarrier.red.and.pred q, %2, %3, p;\n"
       "selp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
       : "r"((uint32_t)v), "r"(id), "r"(n)
       : "memory");
+  __syncwarp();
   return r != 0;
 }
 __device__ __forceinline__ bool aborted(Smem& S) {
@@ -237,10 +245,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t mbar, uint32_t bytes) {
           mbar),
       "r"(bytes)
       : "memory");
-}
-
-__device__ __forceinline__ void st_half(uint8_t* tile, int r, int c, float x) {
-  *reinterpret_cast<__half*>(tile + sw128_offset(64, r, c)) = __float2half_rn(x);
 }
 
 // NB 16-byte chunks of bf16 at src + 1024 k to fp16 at dst + 1024 k; with SCALED the values of
