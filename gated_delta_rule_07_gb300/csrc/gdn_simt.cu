@@ -17,7 +17,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int C = kChunk;
 constexpr int kColBlock = 32;  // state columns per CTA (columns of h, M, U are independent)
-constexpr int kScanCols = 8;   // the scan: narrower blocks, four times the CTAs, for its latency
+constexpr int kScanCols = 16;  // the scan: narrower blocks, twice the CTAs (two per SM), for its latency
 
 // ------------------------------------------------------------------ validation
 
@@ -207,55 +207,69 @@ __global__ void __launch_bounds__(kThreads) simt_summary_kernel(Args a) {
 
 // ------------------------------------------------------------------ phase 2
 
-// One CTA per (sequence, value head, block of 8 state columns); serial over segments:
-// h_in[r] = h, h <- M_r h + U_r.
+// One CTA per (sequence, value head, block of kScanCols state columns); serial over segments:
+// h_in[r] = h, h <- M_r h + U_r.  Each M_r (KD x KD fp32) is read as a batch of 16-byte loads
+// into registers one segment ahead, so that its latency overlaps the previous step; a thread
+// owns one column and NO rows of the product, whose sums run side by side.
 template <int KD, int VD>
 __global__ void __launch_bounds__(kThreads) simt_scan_kernel(Args a) {
-  constexpr int KP = KD + 1, XP = kScanCols + 1;
+  constexpr int KP = KD + 4, XP = kScanCols + 1;  // 16-byte rows for M; conflict-free reads
+  constexpr int NV = KD * KD / 4 / kThreads;      // float4 of M per thread
+  constexpr int RS = kThreads / kScanCols, NO = KD / RS;  // row stride, rows per thread
+  static_assert(NV * 4 * kThreads == KD * KD && RS * NO == KD, "the CTA tiles M and h");
   extern __shared__ float sm[];
   float* Ms = sm;              // [KD][KP]
   float* hs = Ms + KD * KP;    // [KD][XP]
-  float* hn = hs + KD * XP;    // [KD][XP]
   const int n = blockIdx.x, j = blockIdx.y, col0 = blockIdx.z * kScanCols;
-  const int tid = threadIdx.x;
-  for (int e = tid; e < KD * kScanCols; e += kThreads) {
-    const int i = e / kScanCols, c = e % kScanCols;
-    hs[i * XP + c] = a.h0 ? a.h0[(((int64_t)n * a.hv + j) * KD + i) * VD + col0 + c] : 0.f;
-  }
+  const int tid = threadIdx.x, c = tid % kScanCols, i0 = tid / kScanCols;
+  // the segments whose M is read: all but the last, unless the last step feeds h_final
+  const int steps = a.h_final ? a.P : a.P - 1;
+  float4 mv[NV];
+  auto load_m = [&](int r) {
+    const float4* src = reinterpret_cast<const float4*>(
+        a.M + ((((int64_t)n * a.P + r) * a.hv + j) * KD) * KD);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) mv[k] = src[tid + kThreads * k];
+  };
+  if (steps > 0) load_m(0);
+  float h[NO];  // h[i0 + RS m][c]
+#pragma unroll
+  for (int m = 0; m < NO; ++m)
+    h[m] = a.h0 ? a.h0[(((int64_t)n * a.hv + j) * KD + i0 + RS * m) * VD + col0 + c] : 0.f;
   for (int r = 0; r < a.P; ++r) {
-    const int64_t seg = (int64_t)n * a.P + r;
-    if (r == a.P - 1 && a.h_final == nullptr) {  // the last summary only feeds h_final
-      __syncthreads();
-      for (int e = tid; e < KD * kScanCols; e += kThreads) {
-        const int i = e / kScanCols, c = e % kScanCols;
-        a.h_in_out[((seg * a.hv + j) * KD + i) * VD + col0 + c] = hs[i * XP + c];
-      }
-      return;
+    const int64_t base = (((int64_t)n * a.P + r) * a.hv + j) * KD;  // row 0 of segment r
+    if (a.h_in_out) {
+#pragma unroll
+      for (int m = 0; m < NO; ++m) a.h_in_out[(base + i0 + RS * m) * VD + col0 + c] = h[m];
     }
-    __syncthreads();
-    for (int e = tid; e < KD * KD; e += kThreads)
-      Ms[(e / KD) * KP + e % KD] = a.M[((seg * a.hv + j) * KD) * KD + e];
-    for (int e = tid; e < KD * kScanCols; e += kThreads) {
-      const int i = e / kScanCols, c = e % kScanCols;
-      if (a.h_in_out) a.h_in_out[((seg * a.hv + j) * KD + i) * VD + col0 + c] = hs[i * XP + c];
+    if (r == steps) return;  // the last summary only feeds h_final
+    float u[NO];
+#pragma unroll
+    for (int m = 0; m < NO; ++m) u[m] = a.U[(base + i0 + RS * m) * VD + col0 + c];
+    __syncthreads();  // the previous step has read Ms and hs
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+      const int e = 4 * (tid + kThreads * k), i = e / KD, b = e % KD;
+      *reinterpret_cast<float4*>(&Ms[i * KP + b]) = mv[k];
     }
+#pragma unroll
+    for (int m = 0; m < NO; ++m) hs[(i0 + RS * m) * XP + c] = h[m];
     __syncthreads();
-    for (int e = tid; e < KD * kScanCols; e += kThreads) {
-      const int i = e / kScanCols, c = e % kScanCols;
-      float x = a.U[((seg * a.hv + j) * KD + i) * VD + col0 + c];
-      for (int b = 0; b < KD; ++b) x += Ms[i * KP + b] * hs[b * XP + c];
-      hn[i * XP + c] = x;
+    if (r + 1 < steps) load_m(r + 1);  // lands while this step computes
+#pragma unroll 4
+    for (int b = 0; b < KD; ++b) {
+      const float hb = hs[b * XP + c];
+#pragma unroll
+      for (int m = 0; m < NO; ++m) u[m] += Ms[(i0 + RS * m) * KP + b] * hb;
     }
-    __syncthreads();
-    for (int e = tid; e < KD * kScanCols; e += kThreads) hs[(e / kScanCols) * XP + e % kScanCols] =
-        hn[(e / kScanCols) * XP + e % kScanCols];
+#pragma unroll
+    for (int m = 0; m < NO; ++m) h[m] = u[m];
   }
-  __syncthreads();
-  if (a.h_final)
-    for (int e = tid; e < KD * kScanCols; e += kThreads) {
-      const int i = e / kScanCols, c = e % kScanCols;
-      a.h_final[(((int64_t)n * a.hv + j) * KD + i) * VD + col0 + c] = hs[i * XP + c];
-    }
+  if (a.h_final) {
+#pragma unroll
+    for (int m = 0; m < NO; ++m)
+      a.h_final[(((int64_t)n * a.hv + j) * KD + i0 + RS * m) * VD + col0 + c] = h[m];
+  }
 }
 
 // ------------------------------------------------------------------ phase 3
@@ -384,7 +398,7 @@ struct Simt {
                   dim3((unsigned)(a.N * a.P), a.hv, (KD + VD) / kColBlock), smem, s, a);
   }
   static cudaError_t scan(const Args& a, cudaStream_t s) {
-    const size_t smem = sizeof(float) * (KD * (KD + 1) + 2 * KD * (kScanCols + 1));
+    const size_t smem = sizeof(float) * (KD * (KD + 4) + KD * (kScanCols + 1));
     return launch(simt_scan_kernel<KD, VD>, dim3((unsigned)a.N, a.hv, VD / kScanCols), smem, s,
                   a);
   }
