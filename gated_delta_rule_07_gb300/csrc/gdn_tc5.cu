@@ -990,25 +990,30 @@ __global__ void __launch_bounds__(kThreads, 1)
          // the A rows' copies carry beta_t and leave out s = t
         const int t = p, at = t >> 4, k0 = t & 15;
         const float Gt = S.G[gb][t], bt = S.beta[gb][t];
+        // (the summaries read only A's tables, phase 3 from records only attn_i's)
+        constexpr bool kA = MODE != kEmitR, kO = MODE == kEmit || MODE == kEmitR;
 #pragma unroll
         for (int k4 = 0; k4 < 16; k4 += 4) {
           float d[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) d[i] = __expf(Gt - S.G[gb][16 * at + k4 + i]);
-          *reinterpret_cast<float4*>(&S.ddO[t][k4]) =
-              make_float4(k4 + 0 <= k0 ? d[0] : 0.f, k4 + 1 <= k0 ? d[1] : 0.f,
-                          k4 + 2 <= k0 ? d[2] : 0.f, k4 + 3 <= k0 ? d[3] : 0.f);
-          *reinterpret_cast<float4*>(&S.ddA[t][k4]) =
-              make_float4(k4 + 0 < k0 ? bt * d[0] : 0.f, k4 + 1 < k0 ? bt * d[1] : 0.f,
-                          k4 + 2 < k0 ? bt * d[2] : 0.f, k4 + 3 < k0 ? bt * d[3] : 0.f);
+          if (kO)
+            *reinterpret_cast<float4*>(&S.ddO[t][k4]) =
+                make_float4(k4 + 0 <= k0 ? d[0] : 0.f, k4 + 1 <= k0 ? d[1] : 0.f,
+                            k4 + 2 <= k0 ? d[2] : 0.f, k4 + 3 <= k0 ? d[3] : 0.f);
+          if (kA)
+            *reinterpret_cast<float4*>(&S.ddA[t][k4]) =
+                make_float4(k4 + 0 < k0 ? bt * d[0] : 0.f, k4 + 1 < k0 ? bt * d[1] : 0.f,
+                            k4 + 2 < k0 ? bt * d[2] : 0.f, k4 + 3 < k0 ? bt * d[3] : 0.f);
         }
         float4 f;
         f.x = at > 0 ? __expf(Gt - S.G[gb][15]) : 0.f;
         f.y = at > 1 ? __expf(Gt - S.G[gb][31]) : 0.f;
         f.z = at > 2 ? __expf(Gt - S.G[gb][47]) : 0.f;
         f.w = 0.f;
-        *reinterpret_cast<float4*>(&S.rfO[t][0]) = f;
-        *reinterpret_cast<float4*>(&S.rfA[t][0]) = make_float4(bt * f.x, bt * f.y, bt * f.z, 0.f);
+        if (kO) *reinterpret_cast<float4*>(&S.rfO[t][0]) = f;
+        if (kA)
+          *reinterpret_cast<float4*>(&S.rfA[t][0]) = make_float4(bt * f.x, bt * f.y, bt * f.z, 0.f);
       }
       if (MODE == kEmit) wait_bar(S, B_SQ, ci & 1);  // [S ; QK] has read the bf16 Q
       arrive(S, B_TB);
