@@ -213,9 +213,11 @@ def run_ours(args, ws, rank, local):
     ph = {k: statistics.mean(v) for k, v in phase_ms.items()}
 
     # end to end through the C ABI with host buffers: every step copies its inputs in from
-    # pinned host memory, runs the forward and reads its outputs back.  Steps are pipelined on
-    # three streams (copies in, compute, copies out) over two sets of device buffers, so one
-    # step's copies overlap the neighbouring steps' work.
+    # pinned host memory, runs the forward and reads its outputs back.  Steps are pipelined over
+    # two sets of device buffers: the input copies on two streams (q, k, g, beta and v, about
+    # half the bytes each, so that two copy engines work at once), the forward on its own, the
+    # output copies in two halves on two more, so one step's copies overlap its neighbours'
+    # work.
     host = {n: d[n].cpu().pin_memory() for n in d}
     out_h = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
     hf_h = [torch.empty(hf.shape, dtype=hf.dtype).pin_memory() for _ in range(2)]
@@ -226,38 +228,50 @@ def run_ours(args, ws, rank, local):
     dd = [{n: torch.empty_like(d[n]) for n in d} for _ in range(2)]
     outs = [torch.empty_like(out) for _ in range(2)]
     hfs = [torch.empty_like(hf) for _ in range(2)]
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(2)]   # step's inputs are on the device
-    ev_cmp = [torch.cuda.Event() for _ in range(2)]  # step's forward is done
-    ev_out = [torch.cuda.Event() for _ in range(2)]  # step's outputs are on the host
+    groups = (("q", "k", "g", "beta"), ("v",))
+    s_in = [torch.cuda.Stream() for _ in groups]
+    s_out = [torch.cuda.Stream() for _ in range(2)]
+    ev_in = [[torch.cuda.Event() for _ in s_in] for _ in range(2)]    # inputs on the device
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]                   # forward done
+    ev_out = [[torch.cuda.Event() for _ in s_out] for _ in range(2)]  # outputs on the host
+    half = out.shape[0] // 2
 
     def e2e_step(i):
         b = i & 1
-        with torch.cuda.stream(s_in):
-            s_in.wait_event(ev_cmp[b])  # the forward two steps back has read these buffers
-            for n in d:
-                dd[b][n].copy_(host[n], non_blocking=True)
-            ev_in[b].record(s_in)
-        stream.wait_event(ev_in[b])
-        stream.wait_event(ev_out[b])  # its outputs two steps back have been read out
+        for s, names, ev in zip(s_in, groups, ev_in[b]):
+            with torch.cuda.stream(s):
+                s.wait_event(ev_cmp[b])  # the forward two steps back has read these buffers
+                for n in names:
+                    dd[b][n].copy_(host[n], non_blocking=True)
+                ev.record(s)
+        for ev in ev_in[b] + ev_out[b]:  # (its outputs two steps back have been read out)
+            stream.wait_event(ev)
         gdn.gdn_forward(pe, dd[b]["q"], dd[b]["k"], dd[b]["v"], dd[b]["g"], dd[b]["beta"], None,
                         None, outs[b], hfs[b], wse, stream=stream)
         ev_cmp[b].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_cmp[b])
-            out_h[b].copy_(outs[b], non_blocking=True)
-            hf_h[b].copy_(hfs[b], non_blocking=True)
-            ev_out[b].record(s_out)
+        for k, s in enumerate(s_out):
+            with torch.cuda.stream(s):
+                s.wait_event(ev_cmp[b])
+                rows = slice(0, half) if k == 0 else slice(half, out.shape[0])
+                out_h[b][rows].copy_(outs[b][rows], non_blocking=True)
+                if k == 1:
+                    hf_h[b].copy_(hfs[b], non_blocking=True)
+                ev_out[b][k].record(s)
 
     for i in range(args.warmup):
         e2e_step(i)
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
+    e0.record(stream)
+    for s in s_in:
+        s.wait_event(e0)
     for i in range(args.steps):
         e2e_step(args.warmup + i)
-    e1.record(s_out)
+    for evs in ev_out:
+        for ev in evs:
+            stream.wait_event(ev)
+    e1.record(stream)
     torch.cuda.synchronize()
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.steps
@@ -335,8 +349,8 @@ def run_ours(args, ws, rank, local):
                                   + src},
         "e2e": {"value": tokens / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "pipelining": "copies in, forward and copies out on three streams over two "
-                              "buffer sets"},
+                "pipelining": "copies in on two streams, the forward, copies out on two more, "
+                              "over two buffer sets"},
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
