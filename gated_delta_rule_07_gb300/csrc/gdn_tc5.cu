@@ -31,9 +31,12 @@
 // Warp roles (512 threads):
 //   warps 0-7   chain:     TMEM lane = state row c; warps w and w + 4 split the columns
 //   warps 8-11  prepare:   masked gram and attn_i, the triangular solve, -w; one chunk ahead
+//                          (kEmitR: warps 8, 9 attn_i, warps 10, 11 the fp16 Q^T)
 //   warp 12     MMA:       waits for each product's inputs in a fixed order; lane 0 issues
-//   warp 13     loader:    TMA boxes of K, Q, V and cp.async of g, beta into the free stage
-//   warps 14-15 converter: decay tables, fp16 K, V and q_g
+//   warp 13     loader:    TMA boxes of K, Q, V, cp.async of g, beta and bulk copies of the
+//                          factor records into the free stage
+//   warps 14-15 converter: decay tables, fp16 K, V and q_g (kEmitR: the tables only; kSumML:
+//                          idle)
 // Hand-offs use mbarriers: a producing group arrives with every thread (the barrier counts the
 // group), a consumer waits with hardware-suspended try_wait (no issue slots spent).  Every wait
 // is bounded; one that gives up records GDN_ERR_DEVICE_TIMEOUT and the thread carries on, and
