@@ -423,11 +423,11 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=2048)
     ap.add_argument("--path", type=int, default=0,
-                    help="kernel family: 0 auto (tcgen05), 3 mma.sync baseline")
+                    help="kernel family: 0 auto (tcgen05 for this workload), 2 tcgen05")
     args = ap.parse_args()
     args.family = {0: "tcgen05 (TMEM accumulators, fp16 operands, fp32 state)",
-                   2: "tcgen05 (TMEM accumulators, fp16 operands, fp32 state)",
-                   3: "mma.sync (fp16 operands, fp32 state)"}.get(args.path, str(args.path))
+                   2: "tcgen05 (TMEM accumulators, fp16 operands, fp32 state)"}.get(
+                       args.path, str(args.path))
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_env()

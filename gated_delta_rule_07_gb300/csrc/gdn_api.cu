@@ -25,20 +25,13 @@ bool use_tensor_path(const gdn_problem* p) {
   return covers;
 }
 
-bool use_mma_sync(const gdn_problem* p) { return p->path == GDN_PATH_MMA_SYNC; }
-
-// Phase 1 and phase 3 with the factors recomputed on chip, on the selected tensor-core
-// generation.
-cudaError_t fused_summary(const gdn_problem* p, const Args& a, cudaStream_t s,
+// Phase 1 and phase 3 with the factors recomputed on chip (tensor-core kernels).
+cudaError_t fused_summary(const gdn_problem*, const Args& a, cudaStream_t s,
                           cudaEvent_t mid = nullptr) {
-  if (use_mma_sync(p)) {
-    cudaError_t e = gdn::tc_summary(a, true, s);
-    return (e == cudaSuccess && mid) ? cudaEventRecord(mid, s) : e;
-  }
   return gdn::tc5_summary(a, s, mid);
 }
-cudaError_t fused_emit(const gdn_problem* p, const Args& a, cudaStream_t s) {
-  return use_mma_sync(p) ? gdn::tc_emit(a, true, s) : gdn::tc5_emit(a, s);
+cudaError_t fused_emit(const gdn_problem*, const Args& a, cudaStream_t s) {
+  return gdn::tc5_emit(a, s);
 }
 
 gdn_status check_problem(const gdn_problem* p) {
@@ -49,11 +42,11 @@ gdn_status check_problem(const gdn_problem* p) {
     return GDN_ERR_INVALID_ARGUMENT;
   if (p->hv % p->hk != 0) return GDN_ERR_INVALID_ARGUMENT;
   if (p->io_dtype != GDN_BF16 && p->io_dtype != GDN_F32) return GDN_ERR_UNSUPPORTED;
-  if (p->path < GDN_PATH_AUTO || p->path > GDN_PATH_MMA_SYNC) return GDN_ERR_INVALID_ARGUMENT;
+  if (p->path < GDN_PATH_AUTO || p->path > GDN_PATH_TENSOR) return GDN_ERR_INVALID_ARGUMENT;
   if (p->chunk != 64) return GDN_ERR_UNSUPPORTED;
   if ((p->k_dim != 64 && p->k_dim != 128) || (p->v_dim != 64 && p->v_dim != 128))
     return GDN_ERR_UNSUPPORTED;
-  if ((p->path == GDN_PATH_TENSOR || p->path == GDN_PATH_MMA_SYNC) &&
+  if (p->path == GDN_PATH_TENSOR &&
       !(p->io_dtype == GDN_BF16 && p->k_dim == 128 && p->v_dim == 128))
     return GDN_ERR_UNSUPPORTED;
   if (p->hv > 65535) return GDN_ERR_UNSUPPORTED;  // grid.y
@@ -128,7 +121,7 @@ Layout layout(const gdn_problem* p, bool records = true) {
   L.gcum = off;
   off += mat ? align_up(T * p->hv * 4) : 0;
   L.wy = off;  // tcgen05 path: the U summary's per-chunk records for the M summary
-  off += (records && seg && !mat && !use_mma_sync(p))
+  off += (records && seg && !mat)
              ? align_up(gdn::tc5_records_bytes(p->total_tokens, p->num_seqs, p->hv))
              : 0;
   L.total = off;
@@ -189,7 +182,7 @@ gdn_status gdn_chunk_prepare(const gdn_problem* p, const void* k, const void* v,
   a.w_out = w; a.u_out = u; a.gcum_out = gcum; a.status = dev_status;
   if (a.T == 0) return GDN_OK;
   GDN_TRY(gdn::launch_validate_cu(a, stream));
-  return to_status(use_tensor_path(p) ? gdn::tc_prepare(a, stream) : gdn::simt_prepare(a, stream));
+  return to_status(gdn::simt_prepare(a, stream));
 }
 
 gdn_status gdn_segment_summary(const gdn_problem* p, const void* k, const void* w, const void* u,
@@ -206,8 +199,7 @@ gdn_status gdn_segment_summary(const gdn_problem* p, const void* k, const void* 
   a.k = k; a.w = w; a.u = u; a.gcum = gcum; a.cu = cu_seqlens;
   a.M_out = M; a.U_out = U; a.status = dev_status;
   GDN_TRY(gdn::launch_validate_cu(a, stream));
-  return to_status(use_tensor_path(p) ? gdn::tc_summary(a, false, stream)
-                                      : gdn::simt_summary(a, stream));
+  return to_status(gdn::simt_summary(a, stream));
 }
 
 gdn_status gdn_state_prefix_scan(const gdn_problem* p, const float* M, const float* U,
@@ -220,7 +212,7 @@ gdn_status gdn_state_prefix_scan(const gdn_problem* p, const float* M, const flo
     return GDN_ERR_INVALID_ARGUMENT;
   Args a = base_args(p);
   a.M = M; a.U = U; a.h0 = h0; a.h_in_out = h_in; a.h_final = h_final;
-  return to_status(use_tensor_path(p) ? gdn::tc_scan(a, stream) : gdn::simt_scan(a, stream));
+  return to_status(gdn::simt_scan(a, stream));
 }
 
 gdn_status gdn_chunk_emit(const gdn_problem* p, const void* q, const void* k, const void* w,
@@ -239,8 +231,7 @@ gdn_status gdn_chunk_emit(const gdn_problem* p, const void* q, const void* k, co
   a.q = q; a.k = k; a.w = w; a.u = u; a.gcum = gcum; a.h_in = h_in; a.cu = cu_seqlens;
   a.out = out; a.h_final = h_final; a.status = dev_status;
   GDN_TRY(gdn::launch_validate_cu(a, stream));
-  return to_status(use_tensor_path(p) ? gdn::tc_emit(a, false, stream)
-                                      : gdn::simt_emit(a, stream));
+  return to_status(gdn::simt_emit(a, stream));
 }
 
 }  // extern "C"
@@ -279,7 +270,7 @@ gdn_status forward_impl(const gdn_problem* p, const void* q, const void* k, cons
     a.M = a.M_out;
     a.U = a.U_out;
     a.h_in_out = reinterpret_cast<float*>(ws + L.h_in);
-    if (use_tensor_path(p) && !use_mma_sync(p) && L.total == Lr.total && Lr.total > Lr.wy)
+    if (use_tensor_path(p) && L.total == Lr.total && Lr.total > Lr.wy)
       a.wy = ws + L.wy;
   }
   // With P = 1 the incoming state of the only segment is h0 itself.
@@ -295,7 +286,7 @@ gdn_status forward_impl(const gdn_problem* p, const void* q, const void* k, cons
       GDN_TRY(mark(1));
       Args sa = a;
       sa.h_final = nullptr;  // the last segment's emit writes the final state
-      GDN_TRY(gdn::tc_scan(sa, stream));
+      GDN_TRY(gdn::simt_scan(sa, stream));
     } else {
       GDN_TRY(mark(1));
       GDN_TRY(mark(4));

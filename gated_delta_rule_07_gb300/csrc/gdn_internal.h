@@ -40,14 +40,6 @@ cudaError_t simt_summary(const Args& a, cudaStream_t s);
 cudaError_t simt_scan(const Args& a, cudaStream_t s);
 cudaError_t simt_emit(const Args& a, cudaStream_t s);
 
-// Tensor-core kernels, mma.sync generation (fp16 operands, fp32 accumulate and state;
-// K = V = 128).
-bool tc_supported(const Args& a);
-cudaError_t tc_prepare(const Args& a, cudaStream_t s);
-cudaError_t tc_summary(const Args& a, bool fused_prepare, cudaStream_t s);
-cudaError_t tc_scan(const Args& a, cudaStream_t s);
-cudaError_t tc_emit(const Args& a, bool fused_prepare, cudaStream_t s);
-
 // Tensor-core kernels, tcgen05 generation (TMEM accumulators, fp16 operands, fp32 state;
 // bf16 I/O, K = V = 128).  Factors are always recomputed on chip.
 size_t tc5_smem_bytes();

@@ -30,7 +30,7 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPOR
                 3: "GDN_ERR_WORKSPACE", 4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_TIMEOUT",
                 6: "GDN_ERR_DEVICE_INPUT", 7: "GDN_ERR_DEVICE_RANGE"}
 GDN_BF16, GDN_F32 = 0, 1
-PATH_AUTO, PATH_SIMT, PATH_TENSOR, PATH_MMA_SYNC = 0, 1, 2, 3
+PATH_AUTO, PATH_SIMT, PATH_TENSOR = 0, 1, 2
 EXPORTED = ("gdn_status_string", "gdn_check_problem", "gdn_workspace_size", "gdn_forward",
             "gdn_chunk_prepare", "gdn_segment_summary", "gdn_state_prefix_scan",
             "gdn_chunk_emit", "gdn_device_status", "gdn_version",

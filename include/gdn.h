@@ -83,14 +83,11 @@ typedef enum gdn_status {
 typedef enum gdn_dtype { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
 
 /* Kernel family selection (gdn_problem.path).  AUTO picks the tcgen05 tensor-core kernels
- * when they cover the shape (bf16, K = V = 128) and the SIMT kernels otherwise.  MMA_SYNC
- * selects the previous tensor-core generation (warp-level mma.sync, same shapes), kept as a
- * baseline.  All families are independent implementations of the same steps. */
+ * when they cover the shape (bf16, K = V = 128) and the SIMT kernels otherwise. */
 typedef enum gdn_path {
     GDN_PATH_AUTO = 0,
     GDN_PATH_SIMT = 1,
-    GDN_PATH_TENSOR = 2,
-    GDN_PATH_MMA_SYNC = 3
+    GDN_PATH_TENSOR = 2
 } gdn_path;
 
 typedef struct gdn_problem {

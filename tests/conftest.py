@@ -17,3 +17,18 @@ def pytest_configure(config):
 def oracle_lib():
     import oracle
     return oracle.load()
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Prints the error margin of every parity check that ran (value against its bound)."""
+    try:
+        from gdn_testutil import MARGINS
+    except ImportError:
+        return
+    if not MARGINS:
+        return
+    tr = terminalreporter
+    tr.section("parity margins (error / bound)")
+    for test, case, metric, value, bound in MARGINS:
+        tr.write_line(f"{test:48s} {case:28s} {metric:44s} {value:.3e} / {bound:.0e}"
+                      f"  ({value / bound:5.1%} of bound)")

@@ -9,11 +9,23 @@ Tolerances (written in the tests that use them):
         the output itself to bf16.  The plain max form cannot hold for bf16 outputs: the
         exact result rounded to bf16 already exceeds it (tests/test_tolerance_reading.py).
 """
+import os
+
 import numpy as np
 import torch
 
 BF16_TOL = 2e-2
 F32_TOL = 2e-3
+
+# Error margins of every parity check in this session: (test, case, metric, value, bound).
+# tests/conftest.py prints them in the terminal summary, so the headroom against each bound is
+# on record even when pytest captures the tests' own output.
+MARGINS = []
+
+
+def record(case, metric, value, bound):
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0].split("::")[-1]
+    MARGINS.append((test, str(case), metric, float(value), float(bound)))
 
 
 def rel_to_rms(got, ref):
@@ -72,25 +84,45 @@ def excess_over_rounding(got, ref):
     return float(np.max(ex)) / rms if rms > 0 else float(np.max(ex))
 
 
-def check_bf16_out(out_gpu, out_ref, tol=BF16_TOL):
+def check_bf16_out(out_gpu, out_ref, tol=BF16_TOL, case=""):
     e_rms = rms_rel(out_gpu, out_ref)
     e_max = excess_over_rounding(out_gpu, out_ref)
+    record(case, "out rms(err)/rms", e_rms, tol)
+    record(case, "out max excess over bf16 rounding / rms", e_max, tol)
     assert e_rms <= tol, f"out rms-relative error {e_rms:.3e} > {tol}"
     assert e_max <= tol, f"out error beyond bf16 rounding {e_max:.3e} rms > {tol}"
     return e_rms, e_max
 
 
-def check_bf16(out_gpu, hf_gpu, out_ref, hf_ref, valid=None, tol=BF16_TOL):
+def check_bf16(out_gpu, hf_gpu, out_ref, hf_ref, valid=None, tol=BF16_TOL, case=""):
     """Asserts the bf16 tolerances; returns ((out rms-rel, out excess), [state errors])."""
     og = np.asarray(out_gpu)
     orf = np.asarray(out_ref)
     if valid is not None:
         og, orf = og[valid], orf[valid]
-    e_out = check_bf16_out(og, orf, tol)
+    e_out = check_bf16_out(og, orf, tol, case)
     e_h = [rel_to_rms(hf_gpu[n], hf_ref[n]) for n in range(len(hf_ref))]
+    if e_h:
+        record(case, "h_final max|err|/rms (worst sequence)", max(e_h), tol)
     for n, e in enumerate(e_h):
         assert e <= tol, f"h_final[{n}] max-abs / rms error {e:.3e} > {tol}"
     return e_out, e_h
+
+
+def check_f32(name, got, ref, tol=F32_TOL, case=""):
+    """fp32 I/O: max |gpu - oracle| <= tol, recorded."""
+    e = max_abs(got, ref)
+    record(case, f"{name} max|err|", e, tol)
+    assert e <= tol, f"{name} max abs error {e:.3e} > {tol}"
+    return e
+
+
+def check_state(name, got, ref, tol=BF16_TOL, case=""):
+    """fp32 state-like results of the bf16 path: max |gpu - oracle| / rms(oracle) <= tol."""
+    e = rel_to_rms(got, ref)
+    record(case, f"{name} max|err|/rms", e, tol)
+    assert e <= tol, f"{name} max-abs / rms error {e:.3e} > {tol}"
+    return e
 
 
 def gpu_available():

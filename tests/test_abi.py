@@ -49,7 +49,7 @@ def prob(gdn, **kw):
     (dict(), 0), (dict(P=64, T=65536), 0), (dict(N=8, P=4), 0),
     (dict(hk=3), 1), (dict(hv=0), 1), (dict(P=0), 1), (dict(N=0), 1), (dict(T=-1), 1),
     (dict(K=96), 2), (dict(V=256), 2), (dict(chunk=32), 2), (dict(K=64, V=64), 0),
-    (dict(path=2, K=64), 2), (dict(path=3, K=64), 2), (dict(path=3), 0), (dict(path=7), 1),
+    (dict(path=2, K=64), 2), (dict(path=3), 1), (dict(path=7), 1),
 ])
 def test_check_problem(gdn, kw, status):
     p = prob(gdn, **kw)
