@@ -10,6 +10,8 @@ Recipe (per workload; all draws on the CPU from one ``torch.Generator`` seeded a
   * g (natural-log decay per token and value head):
       - ``"log_uniform"``: g = log(alpha), alpha ~ U(0.90, 1.00);
       - ``"softplus"``:    g = -softplus(N(0, 1)) * 0.1;
+      - ``"log_uniform_slow"``: g = log(alpha), alpha ~ U(0.99, 1.00) (tests: slow decay keeps
+        a segment's composed transition M_r well inside the fp32 and fp16 ranges);
   * beta = sigmoid(N(0, 1));
   * h0 = 0, or ~ N(0, std^2) per sequence in fp32;
   * packed variable-length streams: lengths ~ U[lmin, lmax] (integers, drawn first),
@@ -117,6 +119,8 @@ def make(wl: Workload) -> Inputs:
     v = torch.randn(T, wl.hv, wl.V, generator=gen)
     if wl.g_kind == "log_uniform":
         g = torch.log(0.90 + 0.10 * torch.rand(T, wl.hv, generator=gen))
+    elif wl.g_kind == "log_uniform_slow":
+        g = torch.log(0.99 + 0.01 * torch.rand(T, wl.hv, generator=gen))
     elif wl.g_kind == "softplus":
         g = -torch.nn.functional.softplus(torch.randn(T, wl.hv, generator=gen)) * 0.1
     else:
