@@ -252,7 +252,8 @@ namespace {
 gdn_status forward_impl(const gdn_problem* p, const void* q, const void* k, const void* v,
                         const float* g, const float* beta, const float* h0,
                         const int32_t* cu_seqlens, void* out, float* h_final, void* workspace,
-                        size_t ws_bytes, cudaStream_t stream, cudaEvent_t* ev) {
+                        size_t ws_bytes, cudaStream_t stream, cudaEvent_t* ev,
+                        long long wait_cycles = 0, int fault = 0) {
   auto mark = [&](int i) { return ev ? cudaEventRecord(ev[i], stream) : cudaSuccess; };
   gdn_status st = check_problem(p);
   if (st != GDN_OK) return st;
@@ -272,6 +273,8 @@ gdn_status forward_impl(const gdn_problem* p, const void* q, const void* k, cons
   Args a = base_args(p);
   a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.cu = cu_seqlens;
   a.out = out; a.h_final = h_final; a.status = status;
+  a.wait_cycles = wait_cycles;
+  a.fault = fault;
   const bool seg = p->segments_per_seq > 1;
   if (seg) {
     a.M_out = reinterpret_cast<float*>(ws + L.M);
@@ -382,6 +385,16 @@ gdn_status gdn_forward(const gdn_problem* p, const void* q, const void* k, const
                        size_t ws_bytes, cudaStream_t stream) {
   return forward_impl(p, q, k, v, g, beta, h0, cu_seqlens, out, h_final, workspace, ws_bytes,
                       stream, nullptr);
+}
+
+gdn_status gdn_forward_with_limits(const gdn_problem* p, const void* q, const void* k,
+                                   const void* v, const float* g, const float* beta,
+                                   const float* h0, const int32_t* cu_seqlens, void* out,
+                                   float* h_final, void* workspace, size_t ws_bytes,
+                                   cudaStream_t stream, long long wait_cycles, int fault) {
+  if (wait_cycles < 0 || fault < 0 || fault > 1) return GDN_ERR_INVALID_ARGUMENT;
+  return forward_impl(p, q, k, v, g, beta, h0, cu_seqlens, out, h_final, workspace, ws_bytes,
+                      stream, nullptr, wait_cycles, fault);
 }
 
 gdn_status gdn_forward_timed(const gdn_problem* p, const void* q, const void* k, const void* v,

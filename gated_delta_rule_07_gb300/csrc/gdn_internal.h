@@ -36,6 +36,11 @@ struct Args {
   int seg_lo, seg_n, scan_from;
   float* h_next;
   bool h_in_per_seq;  // phase 3: h_in is indexed by sequence ([N, hv, K, V], e.g. h0)
+  // Limit of a bounded device wait in SM cycles (0: the default, about a second), and a fault
+  // to inject for tests of those waits (0: none; 1: the chunk kernels' chain never signals its
+  // first hand-off, so a wait for it expires).
+  long long wait_cycles;
+  int fault;
 };
 
 // Device-side check of cu_seqlens (cu[0] = 0, non-decreasing, cu[N] = T); records

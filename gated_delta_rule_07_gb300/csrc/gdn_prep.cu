@@ -292,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int j = blockIdx.y, kh = j / (a.hv / a.hk);
   const int64_t first = blockIdx.x, stride = gridDim.x;
   if (first >= npairs) return;
+  const long long wl = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;  // this call's limit
   const int iters = (int)((npairs - first + stride - 1) / stride);
 
   if (tid == 0) {
@@ -369,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint32_t id = idesc_f16(128, 128, 0, 0, 1);
       for (int it = 0; it < iters; ++it) {
         // the workers have read the previous gram out of TMEM
-        if (it > 0 && !wait_bounded(S, saddr(&S.bar_tfree), (it - 1) & 1, kWaitCycles, true)) break;
-        if (!wait_bounded(S, saddr(&S.bar_load), it & 1, kWaitCycles, true)) break;
+        if (it > 0 && !wait_bounded(S, saddr(&S.bar_tfree), (it - 1) & 1, wl, true)) break;
+        if (!wait_bounded(S, saddr(&S.bar_load), it & 1, wl, true)) break;
         load_pending = false;
         fence_after_sync();
         const uint32_t kq = saddr(S.k);
@@ -383,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         ++mmas;
         mma_pending = true;
         // the keys are dead once the product has read them: load the next pair's
-        if (!wait_bounded(S, saddr(&S.bar_mma), it & 1, kWaitCycles, true)) break;
+        if (!wait_bounded(S, saddr(&S.bar_mma), it & 1, wl, true)) break;
         mma_pending = false;
         if (it + 1 < iters) {
           issue_load(first + (it + 1) * stride);
@@ -408,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int64_t pr = first + it * stride;
       const Pair P = pair_info(a, pr);
       const Tables* TBp = S.tb[it & 1];
-      bool go = wait_bounded(S, saddr(&S.bar_mma), it & 1, kWaitCycles, true);
+      bool go = wait_bounded(S, saddr(&S.bar_mma), it & 1, wl, true);
       fence_after_sync();
       go = named_bar_and(3, kWorkers, go);
       if (!go) break;

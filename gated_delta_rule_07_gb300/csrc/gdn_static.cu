@@ -10,9 +10,13 @@
 // process exits.
 //
 // Limits and sharing:
-//   * the scratch is kStaticScratchBytes (64 MiB); a problem whose gdn_workspace_size() is
-//     larger is rejected with GDN_ERR_WORKSPACE before anything is enqueued (on the
-//     tensor-core path that is N * P * Hv <= 340 segment-heads at K = V = 128);
+//   * the scratch is kStaticScratchBytes (64 MiB).  What must fit is the workspace without the
+//     optional per-chunk factor tiles (the status word and, with P > 1, the segment summaries
+//     and incoming states): on the tensor-core path at K = V = 128 that is N * P * Hv <= 341
+//     segment-heads of 192 KiB each.  A problem that needs more is rejected with
+//     GDN_ERR_WORKSPACE before anything is enqueued; one whose full gdn_workspace_size() is
+//     larger but whose minimum fits runs without the factor tiles (the kernels that compute
+//     their own factors);
 //   * every call on a device uses the same array, and it keeps the last call's contents;
 //     the status word is cleared by each call and nothing else has to start at zero;
 //   * calls whose work overlaps on the GPU (different streams, or several host threads

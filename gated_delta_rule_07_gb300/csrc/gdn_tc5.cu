@@ -66,7 +66,8 @@ constexpr int C = kChunk;  // 64
 constexpr int KD = 128, VD = 128;
 constexpr int kChainThreads = 256, kPrepThreads = 128, kConvThreads = 64;
 constexpr int kThreads = kChainThreads + kPrepThreads + 64 + kConvThreads;
-constexpr long long kWaitCycles = 2000000000LL;  // about a second at GB300 clocks
+constexpr long long kWaitCycles = 2000000000LL;  // default wait limit: about a second
+constexpr long long kDrainCycles = 200000000LL;  // teardown waits for in-flight copies, products
 
 // With per-chunk factor records in the workspace, the U half stores each chunk's -w^T, fp16 K,
 // u^T and the state update's decay; kSumML (the M half) and kEmitR (phase 3) load them instead
@@ -169,6 +170,7 @@ struct Smem {
   uint32_t tmem_base;
   int abort_flag;
   int range_bad;
+  long long wait_cycles;  // this call's limit on a bounded wait
 };
 
 // Members read or written with 16-byte vector accesses, ldmatrix / stmatrix or the tensor core
@@ -196,7 +198,7 @@ __device__ __forceinline__ void set_abort(Smem& S) {
 // giving up (about a second, or at once when another thread already gave up) it records the
 // abort flag; the caller carries on and leaves at its next group-uniform check.
 __device__ __noinline__ void wait_bar_slow(Smem& S, uint32_t a, uint32_t parity) {
-  const long long t_end = clock64() + kWaitCycles;
+  const long long t_end = clock64() + S.wait_cycles;
   while (!mbar_try(a, parity)) {
     if (clock64() > t_end || aborted(S)) {
       set_abort(S);
@@ -210,6 +212,14 @@ __device__ __forceinline__ void wait_bar(Smem& S, int bar, uint32_t parity) {
   wait_bar_slow(S, a, parity);
 }
 __device__ __forceinline__ void arrive(Smem& S, int bar) { mbar_arrive(saddr(&S.bars[bar])); }
+// Teardown wait for this CTA's own in-flight copies or products: bounded, and it does not give up
+// when the abort flag is set (the TMEM and shared memory must not be released under them).
+__device__ __noinline__ void wait_bar_drain(Smem& S, int bar, uint32_t parity) {
+  const uint32_t a = saddr(&S.bars[bar]);
+  const long long t_end = clock64() + kDrainCycles;
+  while (!mbar_try(a, parity) && clock64() < t_end) {
+  }
+}
 
 // The record of chunk cg (index within sequence n, which starts at token sb) of value head j:
 // slots are the 64-token windows of the packed token axis, plus n so that a sequence's last,
@@ -252,6 +262,7 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
   if (tid == 0) {
     for (int b = 0; b < kNumBars; ++b) mbar_init(saddr(&S.bars[b]), bar_count<MODE>(b));
     S.abort_flag = 0;
+    S.wait_cycles = a.wait_cycles > 0 ? a.wait_cycles : kWaitCycles;
     S.range_bad = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -316,13 +327,16 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
         uint32_t p[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) p[q] = pack_h2(h[16 * piece + 2 * q], h[16 * piece + 2 * q + 1]);
-        tmem_st8(tm + lane_bits + TM_H + 64 * hf + 8 * piece, p);
+        tmem_st8_nw(tm + lane_bits + TM_H + 64 * hf + 8 * piece, p);
       }
     };
     if (nch > 0) {
       publish_h();
+      tmem_wait_st();
       fence_before_sync();
-      arrive(S, B_HR);
+      // (a.fault == 1, for tests of the bounded waits: the first hand-off is never signalled,
+      // so the MMA warp's wait for it must expire)
+      if (a.fault != 1) arrive(S, B_HR);
     }
     if (UM && nch > 0) {  // kSumUMT: the M state starts at I (fp32 in TMEM), with its fp16 copy
 #pragma unroll
@@ -346,68 +360,90 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
       const int64_t t0 = sb + (c0 + ci) * C;
       const int L = (int)((se - t0) < C ? (se - t0) : C);
       const float* eglg = MODE == kSumML ? S.tbl[gb] : S.eGLG[gb];
-      // ---- delta = u + D -> fp16 delta (into D's columns) and delta' (into u's columns)
+      // ---- delta = u + D -> fp16 delta (into D's columns) and delta' (into u's columns).  TMEM
+      // is read two 16-column pieces at a time with one wait, and written without a wait per
+      // store (one wait before the hand-off).
       wait_bar(S, B_D, ci & 1);
       if (MODE == kEmitR) wait_bar(S, B_RL0 + (ci & 1), (ci >> 1) & 1);  // u^T of the record
       fence_after_sync();
+      {
+        uint32_t dr[2][16];
+        tmem_ld16_nw(tm + lane_bits + TM_DO + 32 * hf, dr[0]);
+        tmem_ld16_nw(tm + lane_bits + TM_DO + 32 * hf + 16, dr[1]);
+        tmem_wait_ld16x2(dr[0], dr[1]);
 #pragma unroll
-      for (int piece = 0; piece < 2; ++piece) {
-        float d[16];
-        tmem_ld16(tm + lane_bits + TM_DO + 32 * hf + 16 * piece, d);
-        if (MODE == kEmitR) {  // u^T[c][t], fp16, 128-byte swizzled rows
-          const uint8_t* ur = S.v[ci & 1] + c * 128;
+        for (int piece = 0; piece < 2; ++piece) {
+          float d[16];
 #pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            const int ch = 4 * hf + 2 * piece + h2;
-            const uint4 x = *reinterpret_cast<const uint4*>(ur + ((ch ^ (c & 7)) << 4));
-            const uint32_t* xw = reinterpret_cast<const uint32_t*>(&x);
+          for (int q = 0; q < 16; ++q) d[q] = __uint_as_float(dr[piece][q]);
+          if (MODE == kEmitR) {  // u^T[c][t], fp16, 128-byte swizzled rows
+            const uint8_t* ur = S.v[ci & 1] + c * 128;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw[i]));
-              d[8 * h2 + 2 * i] += f.x;
-              d[8 * h2 + 2 * i + 1] += f.y;
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int ch = 4 * hf + 2 * piece + h2;
+              const uint4 x = *reinterpret_cast<const uint4*>(ur + ((ch ^ (c & 7)) << 4));
+              const uint32_t* xw = reinterpret_cast<const uint32_t*>(&x);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&xw[i]));
+                d[8 * h2 + 2 * i] += f.x;
+                d[8 * h2 + 2 * i + 1] += f.y;
+              }
             }
           }
-        }
-        uint32_t pd[8], pp[8];
+          uint32_t pd[8], pp[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int t = 32 * hf + 16 * piece + 2 * q;
-          range_ok = range_ok && fits_half(d[2 * q]) && fits_half(d[2 * q + 1]);
-          pd[q] = pack_h2(d[2 * q], d[2 * q + 1]);
-          pp[q] = pack_h2(d[2 * q] * eglg[t], d[2 * q + 1] * eglg[t + 1]);
+          for (int q = 0; q < 8; ++q) {
+            const int t = 32 * hf + 16 * piece + 2 * q;
+            range_ok = range_ok && fits_half(d[2 * q]) && fits_half(d[2 * q + 1]);
+            pd[q] = pack_h2(d[2 * q], d[2 * q + 1]);
+            pp[q] = pack_h2(d[2 * q] * eglg[t], d[2 * q + 1] * eglg[t + 1]);
+          }
+          if (OUT) tmem_st8_nw(tm + lane_bits + TM_DO + 32 * hf + 8 * piece, pd);
+          tmem_st8_nw(tm + lane_bits + tmU + 32 * hf + 8 * piece, pp);
         }
-        if (OUT) tmem_st8(tm + lane_bits + TM_DO + 32 * hf + 8 * piece, pd);
-        tmem_st8(tm + lane_bits + tmU + 32 * hf + 8 * piece, pp);
+        tmem_wait_st();
       }
       fence_before_sync();
       arrive(S, B_DR);
       if (UM) {  // delta'_M = diag(e^{G_last - G}) D_M -> fp16 in place; then M^T <- gamma M^T
         wait_bar(S, B_DM, ci & 1);
         fence_after_sync();
+        {
+          uint32_t dr[2][16];
+          tmem_ld16_nw(tm + lane_bits + TM_DM + 32 * hf, dr[0]);
+          tmem_ld16_nw(tm + lane_bits + TM_DM + 32 * hf + 16, dr[1]);
+          tmem_wait_ld16x2(dr[0], dr[1]);
 #pragma unroll
-        for (int piece = 0; piece < 2; ++piece) {
-          float d[16];
-          tmem_ld16(tm + lane_bits + TM_DM + 32 * hf + 16 * piece, d);
-          uint32_t pp[8];
+          for (int piece = 0; piece < 2; ++piece) {
+            uint32_t pp[8];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const int t = 32 * hf + 16 * piece + 2 * q;
-            const float x0 = d[2 * q] * eglg[t], x1 = d[2 * q + 1] * eglg[t + 1];
-            range_ok = range_ok && fits_half(x0) && fits_half(x1);
-            pp[q] = pack_h2(x0, x1);
+            for (int q = 0; q < 8; ++q) {
+              const int t = 32 * hf + 16 * piece + 2 * q;
+              const float x0 = __uint_as_float(dr[piece][2 * q]) * eglg[t];
+              const float x1 = __uint_as_float(dr[piece][2 * q + 1]) * eglg[t + 1];
+              range_ok = range_ok && fits_half(x0) && fits_half(x1);
+              pp[q] = pack_h2(x0, x1);
+            }
+            tmem_st8_nw(tm + lane_bits + TM_DM + 32 * hf + 8 * piece, pp);
           }
-          tmem_st8(tm + lane_bits + TM_DM + 32 * hf + 8 * piece, pp);
         }
         const float gam = S.gamma[gb];
 #pragma unroll
-        for (int piece = 0; piece < 4; ++piece) {
-          float m[16];
-          tmem_ld16(tm + lane_bits + TM_MS + 64 * hf + 16 * piece, m);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t mr[2][16];
+          tmem_ld16_nw(tm + lane_bits + TM_MS + 64 * hf + 32 * half, mr[0]);
+          tmem_ld16_nw(tm + lane_bits + TM_MS + 64 * hf + 32 * half + 16, mr[1]);
+          tmem_wait_ld16x2(mr[0], mr[1]);
 #pragma unroll
-          for (int q = 0; q < 16; ++q) m[q] *= gam;
-          tmem_st16f(tm + lane_bits + TM_MS + 64 * hf + 16 * piece, m);
+          for (int p2 = 0; p2 < 2; ++p2) {
+            float m[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) m[q] = gam * __uint_as_float(mr[p2][q]);
+            tmem_st16f_nw(tm + lane_bits + TM_MS + 64 * hf + 32 * half + 16 * p2, m);
+          }
         }
+        tmem_wait_st();
         fence_before_sync();
         arrive(S, B_DRM);
       }
@@ -418,31 +454,51 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
       {
         const float gam = MODE == kSumML ? S.tbl[gb][64] : S.gamma[gb];
 #pragma unroll
-        for (int piece = 0; piece < 4; ++piece) {
-          float dh[16];
-          tmem_ld16(tm + lane_bits + TM_H + 64 * hf + 16 * piece, dh);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t hr[2][16];
+          tmem_ld16_nw(tm + lane_bits + TM_H + 64 * hf + 32 * half, hr[0]);
+          tmem_ld16_nw(tm + lane_bits + TM_H + 64 * hf + 32 * half + 16, hr[1]);
+          tmem_wait_ld16x2(hr[0], hr[1]);
 #pragma unroll
-          for (int q = 0; q < 16; ++q) h[16 * piece + q] = gam * h[16 * piece + q] + dh[q];
+          for (int p2 = 0; p2 < 2; ++p2)
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              h[32 * half + 16 * p2 + q] =
+                  gam * h[32 * half + 16 * p2 + q] + __uint_as_float(hr[p2][q]);
         }
       }
-      if (ci + 1 < nch) publish_h();
+      if (ci + 1 < nch) publish_h();  // (its stores complete at the wait below)
       uint32_t ob[16];
       if (OUT) {
+        if (MODE == kEmitR) {  // o = e^{G_t} (q h)_t + (attn_i delta)_t, a piece at a time
 #pragma unroll
-        for (int piece = 0; piece < 2; ++piece) {
-          float o[16];
-          tmem_ld16(tm + lane_bits + TM_DO + 64 + 32 * hf + 16 * piece, o);
-          if (MODE == kEmitR) {  // o = e^{G_t} (q h)_t + (attn_i delta)_t
-            float o2[16];
-            tmem_ld16(tm + lane_bits + TM_W + 32 * hf + 16 * piece, o2);
+          for (int piece = 0; piece < 2; ++piece) {
+            uint32_t orr[16], o2r[16];
+            tmem_ld16_nw(tm + lane_bits + TM_DO + 64 + 32 * hf + 16 * piece, orr);
+            tmem_ld16_nw(tm + lane_bits + TM_W + 32 * hf + 16 * piece, o2r);
+            tmem_wait_ld16x2(orr, o2r);
             const float* eg = &S.eG[gb][32 * hf + 16 * piece];
 #pragma unroll
-            for (int q = 0; q < 16; ++q) o[q] = fmaf(eg[q], o[q], o2[q]);
+            for (int q = 0; q < 8; ++q)
+              ob[8 * piece + q] =
+                  pack_bf2(fmaf(eg[2 * q], __uint_as_float(orr[2 * q]), __uint_as_float(o2r[2 * q])),
+                           fmaf(eg[2 * q + 1], __uint_as_float(orr[2 * q + 1]),
+                                __uint_as_float(o2r[2 * q + 1])));
           }
+        } else {
+          uint32_t orr[2][16];
+          tmem_ld16_nw(tm + lane_bits + TM_DO + 64 + 32 * hf, orr[0]);
+          tmem_ld16_nw(tm + lane_bits + TM_DO + 64 + 32 * hf + 16, orr[1]);
+          tmem_wait_ld16x2(orr[0], orr[1]);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) ob[8 * piece + q] = pack_bf2(o[2 * q], o[2 * q + 1]);
+          for (int piece = 0; piece < 2; ++piece)
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              ob[8 * piece + q] = pack_bf2(__uint_as_float(orr[piece][2 * q]),
+                                           __uint_as_float(orr[piece][2 * q + 1]));
         }
       }
+      tmem_wait_st();
       fence_before_sync();
       if (ci + 1 < nch) arrive(S, B_HR);
       if (OUT) {  // o[t][j][c] for t = 32 hf .. 32 hf + 31
@@ -462,14 +518,21 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
         fence_after_sync();
         if (ci + 1 < nch) {
 #pragma unroll
-          for (int piece = 0; piece < 4; ++piece) {
-            float m[16];
-            uint32_t p[8];
-            tmem_ld16(tm + lane_bits + TM_MS + 64 * hf + 16 * piece, m);
+          for (int half = 0; half < 2; ++half) {
+            uint32_t mr[2][16];
+            tmem_ld16_nw(tm + lane_bits + TM_MS + 64 * hf + 32 * half, mr[0]);
+            tmem_ld16_nw(tm + lane_bits + TM_MS + 64 * hf + 32 * half + 16, mr[1]);
+            tmem_wait_ld16x2(mr[0], mr[1]);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) p[q] = pack_h2(m[2 * q], m[2 * q + 1]);
-            tmem_st8(tm + lane_bits + TM_MF + 32 * hf + 8 * piece, p);
+            for (int p2 = 0; p2 < 2; ++p2) {
+              uint32_t p[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                p[q] = pack_h2(__uint_as_float(mr[p2][2 * q]), __uint_as_float(mr[p2][2 * q + 1]));
+              tmem_st8_nw(tm + lane_bits + TM_MF + 32 * hf + 16 * half + 8 * p2, p);
+            }
           }
+          tmem_wait_st();
           fence_before_sync();
           arrive(S, B_HRM);
         }
@@ -926,6 +989,8 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
     }
   } else if (warp == 13) {
     // =============================================================== loader (1 warp)
+    // copies issued per barrier, so that a loader that stops early still waits for them
+    int nl0 = 0, nl1 = 0, nl2 = 0, nr0 = 0, nr1 = 0;
     if (MODE == kSumML) {  // the records of the U half, three stages
       for (int ci = 0; ci < nch; ++ci) {
         const int st = ci % 3;
@@ -940,6 +1005,9 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
           bulk_g2s(dst + 16384u, rec + kRecKh, 16384u, bar);
           bulk_g2s(saddr(S.tbl[st]), rec + kRecTbl, kRecTblBytes, bar);
         }
+        nl0 += st == 0;
+        nl1 += st == 1;
+        nl2 += st == 2;
         __syncwarp();
       }
     }
@@ -985,6 +1053,8 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
       }
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar)
                    : "memory");
+      nl0 += sg == 0;
+      nl1 += sg == 1;
       if (MODE == kEmitT) {  // the chunk's T_w | T_u tiles, once the w, u of ci - 2 are done
         if (ci >= 2) wait_bar(S, B_RF0 + sg, ((ci >> 1) + 1) & 1);
         if (lane == 0) {
@@ -994,6 +1064,8 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
           mbar_expect_tx(rb, 16384u);
           bulk_g2s(saddr(tstage(sg)), rec, 16384u, rb);
         }
+        nr0 += sg == 0;
+        nr1 += sg == 1;
         __syncwarp();
       }
       if (MODE == kEmitR) {  // the chunk's record (-w^T, fp16 K, u^T), once Dh of ci - 2 is done
@@ -1007,10 +1079,20 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
           bulk_g2s(saddr(S.kh[sg]), rec + kRecKh, 16384u, rb);
           bulk_g2s(saddr(S.v[sg]), rec + kRecU, 16384u, rb);
         }
+        nr0 += sg == 0;
+        nr1 += sg == 1;
         __syncwarp();
       }
     }
     asm volatile("cp.async.wait_all;\n" ::: "memory");
+    if (lane == 0) {  // every copy issued has landed before the shared memory is released
+      if (nl0) wait_bar_drain(S, B_L0, (nl0 - 1) & 1);
+      if (nl1) wait_bar_drain(S, B_L1, (nl1 - 1) & 1);
+      if (nl2) wait_bar_drain(S, B_L2, (nl2 - 1) & 1);
+      if (nr0) wait_bar_drain(S, B_RL0, (nr0 - 1) & 1);
+      if (nr1) wait_bar_drain(S, B_RL1, (nr1 - 1) & 1);
+    }
+    __syncwarp();
   } else if (warp >= 14) {
     // =============================================================== converter (64 threads)
     const int p = tid - (kThreads - kConvThreads);  // 0..63
@@ -1403,7 +1485,7 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
     // every product issued has completed before the TMEM is released
     if (leader) mma_commit(saddr(&S.bars[B_END]));
     __syncwarp();
-    wait_bar(S, B_END, 0);
+    wait_bar_drain(S, B_END, 0);  // (also after an abort: committed products land first)
   }
 
   // ---- teardown: every role has left its loop

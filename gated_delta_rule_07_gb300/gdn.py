@@ -35,7 +35,7 @@ EXPORTED = ("gdn_status_string", "gdn_check_problem", "gdn_workspace_size", "gdn
             "gdn_chunk_prepare", "gdn_segment_summary", "gdn_state_prefix_scan",
             "gdn_chunk_emit", "gdn_device_status", "gdn_version",
             "gdn_segment_summary_fused", "gdn_chunk_emit_fused", "gdn_last_error_string",
-            "gdn_forward_static_scratch", "gdn_forward_timed")
+            "gdn_forward_static_scratch", "gdn_forward_timed", "gdn_forward_with_limits")
 
 
 class Problem(ctypes.Structure):
@@ -68,6 +68,8 @@ _lib.gdn_forward.argtypes = [_pp, _vp, _vp, _vp, _fp, _fp, _fp, _ip, _vp, _fp, _
                              ctypes.c_size_t, _vp]
 _lib.gdn_forward_timed.argtypes = [_pp, _vp, _vp, _vp, _fp, _fp, _fp, _ip, _vp, _fp, _vp,
                              ctypes.c_size_t, _vp, ctypes.POINTER(ctypes.c_float)]
+_lib.gdn_forward_with_limits.argtypes = [_pp, _vp, _vp, _vp, _fp, _fp, _fp, _ip, _vp, _fp, _vp,
+                                         ctypes.c_size_t, _vp, ctypes.c_longlong, ctypes.c_int]
 _lib.gdn_chunk_prepare.argtypes = [_pp, _vp, _vp, _fp, _fp, _ip, _vp, _vp, _fp, _ip, _vp]
 _lib.gdn_segment_summary.argtypes = [_pp, _vp, _vp, _vp, _fp, _ip, _fp, _fp, _ip, _vp]
 _lib.gdn_state_prefix_scan.argtypes = [_pp, _fp, _fp, _fp, _fp, _fp, _vp]
@@ -151,6 +153,18 @@ def gdn_forward_timed(p, q, k, v, g, beta, h0, cu_seqlens, out, h_final, workspa
                                   _ptr(workspace), int(ws_bytes), _stream(stream), ms),
            "gdn_forward_timed")
     return float(ms[0]), float(ms[1]), float(ms[2]), float(ms[3])
+
+
+def gdn_forward_with_limits(p, q, k, v, g, beta, h0, cu_seqlens, out, h_final, workspace,
+                            wait_cycles=0, fault=0, ws_bytes=None, stream=None):
+    """gdn_forward with a given limit on the device's bounded waits and an optional injected
+    fault (tests of the failure detection; see include/gdn.h)."""
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
+    _check(_lib.gdn_forward_with_limits(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                        _ptr(beta), _ptr(h0), _ptr(cu_seqlens), _ptr(out),
+                                        _ptr(h_final), _ptr(workspace), int(ws_bytes),
+                                        _stream(stream), int(wait_cycles), int(fault)),
+           "gdn_forward_with_limits")
 
 
 def gdn_forward_static_scratch(p, q, k, v, g, beta, h0, cu_seqlens, out, h_final, stream=None):

@@ -146,6 +146,21 @@ gdn_status gdn_forward_timed(const gdn_problem* p, const void* q, const void* k,
                              void* workspace, size_t ws_bytes, cudaStream_t stream,
                              float* phase_ms);
 
+/* gdn_forward with explicit limits, for tests of the device-side failure detection.
+ *   wait_cycles   limit of every bounded device wait, in SM clock cycles (0 = the default of
+ *                 about a second; a wait that expires records GDN_ERR_DEVICE_TIMEOUT in the
+ *                 status word, and the kernel still lets its own copies and products land
+ *                 before it releases its memory and exits, so the context stays usable)
+ *   fault         0 = none; 1 = the tensor-core chunk kernels' chain never signals its first
+ *                 hand-off, so the wait for it expires (the same fault in every CTA)
+ * The outputs of a call that reports a device error are unspecified.  Errors: those of
+ * gdn_forward; GDN_ERR_INVALID_ARGUMENT for a negative wait_cycles or an unknown fault. */
+gdn_status gdn_forward_with_limits(const gdn_problem* p, const void* q, const void* k,
+                                   const void* v, const float* g, const float* beta,
+                                   const float* h0, const int32_t* cu_seqlens, void* out,
+                                   float* h_final, void* workspace, size_t ws_bytes,
+                                   cudaStream_t stream, long long wait_cycles, int fault);
+
 /* Phase "prepare": the WY/UT factors of every chunk ("Implementation": the WY factors that
  * phase 3 reuses; "Why": w and u of the chunk map).  Writes w [T, hv, K], u [T, hv, V]
  * (fp32) and gcum [T, hv] (fp32, inclusive within-chunk cumulative log-decay; a chunk's
@@ -209,9 +224,12 @@ gdn_status gdn_device_status(const void* status_word, int reset, cudaStream_t st
  * allocations after start-up).  It takes no workspace: its scratch is a 64 MiB array in the
  * library's own device memory, which every GPU that loads the library holds until the process
  * exits.  There is no counterpart on the source pages; this is a deployment convenience.
- *   - Same arguments, results and errors as gdn_forward, minus the workspace.  A problem whose
- *     gdn_workspace_size() exceeds 64 MiB is rejected with GDN_ERR_WORKSPACE before anything is
- *     enqueued.
+ *   - Same arguments, results and errors as gdn_forward, minus the workspace.  What must fit in
+ *     64 MiB is the workspace without the optional per-chunk factor tiles: the status word and,
+ *     with P > 1, the segment summaries and incoming states (192 KiB per segment and value head
+ *     at K = V = 128, so N * P * hv <= 341).  A problem needing more is rejected with
+ *     GDN_ERR_WORKSPACE before anything is enqueued; one whose full gdn_workspace_size() exceeds
+ *     64 MiB but whose minimum fits runs without the factor tiles.
  *   - It allocates nothing (no cudaMalloc, no allocating library call).
  *   - All calls on a device share the one array, which keeps the last call's contents (each
  *     call clears the status word; nothing else needs to start at zero).  Calls whose work

@@ -116,3 +116,14 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
         sys.modules.pop("gated_delta_rule_07_gb300.gdn", None)
         if saved is not None:
             sys.modules["gated_delta_rule_07_gb300.gdn"] = saved
+
+
+def test_forward_with_limits_rejects_bad_limits_on_the_host(gdn):
+    """A negative wait limit or an unknown fault is rejected before any device work."""
+    p = prob(gdn, T=64)
+    fake = 1 << 20
+    for wc, fault in ((-1, 0), (0, 2), (0, -1)):
+        rc = gdn._lib.gdn_forward_with_limits(gdn.ctypes.byref(p), fake, fake, fake, fake, fake,
+                                              None, None, fake, None, fake, 1 << 30, None, wc,
+                                              fault)
+        assert rc == 1

@@ -19,8 +19,9 @@ def gdn():
 
 
 def test_rejects_problems_beyond_the_static_scratch(gdn):
-    """64 MiB holds N*P*Hv <= 340 segment-heads of (M, U, h_in) at K = V = 128; beyond that
-    the call fails before any device work (no GPU needed for this check)."""
+    """64 MiB holds N*P*Hv <= 341 segment-heads of (M, U, h_in) at K = V = 128 (192 KiB each,
+    after the 256-byte status word); beyond that the call fails before any device work (no GPU
+    needed for this check)."""
     p = gdn.make_problem(65536, 1, 16, 32, 128, 128, P=64)
     assert gdn.gdn_workspace_size(p) > 64 << 20
     fake = 1 << 20
@@ -41,6 +42,32 @@ def _both(gdn, inp, P, path):
                                    out, hf)
     torch.cuda.synchronize()
     return to_np(out), to_np(hf), to_np(ref_o), to_np(ref_h)
+
+
+def test_static_scratch_limit_is_the_minimum_workspace(gdn):
+    """342 segment-heads (3 x 342 x 64 KiB + the status word) exceed 64 MiB: rejected before any
+    device work, whatever the optional factor tiles would add (no GPU needed)."""
+    p342 = gdn.make_problem(64 * 400, 1, 1, 1, 128, 128, P=342)
+    assert 256 + 3 * 342 * 65536 > 64 << 20 >= 256 + 3 * 341 * 65536
+    fake = 1 << 20
+    rc = gdn._lib.gdn_forward_static_scratch(
+        gdn.ctypes.byref(p342), fake, fake, fake, fake, fake, None, None, fake, None, None)
+    assert rc == 3  # GDN_ERR_WORKSPACE
+
+
+@pytest.mark.gpu
+def test_static_scratch_runs_when_only_the_minimum_fits(gdn):
+    """A problem whose full workspace (with the factor tiles) exceeds 64 MiB while its minimum
+    fits: the static-scratch call runs the kernels that compute their own factors and matches
+    gdn_forward with a full workspace."""
+    lengths = (64 * 600 + 17,)
+    inp = inputs.custom(sum(lengths), 4, 8, 128, 128, torch.bfloat16, h0_std=0.02,
+                        lengths=lengths, chunk=1, seed=25)
+    d = to_device(inp)
+    p = gdn.problem_for(d["q"], d["v"], None, P=8)
+    assert gdn.gdn_workspace_size(p) > 64 << 20
+    o, h, ro, rh = _both(gdn, inp, 8, path=0)
+    check_bf16(o, h, ro, rh, tol=BF16_TOL, case="static scratch, minimum only")
 
 
 @pytest.mark.gpu
