@@ -5,11 +5,14 @@ Workload (one "step"): the long-context bf16 case -- one packed sequence of T = 
 tokens, 16 key heads shared by 32 value heads, K = V = 128, C = 64, fp32 state, h0 = 0,
 synthetic seeded inputs -- run through all three phases (segment summaries, prefix scan,
 re-emit) with P segments.  Metric: tokens/s (whole job, all ranks).  Inputs plus output are
-about 0.8 GB, far larger than the 129 MB L2, so no flush is needed between steps.
+1.63 GB, far larger than the 129 MB L2, so no flush is needed between steps.
 
 Prints ONE JSON line (rank 0).  ``--impl reference`` times the fp64 CPU oracle instead on a
-bounded sample of the same workload.  Multi-GPU (torchrun): every rank runs its own
-independent sequence (weak scaling, no collective on the data path).
+bounded sample of the same workload.  Multi-GPU (torchrun): by default every rank runs its own
+independent sequence (weak scaling, no collective on the data path); ``--mode seq`` splits one
+sequence over the ranks instead (strong scaling: each rank summarises its contiguous range, one
+all_gather exchanges the fp32 segment summaries, every rank scans them in order and re-emits
+its own range).
 """
 from __future__ import annotations
 
@@ -55,28 +58,82 @@ def dist_env():
 
 
 class Clocks:
-    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+    """Samples the SM clock and the clock-event (throttle) reasons of the benchmark's GPU while the
+    timed region runs.  Read-only NVML queries through ctypes every ~2 ms in a thread (so that a
+    short timed region still gets many samples); `nvidia-smi -lms 20` when NVML cannot be
+    loaded."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, index):
+    def __init__(self, index, period_s=0.002):
         self.index = index
+        self.period = period_s
+        self.samples = []      # (sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self.source = None
         self.proc = None
+        self._thread = None
+        self._stop = None
+
+    def _nvml_handle(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        dev = ctypes.c_void_p()
+        try:  # the CUDA device's PCI address names the same GPU in NVML
+            import torch
+            pr = torch.cuda.get_device_properties(self.index)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(dev)) != 0:
+                raise OSError("no NVML device at " + bus.decode())
+        except (AttributeError, OSError):
+            if lib.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(dev)) != 0:
+                raise OSError("no NVML device")
+        return lib, dev
 
     def __enter__(self):
+        import ctypes
+        import threading
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "20"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            lib, dev = self._nvml_handle()
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(dev, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            self._stop = threading.Event()
+
+            def run():
+                mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+                while not self._stop.is_set():
+                    if (lib.nvmlDeviceGetClockInfo(dev, 1, ctypes.byref(mhz)) == 0 and
+                            reasons_fn(dev, ctypes.byref(rs)) == 0):
+                        self.samples.append((float(mhz.value), int(rs.value)))
+                    time.sleep(self.period)
+
+            self._thread = threading.Thread(target=run, daemon=True)
+            self._thread.start()
+            self.source = "nvml"
+        except (OSError, AttributeError):
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--id={self.index}",
+                     "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+                     "clocks_event_reasons.hw_thermal_slowdown,"
+                     "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                     "--format=csv,noheader,nounits", "-lms", "20"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi"
+            except OSError:
+                self.proc = None
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=2)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -84,28 +141,27 @@ class Clocks:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
-            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            bits = (0x8, 0x40, 0x20, 0x4)
+            for ln in out.splitlines():
+                f = [x.strip() for x in ln.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    self.max_mhz = float(f[1])
+                    mask = sum(b for b, v in zip(bits, f[2:6]) if v.lower() == "active")
+                    self.samples.append((float(f[0]), mask))
+                except ValueError:
+                    continue
         return False
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in getattr(self, "lines", []):
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for name, val in zip(names, f[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
+        if not self.samples:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
-                "reasons": sorted(reasons)}
+        reasons = sorted({name for _, m in self.samples for bit, name in self.REASONS.items()
+                          if m & bit})
+        return {"sm_mhz": statistics.median(x for x, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "samples": len(self.samples), "reasons": reasons,
+                "source": self.source}
 
 
 def make_inputs(T, device, seed):
@@ -137,6 +193,62 @@ def stored_traffic(kernel):
 
 
 # ------------------------------------------------------------------------------ our arm
+
+def run_seq_sharded(args, ws, rank, local):
+    """One T-token sequence split by sequence over the ranks (strong scaling): each rank
+    summarises its contiguous range (P segments), one NCCL all_gather exchanges the fp32
+    summaries, every rank scans all ranks' segments in order and re-emits its own range."""
+    import torch
+    import torch.distributed as dist
+    from gated_delta_rule_07_gb300 import build, sharding
+    build.build()
+    from gated_delta_rule_07_gb300 import gdn
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist.init_process_group("nccl", device_id=dev)
+    T = args.T
+    P = args.P or 4
+    inp = make_inputs(T, dev, seed=0)
+    t0, t1 = sharding.sequence_partition(T, ws, rank)
+    d = {n: getattr(inp, n)[t0:t1].to(dev).contiguous() for n in ("q", "k", "v", "g", "beta")}
+    summary, scan, emit = sharding.gpu_steps(gdn)
+
+    def step():
+        return sharding.sequence_parallel_forward(d["q"], d["k"], d["v"], d["g"], d["beta"], None,
+                                                  summary=summary, scan=scan, emit=emit,
+                                                  P_local=P)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    dist.barrier()
+    ms = torch.tensor([e0.elapsed_time(e1) / args.steps], device=dev)
+    dist.all_reduce(ms, op=dist.ReduceOp.MAX)
+    ms = float(ms.item())
+    if rank != 0:
+        return None
+    return {"metric": METRIC, "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded, as the default mode)",
+            "config": {"workload": f"long-context bf16 T={T} Hk={HK} Hv={HV} K=V={KD} C={C}",
+                       "segments_per_rank": P, "batch": 1, "seq_len": T,
+                       "parallelism": f"sequence-sharded x{ws} (all_gather of fp32 segment "
+                                      f"summaries, {sharding.exchange_bytes(HV, KD, VD, P)} B "
+                                      f"per rank)"},
+            "gpu_launches": None, "e2e": None, "clocks": clk.summary()}
+
 
 def run_ours(args, ws, rank, local):
     import torch
@@ -300,7 +412,6 @@ def run_ours(args, ws, rank, local):
                         "sum_u": "sum_u_records", "sum_m": "sum_m_records"}
     dom = max(kern_ms, key=kern_ms.get)
     emit_bytes = kern_bytes[dom]
-    emit_flops = FLOP_PER_TOKEN * T
     emit_s = kern_ms[dom] / 1e3
     achieved_gbs = emit_bytes / emit_s / 1e9
     tr = stored_traffic(kern_traffic_key[dom])
@@ -340,9 +451,6 @@ def run_ours(args, ws, rank, local):
                 "achieved_gbs": kern_bytes[k] / (kern_ms[k] / 1e3) / 1e9,
                 "frac": kern_bytes[k] / (kern_ms[k] / 1e3) / 1e9 / hbm}
             for k in kern_ms},
-        "emit_tensor": {"tflops": emit_flops / (ph["emit"] / 1e3) / 1e12, "peak": tf,
-                        "frac": emit_flops / (ph["emit"] / 1e3) / 1e12 / tf,
-                        "note": "the path's FLOPs over the phase-3 kernel's time"},
         "path_roofline": {"bound_us": t_bound * 1e6, "step_us": ms * 1e3,
                           "frac": t_bound / (ms / 1e3),
                           "note": "max(FLOP/bf16 peak, bytes/HBM) over the whole step, of "
@@ -422,6 +530,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-tokens", type=int, default=2048)
+    ap.add_argument("--mode", default="replicas", choices=["replicas", "seq"],
+                    help="with several ranks: independent sequences (weak scaling) or one "
+                         "sequence split by sequence over the ranks (strong scaling)")
     ap.add_argument("--path", type=int, default=0,
                     help="kernel family: 0 auto (tcgen05 for this workload), 2 tcgen05")
     args = ap.parse_args()
@@ -434,7 +545,8 @@ def main():
     if args.impl == "reference":
         res = run_reference(args, ws, rank)
     else:
-        res = run_ours(args, ws, rank, local)
+        res = (run_seq_sharded(args, ws, rank, local) if args.mode == "seq" and ws > 1
+               else run_ours(args, ws, rank, local))
     if res is not None:
         print(json.dumps(res), flush=True)
 

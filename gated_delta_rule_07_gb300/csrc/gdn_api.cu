@@ -89,13 +89,8 @@ gdn_status to_status(cudaError_t e) {
     if (_e != cudaSuccess) return to_status(_e);   \
   } while (0)
 
-// Tensor-core pipeline of gdn_forward: the parallel preparation of every chunk's solved T tiles
-// followed by the two-chain summaries and the re-emit from T (true), or the U summary writing
-// per-chunk factor records that the M summary and the re-emit read (false).
-constexpr bool kPreparedT = false;
-
 struct Layout {
-  size_t status, M, U, h_in, w, u, gcum, wy, trec, total;
+  size_t status, M, U, h_in, w, u, gcum, wy, total;
 };
 
 // Workspace: [status word | M | U | h_in | w | u | gcum | records], each piece 256-byte
@@ -126,12 +121,8 @@ Layout layout(const gdn_problem* p, bool records = true) {
   L.gcum = off;
   off += mat ? align_up(T * p->hv * 4) : 0;
   L.wy = off;  // tcgen05 path: the U summary's per-chunk records for the M summary
-  off += (records && seg && !mat && !kPreparedT)
+  off += (records && seg && !mat)
              ? align_up(gdn::tc5_records_bytes(p->total_tokens, p->num_seqs, p->hv))
-             : 0;
-  L.trec = off;  // tcgen05 path: the parallel preparation's solved T tiles, every chunk
-  off += (records && !mat && kPreparedT)
-             ? align_up(gdn::prep_records_bytes(p->total_tokens, p->num_seqs, p->hv))
              : 0;
   L.total = off;
   return L;
@@ -282,60 +273,14 @@ gdn_status forward_impl(const gdn_problem* p, const void* q, const void* k, cons
     a.M = a.M_out;
     a.U = a.U_out;
     a.h_in_out = reinterpret_cast<float*>(ws + L.h_in);
-    if (use_tensor_path(p) && L.total == Lr.total && Lr.trec > Lr.wy)
+    if (use_tensor_path(p) && L.total == Lr.total && Lr.total > Lr.wy)
       a.wy = ws + L.wy;
   }
-  const bool trec = use_tensor_path(p) && L.total == Lr.total && Lr.total > Lr.trec && a.T > 0;
   // With P = 1 the incoming state of the only segment is h0 itself.
   a.h_in = seg ? a.h_in_out : h0;
   GDN_TRY(gdn::launch_validate_cu(a, stream));
 
   GDN_TRY(mark(0));
-  if (use_tensor_path(p) && trec) {
-    // Every chunk's T tiles first (one parallel kernel).  Then segment 0, whose incoming state
-    // h0 is known, re-emits beside the summaries of segments 1 .. P-2 (one grid); its final
-    // state is segment 1's incoming state, from which the scan continues; then segments
-    // 1 .. P-1 re-emit.  The last segment's summary is never needed.
-    GDN_TRY(gdn::prep_launch(a, ws + L.trec, stream));
-    GDN_TRY(mark(4));
-    Args base = a;
-    base.trec = ws + L.trec;
-    const int P = p->segments_per_seq;
-    if (!seg) {
-      GDN_TRY(mark(1));
-      GDN_TRY(mark(2));
-      GDN_TRY(gdn::tc5_emit(base, stream));
-      return to_status(mark(3));
-    }
-    Args ae = base;  // segment 0 from h0, leaving its final state in h_in[segment 1]
-    ae.seg_lo = 0;
-    ae.seg_n = 1;
-    ae.h_in = h0;
-    ae.h_in_per_seq = true;
-    ae.h_next = a.h_in_out;
-    ae.h_final = nullptr;
-    if (P >= 3) {
-      Args as = base;  // the summaries of segments 1 .. P-2
-      as.seg_lo = 1;
-      as.seg_n = P - 2;
-      GDN_TRY(gdn::tc5_phase_a(as, ae, stream));
-    } else {
-      GDN_TRY(gdn::tc5_emit(ae, stream));
-    }
-    GDN_TRY(mark(1));
-    if (P >= 3) {
-      Args sa = base;
-      sa.h_final = nullptr;
-      sa.scan_from = 1;
-      GDN_TRY(gdn::simt_scan(sa, stream));
-    }
-    GDN_TRY(mark(2));
-    Args eb = base;  // segments 1 .. P-1 from their true incoming states
-    eb.seg_lo = 1;
-    eb.seg_n = P - 1;
-    GDN_TRY(gdn::tc5_emit(eb, stream));
-    return to_status(mark(3));
-  }
   if (use_tensor_path(p)) {
     if (seg) {
       Args ma = a;

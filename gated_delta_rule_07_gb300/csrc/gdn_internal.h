@@ -24,18 +24,10 @@ struct Args {
   void* out;
   void *w_out, *u_out;
   void* wy;  // tcgen05 summaries: per-chunk factor records written by the U half (nullable)
-  const void* trec;  // tcgen05: per-chunk solved T_w | T_u tiles from prep_launch (nullable)
   float* gcum_out;
   float *M_out, *U_out, *h_in_out, *h_final;
   int32_t* status;
   bool skip_last_summary;  // the fused forward never reads the last segment's summary
-  // Segment range of a per-segment launch: segments seg_lo .. seg_lo + seg_n - 1 of every
-  // sequence (seg_n = 0: all P).  The scan starts at segment scan_from, whose incoming state is
-  // already in h_in_out (scan_from = 0: from h0).  h_next (phase 3): where a segment r < P-1
-  // leaves its final state, at the slot of segment r + 1 (the next segment's incoming state).
-  int seg_lo, seg_n, scan_from;
-  float* h_next;
-  bool h_in_per_seq;  // phase 3: h_in is indexed by sequence ([N, hv, K, V], e.g. h0)
   // Limit of a bounded device wait in SM cycles (0: the default, about a second), and a fault
   // to inject for tests of those waits (0: none; 1: the chunk kernels' chain never signals its
   // first hand-off, so a wait for it expires).
@@ -63,14 +55,5 @@ size_t tc5_records_bytes(int64_t T, int N, int hv);
 // `mid`, when given, is recorded between the two launches of phase 1.
 cudaError_t tc5_summary(const Args& a, cudaStream_t s, cudaEvent_t mid = nullptr);
 cudaError_t tc5_emit(const Args& a, cudaStream_t s);
-// One grid holding phase 1 of the segments `as` names and phase 3 of those `ae` names.
-cudaError_t tc5_phase_a(const Args& as, const Args& ae, cudaStream_t s);
-
-// The parallel chunk preparation (tcgen05 gram, blocked triangular solve): writes, for every
-// chunk slot and value head, the fp16 tiles T diag(beta e^G) and T diag(beta) (16 KB) that the
-// chain kernels load instead of solving.  Slots are the 64-token windows of the packed token
-// axis plus the sequence index (see slot_to_chunk).
-size_t prep_records_bytes(int64_t T, int N, int hv);
-cudaError_t prep_launch(const Args& a, void* rec, cudaStream_t s);
 
 }  // namespace gdn

@@ -231,17 +231,12 @@ __global__ void __launch_bounds__(kThreads) simt_scan_kernel(Args a) {
 #pragma unroll
     for (int k = 0; k < NV; ++k) mv[k] = src[tid + kThreads * k];
   };
-  // start: from h0 at segment 0, or from the incoming state already stored at segment r0
-  const int r0 = a.scan_from;
-  if (steps > r0) load_m(r0);
+  if (steps > 0) load_m(0);
   float h[NO];  // h[i0 + RS m][c]
 #pragma unroll
-  for (int m = 0; m < NO; ++m) {
-    const int64_t e = (((int64_t)n * a.hv + j) * KD + i0 + RS * m) * VD + col0 + c;
-    const int64_t e0 = ((((int64_t)n * a.P + r0) * a.hv + j) * KD + i0 + RS * m) * VD + col0 + c;
-    h[m] = r0 > 0 ? a.h_in_out[e0] : (a.h0 ? a.h0[e] : 0.f);
-  }
-  for (int r = r0; r < a.P; ++r) {
+  for (int m = 0; m < NO; ++m)
+    h[m] = a.h0 ? a.h0[(((int64_t)n * a.hv + j) * KD + i0 + RS * m) * VD + col0 + c] : 0.f;
+  for (int r = 0; r < a.P; ++r) {
     const int64_t base = (((int64_t)n * a.P + r) * a.hv + j) * KD;  // row 0 of segment r
     if (a.h_in_out) {
 #pragma unroll

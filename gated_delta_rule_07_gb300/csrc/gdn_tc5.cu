@@ -72,13 +72,7 @@ constexpr long long kDrainCycles = 200000000LL;  // teardown waits for in-flight
 // With per-chunk factor records in the workspace, the U half stores each chunk's -w^T, fp16 K,
 // u^T and the state update's decay; kSumML (the M half) and kEmitR (phase 3) load them instead
 // of computing them, and run only what depends on the state (kEmitR also forms attn_i and q_g).
-// kEmitT (phase 3) loads each chunk's solved T diag(.) tiles from the records the parallel
-// preparation kernel wrote, and does everything else as kEmit does.
-// kSumUMT (phase 1) carries both halves of X = [M | U] of a segment in one CTA from the loaded T
-// tiles: the U state in the chain warps' registers, the M state in TMEM (the M update product
-// accumulates onto it after the chain has scaled it by gamma), so that the two independent
-// chains share the loads, the fp16 K, the w product and -w^T, and keep the tensor pipe busy.
-enum Mode { kEmit = 0, kSumM = 1, kSumU = 2, kSumML = 3, kEmitR = 4, kEmitT = 5, kSumUMT = 6 };
+enum Mode { kEmit = 0, kSumM = 1, kSumU = 2, kSumML = 3, kEmitR = 4 };
 
 // Record layout: the fp16 tiles -w^T [i][t] (MN-major), K [t][i] (MN-major) and u^T [c][t]
 // (128-byte swizzled rows) as they sit in shared memory, then e^{G_last - G_t} (64 floats) and
@@ -93,9 +87,6 @@ constexpr uint32_t TM_W = 64;    // w^T                    64 fp32
 constexpr uint32_t TM_U = 128;   // fp16 delta' (columns 32 hf + 0..15)
 constexpr uint32_t TM_DO = 192;  // u^T + D = delta^T, then fp16 delta, in 0-63; o^T in 64-127
 constexpr uint32_t TM_H = 320;   // Dh^T                   128 fp32, then fp16 h^T
-// kSumUMT: M^T state (fp32) in 0-127, w^T in 128-191, u^T + D_U (then fp16 delta'_U) in 192-255,
-// D_M (then fp16 delta'_M) in 256-319, Dh_U / fp16 U^T in 320-447, fp16 M^T in 448-511
-constexpr uint32_t TM_MS = 0, TM_WUM = 128, TM_DM = 256, TM_MF = 448;
 
 // mbarriers: who completes them
 enum Bar {
@@ -116,25 +107,17 @@ enum Bar {
   B_KF0, B_KF1,  // fp16 K tile free (its chunk's Dh is done)         MMA commit
   B_QF0, B_QF1,  // kEmitR: the staged bf16 Q, g and beta have been read  transposer + converter
   B_RL0, B_RL1,  // kEmitR: a record is staged (byte count)              loader
-                 // (kEmitT: a chunk's T tiles are staged)
   B_RF0, B_RF1,  // kEmitR: its record stage is free (D, O2, Dh done)    MMA commit
-                 // (kEmitT: its T stage is free (w, u done))
-  B_DM,        // kSumUMT: D_M of a chunk is in TMEM                  MMA commit
-  B_DRM,       // kSumUMT: fp16 delta'_M is in TMEM, M^T scaled by gamma   chain (256)
-  B_HM,        // kSumUMT: the M update has accumulated                MMA commit
-  B_HRM,       // kSumUMT: fp16 M^T is in TMEM                          chain (256)
   B_END,       // every product issued has completed                  MMA commit
   kNumBars
 };
 template <int MODE>
 __device__ __forceinline__ uint32_t bar_count(int b) {
-  return (b == B_E2 && (MODE == kEmitR || MODE == kEmitT)) ? 64u  // (the two attn_i warps)
+  return (b == B_E2 && MODE == kEmitR)         ? 64u  // (kEmitR: the two gram warps)
          : (b == B_QF0 || b == B_QF1)          ? (uint32_t)(64 + kConvThreads)
          : (b == B_E2 || b == B_T || b == B_WR)  ? (uint32_t)kPrepThreads
-         : (b == B_CV && MODE == kSumUMT)     ? (uint32_t)(kConvThreads + kPrepThreads)
-         : (b == B_CV && MODE == kEmitT)      ? (uint32_t)(kConvThreads + 64)
          : (b == B_TB || b == B_CV) ? (uint32_t)kConvThreads
-         : (b == B_HR || b == B_DR || b == B_HRM || b == B_DRM) ? (uint32_t)kChainThreads
+         : (b == B_HR || b == B_DR)            ? (uint32_t)kChainThreads
          : (b >= B_L0 && b <= B_L2)            ? (MODE == kSumML ? 1u : 33u)
          : (b == B_RL0 || b == B_RL1)          ? 1u
                                                : 1u;
@@ -155,7 +138,7 @@ struct Smem {
   alignas(16) float adiag[C][20];  // the diagonal 16 x 16 blocks of A, fp32 (padded rows)
   float wd[4][16 * 17];          // per-warp fp32 16 x 16 block of T (padded rows)
   float gst[2][2][C];            // g and beta of a staged chunk
-  float G[4][C], eG[4][C], eGLG[4][C], beta[4][C], gamma[4];  // (kSumUMT: 4 chunks deep)
+  float G[3][C], eG[3][C], eGLG[3][C], beta[3][C], gamma[4];
   // decay e^{G_t - G_s} (s <= t) of the chunk the gram reads next: on the 16-block of t it is
   // dd*[t][s & 15]; for s in an earlier block b it is rf*[t][b] * cf[s], with
   // rf = e^{G_t - G_e}, cf = e^{G_e - G_s} and e the last row of block b (both <= 1 for g <= 0).
@@ -232,24 +215,17 @@ __device__ __forceinline__ char* chunk_record(const Args& a, int n, int64_t sb, 
 
 // ------------------------------------------------------------------ the kernel
 
-// One CTA's work: segment r = seg_lo + bseg % seg_n of sequence bseg / seg_n (all P segments
-// when seg_n is 0), value head blockIdx.y.
 template <int MODE>
-__device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_k,
-                                           const CUtensorMap* tm_q, const CUtensorMap* tm_v,
-                                           int bseg) {
+__global__ void __launch_bounds__(kThreads, 1)
+    tc5_chunk_kernel(Args a, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_v) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = saddr(smem_raw);
   Smem& S = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (raw & 1023u)) & 1023u));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int sn = a.seg_n > 0 ? a.seg_n : a.P;
-  const int n_seq = bseg / sn, r = a.seg_lo + bseg % sn;
-  const int seg = n_seq * a.P + r, j = blockIdx.y;
-  constexpr bool OUT = MODE == kEmit || MODE == kEmitR || MODE == kEmitT;  // phase 3: outputs o
-  constexpr bool UM = MODE == kSumUMT;
-  constexpr int kTb = UM ? 4 : 3;                    // chunks of decay tables kept
-  constexpr uint32_t tmW = UM ? TM_WUM : TM_W;       // w^T
-  constexpr uint32_t tmU = UM ? TM_DO : TM_U;        // fp16 delta' of the chain (UM: in place)
+  const int seg = blockIdx.x, j = blockIdx.y;
+  const int n_seq = seg / a.P, r = seg % a.P;
+  constexpr bool OUT = MODE == kEmit || MODE == kEmitR;  // phase 3: outputs o
   if (!OUT && r == a.P - 1 && a.skip_last_summary) return;
   const int kh = j / (a.hv / a.hk);
   int64_t sb, se;
@@ -272,11 +248,11 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
   }
   if (MODE != kSumML && tid == kChainThreads) {
     if (MODE != kEmitR)
-      asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(tm_k)) : "memory");
+      asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_k)) : "memory");
     if (OUT)
-      asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(tm_q)) : "memory");
+      asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_q)) : "memory");
     if (MODE != kSumM && MODE != kEmitR)
-      asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(tm_v)) : "memory");
+      asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
   }
   fence_before_sync();
   __syncthreads();
@@ -293,12 +269,6 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
   // stage's K | Q tile holds [-w^T rows 0-63 | Q^T box 0 | -w^T rows 64-127 | Q^T box 1], so
   // that one MN-major operand with its second 64 columns 8 KB on is [-w^T | Q^T]
   auto qstage = [&](int sg) -> uint8_t* { return sg ? S.nw : S.tw; };
-  // kEmitT: the staged T_w | T_u tiles of a chunk (16 KB) sit where the solve would write them
-  // (stage 0: tw, tu) or in the gram and T tiles it leaves unused (stage 1: ah, th)
-  auto tstage = [&](int sg) -> uint8_t* { return sg ? S.ah : S.tw; };
-  static_assert(offsetof(Smem, tu) == offsetof(Smem, tw) + 8192 &&
-                    offsetof(Smem, th) == offsetof(Smem, ah) + 8192,
-                "T stages are 16 KB contiguous");
 
   if (warp < 8) {
     // =============================================================== chain (256 threads)
@@ -309,7 +279,7 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
     float h[64];                              // h^T[c][64 hf .. 64 hf + 63]
     {
       const float* src = nullptr;
-      if (OUT && a.h_in) src = a.h_in + ((int64_t)(a.h_in_per_seq ? n_seq : seg) * a.hv + j) * KD * VD;
+      if (OUT && a.h_in) src = a.h_in + ((int64_t)seg * a.hv + j) * KD * VD;
 #pragma unroll
       for (int q = 0; q < 64; ++q) {
         const int i = 64 * hf + q;
@@ -338,25 +308,9 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
       // so the MMA warp's wait for it must expire)
       if (a.fault != 1) arrive(S, B_HR);
     }
-    if (UM && nch > 0) {  // kSumUMT: the M state starts at I (fp32 in TMEM), with its fp16 copy
-#pragma unroll
-      for (int piece = 0; piece < 4; ++piece) {
-        uint32_t x[16], p[8];
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-          x[q] = __float_as_uint(64 * hf + 16 * piece + q == c ? 1.f : 0.f);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          p[q] = pack_h2(__uint_as_float(x[2 * q]), __uint_as_float(x[2 * q + 1]));
-        tmem_st16(tm + lane_bits + TM_MS + 64 * hf + 16 * piece, x);
-        tmem_st8(tm + lane_bits + TM_MF + 32 * hf + 8 * piece, p);
-      }
-      fence_before_sync();
-      arrive(S, B_HRM);
-    }
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
     for (int ci = 0; ci < nch; ++ci) {
-      const int gb = ci % kTb;
+      const int gb = ci % 3;
       const int64_t t0 = sb + (c0 + ci) * C;
       const int L = (int)((se - t0) < C ? (se - t0) : C);
       const float* eglg = MODE == kSumML ? S.tbl[gb] : S.eGLG[gb];
@@ -400,53 +354,12 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
             pp[q] = pack_h2(d[2 * q] * eglg[t], d[2 * q + 1] * eglg[t + 1]);
           }
           if (OUT) tmem_st8_nw(tm + lane_bits + TM_DO + 32 * hf + 8 * piece, pd);
-          tmem_st8_nw(tm + lane_bits + tmU + 32 * hf + 8 * piece, pp);
+          tmem_st8_nw(tm + lane_bits + TM_U + 32 * hf + 8 * piece, pp);
         }
         tmem_wait_st();
       }
       fence_before_sync();
       arrive(S, B_DR);
-      if (UM) {  // delta'_M = diag(e^{G_last - G}) D_M -> fp16 in place; then M^T <- gamma M^T
-        wait_bar(S, B_DM, ci & 1);
-        fence_after_sync();
-        {
-          uint32_t dr[2][16];
-          tmem_ld16_nw(tm + lane_bits + TM_DM + 32 * hf, dr[0]);
-          tmem_ld16_nw(tm + lane_bits + TM_DM + 32 * hf + 16, dr[1]);
-          tmem_wait_ld16x2(dr[0], dr[1]);
-#pragma unroll
-          for (int piece = 0; piece < 2; ++piece) {
-            uint32_t pp[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              const int t = 32 * hf + 16 * piece + 2 * q;
-              const float x0 = __uint_as_float(dr[piece][2 * q]) * eglg[t];
-              const float x1 = __uint_as_float(dr[piece][2 * q + 1]) * eglg[t + 1];
-              range_ok = range_ok && fits_half(x0) && fits_half(x1);
-              pp[q] = pack_h2(x0, x1);
-            }
-            tmem_st8_nw(tm + lane_bits + TM_DM + 32 * hf + 8 * piece, pp);
-          }
-        }
-        const float gam = S.gamma[gb];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t mr[2][16];
-          tmem_ld16_nw(tm + lane_bits + TM_MS + 64 * hf + 32 * half, mr[0]);
-          tmem_ld16_nw(tm + lane_bits + TM_MS + 64 * hf + 32 * half + 16, mr[1]);
-          tmem_wait_ld16x2(mr[0], mr[1]);
-#pragma unroll
-          for (int p2 = 0; p2 < 2; ++p2) {
-            float m[16];
-#pragma unroll
-            for (int q = 0; q < 16; ++q) m[q] = gam * __uint_as_float(mr[p2][q]);
-            tmem_st16f_nw(tm + lane_bits + TM_MS + 64 * hf + 32 * half + 16 * p2, m);
-          }
-        }
-        tmem_wait_st();
-        fence_before_sync();
-        arrive(S, B_DRM);
-      }
 
       // ---- the state update; its fp16 copy and the read of o^T before the hand-off
       wait_bar(S, B_H, ci & 1);
@@ -513,56 +426,13 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
           po += 2 * stride;
         }
       }
-      if (UM) {  // fp16 M^T for the next chunk's D_M, once the M update has accumulated
-        wait_bar(S, B_HM, ci & 1);
-        fence_after_sync();
-        if (ci + 1 < nch) {
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t mr[2][16];
-            tmem_ld16_nw(tm + lane_bits + TM_MS + 64 * hf + 32 * half, mr[0]);
-            tmem_ld16_nw(tm + lane_bits + TM_MS + 64 * hf + 32 * half + 16, mr[1]);
-            tmem_wait_ld16x2(mr[0], mr[1]);
-#pragma unroll
-            for (int p2 = 0; p2 < 2; ++p2) {
-              uint32_t p[8];
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                p[q] = pack_h2(__uint_as_float(mr[p2][2 * q]), __uint_as_float(mr[p2][2 * q + 1]));
-              tmem_st8_nw(tm + lane_bits + TM_MF + 32 * hf + 16 * half + 8 * p2, p);
-            }
-          }
-          tmem_wait_st();
-          fence_before_sync();
-          arrive(S, B_HRM);
-        }
-      }
       if (!named_bar_and(2, kChainThreads, !aborted(S))) break;
     }
     if (!range_ok) S.range_bad = 1;
-    if (UM) {  // kSumUMT: M_r from TMEM (M^T[c][i] = M[i][c]); an empty segment's is I
-      const bool ok = __shfl_sync(0xffffffffu, !aborted(S) ? 1 : 0, 0) != 0;
-      float* dm = a.M_out + ((int64_t)seg * a.hv + j) * KD * KD;
-#pragma unroll
-      for (int piece = 0; piece < 4; ++piece) {
-        float m[16];
-        if (nch > 0 && ok) {
-          tmem_ld16(tm + lane_bits + TM_MS + 64 * hf + 16 * piece, m);
-        } else {
-#pragma unroll
-          for (int q = 0; q < 16; ++q) m[q] = 64 * hf + 16 * piece + q == c ? 1.f : 0.f;
-        }
-        if (ok) {
-#pragma unroll
-          for (int q = 0; q < 16; ++q) dm[(64 * hf + 16 * piece + q) * KD + c] = m[q];
-        }
-      }
-    }
     // ---- the final state: h^T[c][i] = h[i][c]
     float* dst = nullptr;
     if (OUT) {
       if (a.h_final && r == a.P - 1) dst = a.h_final + ((int64_t)n_seq * a.hv + j) * KD * VD;
-      else if (a.h_next && r < a.P - 1) dst = a.h_next + ((int64_t)(seg + 1) * a.hv + j) * KD * VD;
     } else if (MODE == kSumM || MODE == kSumML) {
       dst = a.M_out + ((int64_t)seg * a.hv + j) * KD * KD;
     } else {
@@ -585,11 +455,11 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
     // the strictly upper blocks of T diag(.), rows 0-31 x columns 32-63 of A and attn_i, and the
     // upper right 8 x 8 of each warp's fp32 block of T are zero for every chunk
     for (int e = pt; e < 64 * 128 / 16; e += kPrepThreads) {
-      if (MODE != kEmitR && MODE != kEmitT) {  // (kEmitR, kEmitT stage loads there)
+      if (MODE != kEmitR) {  // (kEmitR stages records there)
         reinterpret_cast<uint4*>(S.tw)[e] = make_uint4(0u, 0u, 0u, 0u);
         reinterpret_cast<uint4*>(S.tu)[e] = make_uint4(0u, 0u, 0u, 0u);
-        reinterpret_cast<uint4*>(S.ah)[e] = make_uint4(0u, 0u, 0u, 0u);
       }
+      if (MODE != kEmitR) reinterpret_cast<uint4*>(S.ah)[e] = make_uint4(0u, 0u, 0u, 0u);
       reinterpret_cast<uint4*>(S.att[0])[e] = make_uint4(0u, 0u, 0u, 0u);
       reinterpret_cast<uint4*>(S.att[1])[e] = make_uint4(0u, 0u, 0u, 0u);
     }
@@ -615,13 +485,12 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
     // upper blocks in columns 32-63 (left zero from the start), so each row computes one plain
     // half at most and one half holding its own block.
     auto gram = [&](int ci) {
-      if (MODE == kEmitT && pt < 64) return;  // (kEmitT: the T tiles are loaded; attn_i only)
       wait_bar(S, B_SQ, ci & 1);
       wait_bar(S, B_TB, ci & 1);
       fence_after_sync();
       // warps 8, 9: rows of A (kEmitR: of attn_i, from Q K^T); warps 10, 11: rows of attn_i
-      const bool lo = pt < 64, is_s = MODE != kEmitR && MODE != kEmitT && lo;
-      if (MODE == kEmit || MODE == kEmitT || lo) {
+      const bool lo = pt < 64, is_s = MODE != kEmitR && lo;
+      if (MODE == kEmit || lo) {
         const int t = pt & 63, hi = t >> 5, ab = (t >> 4) & 1;  // hi is warp-uniform
         const float4 rf4 = *reinterpret_cast<const float4*>(is_s ? S.rfA[t] : S.rfO[t]);
         uint8_t* dst = is_s ? S.ah : S.att[ci & 1];
@@ -722,7 +591,7 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
     // ---- T = (I + A)^-1 and the two scaled copies the w / u products read.  T, w and h^T are
     // not range-checked: an infinite fp16 value there makes delta infinite or NaN.
     auto solve = [&](int ci) {
-      const int gb = ci % kTb;
+      const int gb = ci % 3;
       {  // Diagonal block wb = [[P, 0], [R, Q]] (8 x 8 parts): P^-1 and Q^-1 by forward
          // substitution side by side (lane c < 8: column c of P^-1, 8 <= c < 16: column c - 8
          // of Q^-1), then the lower left block -Q^-1 (R P^-1) by all lanes, in fp32 in wd.
@@ -840,7 +709,7 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
 #pragma unroll
       for (int hb = 0; hb < 2; ++hb) {
         float wv[32];
-        tmem_ld32(tm + lane_bits + tmW + 32 * hb, wv);
+        tmem_ld32(tm + lane_bits + TM_W + 32 * hb, wv);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
           uint4 pk;
@@ -917,62 +786,15 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
       if (!(fmaxf(mx.x, mx.y) <= kHalfMax)) S.range_bad = 1;
     }
     // one chunk ahead: the gram of chunk ci + 1 is built while w of chunk ci is computed
-    if (UM) {  // kSumUMT: fp16 V of the next chunk (in place) and -w^T; the T tiles are loaded
-      float vmax = 0.f;
-      auto convert_v = [&](int cn) {
-        wait_bar(S, B_L0 + (cn & 1), (cn >> 1) & 1);
-        uint8_t* vb = S.v[cn & 1] + 16 * (pt & 63) + 8192 * (pt >> 6);
-#pragma unroll 1
-        for (int k0 = 0; k0 < 8; k0 += 4)
-          vmax = to_half_chunks<4, false>(vb + 1024 * k0, vb + 1024 * k0, nullptr, vmax);
-        fence_async_smem();
-      };
-      if (nch > 0) {
-        convert_v(0);
-        arrive(S, B_CV);
-      }
-      for (int ci = 0; ci < nch; ++ci) {
-        if (ci + 1 < nch) convert_v(ci + 1);
-        neg_w(ci);  // (waits for w of chunk ci: the MMA warp has taken the previous hand-off)
-        if (ci + 1 < nch) arrive(S, B_CV);
-        if (!named_bar_and(1, kPrepThreads, !aborted(S))) break;
-      }
-      if (!(vmax <= kHalfMax)) S.range_bad = 1;
-    }
-    // kEmitT: warps 8, 9 (no gram rows to form) convert K (into its fp16 tile) and V (in place)
-    // of the chunk the gram of warps 10, 11 is working on
-    float kvmax = 0.f;
-    auto convert_kv = [&](int cn) {
-      const int sg = cn & 1;
-      wait_bar(S, B_L0 + sg, (cn >> 1) & 1);
-      if (cn >= 2) wait_bar(S, B_KF0 + sg, ((cn >> 1) + 1) & 1);  // Dh of cn - 2 read the tile
-      uint8_t* vb = S.v[sg] + 16 * pt;
-#pragma unroll 1
-      for (int k0 = 0; k0 < 16; k0 += 4)
-        kvmax = to_half_chunks<4, false>(vb + 1024 * k0, vb + 1024 * k0, nullptr, kvmax);
-      const uint8_t* kb = S.kq[sg] + 16 * pt;
-      uint8_t* kd = S.kh[sg] + 16 * pt;
-#pragma unroll 1
-      for (int k0 = 0; k0 < 16; k0 += 4)
-        kvmax = to_half_chunks<4, false>(kb + (k0 >> 3) * 16384 + 1024 * (k0 & 7),
-                                          kd + (k0 >> 3) * 8192 + 1024 * (k0 & 7), nullptr, kvmax);
-      fence_async_smem();
-    };
-    bool go = MODE != kEmitR && !UM && nch > 0;
+    bool go = MODE != kEmitR && nch > 0;
     if (go) {
       gram(0);
-      if (MODE == kEmitT && lo_warps) {
-        convert_kv(0);
-        arrive(S, B_CV);
-      }
       go = named_bar_and(1, kPrepThreads, !aborted(S));
     }
     for (int ci = 0; go && ci < nch; ++ci) {
-      if (MODE != kEmitT) solve(ci);
+      solve(ci);
       if (ci + 1 < nch) gram(ci + 1);
-      if (MODE == kEmitT && lo_warps && ci + 1 < nch) convert_kv(ci + 1);
-      neg_w(ci);  // (waits for w of chunk ci: the MMA warp has taken the previous hand-off)
-      if (MODE == kEmitT && lo_warps && ci + 1 < nch) arrive(S, B_CV);
+      neg_w(ci);
       // the U half stores -w^T for the M half; the tile is rewritten two chunks later, and
       // this thread has seen its earlier copy read before the barrier of the chunk between
       if (MODE == kSumU && a.wy && pt == 0) bulk_wait_read();
@@ -984,7 +806,6 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
         bulk_s2g(rec + kRecU + 8192, saddr(S.kq[ci & 1]) + 16384 + 8192, 8192);
       }
     }
-    if (MODE == kEmitT && !(kvmax <= kHalfMax)) S.range_bad = 1;
     if (MODE == kSumU && a.wy && pt == 0) bulk_wait_all();
     }
   } else if (warp == 13) {
@@ -1023,24 +844,17 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
       if (lane == 0) {  // rows past T read zeros; rows in [L, 64) only meet zero weights
         const uint32_t kq = saddr(S.kq[sg]), vv = saddr(S.v[sg]);
         const uint32_t bytes = MODE == kEmitR ? 2u * 8192u
-                                              : (OUT ? 4u : 2u) * 8192u + (MODE != kSumM ? 2u : 0u) * 8192u +
-                                                    (UM ? 16384u : 0u);
+                                              : (OUT ? 4u : 2u) * 8192u + (MODE != kSumM ? 2u : 0u) * 8192u;
         mbar_expect_tx(bar, bytes);
-        if (UM) {  // the chunk's T_w and T_u tiles into the Q rows of the stage (never loaded)
-          const int64_t slot = ((sb + C * (c0 + ci)) >> 6) + n_seq;
-          const char* rec = static_cast<const char*>(a.trec) + (slot * a.hv + j) * (int64_t)16384;
-          bulk_g2s(kq + 8192u, rec, 8192u, bar);
-          bulk_g2s(kq + 16384u + 8192u, rec + 8192, 8192u, bar);
-        }
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
           if (MODE == kEmitR) {  // Q only: [S ; QK] takes fp16 K from the record
-            tma_box(saddr(qstage(sg)) + kb * 8192, tm_q, 64 * kb, kh, (int)t0, bar);
+            tma_box(saddr(qstage(sg)) + kb * 8192, &tm_q, 64 * kb, kh, (int)t0, bar);
             continue;
           }
-          tma_box(kq + kb * 16384, tm_k, 64 * kb, kh, (int)t0, bar);
-          if (OUT) tma_box(kq + kb * 16384 + 8192, tm_q, 64 * kb, kh, (int)t0, bar);
-          if (MODE != kSumM) tma_box(vv + kb * 8192, tm_v, 64 * kb, j, (int)t0, bar);
+          tma_box(kq + kb * 16384, &tm_k, 64 * kb, kh, (int)t0, bar);
+          if (OUT) tma_box(kq + kb * 16384 + 8192, &tm_q, 64 * kb, kh, (int)t0, bar);
+          if (MODE != kSumM) tma_box(vv + kb * 8192, &tm_v, 64 * kb, j, (int)t0, bar);
         }
       }
 #pragma unroll
@@ -1055,19 +869,6 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
                    : "memory");
       nl0 += sg == 0;
       nl1 += sg == 1;
-      if (MODE == kEmitT) {  // the chunk's T_w | T_u tiles, once the w, u of ci - 2 are done
-        if (ci >= 2) wait_bar(S, B_RF0 + sg, ((ci >> 1) + 1) & 1);
-        if (lane == 0) {
-          const int64_t slot = ((sb + C * (c0 + ci)) >> 6) + n_seq;
-          const char* rec = static_cast<const char*>(a.trec) + (slot * a.hv + j) * (int64_t)16384;
-          const uint32_t rb = saddr(&S.bars[B_RL0 + sg]);
-          mbar_expect_tx(rb, 16384u);
-          bulk_g2s(saddr(tstage(sg)), rec, 16384u, rb);
-        }
-        nr0 += sg == 0;
-        nr1 += sg == 1;
-        __syncwarp();
-      }
       if (MODE == kEmitR) {  // the chunk's record (-w^T, fp16 K, u^T), once Dh of ci - 2 is done
         if (ci >= 2) wait_bar(S, B_RF0 + sg, ((ci >> 1) + 1) & 1);
         if (lane == 0) {
@@ -1098,13 +899,12 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
     const int p = tid - (kThreads - kConvThreads);  // 0..63
     float maxabs = 0.f;
     for (int ci = 0; MODE != kSumML && ci < nch; ++ci) {
-      const int sg = ci & 1, gb = ci % kTb;
+      const int sg = ci & 1, gb = ci % 3;
       const int64_t t0 = sb + (c0 + ci) * C;
       const int L = (int)((se - t0) < C ? (se - t0) : C);
       wait_bar(S, B_L0 + sg, (ci >> 1) & 1);
-      // the decay tables are single: the previous chunk's gram must be done with them (kSumUMT
-      // has no gram; its tables are four chunks deep)
-      if (!UM && ci >= 1) wait_bar(S, B_E2, (ci - 1) & 1);
+      // the decay tables are single: the previous chunk's gram must be done with them
+      if (ci >= 1) wait_bar(S, B_E2, (ci - 1) & 1);
       if (p < 32) {  // within-chunk inclusive scan of g; rows >= L decay by nothing
         float x0 = S.gst[sg][0][p], x1 = S.gst[sg][0][p + 32];
 #pragma unroll
@@ -1146,8 +946,7 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
         const int t = p, at = t >> 4, k0 = t & 15;
         const float Gt = S.G[gb][t], bt = S.beta[gb][t];
         // (the summaries read only A's tables, phase 3 from records only attn_i's)
-        constexpr bool kA = MODE != kEmitR && MODE != kEmitT && !UM;
-        constexpr bool kO = MODE == kEmit || MODE == kEmitR || MODE == kEmitT;
+        constexpr bool kA = MODE != kEmitR, kO = MODE == kEmit || MODE == kEmitR;
 #pragma unroll
         for (int k4 = 0; k4 < 16; k4 += 4) {
           float d[4];
@@ -1171,18 +970,17 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
         if (kA)
           *reinterpret_cast<float4*>(&S.rfA[t][0]) = make_float4(bt * f.x, bt * f.y, bt * f.z, 0.f);
       }
-      if (MODE == kEmit || MODE == kEmitT) wait_bar(S, B_SQ, ci & 1);  // [S ; QK] has read Q
+      if (MODE == kEmit) wait_bar(S, B_SQ, ci & 1);  // [S ; QK] has read the bf16 Q
       arrive(S, B_TB);
-      if (MODE != kSumM && MODE != kEmitR && MODE != kEmitT && !UM) {  // V -> fp16 in place
+      if (MODE != kSumM && MODE != kEmitR) {  // V -> fp16 in place (read only by the u product)
         uint8_t* vb = S.v[sg] + 16 * p;
 #pragma unroll 1
         for (int k0 = 0; k0 < 16; k0 += 4)
           maxabs = to_half_chunks<4, false>(vb + 1024 * k0, vb + 1024 * k0, nullptr, maxabs);
       }
       // fp16 K into its tile, once the chunk that last used the tile has finished Dh
-      // (kEmitR: fp16 K comes with the record; kEmitT: two prepare warps convert K and V)
-      if (MODE != kEmitR && MODE != kEmitT && ci >= 2) wait_bar(S, B_KF0 + sg, ((ci >> 1) + 1) & 1);
-      if (MODE != kEmitR && MODE != kEmitT) {
+      if (MODE != kEmitR && ci >= 2) wait_bar(S, B_KF0 + sg, ((ci >> 1) + 1) & 1);
+      if (MODE != kEmitR) {  // (kEmitR: fp16 K comes with the record)
         const uint8_t* kb = S.kq[sg] + 16 * p;
         uint8_t* kd = S.kh[sg] + 16 * p;
 #pragma unroll 1
@@ -1196,7 +994,7 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
         if (p == 0)
           bulk_s2g(chunk_record(a, n_seq, sb, c0 + ci, j) + kRecKh, saddr(S.kh[sg]), 16384);
       }
-      if (MODE == kEmit || MODE == kEmitT) {  // q_g = diag(e^G) Q as fp16 in place: the B of q_g h
+      if (MODE == kEmit) {  // q_g = diag(e^G) Q as fp16, in place: the K-major B of q_g h
         uint8_t* qb = S.kq[sg] + 8192 + 16 * p;
 #pragma unroll 1
         for (int k0 = 0; k0 < 16; k0 += 4) {
@@ -1265,7 +1063,7 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
       }
       __syncwarp();
     };
-    if (MODE != kSumML && MODE != kEmitR && !UM && nch > 0) {
+    if (MODE != kSumML && MODE != kEmitR && nch > 0) {
       wait_bar(S, B_L0, 0);
       sq(0);
       if (nch > 1) {  // the SQ columns are reused once the first gram has read them
@@ -1273,89 +1071,6 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
         wait_bar(S, B_L1, 0);
         sq(1);
       }
-    }
-    // kSumUMT, per chunk c: D_U (c), D_M (c), w (c + 1), Dh_U (c), Dh_M (c), u (c + 1).  The T
-    // tiles sit in the stage's Q rows; u^T goes into D_U's columns (D_U accumulates onto it),
-    // and Dh_M accumulates onto the M state the chain has scaled by gamma.
-    auto um_w = [&](int cn) {
-      const uint32_t kq = saddr(S.kq[cn & 1]), khs = saddr(S.kh[cn & 1]);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tm + TM_WUM, sdesc(khs + ks * 2048, 8192, 1024),
-               sdesc(kq + 8192 + ks * 32, 16, 1024), ID_WU, ks > 0);
-      mma_commit(saddr(&S.bars[B_WU]));
-    };
-    auto um_u = [&](int cn) {
-      const uint32_t kq = saddr(S.kq[cn & 1]), vv = saddr(S.v[cn & 1]);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_ss(tm + TM_DO, sdesc(vv + ks * 2048, 8192, 1024),
-               sdesc(kq + 16384 + 8192 + ks * 32, 16, 1024), ID_WU, ks > 0);
-      mma_commit(saddr(&S.bars[B_F0 + (cn & 1)]));  // the stage (K, V, T tiles) is free
-    };
-    if (UM && nch > 0) {
-      wait_bar(S, B_L0, 0);
-      wait_bar(S, B_CV, 0);
-      fence_after_sync();
-      if (leader) {
-        um_w(0);
-        um_u(0);
-      }
-      __syncwarp();
-    }
-    for (int ci = 0; UM && ci < nch; ++ci) {
-      const uint32_t khs = saddr(S.kh[ci & 1]), nw = saddr(S.nw);
-      wait_bar(S, B_WR, ci & 1);
-      wait_bar(S, B_HR, ci & 1);
-      fence_after_sync();
-      if (leader) {  // D_U^T = u^T + U^T (-w)^T
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ts(tm + TM_DO, tm + TM_H + 64 * (ks >> 2) + 8 * (ks & 3),
-                 sdesc(nw + ks * 2048, 16384, 1024), ID_D, 1);
-        mma_commit(saddr(&S.bars[B_D]));
-      }
-      __syncwarp();
-      wait_bar(S, B_HRM, ci & 1);
-      fence_after_sync();
-      if (leader) {  // D_M^T = M^T (-w)^T
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          mma_ts(tm + TM_DM, tm + TM_MF + 32 * (ks >> 2) + 8 * (ks & 3),
-                 sdesc(nw + ks * 2048, 16384, 1024), ID_D, ks > 0);
-        mma_commit(saddr(&S.bars[B_DM]));
-      }
-      __syncwarp();
-      if (ci + 1 < nch) {  // w of the next chunk (its -w^T overwrites the tile once D_M is done)
-        wait_bar(S, B_L0 + ((ci + 1) & 1), ((ci + 1) >> 1) & 1);
-        wait_bar(S, B_CV, (ci + 1) & 1);
-        fence_after_sync();
-        if (leader) um_w(ci + 1);
-        __syncwarp();
-      }
-      wait_bar(S, B_DR, ci & 1);
-      fence_after_sync();
-      if (leader) {  // Dh_U^T = delta'_U^T K
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ts(tm + TM_H, tm + TM_DO + 32 * (ks >> 1) + 8 * (ks & 1),
-                 sdesc(khs + ks * 2048, 8192, 1024), ID_DH, ks > 0);
-        mma_commit(saddr(&S.bars[B_H]));
-      }
-      __syncwarp();
-      wait_bar(S, B_DRM, ci & 1);
-      fence_after_sync();
-      if (leader) {  // M^T <- gamma M^T + delta'_M^T K
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_ts(tm + TM_MS, tm + TM_DM + 32 * (ks >> 1) + 8 * (ks & 1),
-                 sdesc(khs + ks * 2048, 8192, 1024), ID_DH, 1);
-        mma_commit(saddr(&S.bars[B_HM]));
-        mma_commit(saddr(&S.bars[B_KF0 + (ci & 1)]));  // fp16 K of this chunk is free
-        if (ci + 1 < nch) um_u(ci + 1);  // (after Dh_U has read delta'_U from the same columns)
-      }
-      __syncwarp();
-      if (__any_sync(0xffffffffu, aborted(S))) break;
     }
     // kEmitR, per chunk c: [D | q h] (c); O2, Dh (c); Q K^T (c + 1).  Q K^T takes Q^T (MN-major
     // A; only its 64 rows t are read out) and the record's fp16 K.
@@ -1408,31 +1123,27 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
       if (ci + 1 < nch) sqr(ci + 1);
       if (__any_sync(0xffffffffu, aborted(S))) break;
     }
-    for (int ci = 0; MODE != kSumML && MODE != kEmitR && !UM && ci < nch; ++ci) {
+    for (int ci = 0; MODE != kSumML && MODE != kEmitR && ci < nch; ++ci) {
       const uint32_t khs = saddr(S.kh[ci & 1]), vv = saddr(S.v[ci & 1]);
       // w^T = K^T T_w^T ;  u^T = V^T T_u^T; then the stage is free for the loader
-      if (MODE == kEmitT) wait_bar(S, B_RL0 + (ci & 1), (ci >> 1) & 1);
-      else wait_bar(S, B_T, ci & 1);
+      wait_bar(S, B_T, ci & 1);
       wait_bar(S, B_CV, ci & 1);
       if (leader) {
-        const uint32_t tws = MODE == kEmitT ? saddr(tstage(ci & 1)) : saddr(S.tw);
-        const uint32_t tus = MODE == kEmitT ? tws + 8192u : saddr(S.tu);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           mma_ss(tm + TM_W, sdesc(khs + ks * 2048, 8192, 1024),
-                 sdesc(tws + ks * 32, 16, 1024), ID_WU, ks > 0);
+                 sdesc(saddr(S.tw) + ks * 32, 16, 1024), ID_WU, ks > 0);
         if (MODE != kSumM) {
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             mma_ss(tm + TM_DO, sdesc(vv + ks * 2048, 8192, 1024),
-                   sdesc(tus + ks * 32, 16, 1024), ID_WU, ks > 0);
+                   sdesc(saddr(S.tu) + ks * 32, 16, 1024), ID_WU, ks > 0);
         }
         mma_commit(saddr(&S.bars[B_WU]));
-        if (MODE == kEmitT) mma_commit(saddr(&S.bars[B_RF0 + (ci & 1)]));
-        if (MODE != kEmit && MODE != kEmitT) mma_commit(saddr(&S.bars[B_F0 + (ci & 1)]));
+        if (MODE != kEmit) mma_commit(saddr(&S.bars[B_F0 + (ci & 1)]));
       }
       __syncwarp();
-      if (MODE == kEmit || MODE == kEmitT) {  // o^T = h^T q_g^T starts O; then the stage is free
+      if (MODE == kEmit) {  // o^T = h^T q_g^T starts the O accumulator; then the stage is free
         wait_bar(S, B_HR, ci & 1);
         fence_after_sync();
         if (leader) {
@@ -1447,7 +1158,7 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
       }
       // delta^T = u^T + h^T (-w)^T
       wait_bar(S, B_WR, ci & 1);
-      if (MODE != kEmit && MODE != kEmitT) wait_bar(S, B_HR, ci & 1);
+      if (MODE != kEmit) wait_bar(S, B_HR, ci & 1);
       fence_after_sync();
       if (leader) {
         const uint32_t nw = saddr(nw_tile(ci));
@@ -1466,7 +1177,7 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const uint32_t col = 32 * (ks >> 1) + 8 * (ks & 1);
-          if (MODE == kEmit || MODE == kEmitT)
+          if (MODE == kEmit)
             mma_ts(tm + TM_DO + 64, tm + TM_DO + col, sdesc(att + ks * 32, 16, 1024), ID_O2, 1);
           mma_ts(tm + TM_H, tm + TM_U + col, sdesc(khs + ks * 2048, 8192, 1024), ID_DH, ks > 0);
         }
@@ -1502,26 +1213,8 @@ __device__ __forceinline__ void chunk_body(const Args& a, const CUtensorMap* tm_
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
-    tc5_chunk_kernel(Args a, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_v) {
-  chunk_body<MODE>(a, &tm_k, &tm_q, &tm_v, blockIdx.x);
-}
-
-// Phase 1 of segments 1 .. P-2 (both summary halves) and phase 3 of segment 0 in one grid: the
-// first segment's incoming state is the known h0, so its re-emit needs no summary and runs
-// beside the others' summaries; its final state is the next segment's incoming state.
-__global__ void __launch_bounds__(kThreads, 1)
-    tc5_phase_a_kernel(Args as, Args ae, int n_sum, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_q,
-                       const __grid_constant__ CUtensorMap tm_v) {
-  if ((int)blockIdx.x < n_sum) chunk_body<kSumUMT>(as, &tm_k, &tm_q, &tm_v, blockIdx.x);
-  else chunk_body<kEmitT>(ae, &tm_k, &tm_q, &tm_v, blockIdx.x - n_sum);
-}
-
-template <int MODE>
 cudaError_t launch5(const Args& a, cudaStream_t s) {
-  const dim3 grid((unsigned)(a.N * (a.seg_n > 0 ? a.seg_n : a.P)), a.hv, 1);
+  const dim3 grid((unsigned)(a.N * a.P), a.hv, 1);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
   const size_t smem = sizeof(Smem) + 1024;
   cudaError_t e = cudaFuncSetAttribute(tc5_chunk_kernel<MODE>,
@@ -1532,7 +1225,7 @@ cudaError_t launch5(const Args& a, cudaStream_t s) {
   if ((e = make_map(&mk, empty || MODE == kSumML || MODE == kEmitR ? nullptr : a.k, a.T, a.hk)) !=
       cudaSuccess)
     return e;
-  if ((e = make_map(&mq, empty || !(MODE == kEmit || MODE == kEmitR || MODE == kEmitT) ? nullptr : a.q, a.T,
+  if ((e = make_map(&mq, empty || (MODE != kEmit && MODE != kEmitR) ? nullptr : a.q, a.T,
                     a.hk)) != cudaSuccess)
     return e;
   if ((e = make_map(&mv, empty || MODE == kSumM || MODE == kSumML || MODE == kEmitR ? nullptr : a.v,
@@ -1555,11 +1248,6 @@ size_t tc5_records_bytes(int64_t T, int N, int hv) {
 // With records (a.wy), the U half runs first and stores each chunk's -w^T, fp16 K and decay,
 // and the M half only loads them; without, each half computes its own factors.
 cudaError_t tc5_summary(const Args& a, cudaStream_t s, cudaEvent_t mid) {
-  if (a.trec) {  // both halves in one launch, from the prepared T tiles
-    cudaError_t e = launch5<kSumUMT>(a, s);
-    if (e == cudaSuccess && mid) e = cudaEventRecord(mid, s);
-    return e;
-  }
   if (a.wy) {  // the U half also runs on the last segment: phase 3 reads its records
     Args ua = a;
     ua.skip_last_summary = false;
@@ -1574,24 +1262,7 @@ cudaError_t tc5_summary(const Args& a, cudaStream_t s, cudaEvent_t mid) {
   return launch5<kSumU>(a, s);
 }
 
-cudaError_t tc5_phase_a(const Args& as, const Args& ae, cudaStream_t s) {
-  const int n_sum = as.N * as.seg_n, n_emit = ae.N * ae.seg_n;
-  const dim3 grid((unsigned)(n_sum + n_emit), as.hv, 1);
-  if (grid.x == 0 || grid.y == 0 || as.T == 0) return cudaSuccess;
-  const size_t smem = sizeof(Smem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(tc5_phase_a_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  CUtensorMap mk, mq, mv;
-  if ((e = make_map(&mk, as.k, as.T, as.hk)) != cudaSuccess) return e;
-  if ((e = make_map(&mq, ae.q, as.T, as.hk)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, as.v, as.T, as.hv)) != cudaSuccess) return e;
-  tc5_phase_a_kernel<<<grid, kThreads, smem, s>>>(as, ae, n_sum, mk, mq, mv);
-  return cudaGetLastError();
-}
-
 cudaError_t tc5_emit(const Args& a, cudaStream_t s) {
-  if (a.trec) return launch5<kEmitT>(a, s);
   return a.wy ? launch5<kEmitR>(a, s) : launch5<kEmit>(a, s);
 }
 
