@@ -276,7 +276,7 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
 
     def timed_forward(P, steps, warmup):
-        p = gdn.problem_for(d["q"], d["v"], None, P=P, path=args.path)
+        p = gdn.problem_for(d["q"], d["v"], None, P=P)
         wsb = gdn.workspace_for(p, dev)
         for _ in range(warmup):
             gdn.gdn_forward(p, d["q"], d["k"], d["v"], d["g"], d["beta"], None, None, out, hf,
@@ -311,7 +311,7 @@ def run_ours(args, ws, rank, local):
         ms = float(t.item())
 
     # per-phase times of the forward itself: CUDA events between its launches
-    p = gdn.problem_for(d["q"], d["v"], None, P=P_best, path=args.path)
+    p = gdn.problem_for(d["q"], d["v"], None, P=P_best)
     wsp = gdn.workspace_for(p, dev)
     phase_ms = {"summary": [], "scan": [], "emit": [], "summary_first": []}
     for it in range(args.warmup + args.steps):
@@ -335,7 +335,7 @@ def run_ours(args, ws, rank, local):
     hf_h = [torch.empty(hf.shape, dtype=hf.dtype).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h[0].numel() * out_h[0].element_size() + hf_h[0].numel() * hf_h[0].element_size()
-    pe = gdn.problem_for(d["q"], d["v"], None, P=P_best, path=args.path)
+    pe = gdn.problem_for(d["q"], d["v"], None, P=P_best)
     wse = gdn.workspace_for(pe, dev)
     dd = [{n: torch.empty_like(d[n]) for n in d} for _ in range(2)]
     outs = [torch.empty_like(out) for _ in range(2)]
@@ -533,12 +533,8 @@ def main():
     ap.add_argument("--mode", default="replicas", choices=["replicas", "seq"],
                     help="with several ranks: independent sequences (weak scaling) or one "
                          "sequence split by sequence over the ranks (strong scaling)")
-    ap.add_argument("--path", type=int, default=0,
-                    help="kernel family: 0 auto (tcgen05 for this workload), 2 tcgen05")
     args = ap.parse_args()
-    args.family = {0: "tcgen05 (TMEM accumulators, fp16 operands, fp32 state)",
-                   2: "tcgen05 (TMEM accumulators, fp16 operands, fp32 state)"}.get(
-                       args.path, str(args.path))
+    args.family = "tcgen05 (TMEM accumulators, fp16 operands, fp32 state)"
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_env()

@@ -18,11 +18,10 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Resolved kernel family for a problem.
+// The kernel family a problem runs on (the problem decides; there is no caller-side choice):
+// the tcgen05 tensor-core kernels cover bf16 I/O with K = V = 128.
 bool use_tensor_path(const gdn_problem* p) {
-  const bool covers = p->io_dtype == GDN_BF16 && p->k_dim == 128 && p->v_dim == 128;
-  if (p->path == GDN_PATH_SIMT) return false;
-  return covers;
+  return p->io_dtype == GDN_BF16 && p->k_dim == 128 && p->v_dim == 128;
 }
 
 // Phase 1 and phase 3 with the factors recomputed on chip (tensor-core kernels).
@@ -42,12 +41,8 @@ gdn_status check_problem(const gdn_problem* p) {
     return GDN_ERR_INVALID_ARGUMENT;
   if (p->hv % p->hk != 0) return GDN_ERR_INVALID_ARGUMENT;
   if (p->io_dtype != GDN_BF16 && p->io_dtype != GDN_F32) return GDN_ERR_UNSUPPORTED;
-  if (p->path < GDN_PATH_AUTO || p->path > GDN_PATH_TENSOR) return GDN_ERR_INVALID_ARGUMENT;
   if (p->chunk != 64) return GDN_ERR_UNSUPPORTED;
   if ((p->k_dim != 64 && p->k_dim != 128) || (p->v_dim != 64 && p->v_dim != 128))
-    return GDN_ERR_UNSUPPORTED;
-  if (p->path == GDN_PATH_TENSOR &&
-      !(p->io_dtype == GDN_BF16 && p->k_dim == 128 && p->v_dim == 128))
     return GDN_ERR_UNSUPPORTED;
   if (p->hv > 65535) return GDN_ERR_UNSUPPORTED;  // grid.y
   // grid.x of the per-segment kernels and element offsets in 64 bits

@@ -30,7 +30,6 @@ STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARGUMENT", 2: "GDN_ERR_UNSUPPOR
                 3: "GDN_ERR_WORKSPACE", 4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_TIMEOUT",
                 6: "GDN_ERR_DEVICE_INPUT", 7: "GDN_ERR_DEVICE_RANGE"}
 GDN_BF16, GDN_F32 = 0, 1
-PATH_AUTO, PATH_SIMT, PATH_TENSOR = 0, 1, 2
 EXPORTED = ("gdn_status_string", "gdn_check_problem", "gdn_workspace_size", "gdn_forward",
             "gdn_chunk_prepare", "gdn_segment_summary", "gdn_state_prefix_scan",
             "gdn_chunk_emit", "gdn_device_status", "gdn_version",
@@ -42,8 +41,7 @@ class Problem(ctypes.Structure):
     _fields_ = [("total_tokens", ctypes.c_int64), ("num_seqs", ctypes.c_int32),
                 ("hk", ctypes.c_int32), ("hv", ctypes.c_int32), ("k_dim", ctypes.c_int32),
                 ("v_dim", ctypes.c_int32), ("chunk", ctypes.c_int32),
-                ("segments_per_seq", ctypes.c_int32), ("io_dtype", ctypes.c_int32),
-                ("path", ctypes.c_int32)]
+                ("segments_per_seq", ctypes.c_int32), ("io_dtype", ctypes.c_int32)]
 
 
 class GdnError(RuntimeError):
@@ -111,19 +109,18 @@ def _check(status, where):
         raise GdnError(status, where)
 
 
-def make_problem(T, N, hk, hv, K, V, P=1, dtype=torch.bfloat16, chunk=64, path=PATH_AUTO):
+def make_problem(T, N, hk, hv, K, V, P=1, dtype=torch.bfloat16, chunk=64):
     io = {torch.bfloat16: GDN_BF16, torch.float32: GDN_F32}.get(dtype)
     if io is None:
         raise GdnError(2, f"dtype {dtype}")
-    return Problem(int(T), int(N), int(hk), int(hv), int(K), int(V), int(chunk), int(P), io,
-                   int(path))
+    return Problem(int(T), int(N), int(hk), int(hv), int(K), int(V), int(chunk), int(P), io)
 
 
-def problem_for(q, v, cu_seqlens=None, P=1, path=PATH_AUTO) -> Problem:
+def problem_for(q, v, cu_seqlens=None, P=1) -> Problem:
     T, hk, K = q.shape
     hv, V = v.shape[1], v.shape[2]
     N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
-    return make_problem(T, N, hk, hv, K, V, P, q.dtype, path=path)
+    return make_problem(T, N, hk, hv, K, V, P, q.dtype)
 
 
 def gdn_check_problem(p: Problem) -> int:
@@ -227,13 +224,13 @@ def workspace_for(p: Problem, device="cuda") -> torch.Tensor:
     return torch.empty(max(gdn_workspace_size(p), 256), dtype=torch.uint8, device=device)
 
 
-def forward(q, k, v, g, beta, h0=None, cu_seqlens=None, P=1, path=PATH_AUTO, out=None,
+def forward(q, k, v, g, beta, h0=None, cu_seqlens=None, P=1, out=None,
             h_final=None, workspace=None, want_final=True, check_status=False, stream=None):
     """out, h_final = forward(...) on CUDA tensors (layouts of include/gdn.h).
 
     ``cu_seqlens`` is an int32 CUDA tensor [N+1] or None (one sequence).  With
     ``check_status`` the device status word is read back (a synchronisation)."""
-    p = problem_for(q, v, cu_seqlens, P, path)
+    p = problem_for(q, v, cu_seqlens, P)
     N = p.num_seqs
     if out is None:
         out = torch.empty_like(v)

@@ -50,6 +50,11 @@
  *               GDN_ERR_DEVICE_INPUT in the status word, read by gdn_device_status().
  *   Supported   io dtype bf16 or fp32; K, V in {64, 128}; C = 64; hv % hk == 0; P >= 1;
  *               16-byte aligned tensor pointers.
+ *   Kernels     the problem decides, with no caller-side selection: gdn_forward and the *_fused
+ *               stage calls run on the tcgen05 tensor-core kernels for bf16 I/O with K = V = 128
+ *               and on the fp32 CUDA-core kernels otherwise; the stage calls that take the
+ *               materialised fp32 factors (gdn_chunk_prepare, gdn_segment_summary,
+ *               gdn_chunk_emit) run on the fp32 CUDA-core kernels for every I/O dtype.
  *   Precision   fp32 I/O runs on fp32 CUDA-core kernels.  bf16 I/O with K = V = 128 runs on the
  *               tensor cores: K K^T and Q K^T on the bf16 inputs as given, every later product
  *               on fp16 operands (inputs converted exactly in range), fp32 accumulation, an
@@ -82,14 +87,6 @@ typedef enum gdn_status {
 
 typedef enum gdn_dtype { GDN_BF16 = 0, GDN_F32 = 1 } gdn_dtype;
 
-/* Kernel family selection (gdn_problem.path).  AUTO picks the tcgen05 tensor-core kernels
- * when they cover the shape (bf16, K = V = 128) and the SIMT kernels otherwise. */
-typedef enum gdn_path {
-    GDN_PATH_AUTO = 0,
-    GDN_PATH_SIMT = 1,
-    GDN_PATH_TENSOR = 2
-} gdn_path;
-
 typedef struct gdn_problem {
     int64_t total_tokens;     /* T >= 0: tokens of the packed stream                     */
     int32_t num_seqs;         /* N >= 1                                                  */
@@ -98,7 +95,6 @@ typedef struct gdn_problem {
     int32_t chunk;            /* C (64)                                                  */
     int32_t segments_per_seq; /* P >= 1                                                  */
     int32_t io_dtype;         /* gdn_dtype of q, k, v and out                            */
-    int32_t path;             /* gdn_path                                                */
 } gdn_problem;
 
 /* Status text (static storage; never NULL). */

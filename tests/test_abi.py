@@ -49,7 +49,6 @@ def prob(gdn, **kw):
     (dict(), 0), (dict(P=64, T=65536), 0), (dict(N=8, P=4), 0),
     (dict(hk=3), 1), (dict(hv=0), 1), (dict(P=0), 1), (dict(N=0), 1), (dict(T=-1), 1),
     (dict(K=96), 2), (dict(V=256), 2), (dict(chunk=32), 2), (dict(K=64, V=64), 0),
-    (dict(path=2, K=64), 2), (dict(path=3), 1), (dict(path=7), 1),
 ])
 def test_check_problem(gdn, kw, status):
     p = prob(gdn, **kw)
@@ -62,9 +61,9 @@ def test_workspace_size_accounts_for_segments(gdn):
     p16 = prob(gdn, T=65536, P=16)
     per_seg = 32 * 128 * 128 * 4 * 3  # M, U, h_in
     assert gdn.gdn_workspace_size(p16) - gdn.gdn_workspace_size(p1) >= 16 * per_seg
-    simt = prob(gdn, T=65536, P=1, path=1)
-    # the SIMT path materialises w, u and gcum (fp32)
-    assert gdn.gdn_workspace_size(simt) >= 65536 * 32 * (256 * 4 + 4)
+    simt = prob(gdn, T=65536, P=1, K=64, V=64)
+    # the CUDA-core kernels (K = V = 64) materialise w, u and gcum in fp32
+    assert gdn.gdn_workspace_size(simt) >= 65536 * 32 * ((64 + 64) * 4 + 4)
 
 
 def test_entry_points_reject_bad_arguments_before_any_launch(gdn):

@@ -30,12 +30,12 @@ def test_rejects_problems_beyond_the_static_scratch(gdn):
     assert rc == 3  # GDN_ERR_WORKSPACE
 
 
-def _both(gdn, inp, P, path):
+def _both(gdn, inp, P):
     d = to_device(inp)
     cu = d["cu_seqlens"] if len(inp.lengths) > 1 else None
     ref_o, ref_h = gdn.forward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], cu, P=P,
-                               path=path, check_status=True)
-    p = gdn.problem_for(d["q"], d["v"], cu, P=P, path=path)
+                               check_status=True)
+    p = gdn.problem_for(d["q"], d["v"], cu, P=P)
     out = torch.empty_like(d["v"])
     hf = torch.empty_like(ref_h)
     gdn.gdn_forward_static_scratch(p, d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], cu,
@@ -66,7 +66,7 @@ def test_static_scratch_runs_when_only_the_minimum_fits(gdn):
     d = to_device(inp)
     p = gdn.problem_for(d["q"], d["v"], None, P=8)
     assert gdn.gdn_workspace_size(p) > 64 << 20
-    o, h, ro, rh = _both(gdn, inp, 8, path=0)
+    o, h, ro, rh = _both(gdn, inp, 8)
     check_bf16(o, h, ro, rh, tol=BF16_TOL, case="static scratch, minimum only")
 
 
@@ -77,11 +77,11 @@ def test_static_scratch_matches_workspace_entry_point_on_consecutive_calls(gdn):
     for seed, P, lengths in ((21, 2, (300, 64, 129)), (22, 5, (700,))):
         inp = inputs.custom(sum(lengths), 2, 4, 128, 128, torch.bfloat16, h0_std=0.02,
                             lengths=lengths, chunk=1, seed=seed)
-        o, h, ro, rh = _both(gdn, inp, P, path=0)
+        o, h, ro, rh = _both(gdn, inp, P)
         check_bf16(o, h, ro, rh, tol=BF16_TOL)
     # fp32 on the SIMT kernels (materialised factors live in the scratch too), twice
     for seed in (23, 24):
         inp = inputs.custom(64 * 3 + 7, 1, 2, 64, 64, torch.float32, g_kind="log_uniform",
                             h0_std=0.02, seed=seed)
-        o, h, ro, rh = _both(gdn, inp, 2, path=1)
+        o, h, ro, rh = _both(gdn, inp, 2)
         assert max_abs(o, ro) <= F32_TOL and max_abs(h, rh) <= F32_TOL
