@@ -172,7 +172,8 @@ def make_inputs(T, device, seed):
 
 def source_hash():
     h = hashlib.sha256()
-    for name in ("gdn_tc5.cu", "gdn_sm100.cuh", "gdn_common.cuh", "gdn_warp_mma.cuh"):
+    for name in ("gdn_tc5.cu", "gdn_tc5_util.cuh", "gdn_sm100.cuh", "gdn_common.cuh",
+                 "gdn_warp_mma.cuh"):
         with open(os.path.join(ROOT, "gated_delta_rule_07_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
