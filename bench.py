@@ -37,6 +37,11 @@ BYTES_PER_TOKEN = HK * KD * 2 * 2 + HV * VD * 2 * 2 + HV * 4 * 2
 # what each phase-1 kernel must read per token: k, v, g, beta (U half); k, g, beta (M half)
 SUM_U_BYTES_PER_TOKEN = HK * KD * 2 + HV * VD * 2 + HV * 4 * 2
 SUM_M_BYTES_PER_TOKEN = HK * KD * 2 + HV * 4 * 2
+# decode: requests per step, slots in the state pool, timed steps; bytes one step must move
+# (each request's fp32 state read and written once per value head, q, k, v, out, g, beta, slot)
+DEC_B, DEC_SLOTS, DEC_STEPS = 256, 256, 200
+DEC_BYTES = (DEC_B * HV * KD * VD * 4 * 2 + DEC_B * HK * KD * 2 * 2 + DEC_B * HV * VD * 2 * 2
+             + DEC_B * HV * 4 * 2 + DEC_B * 4)
 
 
 def peaks():
@@ -170,23 +175,26 @@ def make_inputs(T, device, seed):
     return inp
 
 
-def source_hash():
+TC5_SOURCES = ("gdn_tc5.cu", "gdn_tc5_util.cuh", "gdn_sm100.cuh", "gdn_common.cuh",
+               "gdn_warp_mma.cuh")
+
+
+def source_hash(names=TC5_SOURCES):
     h = hashlib.sha256()
-    for name in ("gdn_tc5.cu", "gdn_tc5_util.cuh", "gdn_sm100.cuh", "gdn_common.cuh",
-                 "gdn_warp_mma.cuh"):
+    for name in names:
         with open(os.path.join(ROOT, "gated_delta_rule_07_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def stored_traffic(kernel):
-    """DRAM bytes per token of `kernel` from the committed ncu summary, if the kernel source
-    has not changed since it was captured (else None)."""
+    """DRAM bytes per token (decode: per request) of `kernel` from the committed ncu summary,
+    if the kernel's sources have not changed since it was captured (else None)."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             d = json.load(f)
         e = d[kernel]
-        if e.get("source_sha") != source_hash():
+        if e.get("source_sha") != source_hash(tuple(e.get("sources", TC5_SOURCES))):
             return None
         return float(e["dram_bytes_per_token"])
     except (OSError, KeyError, ValueError):
@@ -389,6 +397,34 @@ def run_ours(args, ws, rank, local):
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.steps
 
+    # the decode step: one token per request over a pool of per-slot states (every step reads
+    # and writes each named slot's fp32 state once; the pool is larger than L2)
+    from gated_delta_rule_07_gb300 import inputs as inputs_mod
+    dec = inputs_mod.decode_batch(DEC_B, DEC_SLOTS, HK, HV, KD, VD, seed=rank)
+    dd_ = {n: getattr(dec, n).to(dev).contiguous() for n in ("q", "k", "v", "g", "beta", "slot",
+                                                              "state")}
+    dec_out = torch.empty_like(dd_["v"])
+    dec_st = torch.zeros(1, dtype=torch.int32, device=dev)
+    dp = gdn.decode_problem_for(dd_["q"], dd_["v"], dd_["state"])
+
+    def dec_step():
+        gdn.gdn_decode_step(dp, dd_["q"], dd_["k"], dd_["v"], dd_["g"], dd_["beta"], dd_["slot"],
+                            dd_["state"], dec_out, dec_st, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        dec_step()
+    barrier()
+    e0.record(stream)
+    for _ in range(DEC_STEPS):
+        dec_step()
+    e1.record(stream)
+    barrier()
+    dec_us = e0.elapsed_time(e1) / DEC_STEPS * 1e3
+    st = gdn.gdn_device_status(dec_st)
+    if st != 0:
+        raise gdn.GdnError(st, "decode device status")
+    del dd_
+
     if rank != 0:
         return None
     hbm, tf, tf_sus, src = peaks()
@@ -461,6 +497,19 @@ def run_ours(args, ws, rank, local):
                 "pipelining": "copies in on two streams, the forward, copies out on two more, "
                               "over two buffer sets"},
         "clocks": clk.summary(),
+        "decode": {
+            "workload": f"decode bf16 B={DEC_B} requests, pool of {DEC_SLOTS} slots, Hk={HK} "
+                        f"Hv={HV} K=V={KD}; fp32 state pool "
+                        f"{DEC_SLOTS * HV * KD * VD * 4 / 2**20:.0f} MiB (> L2)",
+            "us_per_step": dec_us, "tokens_per_s": DEC_B / (dec_us / 1e6), "steps": DEC_STEPS,
+            "gpu_launches_per_step": 1,
+            "roofline": {"kernel": "decode_kernel (one CTA per request and value head)",
+                         "bound": "hbm", "achieved": DEC_BYTES / (dec_us / 1e6) / 1e9,
+                         "peak": hbm, "unit": "GB/s",
+                         "frac": DEC_BYTES / (dec_us / 1e6) / 1e9 / hbm, "peak_source": src,
+                         "algorithmic_bytes_per_launch": DEC_BYTES,
+                         "traffic": (None if stored_traffic("decode") is None
+                                     else stored_traffic("decode") * DEC_B)}},
     }
     if not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.cpu_seconds, inp=inp)

@@ -400,6 +400,50 @@ gdn_status gdn_chunk_emit_fused(const gdn_problem* p, const void* q, const void*
   return to_status(fused_emit(p, a, stream));
 }
 
+gdn_status gdn_check_decode_problem(const gdn_decode_problem* p) {
+  if (!p) return GDN_ERR_INVALID_ARGUMENT;
+  if (p->batch < 0 || p->slots < 1 || p->hk < 1 || p->hv < 1 || p->k_dim < 1 || p->v_dim < 1)
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (p->hv % p->hk != 0) return GDN_ERR_INVALID_ARGUMENT;
+  if (p->io_dtype != GDN_BF16 && p->io_dtype != GDN_F32) return GDN_ERR_UNSUPPORTED;
+  if ((p->k_dim != 64 && p->k_dim != 128) || (p->v_dim != 64 && p->v_dim != 128))
+    return GDN_ERR_UNSUPPORTED;
+  if (p->hv > 65535) return GDN_ERR_UNSUPPORTED;  // grid.y
+  return GDN_OK;
+}
+
+gdn_status gdn_decode_step(const gdn_decode_problem* p, const void* q, const void* k,
+                           const void* v, const float* g, const float* beta,
+                           const int32_t* slot, float* state, void* out, int32_t* dev_status,
+                           cudaStream_t stream) {
+  gdn_status st = gdn_check_decode_problem(p);
+  if (st != GDN_OK) return st;
+  if (p->batch == 0) return GDN_OK;
+  if (!q || !k || !v || !g || !beta || !slot || !state || !out) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(beta) ||
+      !aligned16(slot) || !aligned16(state) || !aligned16(out))
+    return GDN_ERR_INVALID_ARGUMENT;
+  gdn::DecodeArgs a;
+  memset(&a, 0, sizeof(a));
+  a.batch = p->batch;
+  a.slots = p->slots;
+  a.hk = p->hk;
+  a.hv = p->hv;
+  a.K = p->k_dim;
+  a.V = p->v_dim;
+  a.bf16 = p->io_dtype == GDN_BF16;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.slot = slot;
+  a.state = state;
+  a.out = out;
+  a.status = dev_status;
+  return to_status(gdn::decode_step(a, stream));
+}
+
 gdn_status gdn_device_status(const void* status_word, int reset, cudaStream_t stream) {
   if (!status_word) return GDN_ERR_INVALID_ARGUMENT;
   int32_t host = 0;

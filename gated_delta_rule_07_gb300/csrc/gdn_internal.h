@@ -56,4 +56,17 @@ size_t tc5_records_bytes(int64_t T, int N, int hv);
 cudaError_t tc5_summary(const Args& a, cudaStream_t s, cudaEvent_t mid = nullptr);
 cudaError_t tc5_emit(const Args& a, cudaStream_t s);
 
+// One decode step over a pool of per-slot states (gdn_decode_step).
+struct DecodeArgs {
+  int batch, slots, hk, hv, K, V;
+  bool bf16;
+  const void *q, *k, *v;
+  const float *g, *beta;
+  const int32_t* slot;
+  float* state;
+  void* out;
+  int32_t* status;
+};
+cudaError_t decode_step(const DecodeArgs& a, cudaStream_t s);
+
 }  // namespace gdn

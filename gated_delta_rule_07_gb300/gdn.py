@@ -34,7 +34,8 @@ EXPORTED = ("gdn_status_string", "gdn_check_problem", "gdn_workspace_size", "gdn
             "gdn_chunk_prepare", "gdn_segment_summary", "gdn_state_prefix_scan",
             "gdn_chunk_emit", "gdn_device_status", "gdn_version",
             "gdn_segment_summary_fused", "gdn_chunk_emit_fused", "gdn_last_error_string",
-            "gdn_forward_static_scratch", "gdn_forward_timed", "gdn_forward_with_limits")
+            "gdn_forward_static_scratch", "gdn_forward_timed", "gdn_forward_with_limits",
+            "gdn_check_decode_problem", "gdn_decode_step")
 
 
 class Problem(ctypes.Structure):
@@ -42,6 +43,12 @@ class Problem(ctypes.Structure):
                 ("hk", ctypes.c_int32), ("hv", ctypes.c_int32), ("k_dim", ctypes.c_int32),
                 ("v_dim", ctypes.c_int32), ("chunk", ctypes.c_int32),
                 ("segments_per_seq", ctypes.c_int32), ("io_dtype", ctypes.c_int32)]
+
+
+class DecodeProblem(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("slots", ctypes.c_int32), ("hk", ctypes.c_int32),
+                ("hv", ctypes.c_int32), ("k_dim", ctypes.c_int32), ("v_dim", ctypes.c_int32),
+                ("io_dtype", ctypes.c_int32)]
 
 
 class GdnError(RuntimeError):
@@ -77,6 +84,9 @@ _lib.gdn_segment_summary_fused.argtypes = [_pp, _vp, _vp, _fp, _fp, _ip, _fp, _f
                                            _ip, _vp]
 _lib.gdn_chunk_emit_fused.argtypes = [_pp, _vp, _vp, _vp, _fp, _fp, _fp, _ip, _vp, _fp, _ip, _vp]
 _lib.gdn_forward_static_scratch.argtypes = [_pp, _vp, _vp, _vp, _fp, _fp, _fp, _ip, _vp, _fp, _vp]
+_dpp = ctypes.POINTER(DecodeProblem)
+_lib.gdn_check_decode_problem.argtypes = [_dpp]
+_lib.gdn_decode_step.argtypes = [_dpp, _vp, _vp, _vp, _fp, _fp, _ip, _fp, _vp, _ip, _vp]
 for _n in EXPORTED:
     if _n not in ("gdn_status_string", "gdn_workspace_size", "gdn_last_error_string"):
         getattr(_lib, _n).restype = ctypes.c_int
@@ -211,6 +221,41 @@ def gdn_chunk_emit_fused(p, q, k, v, g, beta, h_in, cu_seqlens, out, h_final, de
                                      _ptr(beta), _ptr(h_in), _ptr(cu_seqlens), _ptr(out),
                                      _ptr(h_final), _ptr(dev_status), _stream(stream)),
            "gdn_chunk_emit_fused")
+
+
+def make_decode_problem(B, slots, hk, hv, K, V, dtype=torch.bfloat16) -> DecodeProblem:
+    io = {torch.bfloat16: GDN_BF16, torch.float32: GDN_F32}.get(dtype)
+    if io is None:
+        raise GdnError(2, f"dtype {dtype}")
+    return DecodeProblem(int(B), int(slots), int(hk), int(hv), int(K), int(V), io)
+
+
+def decode_problem_for(q, v, state) -> DecodeProblem:
+    B, hk, K = q.shape
+    return make_decode_problem(B, state.shape[0], hk, v.shape[1], K, v.shape[2], q.dtype)
+
+
+def gdn_check_decode_problem(p: DecodeProblem) -> int:
+    return _lib.gdn_check_decode_problem(ctypes.byref(p))
+
+
+def gdn_decode_step(p, q, k, v, g, beta, slot, state, out, dev_status=None, stream=None):
+    _check(_lib.gdn_decode_step(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                _ptr(slot), _ptr(state), _ptr(out), _ptr(dev_status),
+                                _stream(stream)), "gdn_decode_step")
+
+
+def decode(q, k, v, g, beta, slot, state, out=None, check_status=False, stream=None):
+    """One decode step: row b continues the request held in state[slot[b]] (updated in place).
+    Returns out [B, hv, V]; with check_status, waits and raises on a device-side error."""
+    p = decode_problem_for(q, v, state)
+    if out is None:
+        out = torch.empty_like(v)
+    st = torch.zeros(1, dtype=torch.int32, device=q.device) if check_status else None
+    gdn_decode_step(p, q, k, v, g, beta, slot, state, out, st, stream)
+    if check_status:
+        _check(gdn_device_status(st, reset=True, stream=stream), "gdn_decode_step (device status)")
+    return out
 
 
 def gdn_device_status(status_word, reset=True, stream=None) -> int:

@@ -146,3 +146,40 @@ def custom(T, hk, hv, K, V, dtype=torch.float32, g_kind="softplus", h0_std=0.0, 
                   lengths=tuple(lengths) if lengths is not None else None,
                   n_seqs=len(lengths) if lengths is not None else 1, seed=seed)
     return make(wl)
+
+
+@dataclasses.dataclass
+class DecodeInputs:
+    q: torch.Tensor       # [B, hk, K] io dtype
+    k: torch.Tensor       # [B, hk, K]
+    v: torch.Tensor       # [B, hv, V]
+    g: torch.Tensor       # [B, hv] fp32
+    beta: torch.Tensor    # [B, hv] fp32
+    slot: torch.Tensor    # int32 [B]; -1 marks a padding row
+    state: torch.Tensor   # fp32 [slots, hv, K, V]
+
+
+def decode_batch(B, slots, hk=16, hv=32, K=128, V=128, dtype=torch.bfloat16, pad_rows=0,
+                 state_std=0.12, seed=0) -> DecodeInputs:
+    """One decode step's inputs.  Draw order: the rows' slots (distinct, a random subset of
+    the pool; the last pad_rows rows are padding with slot -1 and q = k = v = 0), then q, k,
+    v, g, beta with the forward recipe (g = -softplus(N(0, 1)) * 0.1), then the pool's states
+    ~ N(0, state_std^2) in fp32 (0.12 is the rms of the state a 512-token prefill with this
+    recipe leaves)."""
+    if B - pad_rows > slots or pad_rows > B:
+        raise ValueError("more live rows than slots")
+    gen = torch.Generator().manual_seed(seed)
+    live = torch.randperm(slots, generator=gen)[:B - pad_rows]
+    slot = torch.cat([live, -torch.ones(pad_rows, dtype=torch.long)]).to(torch.int32)
+    q = _l2norm(torch.randn(B, hk, K, generator=gen))
+    k = _l2norm(torch.randn(B, hk, K, generator=gen))
+    v = torch.randn(B, hv, V, generator=gen)
+    g = -torch.nn.functional.softplus(torch.randn(B, hv, generator=gen)) * 0.1
+    beta = torch.sigmoid(torch.randn(B, hv, generator=gen))
+    state = torch.randn(slots, hv, K, V, generator=gen) * state_std
+    if pad_rows:
+        q[B - pad_rows:] = 0
+        k[B - pad_rows:] = 0
+        v[B - pad_rows:] = 0
+    return DecodeInputs(q.to(dtype), k.to(dtype), v.to(dtype), g.float().contiguous(),
+                        beta.float().contiguous(), slot, state.float().contiguous())

@@ -240,6 +240,45 @@ gdn_status gdn_forward_static_scratch(const gdn_problem* p, const void* q, const
                                       const float* h0, const int32_t* cu_seqlens, void* out,
                                       float* h_final, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------------------- */
+/* Decode: one token per request over a pool of per-slot recurrent states.                   */
+
+typedef struct gdn_decode_problem {
+    int32_t batch;            /* B >= 0 rows (requests), one token each                     */
+    int32_t slots;            /* S >= 1 states in the pool                                  */
+    int32_t hk, hv;           /* key heads, value heads (hv % hk == 0)                      */
+    int32_t k_dim, v_dim;     /* K, V in {64, 128}                                          */
+    int32_t io_dtype;         /* gdn_dtype of q, k, v and out                               */
+} gdn_decode_problem;
+
+/* Checks a decode problem description on the host (no device work). */
+gdn_status gdn_check_decode_problem(const gdn_decode_problem* p);
+
+/* One decode step (page "RFC(qwen35): TP Phase2": section "Execution Contract" -- the decode
+ * kernels run against the head and state shapes and update only request-local recurrent
+ * state; section "Partition Contract" -- the state is [Hv, K, V] f32 per request; section
+ * "Request-State Lifecycle" -- requests live in slots that are reused).  Row b is the next
+ * token of the request whose state is state[slot[b]]; per value head j (key head
+ * j / (hv / hk)), with h that state:
+ *     h <- exp(g) (I - beta k k^T) h + beta k v^T,     out = h^T q
+ * -- the token recurrence of gdn_forward, one token long, continuing from the slot's state.
+ *   q, k        [B, hk, K] io dtype          v, out   [B, hv, V] io dtype
+ *   g, beta     [B, hv] fp32                 state    [S, hv, K, V] fp32, updated in place
+ *   slot        device int32 [B]: the state slot of each row.  A negative entry marks a
+ *               padding row: its out row is set to 0 and no state is read or written.
+ *   dev_status  device int32 status word, or NULL
+ * Slots are checked on the device: a row whose slot is >= S, or is named by another row too,
+ * is skipped (its state and out row are left untouched) and GDN_ERR_DEVICE_INPUT is recorded in
+ * dev_status; the other rows are computed.  A slot is started from a prefill by passing
+ * state + slot * hv * K * V as gdn_forward's h_final (one sequence), or from zero by clearing
+ * it; nothing of a previous request survives either.  All tensor pointers 16-byte aligned.
+ * Runs on fp32 CUDA-core arithmetic (the step is bound by the state's HBM traffic: 2 * 4 * K * V
+ * bytes per row and value head).  Returns GDN_OK once the work is enqueued. */
+gdn_status gdn_decode_step(const gdn_decode_problem* p, const void* q, const void* k,
+                           const void* v, const float* g, const float* beta,
+                           const int32_t* slot, float* state, void* out, int32_t* dev_status,
+                           cudaStream_t stream);
+
 /* Text of the last CUDA error that made an entry point return GDN_ERR_CUDA on the calling
  * host thread ("no CUDA error" when there was none).  Static storage. */
 const char* gdn_last_error_string(void);

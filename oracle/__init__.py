@@ -160,6 +160,31 @@ def token(q, k, v, g, beta, h0=None, cu_seqlens=None, nthreads=None):
     return out, hf
 
 
+def decode(q, k, v, g, beta, state, slot, nthreads=None):
+    """One decode step over a pool of per-slot states ("RFC(qwen35): TP Phase2", sections
+    "Execution Contract" -- decode updates only the request's own recurrent state -- and
+    "Request-State Lifecycle" -- requests live in reusable slots).  Row b continues the request
+    whose state is state[slot[b]] by one token of the recurrence: ``token`` on a one-token
+    sequence per row, with that state as h0.  A negative slot is a padding row (output 0, no
+    state).  Slots must be distinct and in range (ValueError otherwise).  Returns
+    (out [B, hv, V], new_state [S, hv, K, V]) in fp64; `state` itself is not modified."""
+    q, k, v, g, beta, state = map(_f64, (q, k, v, g, beta, state))
+    slot = np.asarray(slot, dtype=np.int64)
+    B, hv, V = v.shape
+    live = np.nonzero(slot >= 0)[0]
+    sl = slot[live]
+    if np.any(sl >= state.shape[0]) or len(set(sl.tolist())) != len(sl):
+        raise ValueError("slots must be distinct and below the pool size")
+    out = np.zeros((B, hv, V))
+    new_state = state.copy()
+    if len(live):
+        o, hf = token(q[live], k[live], v[live], g[live], beta[live], state[sl],
+                      np.arange(len(live) + 1, dtype=np.int64), nthreads=nthreads)
+        out[live] = o
+        new_state[sl] = hf
+    return out, new_state
+
+
 def chunk_factors(kc, vc, gc, bc):
     """WY/UT factors of one chunk of L rows: dict of G, A, T, w, u, ktilde, gamma."""
     kc, vc, gc, bc = map(_f64, (kc, vc, gc, bc))

@@ -126,3 +126,40 @@ def test_forward_with_limits_rejects_bad_limits_on_the_host(gdn):
                                               None, None, fake, None, fake, 1 << 30, None, wc,
                                               fault)
         assert rc == 1
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(), 0), (dict(B=0), 0), (dict(K=64, V=64), 0), (dict(K=128, V=64), 0),
+    (dict(B=-1), 1), (dict(slots=0), 1), (dict(hk=3), 1), (dict(hv=0), 1),
+    (dict(K=96), 2), (dict(V=32), 2), (dict(dtype=None), 2),
+])
+def test_check_decode_problem(gdn, kw, status):
+    base = dict(B=64, slots=128, hk=16, hv=32, K=128, V=128)
+    dtype = kw.pop("dtype", "bf16")
+    base.update(kw)
+    if dtype is None:  # an io dtype outside gdn_dtype
+        p = gdn.DecodeProblem(base["B"], base["slots"], base["hk"], base["hv"], base["K"],
+                              base["V"], 9)
+    else:
+        p = gdn.make_decode_problem(**base)
+    assert gdn.gdn_check_decode_problem(p) == status
+
+
+def test_decode_step_rejects_bad_arguments_before_any_launch(gdn):
+    p = gdn.make_decode_problem(8, 16, 16, 32, 128, 128)
+    fake = 1 << 20
+    L = gdn._lib
+    by = ctypes.byref
+    # null slot table, null state, misaligned q, bad problem
+    assert L.gdn_decode_step(by(p), fake, fake, fake, fake, fake, None, fake, fake, None,
+                             None) == 1
+    assert L.gdn_decode_step(by(p), fake, fake, fake, fake, fake, fake, None, fake, None,
+                             None) == 1
+    assert L.gdn_decode_step(by(p), fake + 4, fake, fake, fake, fake, fake, fake, fake, None,
+                             None) == 1
+    assert L.gdn_decode_step(None, fake, fake, fake, fake, fake, fake, fake, fake, None,
+                             None) == 1
+    # an empty batch is a no-op, whatever the pointers
+    p0 = gdn.make_decode_problem(0, 16, 16, 32, 128, 128)
+    assert L.gdn_decode_step(by(p0), None, None, None, None, None, None, None, None, None,
+                             None) == 0

@@ -412,3 +412,54 @@ def test_oracle_rejects_bad_geometry():
         oracle.token(**dict(p, cu_seqlens=[0, 10]))          # cu[N] != T
     with pytest.raises(ValueError):
         oracle.token(**dict(p, cu_seqlens=[0, 30, 20, 40]))  # decreasing
+
+
+# ------------------------------------------------------------------------ decode over slots
+
+def test_decode_steps_over_a_slot_pool_equal_the_recurrence():
+    """Three requests in a pool of five slots, decoded token by token in an interleaved order
+    with padding rows, equal the dense recurrence of each request's own sequence; the slots
+    no request uses keep their states ("RFC(qwen35): TP Phase2", "Request-State
+    Lifecycle": one request's state is never touched by another's work)."""
+    rng = np.random.default_rng(11)
+    hk, hv, K, V, S = 1, 2, 4, 3, 5
+    lengths = [4, 6, 3]
+    home = [3, 0, 4]  # slot of each request
+    seqs = [rand_problem(20 + i, T=L, hk=hk, hv=hv, K=K, V=V) for i, L in enumerate(lengths)]
+    state = rng.standard_normal((S, hv, K, V))
+    start = state.copy()
+    for i, sl in enumerate(home):
+        state[sl] = seqs[i]["h0"][0]
+    pos = [0, 0, 0]
+    outs = [np.zeros((L, hv, V)) for L in lengths]
+    while any(pos[i] < lengths[i] for i in range(3)):
+        rows = [i for i in range(3) if pos[i] < lengths[i] and rng.random() < 0.7]
+        if not rows:
+            continue
+        order = list(rng.permutation(rows))
+        pad = int(rng.integers(0, 2))
+        B = len(order) + pad
+        q = np.zeros((B, hk, K)); k = np.zeros((B, hk, K)); v = np.zeros((B, hv, V))
+        g = np.zeros((B, hv)); beta = np.zeros((B, hv)); slot = -np.ones(B, dtype=np.int64)
+        for b, i in enumerate(order):
+            t = pos[i]
+            q[b], k[b], v[b] = seqs[i]["q"][t], seqs[i]["k"][t], seqs[i]["v"][t]
+            g[b], beta[b], slot[b] = seqs[i]["g"][t], seqs[i]["beta"][t], home[i]
+        o, state = oracle.decode(q, k, v, g, beta, state, slot)
+        for b, i in enumerate(order):
+            outs[i][pos[i]] = o[b]
+            pos[i] += 1
+        assert np.all(o[len(order):] == 0)  # padding rows
+    for i, sl in enumerate(home):
+        ref_o, ref_h = dense_reference(**seqs[i])
+        assert maxdiff(outs[i], ref_o) < 1e-12 and maxdiff(state[sl], ref_h[0]) < 1e-12
+    for sl in set(range(S)) - set(home):
+        assert np.array_equal(state[sl], start[sl])
+
+
+def test_decode_rejects_shared_or_out_of_range_slots():
+    z = lambda *s: np.zeros(s)
+    with pytest.raises(ValueError):
+        oracle.decode(z(2, 1, 4), z(2, 1, 4), z(2, 1, 4), z(2, 1), z(2, 1), z(3, 1, 4, 4), [1, 1])
+    with pytest.raises(ValueError):
+        oracle.decode(z(1, 1, 4), z(1, 1, 4), z(1, 1, 4), z(1, 1), z(1, 1), z(3, 1, 4, 4), [3])
