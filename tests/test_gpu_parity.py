@@ -79,16 +79,21 @@ def test_other_head_dims_simt(gdn, KV):
 
 # ------------------------------------------------------------------ stage entry points
 
-def test_stage_entry_points_match_oracle_stages(gdn):
-    inp = inputs.custom(64 * 4 + 9, 1, 2, 64, 64, torch.float32, g_kind="log_uniform",
+@pytest.mark.parametrize("dtype,KV", [(torch.float32, 64), (torch.bfloat16, 128)],
+                         ids=["fp32-K64", "bf16-K128"])
+def test_stage_entry_points_match_oracle_stages(gdn, dtype, KV):
+    """The materialising stage calls (prepare -> summary -> scan -> emit, fp32 factors in HBM)
+    against the oracle's stages, for fp32 I/O and for the headline geometry's bf16 I/O with
+    K = V = 128 (the same inputs, rounded to bf16, feed both sides)."""
+    inp = inputs.custom(64 * 4 + 9, 1, 2, KV, KV, dtype, g_kind="log_uniform",
                         h0_std=0.05, seed=5, lengths=(120, 153))
     P = 2
     d = to_device(inp)
     p = gdn.problem_for(d["q"], d["v"], d["cu_seqlens"], P=P)
     T, hv = inp.v.shape[0], inp.v.shape[1]
     dev = "cuda"
-    w = torch.empty(T, hv, 64, device=dev)  # fp32
-    u = torch.empty(T, hv, 64, device=dev)
+    w = torch.empty(T, hv, KV, device=dev)  # fp32
+    u = torch.empty(T, hv, KV, device=dev)
     gcum = torch.empty(T, hv, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     gdn.gdn_chunk_prepare(p, d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], w, u, gcum, st)
@@ -97,14 +102,14 @@ def test_stage_entry_points_match_oracle_stages(gdn):
     assert max_abs(to_np(w), rw) < 1e-4 and max_abs(to_np(u), ru) < 1e-4
     assert max_abs(to_np(gcum), rg) < 1e-5
     S = 2 * P
-    M = torch.empty(S, hv, 64, 64, device=dev)
-    U = torch.empty(S, hv, 64, 64, device=dev)
+    M = torch.empty(S, hv, KV, KV, device=dev)
+    U = torch.empty(S, hv, KV, KV, device=dev)
     gdn.gdn_segment_summary(p, d["k"], w, u, gcum, d["cu_seqlens"], M, U, st)
     rM, rU = oracle.summary(inp.k, inp.v, inp.g, inp.beta, inp.cu_seqlens, C=64, P=P)
     torch.cuda.synchronize()
     assert max_abs(to_np(M), rM) < 1e-4 and max_abs(to_np(U), rU) < 1e-4
-    h_in = torch.empty(S, hv, 64, 64, device=dev)
-    hf = torch.empty(2, hv, 64, 64, device=dev)
+    h_in = torch.empty(S, hv, KV, KV, device=dev)
+    hf = torch.empty(2, hv, KV, KV, device=dev)
     gdn.gdn_state_prefix_scan(p, M, U, d["h0"], h_in, hf)
     rh_in, rhf = oracle.scan(rM, rU, inp.h0, N=2, P=P)
     torch.cuda.synchronize()
@@ -114,7 +119,11 @@ def test_stage_entry_points_match_oracle_stages(gdn):
     gdn.gdn_chunk_emit(p, d["q"], d["k"], w, u, gcum, h_in, d["cu_seqlens"], out, hf2, st)
     ro = oracle.emit(inp.q, inp.k, inp.v, inp.g, inp.beta, rh_in, inp.cu_seqlens, C=64, P=P)
     torch.cuda.synchronize()
-    assert max_abs(to_np(out), ro) < F32_TOL and max_abs(to_np(hf2), rhf) < F32_TOL
+    if dtype == torch.float32:
+        check_f32("out", to_np(out), ro, case="stage calls fp32 K=64")
+        check_f32("h_final", to_np(hf2), rhf, case="stage calls fp32 K=64")
+    else:
+        check_bf16(to_np(out), to_np(hf2), ro, rhf, case="stage calls bf16 K=128")
     assert gdn.gdn_device_status(st) == 0
 
 
