@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the gated delta rule forward -- TEST INFRASTRUCTURE.
+"""fp64 CPU oracle for the gated delta rule forward and its reverse mode -- TEST
+INFRASTRUCTURE.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
 import this package.  The CUDA library never imports, links or calls it, and it imports
@@ -67,9 +68,12 @@ def _declare(lib):
     lib.gdn_oracle_emit.argtypes = [d, d, d, d, d, d, i64, i, _i64p, i, i, i, i, i, i, i, d]
     lib.gdn_oracle_segmented.argtypes = [d, d, d, d, d, d, i64, i, _i64p, i, i, i, i, i, i, i,
                                          d, d]
+    lib.gdn_oracle_token_backward.argtypes = [d, d, d, d, d, d, d, d, i64, i, _i64p, i, i, i, i,
+                                              i, d, d, d, d, d, d]
     for name in ("gdn_oracle_token", "gdn_oracle_chunk_factors", "gdn_oracle_prepare",
                  "gdn_oracle_chunked", "gdn_oracle_summary", "gdn_oracle_dense_transition",
-                 "gdn_oracle_scan", "gdn_oracle_emit", "gdn_oracle_segmented"):
+                 "gdn_oracle_scan", "gdn_oracle_emit", "gdn_oracle_segmented",
+                 "gdn_oracle_token_backward"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -158,6 +162,28 @@ def token(q, k, v, g, beta, h0=None, cu_seqlens=None, nthreads=None):
                                  _threads(nthreads), _ptr(out), _ptr(hf))
     _check(rc, "token")
     return out, hf
+
+
+def token_backward(q, k, v, g, beta, dout, h0=None, dh_final=None, cu_seqlens=None,
+                   nthreads=None):
+    """Reverse mode of the per-token recurrence: the gradients of
+    L = <dout, out> + <dh_final, h_final> with respect to q, k, v, g, beta and h0, in fp64.
+    The pages state no backward formulas; this follows from the recurrence alone (the
+    derivation is in gdn_oracle.c, section 7).  Returns a dict of dq, dk [T, hk, K],
+    dv [T, hv, V], dg, dbeta [T, hv] and dh0 [N, hv, K, V]."""
+    q, k, v, g, beta, dout, h0, dh_final = map(_f64, (q, k, v, g, beta, dout, h0, dh_final))
+    p = Problem(q, k, v, g, beta, cu_seqlens)
+    assert dout.shape == v.shape
+    r = {"dq": np.zeros((p.T, p.hk, p.K)), "dk": np.zeros((p.T, p.hk, p.K)),
+         "dv": np.zeros((p.T, p.hv, p.V)), "dg": np.zeros((p.T, p.hv)),
+         "dbeta": np.zeros((p.T, p.hv)), "dh0": np.zeros((p.N, p.hv, p.K, p.V))}
+    rc = load().gdn_oracle_token_backward(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0), _ptr(dout), _ptr(dh_final),
+        p.T, p.N, p.cu.ctypes.data_as(_i64p), p.hk, p.hv, p.K, p.V, _threads(nthreads),
+        _ptr(r["dq"]), _ptr(r["dk"]), _ptr(r["dv"]), _ptr(r["dg"]), _ptr(r["dbeta"]),
+        _ptr(r["dh0"]))
+    _check(rc, "token_backward")
+    return r
 
 
 def decode(q, k, v, g, beta, state, slot, nthreads=None):

@@ -1,5 +1,5 @@
 /*
- * gdn_oracle.c -- fp64 CPU oracle for the gated delta rule (GDN) forward.
+ * gdn_oracle.c -- fp64 CPU oracle for the gated delta rule (GDN) forward and its reverse mode.
  *
  * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the tests, the smoke check and the
  * benchmark's CPU-baseline leg may load or call this file.  It shares no code, header,
@@ -650,4 +650,157 @@ int gdn_oracle_segmented(const double* q, const double* k, const double* v, cons
     free(U);
     free(h_in);
     return rc;
+}
+
+/* --------------------------------------- 7. reverse mode of the per-token recurrence */
+
+/* Gradients of L = <dout, out> + <dh_final, h_final> with respect to q, k, v, g, beta and
+ * h0, by reverse mode through the token recurrence of section 1 (the plain definition; the
+ * pages state no backward formulas, and this one follows from the recurrence alone).  Per
+ * token, with h_prev the state before it, h its state after, F = dL/dh (the gradient from
+ * later tokens plus q dout^T), alpha = exp(g), P = h_prev^T k, delta = beta (v - alpha P):
+ *     dq = h dout                    dd = F^T k (dL/d delta)
+ *     dv = beta dd                   dbeta = dd . (v - alpha P)
+ *     dk = F delta - alpha beta h_prev dd
+ *     dg = alpha (<F, h_prev> - beta dd . P)
+ *     dh_prev = alpha (F - beta k dd^T)
+ * States are recomputed from a checkpoint every 64 tokens.  One work item = (sequence n,
+ * key head kh): its value heads run in turn, so dq and dk of a key head (summed over the
+ * value heads that read it) have a single writer.
+ * Layouts: dout [T, hv, V]; dh_final, dh0 [N, hv, K, V] (dh_final may be NULL = zeros);
+ * dq, dk [T, hk, K]; dv [T, hv, V]; dg, dbeta [T, hv]; dh0 may be NULL. */
+typedef struct {
+    const double *q, *k, *v, *g, *beta, *h0, *dout, *dhf;
+    const int64_t* cu;
+    int N, hk, hv, K, V;
+    double *dq, *dk, *dv, *dg, *dbeta, *dh0;
+} bwd_ctx;
+
+enum { kBwdBlock = 64 };
+
+/* one token of the recurrence: h <- alpha h + k delta^T (delta, P returned) */
+static void bwd_step(int K, int V, double* h, const double* kt, const double* vt, double alpha,
+                     double b, double* P, double* delta) {
+    for (int c = 0; c < V; ++c) P[c] = 0.0;
+    for (int i = 0; i < K; ++i)
+        for (int c = 0; c < V; ++c) P[c] += h[(size_t)i * V + c] * kt[i];
+    for (int c = 0; c < V; ++c) delta[c] = b * (vt[c] - alpha * P[c]);
+    for (int i = 0; i < K; ++i)
+        for (int c = 0; c < V; ++c) h[(size_t)i * V + c] = alpha * h[(size_t)i * V + c] + kt[i] * delta[c];
+}
+
+static void bwd_item(void* vctx, int64_t item) {
+    const bwd_ctx* c = (const bwd_ctx*)vctx;
+    const int K = c->K, V = c->V, hk = c->hk, hv = c->hv, grp = hv / hk;
+    const int kh = (int)(item % hk);
+    const int n = (int)(item / hk);
+    const int64_t t0 = c->cu[n], t1 = c->cu[n + 1], L = t1 - t0;
+    const int64_t nblk = (L + kBwdBlock - 1) / kBwdBlock;
+    const size_t KV = (size_t)K * V;
+    double* ck = (double*)malloc(sizeof(double) * KV * (size_t)(nblk > 0 ? nblk : 1));
+    double* hs = (double*)malloc(sizeof(double) * KV * (kBwdBlock + 1));
+    double* F = (double*)malloc(sizeof(double) * KV);
+    double* P = (double*)malloc(sizeof(double) * V);
+    double* delta = (double*)malloc(sizeof(double) * V);
+    double* dd = (double*)malloc(sizeof(double) * V);
+    for (int64_t t = t0; t < t1; ++t)
+        for (int i = 0; i < K; ++i) {
+            c->dq[((size_t)t * hk + kh) * K + i] = 0.0;
+            c->dk[((size_t)t * hk + kh) * K + i] = 0.0;
+        }
+    for (int jj = 0; jj < grp; ++jj) {
+        const int j = kh * grp + jj;
+        /* forward: the state entering every block */
+        double* h = hs;
+        for (size_t e = 0; e < KV; ++e) h[e] = c->h0 ? c->h0[((size_t)n * hv + j) * KV + e] : 0.0;
+        for (int64_t t = t0; t < t1; ++t) {
+            if ((t - t0) % kBwdBlock == 0) memcpy(ck + (size_t)((t - t0) / kBwdBlock) * KV, h, sizeof(double) * KV);
+            bwd_step(K, V, h, c->k + ((size_t)t * hk + kh) * K, c->v + ((size_t)t * hv + j) * V,
+                     exp(c->g[(size_t)t * hv + j]), c->beta[(size_t)t * hv + j], P, delta);
+        }
+        /* backward, block by block from the end */
+        for (size_t e = 0; e < KV; ++e) F[e] = c->dhf ? c->dhf[((size_t)n * hv + j) * KV + e] : 0.0;
+        for (int64_t bi = nblk - 1; bi >= 0; --bi) {
+            const int64_t b0 = t0 + bi * kBwdBlock;
+            const int64_t b1 = (b0 + kBwdBlock < t1) ? b0 + kBwdBlock : t1;
+            memcpy(hs, ck + (size_t)bi * KV, sizeof(double) * KV);
+            for (int64_t t = b0; t < b1; ++t) {  /* hs[i] = state before token b0 + i */
+                memcpy(hs + (size_t)(t - b0 + 1) * KV, hs + (size_t)(t - b0) * KV, sizeof(double) * KV);
+                bwd_step(K, V, hs + (size_t)(t - b0 + 1) * KV, c->k + ((size_t)t * hk + kh) * K,
+                         c->v + ((size_t)t * hv + j) * V, exp(c->g[(size_t)t * hv + j]),
+                         c->beta[(size_t)t * hv + j], P, delta);
+            }
+            for (int64_t t = b1 - 1; t >= b0; --t) {
+                const double* hp = hs + (size_t)(t - b0) * KV;      /* before token t */
+                const double* ha = hs + (size_t)(t - b0 + 1) * KV;  /* after token t */
+                const double* kt = c->k + ((size_t)t * hk + kh) * K;
+                const double* qt = c->q + ((size_t)t * hk + kh) * K;
+                const double* vt = c->v + ((size_t)t * hv + j) * V;
+                const double* ot = c->dout + ((size_t)t * hv + j) * V;
+                const double alpha = exp(c->g[(size_t)t * hv + j]);
+                const double b = c->beta[(size_t)t * hv + j];
+                double* dqt = c->dq + ((size_t)t * hk + kh) * K;
+                double* dkt = c->dk + ((size_t)t * hk + kh) * K;
+                /* F = dL/dh_t: the later tokens' gradient plus this token's output */
+                for (int i = 0; i < K; ++i)
+                    for (int cc = 0; cc < V; ++cc) F[(size_t)i * V + cc] += qt[i] * ot[cc];
+                /* dq = h_t dout */
+                for (int i = 0; i < K; ++i) {
+                    double s = 0.0;
+                    for (int cc = 0; cc < V; ++cc) s += ha[(size_t)i * V + cc] * ot[cc];
+                    dqt[i] += s;
+                }
+                /* P = h_prev^T k, delta, dd = F^T k */
+                for (int cc = 0; cc < V; ++cc) { P[cc] = 0.0; dd[cc] = 0.0; }
+                for (int i = 0; i < K; ++i)
+                    for (int cc = 0; cc < V; ++cc) {
+                        P[cc] += hp[(size_t)i * V + cc] * kt[i];
+                        dd[cc] += F[(size_t)i * V + cc] * kt[i];
+                    }
+                double dbeta = 0.0, dPd = 0.0, Fh = 0.0;
+                for (int cc = 0; cc < V; ++cc) {
+                    const double r = vt[cc] - alpha * P[cc];
+                    delta[cc] = b * r;
+                    c->dv[((size_t)t * hv + j) * V + cc] = b * dd[cc];
+                    dbeta += dd[cc] * r;
+                    dPd += dd[cc] * P[cc];
+                }
+                for (size_t e = 0; e < KV; ++e) Fh += F[e] * hp[e];
+                c->dbeta[(size_t)t * hv + j] = dbeta;
+                c->dg[(size_t)t * hv + j] = alpha * (Fh - b * dPd);
+                /* dk = F delta - alpha beta h_prev dd */
+                for (int i = 0; i < K; ++i) {
+                    double s = 0.0;
+                    for (int cc = 0; cc < V; ++cc)
+                        s += F[(size_t)i * V + cc] * delta[cc] - alpha * b * hp[(size_t)i * V + cc] * dd[cc];
+                    dkt[i] += s;
+                }
+                /* dh_prev = alpha (F - beta k dd^T) */
+                for (int i = 0; i < K; ++i)
+                    for (int cc = 0; cc < V; ++cc)
+                        F[(size_t)i * V + cc] = alpha * (F[(size_t)i * V + cc] - b * kt[i] * dd[cc]);
+            }
+        }
+        if (c->dh0) memcpy(c->dh0 + ((size_t)n * hv + j) * KV, F, sizeof(double) * KV);
+    }
+    free(ck);
+    free(hs);
+    free(F);
+    free(P);
+    free(delta);
+    free(dd);
+}
+
+int gdn_oracle_token_backward(const double* q, const double* k, const double* v, const double* g,
+                              const double* beta, const double* h0, const double* dout,
+                              const double* dh_final, int64_t T, int N, const int64_t* cu,
+                              int hk, int hv, int K, int V, int nthreads, double* dq, double* dk,
+                              double* dv, double* dg, double* dbeta, double* dh0) {
+    int rc = check_geometry(T, N, cu, hk, hv, K, V);
+    if (rc) return rc;
+    if (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta) return -1;
+    bwd_ctx c = {q, k, v, g, beta, h0, dout, dh_final, cu, N, hk, hv, K, V,
+                 dq, dk, dv, dg, dbeta, dh0};
+    run_items(bwd_item, &c, (int64_t)N * hk, nthreads);
+    return 0;
 }
