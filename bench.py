@@ -37,6 +37,14 @@ BYTES_PER_TOKEN = HK * KD * 2 * 2 + HV * VD * 2 * 2 + HV * 4 * 2
 # what each phase-1 kernel must read per token: k, v, g, beta (U half); k, g, beta (M half)
 SUM_U_BYTES_PER_TOKEN = HK * KD * 2 + HV * VD * 2 + HV * 4 * 2
 SUM_M_BYTES_PER_TOKEN = HK * KD * 2 + HV * 4 * 2
+# backward (fp32 CUDA-core arithmetic): FLOPs per token of what it computes -- per chunk and
+# value head 6 CKV + 6 C^2 K + 3 C^2 V products and two C x C triangular solves over V columns,
+# per token and value head the two state-column recurrences (2 KV + 3 KV multiply-adds)
+BWD_FLOP_PER_TOKEN = HV * (2 * (6 * C * KD * VD + 6 * C * C * KD + 3 * C * C * VD
+                                 + C * (C - 1) * VD) / C + 2 * 5 * KD * VD)
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (maximum SM clock)
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+BWD_STEPS = 5
 # decode: requests per step, slots in the state pool, timed steps; bytes one step must move
 # (each request's fp32 state read and written once per value head, q, k, v, out, g, beta, slot)
 DEC_B, DEC_SLOTS, DEC_STEPS = 256, 256, 200
@@ -425,6 +433,31 @@ def run_ours(args, ws, rank, local):
         raise gdn.GdnError(st, "decode device status")
     del dd_
 
+    # the backward at the same workload: gradients of <dout, out> through the forward
+    gen = torch.Generator().manual_seed(100 + rank)
+    dout = torch.randn(d["v"].shape, generator=gen).to(torch.bfloat16).to(dev)
+    pb = gdn.problem_for(d["q"], d["v"], None)
+    bws = torch.empty(gdn.gdn_backward_workspace_size(pb), dtype=torch.uint8, device=dev)
+    bo = [torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"]),
+          torch.empty_like(d["g"]), torch.empty_like(d["beta"])]
+
+    def bwd_step():
+        gdn.gdn_backward(pb, d["q"], d["k"], d["v"], d["g"], d["beta"], None, None, dout, None,
+                         *bo, None, bws, stream=stream)
+
+    bwd_step()
+    barrier()
+    e0.record(stream)
+    for _ in range(BWD_STEPS):
+        bwd_step()
+    e1.record(stream)
+    barrier()
+    bwd_ms = e0.elapsed_time(e1) / BWD_STEPS
+    st = gdn.gdn_device_status(bws)
+    if st != 0:
+        raise gdn.GdnError(st, "backward device status")
+    del bws, bo, dout
+
     if rank != 0:
         return None
     hbm, tf, tf_sus, src = peaks()
@@ -497,6 +530,18 @@ def run_ours(args, ws, rank, local):
                 "pipelining": "copies in on two streams, the forward, copies out on two more, "
                               "over two buffer sets"},
         "clocks": clk.summary(),
+        "backward": {
+            "workload": f"long-context bf16 T={T} Hk={HK} Hv={HV} K=V={KD}: gradients of q, k, "
+                        "v, g, beta, h0 for a random dout",
+            "ms_per_step": bwd_ms, "tokens_per_s": T / (bwd_ms / 1e3), "steps": BWD_STEPS,
+            "gpu_launches_per_step": 4,
+            "roofline": {"bound": "alu", "unit": "TFLOP/s",
+                         "achieved": BWD_FLOP_PER_TOKEN * T / (bwd_ms / 1e3) / 1e12,
+                         "peak": FP32_ALU_TFLOPS,
+                         "frac": BWD_FLOP_PER_TOKEN * T / (bwd_ms / 1e3) / 1e12 / FP32_ALU_TFLOPS,
+                         "peak_source": "fp32 FMA units x maximum SM clock (not measured)",
+                         "algorithmic_flop_per_step": BWD_FLOP_PER_TOKEN * T,
+                         "traffic": None}},
         "decode": {
             "workload": f"decode bf16 B={DEC_B} requests, pool of {DEC_SLOTS} slots, Hk={HK} "
                         f"Hv={HV} K=V={KD}; fp32 state pool "

@@ -400,6 +400,37 @@ gdn_status gdn_chunk_emit_fused(const gdn_problem* p, const void* q, const void*
   return to_status(fused_emit(p, a, stream));
 }
 
+// ------------------------------------------------------------------ backward
+
+// CTAs of the per-chunk gradient kernel (two per SM of a 152-SM GB300); the workspace holds one
+// slice of intermediates for each.  The kernel walks all units with a grid stride, so any SM
+// count computes the same result.
+constexpr int kGradCtas = 304;
+
+struct BwdLayout {
+  size_t status, states, dstates, dqv, dkv, scratch, total;
+};
+BwdLayout bwd_layout(const gdn_problem* p) {
+  BwdLayout L;
+  const size_t K = p->k_dim, V = p->v_dim, T = (size_t)p->total_tokens;
+  const size_t slots = (size_t)gdn::bwd_slots(p->total_tokens, p->num_seqs);
+  size_t off = 0;
+  L.status = off;
+  off += kStatusBytes;
+  L.states = off;
+  off += align_up(slots * p->hv * K * V * 4);
+  L.dstates = off;
+  off += align_up(slots * p->hv * K * V * 4);
+  L.dqv = off;
+  off += align_up(T * p->hv * K * 4);
+  L.dkv = off;
+  off += align_up(T * p->hv * K * 4);
+  L.scratch = off;
+  off += align_up(gdn::bwd_scratch_floats(p->k_dim, p->v_dim, kGradCtas) * 4);
+  L.total = off;
+  return L;
+}
+
 gdn_status gdn_check_decode_problem(const gdn_decode_problem* p) {
   if (!p) return GDN_ERR_INVALID_ARGUMENT;
   if (p->batch < 0 || p->slots < 1 || p->hk < 1 || p->hv < 1 || p->k_dim < 1 || p->v_dim < 1)
@@ -442,6 +473,67 @@ gdn_status gdn_decode_step(const gdn_decode_problem* p, const void* q, const voi
   a.out = out;
   a.status = dev_status;
   return to_status(gdn::decode_step(a, stream));
+}
+
+size_t gdn_backward_workspace_size(const gdn_problem* p) {
+  return check_problem(p) != GDN_OK ? 0 : bwd_layout(p).total;
+}
+
+gdn_status gdn_backward(const gdn_problem* p, const void* q, const void* k, const void* v,
+                        const float* g, const float* beta, const float* h0,
+                        const int32_t* cu_seqlens, const void* dout, const float* dh_final,
+                        void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dh0,
+                        void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  gdn_status st = check_problem(p);
+  if (st != GDN_OK) return st;
+  if (p->total_tokens > 0 && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv ||
+                              !dg || !dbeta))
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (!cu_ok(p, cu_seqlens)) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || !aligned16(h0) || !aligned16(dh_final) ||
+      !aligned16(dh0))
+    return GDN_ERR_INVALID_ARGUMENT;
+  const BwdLayout L = bwd_layout(p);
+  if (!workspace || ws_bytes < L.total || !aligned16(workspace)) return GDN_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+  GDN_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), stream));
+  Args va = base_args(p);
+  va.cu = cu_seqlens;
+  va.status = status;
+  GDN_TRY(gdn::launch_validate_cu(va, stream));
+  gdn::BwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.T = p->total_tokens;
+  a.nslots = gdn::bwd_slots(p->total_tokens, p->num_seqs);
+  a.N = p->num_seqs;
+  a.hk = p->hk;
+  a.hv = p->hv;
+  a.K = p->k_dim;
+  a.V = p->v_dim;
+  a.bf16 = p->io_dtype == GDN_BF16;
+  a.q = q; a.k = k; a.v = v; a.dout = dout;
+  a.g = g; a.beta = beta; a.h0 = h0; a.dh_final = dh_final; a.cu = cu_seqlens;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
+  a.states = reinterpret_cast<float*>(ws + L.states);
+  a.dstates = reinterpret_cast<float*>(ws + L.dstates);
+  a.dqv = reinterpret_cast<float*>(ws + L.dqv);
+  a.dkv = reinterpret_cast<float*>(ws + L.dkv);
+  a.scratch = reinterpret_cast<float*>(ws + L.scratch);
+  a.grad_ctas = kGradCtas;
+  a.status = status;
+  if (a.T == 0) {  // no tokens: the state passes through, dh0 = dh_final
+    if (dh0) {
+      const size_t bytes = (size_t)p->num_seqs * p->hv * p->k_dim * p->v_dim * 4;
+      if (dh_final)
+        GDN_TRY(cudaMemcpyAsync(dh0, dh_final, bytes, cudaMemcpyDeviceToDevice, stream));
+      else
+        GDN_TRY(cudaMemsetAsync(dh0, 0, bytes, stream));
+    }
+    return GDN_OK;
+  }
+  return to_status(gdn::backward(a, stream));
 }
 
 gdn_status gdn_device_status(const void* status_word, int reset, cudaStream_t stream) {

@@ -69,4 +69,25 @@ struct DecodeArgs {
 };
 cudaError_t decode_step(const DecodeArgs& a, cudaStream_t s);
 
+// Gradients of the forward (gdn_backward).  Workspace pieces: states / dstates
+// [nslots, hv, V, K] fp32 (the state entering / the gradient of the state leaving every chunk,
+// a state column contiguous), dqv / dkv [T, hv, K] fp32 (per value head, before the sum over
+// the key head's group), scratch (grad_ctas slices of the per-chunk kernel's intermediates).
+struct BwdArgs {
+  int64_t T, nslots;
+  int N, hk, hv, K, V;
+  bool bf16;
+  const void *q, *k, *v, *dout;
+  const float *g, *beta, *h0, *dh_final;
+  const int32_t* cu;
+  void *dq, *dk, *dv;
+  float *dg, *dbeta, *dh0;
+  float *states, *dstates, *dqv, *dkv, *scratch;
+  int grad_ctas;
+  int32_t* status;
+};
+int64_t bwd_slots(int64_t T, int N);
+size_t bwd_scratch_floats(int K, int V, int ctas);
+cudaError_t backward(const BwdArgs& a, cudaStream_t s);
+
 }  // namespace gdn

@@ -35,7 +35,8 @@ EXPORTED = ("gdn_status_string", "gdn_check_problem", "gdn_workspace_size", "gdn
             "gdn_chunk_emit", "gdn_device_status", "gdn_version",
             "gdn_segment_summary_fused", "gdn_chunk_emit_fused", "gdn_last_error_string",
             "gdn_forward_static_scratch", "gdn_forward_timed", "gdn_forward_with_limits",
-            "gdn_check_decode_problem", "gdn_decode_step")
+            "gdn_check_decode_problem", "gdn_decode_step", "gdn_backward_workspace_size",
+            "gdn_backward")
 
 
 class Problem(ctypes.Structure):
@@ -84,11 +85,16 @@ _lib.gdn_segment_summary_fused.argtypes = [_pp, _vp, _vp, _fp, _fp, _ip, _fp, _f
                                            _ip, _vp]
 _lib.gdn_chunk_emit_fused.argtypes = [_pp, _vp, _vp, _vp, _fp, _fp, _fp, _ip, _vp, _fp, _ip, _vp]
 _lib.gdn_forward_static_scratch.argtypes = [_pp, _vp, _vp, _vp, _fp, _fp, _fp, _ip, _vp, _fp, _vp]
+_lib.gdn_backward_workspace_size.restype = ctypes.c_size_t
+_lib.gdn_backward_workspace_size.argtypes = [_pp]
+_lib.gdn_backward.argtypes = [_pp, _vp, _vp, _vp, _fp, _fp, _fp, _ip, _vp, _fp, _vp, _vp, _vp,
+                              _fp, _fp, _fp, _vp, ctypes.c_size_t, _vp]
 _dpp = ctypes.POINTER(DecodeProblem)
 _lib.gdn_check_decode_problem.argtypes = [_dpp]
 _lib.gdn_decode_step.argtypes = [_dpp, _vp, _vp, _vp, _fp, _fp, _ip, _fp, _vp, _ip, _vp]
 for _n in EXPORTED:
-    if _n not in ("gdn_status_string", "gdn_workspace_size", "gdn_last_error_string"):
+    if _n not in ("gdn_status_string", "gdn_workspace_size", "gdn_last_error_string",
+                  "gdn_backward_workspace_size"):
         getattr(_lib, _n).restype = ctypes.c_int
 
 
@@ -221,6 +227,38 @@ def gdn_chunk_emit_fused(p, q, k, v, g, beta, h_in, cu_seqlens, out, h_final, de
                                      _ptr(beta), _ptr(h_in), _ptr(cu_seqlens), _ptr(out),
                                      _ptr(h_final), _ptr(dev_status), _stream(stream)),
            "gdn_chunk_emit_fused")
+
+
+def gdn_backward_workspace_size(p: Problem) -> int:
+    return int(_lib.gdn_backward_workspace_size(ctypes.byref(p)))
+
+
+def gdn_backward(p, q, k, v, g, beta, h0, cu_seqlens, dout, dh_final, dq, dk, dv, dg, dbeta,
+                 dh0, workspace, ws_bytes=None, stream=None):
+    ws_bytes = workspace.numel() * workspace.element_size() if ws_bytes is None else ws_bytes
+    _check(_lib.gdn_backward(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                             _ptr(h0), _ptr(cu_seqlens), _ptr(dout), _ptr(dh_final), _ptr(dq),
+                             _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(dh0),
+                             _ptr(workspace), int(ws_bytes), _stream(stream)), "gdn_backward")
+
+
+def backward(q, k, v, g, beta, dout, h0=None, dh_final=None, cu_seqlens=None, workspace=None,
+             check_status=False, stream=None):
+    """Gradients (dq, dk, dv, dg, dbeta, dh0) of <dout, out> + <dh_final, h_final> through the
+    forward on the same inputs; allocates the outputs (and the workspace unless given)."""
+    p = problem_for(q, v, cu_seqlens)
+    N = p.num_seqs
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dg, dbeta = torch.empty_like(g), torch.empty_like(beta)
+    dh0 = torch.empty(N, p.hv, p.k_dim, p.v_dim, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(max(gdn_backward_workspace_size(p), 256), dtype=torch.uint8,
+                                device=q.device)
+    gdn_backward(p, q, k, v, g, beta, h0, cu_seqlens, dout, dh_final, dq, dk, dv, dg, dbeta,
+                 dh0, workspace, stream=stream)
+    if check_status:
+        _check(gdn_device_status(workspace, True, stream), "gdn_backward (device status)")
+    return dq, dk, dv, dg, dbeta, dh0
 
 
 def make_decode_problem(B, slots, hk, hv, K, V, dtype=torch.bfloat16) -> DecodeProblem:

@@ -241,6 +241,33 @@ gdn_status gdn_forward_static_scratch(const gdn_problem* p, const void* q, const
                                       float* h_final, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------- */
+/* Backward: gradients of the forward pass.                                                 */
+
+/* Bytes of device workspace gdn_backward needs for problem p (0 when p is invalid): the status
+ * word, the state entering and the gradient of the state leaving every chunk (fp32, 2 * 4 * K *
+ * V bytes per chunk and value head each way), per-value-head dq and dk (fp32), and the
+ * intermediates of 304 concurrent per-chunk blocks. */
+size_t gdn_backward_workspace_size(const gdn_problem* p);
+
+/* Gradients of L = <dout, out> + <dh_final, h_final> through the forward of gdn_forward
+ * (the same problem, inputs and h0) with respect to q, k, v, g, beta and h0.  The page "Add
+ * context parallelism to the Gated Delta Net" holds the layer's backward to parity (sections
+ * "Tests" and "Measured results"); its formulas follow from the chunk map of section "Why".
+ *   dout        [T, hv, V] io dtype            dh_final  [N, hv, K, V] fp32, or NULL (zeros)
+ *   dq, dk      [T, hk, K] io dtype (a key head's gradient sums over the value heads reading it)
+ *   dv          [T, hv, V] io dtype            dg, dbeta [T, hv] fp32
+ *   dh0         [N, hv, K, V] fp32, or NULL to skip
+ *   workspace   ws_bytes >= gdn_backward_workspace_size(p), 16-byte aligned; its first 4 bytes
+ *               are the status word (reset by this call)
+ * segments_per_seq is not used.  All arithmetic is fp32 on CUDA cores.  Tails, padding, cu_seqlens
+ * checks and errors as for gdn_forward.  Returns GDN_OK once the work is enqueued. */
+gdn_status gdn_backward(const gdn_problem* p, const void* q, const void* k, const void* v,
+                        const float* g, const float* beta, const float* h0,
+                        const int32_t* cu_seqlens, const void* dout, const float* dh_final,
+                        void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dh0,
+                        void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------- */
 /* Decode: one token per request over a pool of per-slot recurrent states.                   */
 
 typedef struct gdn_decode_problem {

@@ -163,3 +163,24 @@ def test_decode_step_rejects_bad_arguments_before_any_launch(gdn):
     p0 = gdn.make_decode_problem(0, 16, 16, 32, 128, 128)
     assert L.gdn_decode_step(by(p0), None, None, None, None, None, None, None, None, None,
                              None) == 0
+
+
+def test_backward_rejects_bad_arguments_before_any_launch(gdn):
+    p = prob(gdn)
+    fake = 1 << 20
+    L = gdn._lib
+    by = ctypes.byref
+    args = [fake] * 5 + [None, None, fake, None] + [fake] * 5 + [None]
+    # complete call shape: p, q k v g beta, h0, cu, dout, dh_final, dq dk dv dg dbeta, dh0, ws, bytes
+    ok = [by(p)] + args[:5] + [None, None, fake, None, fake, fake, fake, fake, fake, None]
+    assert L.gdn_backward(*ok, fake, 1, None) == 3           # workspace too small
+    bad = list(ok)
+    bad[8] = None                                            # no dout
+    assert L.gdn_backward(*bad, fake, 1 << 40, None) == 1
+    bad = list(ok)
+    bad[1] = fake + 8                                        # misaligned q
+    assert L.gdn_backward(*bad, fake, 1 << 40, None) == 1
+    assert gdn.gdn_backward_workspace_size(prob(gdn, K=96)) == 0
+    # the state and state-gradient checkpoints: 2 * 4 * K * V bytes per chunk and value head
+    ws = gdn.gdn_backward_workspace_size(prob(gdn, T=65536))
+    assert ws >= 2 * (65536 // 64) * 32 * 128 * 128 * 4
