@@ -40,7 +40,7 @@ namespace {
 
 constexpr int C = kChunk;  // 64
 constexpr int kColThreads = 128;   // 32 state columns per CTA, 4 lanes per column
-constexpr int kGradThreads = 256;
+constexpr int kGradThreads = 512;
 
 __device__ __forceinline__ float ld_io(const void* p, int64_t i, bool bf16) {
   return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i])
@@ -60,16 +60,30 @@ __device__ __forceinline__ int64_t slot_base(const int32_t* cu, int n) {
 
 // ------------------------------------------------------------------ column recurrences
 
-// One CTA: sequence n, value head j, 32 state columns; thread = (column, quarter of the rows).
-// Forward: stores the state entering every chunk, as states[slot][j][v][i] (a column of the
-// state contiguous).  Reverse: stores the gradient of the state leaving every chunk in the same
-// layout, and dh0.
+// Shared memory of one column CTA: a chunk of k (and, reversed, q) as fp32 rows, the CTA's 32
+// columns of v (or dout), g and beta.
+template <int K, bool REVERSE>
+constexpr size_t column_smem() {
+  return sizeof(float) * ((size_t)C * K * (REVERSE ? 2 : 1) + (size_t)C * 32 + 2 * C);
+}
+
+// One CTA: sequence n, value head j, 32 state columns; thread (column, row phase p) holds rows
+// p, p + 4, p + 8, ... of its column (the four phases of a column then read four banks of a
+// staged key row).  Each chunk's inputs are staged in shared memory first.  Forward: stores the
+// state entering every chunk as states[slot][j][v][i] (a state column contiguous).  Reverse:
+// stores the gradient of the state leaving every chunk in the same layout, and dh0.
 template <int K, bool REVERSE>
 __global__ void __launch_bounds__(kColThreads) column_kernel(BwdArgs a) {
   constexpr int RPL = K / 4;
+  extern __shared__ __align__(16) float csm[];
+  float* ks = csm;                                 // [C][K]
+  float* qs = ks + C * K;                          // [C][K] (reverse)
+  float* vs = qs + (REVERSE ? C * K : 0);          // [C][32]
+  float* gs = vs + C * 32;                         // [C]
+  float* bs = gs + C;                              // [C]
   const int nj = blockIdx.x, n = nj / a.hv, j = nj % a.hv, kh = j / (a.hv / a.hk);
-  const int v = blockIdx.y * 32 + (threadIdx.x >> 2), part = threadIdx.x & 3;
-  const int r0 = part * RPL;
+  const int col = threadIdx.x >> 2, p = threadIdx.x & 3;
+  const int v0 = blockIdx.y * 32, v = v0 + col;
   int64_t t0, t1;
   if (!seq_bounds(a.cu, n, a.T, a.status, t0, t1)) return;
   const int64_t KV = (int64_t)K * a.V;
@@ -77,72 +91,79 @@ __global__ void __launch_bounds__(kColThreads) column_kernel(BwdArgs a) {
   const float* init = REVERSE ? a.dh_final : a.h0;
 #pragma unroll
   for (int i = 0; i < RPL; ++i)
-    h[i] = init ? init[((int64_t)n * a.hv + j) * KV + (int64_t)(r0 + i) * a.V + v] : 0.f;
+    h[i] = init ? init[((int64_t)n * a.hv + j) * KV + (int64_t)(p + 4 * i) * a.V + v] : 0.f;
   float* store = REVERSE ? a.dstates : a.states;
+  const void* vin = REVERSE ? a.dout : a.v;
   const int64_t nc = (t1 - t0 + C - 1) / C, sb = slot_base(a.cu, n);
   for (int64_t ci = 0; ci < nc; ++ci) {
     const int64_t c = REVERSE ? nc - 1 - ci : ci;
-    const int64_t c0 = t0 + c * C, c1 = (c0 + C < t1) ? c0 + C : t1;
-    float* dst = store + (((sb + c) * a.hv + j) * a.V + v) * K + r0;
+    const int64_t c0 = t0 + c * C;
+    const int L = (int)((t1 - c0) < C ? (t1 - c0) : C);
+    float* dst = store + (((sb + c) * a.hv + j) * a.V + v) * K;
 #pragma unroll
-    for (int i = 0; i < RPL; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(h[i], h[i + 1], h[i + 2], h[i + 3]);
-    for (int64_t s = 0; s < c1 - c0; ++s) {
-      const int64_t t = REVERSE ? c1 - 1 - s : c0 + s;
-      const float alpha = __expf(a.g[t * a.hv + j]), beta = a.beta[t * a.hv + j];
-      float kk[RPL];
+    for (int i = 0; i < RPL; ++i) dst[p + 4 * i] = h[i];
+    __syncthreads();  // the previous chunk's inputs have been used
+    for (int e = threadIdx.x; e < L * K; e += kColThreads) {
+      const int t = e / K, i = e % K;
+      ks[e] = ld_io(a.k, ((c0 + t) * a.hk + kh) * K + i, a.bf16);
+      if (REVERSE) qs[e] = ld_io(a.q, ((c0 + t) * a.hk + kh) * K + i, a.bf16);
+    }
+    for (int e = threadIdx.x; e < L * 32; e += kColThreads) {
+      const int t = e / 32, cc = e % 32;
+      vs[e] = ld_io(vin, ((c0 + t) * a.hv + j) * a.V + v0 + cc, a.bf16);
+    }
+    for (int t = threadIdx.x; t < L; t += kColThreads) {
+      gs[t] = __expf(a.g[(c0 + t) * a.hv + j]);
+      bs[t] = a.beta[(c0 + t) * a.hv + j];
+    }
+    __syncthreads();
+    for (int s = 0; s < L; ++s) {
+      const int t = REVERSE ? L - 1 - s : s;
+      const float alpha = gs[t], beta = bs[t], x = vs[t * 32 + col];
+      const float* kr = ks + t * K + p;
+      if (REVERSE) {  // F = dh + q dout^T
+        const float* qr = qs + t * K + p;
 #pragma unroll
-      for (int i = 0; i < RPL; ++i) kk[i] = ld_io(a.k, (t * a.hk + kh) * K + r0 + i, a.bf16);
-      if (REVERSE) {  // F = dh + q dout^T;  dd = k . F;  dh <- alpha (F - beta k dd)
-        const float dov = ld_io(a.dout, (t * a.hv + j) * a.V + v, a.bf16);
-#pragma unroll
-        for (int i = 0; i < RPL; ++i) h[i] = fmaf(ld_io(a.q, (t * a.hk + kh) * K + r0 + i, a.bf16), dov, h[i]);
+        for (int i = 0; i < RPL; ++i) h[i] = fmaf(qr[4 * i], x, h[i]);
       }
-      float p = 0.f;
+      float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-      for (int i = 0; i < RPL; ++i) p = fmaf(kk[i], h[i], p);
-      p += __shfl_xor_sync(0xffffffffu, p, 1);
-      p += __shfl_xor_sync(0xffffffffu, p, 2);
-      if (REVERSE) {
-        const float bd = beta * p;
+      for (int i = 0; i < RPL; i += 2) {
+        d0 = fmaf(kr[4 * i], h[i], d0);
+        d1 = fmaf(kr[4 * i + 4], h[i + 1], d1);
+      }
+      float d = d0 + d1;
+      d += __shfl_xor_sync(0xffffffffu, d, 1);
+      d += __shfl_xor_sync(0xffffffffu, d, 2);
+      if (REVERSE) {  // dd = k . F;  dh <- alpha (F - beta k dd)
+        const float bd = beta * d;
 #pragma unroll
-        for (int i = 0; i < RPL; ++i) h[i] = alpha * fmaf(-kk[i], bd, h[i]);
-      } else {  // delta = beta (v - alpha p);  h <- alpha h + k delta
-        const float d = beta * (ld_io(a.v, (t * a.hv + j) * a.V + v, a.bf16) - alpha * p);
+        for (int i = 0; i < RPL; ++i) h[i] = alpha * fmaf(-kr[4 * i], bd, h[i]);
+      } else {  // delta = beta (v - alpha k . h);  h <- alpha h + k delta
+        const float dl = beta * (x - alpha * d);
 #pragma unroll
-        for (int i = 0; i < RPL; ++i) h[i] = fmaf(kk[i], d, alpha * h[i]);
+        for (int i = 0; i < RPL; ++i) h[i] = fmaf(kr[4 * i], dl, alpha * h[i]);
       }
     }
   }
   if (REVERSE && a.dh0) {
 #pragma unroll
-    for (int i = 0; i < RPL; ++i) a.dh0[((int64_t)n * a.hv + j) * KV + (int64_t)(r0 + i) * a.V + v] = h[i];
+    for (int i = 0; i < RPL; ++i)
+      a.dh0[((int64_t)n * a.hv + j) * KV + (int64_t)(p + 4 * i) * a.V + v] = h[i];
   }
 }
 
 // ------------------------------------------------------------------ per-chunk gradients
 
-// out[i][c] (+)= sum_y A(i, y) B(y, c) for i < M, c < N: every thread takes output elements in
-// turn; operands are read through accessor functors (smem or the CTA's workspace slice).
-template <typename FA, typename FB, typename FO>
-__device__ __forceinline__ void mm(int M, int N, int Y, FA A, FB B, FO out) {
-  for (int e = threadIdx.x; e < M * N; e += blockDim.x) {
-    const int i = e / N, c = e % N;
-    float s0 = 0.f, s1 = 0.f;
-    int y = 0;
-    for (; y + 1 < Y; y += 2) {
-      s0 = fmaf(A(i, y), B(y, c), s0);
-      s1 = fmaf(A(i, y + 1), B(y + 1, c), s1);
-    }
-    if (y < Y) s0 = fmaf(A(i, y), B(y, c), s0);
-    out(i, c, s0 + s1);
-  }
-}
-
 struct GradSmem {
-  float KK[C][C + 1], QK[C][C + 1], Am[C][C + 1], At[C][C + 1];  // A, attn; then dA o Gamma etc.
+  float GKK[C][C + 1];  // Gamma o K K^T, strictly lower (A = diag(beta) GKK)
+  float At[C][C + 1];   // attn = Gamma o Q K^T, lower
   float dA[C][C + 1], dat[C][C + 1];
-  float G[C], eG[C], ekt[C], b[C], dG[C], red[C];
+  float G[C], eG[C], ekt[C], b[C], dG[C];
   float scal[4];
+  float As[C][33];      // product tiles
+  float Bs[32][129];
+  float X[C][129];      // the triangular solves
 };
 
 // floats of one CTA's workspace slice: K S, Q S, R, delta, d_delta (then dB), dout as [C][V];
@@ -150,23 +171,66 @@ struct GradSmem {
 template <int K, int V>
 __host__ __device__ constexpr int64_t grad_slice() { return 6 * (int64_t)C * V + 3 * (int64_t)C * K; }
 
+// out(i, c, x) for i < C, c < N with x = sum_{y < Y} A(i, y) B(y, c) (Y a multiple of 32):
+// 32-wide slices of y are staged in shared memory; thread (ty, tx) of 16 x 32 accumulates rows
+// ty + 16 r and columns tx + 32 m in registers.  AI / BY: the operand's contiguous index is i
+// (for A) / y (for B), so that the staging loads walk memory in order.
+template <int N, bool AI, bool BY, typename FA, typename FB, typename FO>
+__device__ __forceinline__ void mm(GradSmem& sm, int Y, FA A, FB B, FO out) {
+  constexpr int RM = C / 16, RN = N / 32;
+  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+  float acc[RM][RN];
+#pragma unroll
+  for (int r = 0; r < RM; ++r)
+#pragma unroll
+    for (int m = 0; m < RN; ++m) acc[r][m] = 0.f;
+  for (int y0 = 0; y0 < Y; y0 += 32) {
+    __syncthreads();
+    for (int e = tid; e < C * 32; e += kGradThreads) {
+      const int i = AI ? e % C : e / 32, yy = AI ? e / C : e % 32;
+      sm.As[i][yy] = A(i, y0 + yy);
+    }
+    for (int e = tid; e < 32 * N; e += kGradThreads) {
+      const int c = BY ? e / 32 : e % N, yy = BY ? e % 32 : e / N;
+      sm.Bs[yy][c] = B(y0 + yy, c);
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int yy = 0; yy < 32; ++yy) {
+      float av[RM], bv[RN];
+#pragma unroll
+      for (int r = 0; r < RM; ++r) av[r] = sm.As[ty + 16 * r][yy];
+#pragma unroll
+      for (int m = 0; m < RN; ++m) bv[m] = sm.Bs[yy][tx + 32 * m];
+#pragma unroll
+      for (int r = 0; r < RM; ++r)
+#pragma unroll
+        for (int m = 0; m < RN; ++m) acc[r][m] = fmaf(av[r], bv[m], acc[r][m]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < RM; ++r)
+#pragma unroll
+    for (int m = 0; m < RN; ++m) out(ty + 16 * r, tx + 32 * m, acc[r][m]);
+}
+
 // One CTA per (chunk slot, value head); grid-stride over the units.
 template <int K, int V>
 __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
   extern __shared__ __align__(16) uint8_t smraw[];
   GradSmem& sm = *reinterpret_cast<GradSmem*>(smraw);
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int64_t nslots = a.nslots, units = nslots * a.hv;
   float* ws = a.scratch + (int64_t)blockIdx.x * grad_slice<K, V>();
   float* KS = ws;            // [C][V]  K S
   float* QS = KS + C * V;    // [C][V]  Q S
   float* R = QS + C * V;     // [C][V]  V - e^G K S
   float* DL = R + C * V;     // [C][V]  delta
-  float* DD = DL + C * V;    // [C][V]  d_delta, then dB in place
+  float* DD = DL + C * V;    // [C][V]  d_delta, then dB
   float* DO = DD + C * V;    // [C][V]  dout (fp32)
   float* KF = DO + C * V;    // [C][K]  k (fp32)
   float* QF = KF + C * K;    // [C][K]  q (fp32)
-  float* X = QF + C * K;     // [C][K]  delta D^T
+  float* XD = QF + C * K;    // [C][K]  delta D^T
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const int64_t slot = u / a.hv;
     const int j = (int)(u % a.hv), kh = j / (a.hv / a.hk);
@@ -180,7 +244,7 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
     const float* Sx = a.states + ((slot * a.hv + j) * (int64_t)V) * K;   // S[i][v] = Sx[v K + i]
     const float* Dx = a.dstates + ((slot * a.hv + j) * (int64_t)V) * K;
     __syncthreads();  // the previous unit is done with the shared and workspace buffers
-    // ---- inputs: decays (running sum by one warp), q, k, dout as fp32
+    // ---- decays (running sum by one warp); q, k, dout as fp32
     if (tid < 32) {
       const float g0 = tid < L ? a.g[(t0 + tid) * a.hv + j] : 0.f;
       const float g1 = tid + 32 < L ? a.g[(t0 + tid + 32) * a.hv + j] : 0.f;
@@ -214,118 +278,128 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
       DO[e] = t < L ? ld_io(a.dout, ((t0 + t) * a.hv + j) * V + c, a.bf16) : 0.f;
     }
     __syncthreads();
-    // ---- K K^T, Q K^T; K S, Q S
-    mm(C, C, K, [&](int t, int y) { return KF[t * K + y]; }, [&](int y, int s) { return KF[s * K + y]; },
-       [&](int t, int s, float x) { sm.KK[t][s] = x; });
-    mm(C, C, K, [&](int t, int y) { return QF[t * K + y]; }, [&](int y, int s) { return KF[s * K + y]; },
-       [&](int t, int s, float x) { sm.QK[t][s] = x; });
-    mm(C, V, K, [&](int t, int y) { return KF[t * K + y]; }, [&](int y, int c) { return Sx[c * K + y]; },
-       [&](int t, int c, float x) { KS[t * V + c] = x; });
-    mm(C, V, K, [&](int t, int y) { return QF[t * K + y]; }, [&](int y, int c) { return Sx[c * K + y]; },
-       [&](int t, int c, float x) { QS[t * V + c] = x; });
+    auto gam = [&](int t, int s) { return __expf(sm.G[t] - sm.G[s]); };  // for s <= t
+    // ---- Gamma o K K^T (strictly lower), attn; K S, Q S
+    mm<C, false, true>(sm, K, [&](int t, int y) { return KF[t * K + y]; },
+                       [&](int y, int s) { return KF[s * K + y]; },
+                       [&](int t, int s, float x) { sm.GKK[t][s] = (s < t && t < L) ? gam(t, s) * x : 0.f; });
+    mm<C, false, true>(sm, K, [&](int t, int y) { return QF[t * K + y]; },
+                       [&](int y, int s) { return KF[s * K + y]; },
+                       [&](int t, int s, float x) { sm.At[t][s] = (s <= t && t < L) ? gam(t, s) * x : 0.f; });
+    mm<V, false, true>(sm, K, [&](int t, int y) { return KF[t * K + y]; },
+                       [&](int y, int c) { return Sx[c * K + y]; },
+                       [&](int t, int c, float x) { KS[t * V + c] = x; });
+    mm<V, false, true>(sm, K, [&](int t, int y) { return QF[t * K + y]; },
+                       [&](int y, int c) { return Sx[c * K + y]; },
+                       [&](int t, int c, float x) { QS[t * V + c] = x; });
     __syncthreads();
-    // ---- A, attn (rows >= L are zero); R = V - e^G K S
-    for (int e = tid; e < C * C; e += kGradThreads) {
-      const int t = e / C, s = e % C;
-      const bool in = t < L && s < L;
-      const float gam = __expf(sm.G[t] - sm.G[s < t ? s : t]);  // Gamma for s <= t
-      sm.Am[t][s] = (in && s < t) ? sm.b[t] * gam * sm.KK[t][s] : 0.f;
-      sm.At[t][s] = (in && s <= t) ? gam * sm.QK[t][s] : 0.f;
-    }
+    // ---- R = V - e^G K S;  delta = (I + A)^-1 diag(beta) R by forward substitution in shared
+    // memory: four threads per column split each row's sum
     for (int e = tid; e < C * V; e += kGradThreads) {
       const int t = e / V, c = e % V;
-      R[e] = t < L ? ld_io(a.v, ((t0 + t) * a.hv + j) * V + c, a.bf16) - sm.eG[t] * KS[e] : 0.f;
+      const float r = t < L ? ld_io(a.v, ((t0 + t) * a.hv + j) * V + c, a.bf16) - sm.eG[t] * KS[e] : 0.f;
+      R[e] = r;
+      sm.X[t][c] = sm.b[t] * r;
     }
     __syncthreads();
-    // ---- delta = (I + A)^-1 diag(beta) R: forward substitution, one column per thread
-    for (int c = tid; c < V; c += kGradThreads) {
-      for (int t = 0; t < L; ++t) {
-        float x = sm.b[t] * R[t * V + c];
-        for (int s = 0; s < t; ++s) x = fmaf(-sm.Am[t][s], DL[s * V + c], x);
-        DL[t * V + c] = x;
+    {
+      const int c = tid >> 2, p = tid & 3;
+      for (int t = 1; t < L; ++t) {
+        float x = 0.f;
+        if (c < V)
+          for (int s = p; s < t; s += 4) x = fmaf(sm.b[t] * sm.GKK[t][s], sm.X[s][c], x);
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        if (c < V && p == 0) sm.X[t][c] -= x;
+        __syncwarp();
       }
-      for (int t = L; t < C; ++t) DL[t * V + c] = 0.f;
     }
+    __syncthreads();
+    for (int e = tid; e < C * V; e += kGradThreads) DL[e] = sm.X[e / V][e % V];
     __syncthreads();
     // ---- d_delta = attn^T dO + Kt D
-    mm(C, V, C, [&](int t, int s) { return sm.At[s][t]; }, [&](int s, int c) { return DO[s * V + c]; },
-       [&](int t, int c, float x) { DD[t * V + c] = x; });
+    mm<V, true, false>(sm, C, [&](int t, int s) { return sm.At[s][t]; },
+                       [&](int s, int c) { return DO[s * V + c]; },
+                       [&](int t, int c, float x) { DD[t * V + c] = x; });
+    mm<V, false, true>(sm, K, [&](int t, int y) { return sm.ekt[t] * KF[t * K + y]; },
+                       [&](int y, int c) { return Dx[c * K + y]; },
+                       [&](int t, int c, float x) { sm.X[t][c] = t < L ? DD[t * V + c] + x : 0.f; });
     __syncthreads();
-    mm(C, V, K, [&](int t, int y) { return sm.ekt[t] * KF[t * K + y]; }, [&](int y, int c) { return Dx[c * K + y]; },
-       [&](int t, int c, float x) { DD[t * V + c] += t < L ? x : 0.f; });
-    __syncthreads();
-    // ---- dB = (I + A)^-T d_delta: back substitution in place
-    for (int c = tid; c < V; c += kGradThreads) {
-      for (int t = L - 1; t >= 0; --t) {
-        float x = DD[t * V + c];
-        for (int s = t + 1; s < L; ++s) x = fmaf(-sm.Am[s][t], DD[s * V + c], x);
-        DD[t * V + c] = x;
+    // ---- dB = (I + A)^-T d_delta by back substitution
+    {
+      const int c = tid >> 2, p = tid & 3;
+      for (int t = L - 2; t >= 0; --t) {
+        float x = 0.f;
+        if (c < V)
+          for (int s = t + 1 + p; s < L; s += 4) x = fmaf(sm.b[s] * sm.GKK[s][t], sm.X[s][c], x);
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        if (c < V && p == 0) sm.X[t][c] -= x;
+        __syncwarp();
       }
     }
     __syncthreads();
-    // ---- dA = -(dB delta^T) o strictly lower, dattn = (dO delta^T) o lower;  dv = beta dB
-    mm(C, C, V, [&](int t, int c) { return DD[t * V + c]; }, [&](int c, int s) { return DL[s * V + c]; },
-       [&](int t, int s, float x) { sm.dA[t][s] = (s < t && t < L) ? -x : 0.f; });
-    mm(C, C, V, [&](int t, int c) { return DO[t * V + c]; }, [&](int c, int s) { return DL[s * V + c]; },
-       [&](int t, int s, float x) { sm.dat[t][s] = (s <= t && t < L) ? x : 0.f; });
-    for (int e = tid; e < L * V; e += kGradThreads) {
+    for (int e = tid; e < C * V; e += kGradThreads) {
       const int t = e / V, c = e % V;
-      st_io(a.dv, ((t0 + t) * a.hv + j) * V + c, sm.b[t] * DD[e], a.bf16);
+      const float x = sm.X[t][c];
+      DD[e] = x;
+      if (t < L) st_io(a.dv, ((t0 + t) * a.hv + j) * V + c, sm.b[t] * x, a.bf16);
     }
     __syncthreads();
-    // ---- per-row sums: dbeta and the decay gradient dG
-    for (int t = tid; t < C; t += kGradThreads) {
-      float db = 0.f, dg = 0.f;
+    // ---- dA = -(dB delta^T) o strictly lower, dattn = (dO delta^T) o lower
+    mm<C, false, true>(sm, V, [&](int t, int c) { return DD[t * V + c]; },
+                       [&](int c, int s) { return DL[s * V + c]; },
+                       [&](int t, int s, float x) { sm.dA[t][s] = (s < t && t < L) ? -x : 0.f; });
+    mm<C, false, true>(sm, V, [&](int t, int c) { return DO[t * V + c]; },
+                       [&](int c, int s) { return DL[s * V + c]; },
+                       [&](int t, int s, float x) { sm.dat[t][s] = (s <= t && t < L) ? x : 0.f; });
+    // ---- delta D^T
+    mm<K, false, false>(sm, V, [&](int t, int c) { return DL[t * V + c]; },
+                        [&](int c, int i) { return Dx[c * K + i]; },
+                        [&](int t, int i, float x) { XD[t * K + i] = x; });
+    __syncthreads();
+    // ---- per row: dbeta and dG (eight threads a row)
+    {
+      const int t = tid >> 3, p = tid & 7;
+      float db = 0.f, dg = 0.f, kd = 0.f;
       if (t < L) {
-        for (int c = 0; c < V; ++c) {
+        for (int c = p; c < V; c += 8) {
           db = fmaf(DD[t * V + c], R[t * V + c], db);
           dg = fmaf(-sm.b[t] * sm.eG[t] * DD[t * V + c], KS[t * V + c], dg);
           dg = fmaf(sm.eG[t] * DO[t * V + c], QS[t * V + c], dg);
         }
-        for (int s = 0; s < L; ++s) {
-          const float gam = __expf(sm.G[t] - sm.G[s < t ? s : t]);
-          if (s < t) db = fmaf(sm.dA[t][s] * gam, sm.KK[t][s], db);
-          dg += sm.dA[t][s] * sm.Am[t][s] - sm.dA[s][t] * sm.Am[s][t];
+        for (int s = p; s < L; s += 8) {
+          if (s < t) db = fmaf(sm.dA[t][s], sm.GKK[t][s], db);
+          dg += sm.dA[t][s] * sm.b[t] * sm.GKK[t][s] - sm.dA[s][t] * sm.b[s] * sm.GKK[s][t];
           dg += sm.dat[t][s] * sm.At[t][s] - sm.dat[s][t] * sm.At[s][t];
         }
-        a.dbeta[(t0 + t) * a.hv + j] = db;
+        for (int i = p; i < K; i += 8) kd = fmaf(KF[t * K + i], XD[t * K + i], kd);
       }
-      sm.dG[t] = dg;
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) {
+        db += __shfl_xor_sync(0xffffffffu, db, o);
+        dg += __shfl_xor_sync(0xffffffffu, dg, o);
+        kd += __shfl_xor_sync(0xffffffffu, kd, o);
+      }
+      kd *= sm.ekt[t];
+      if (p == 0) {
+        if (t < L) a.dbeta[(t0 + t) * a.hv + j] = db;
+        sm.dG[t] = t < L ? dg - kd : 0.f;
+        sm.X[t][0] = t < L ? kd : 0.f;  // (summed below)
+      }
     }
     __syncthreads();
-    // ---- dA o Gamma and dattn o Gamma in place
-    for (int e = tid; e < C * C; e += kGradThreads) {
-      const int t = e / C, s = e % C;
-      const float gam = s <= t ? __expf(sm.G[t] - sm.G[s]) : 0.f;
-      sm.dA[t][s] *= gam;
-      sm.dat[t][s] *= gam;
-    }
-    __syncthreads();
-    // ---- delta D^T into X ([C][K] rows): its row sums against Kt go to dG, dk takes it
-    mm(C, K, V, [&](int t, int c) { return DL[t * V + c]; }, [&](int c, int i) { return Dx[c * K + i]; },
-       [&](int t, int i, float x) { X[t * K + i] = x; });
-    __syncthreads();
-    if (tid < 32) {  // dG_t -= Kt_t . (delta D^T)_t;  dG_L += sum of it + e^{G_L} <D, S>
-      float tot = 0.f;
-      for (int t = tid; t < L; t += 32) {
-        float s = 0.f;
-        for (int i = 0; i < K; ++i) s = fmaf(KF[t * K + i], X[t * K + i], s);
-        s *= sm.ekt[t];
-        sm.dG[t] -= s;
-        tot += s;
-      }
-      float ds = 0.f;
+    if (tid < 32) {  // dG_L += sum_t Kt_t . (delta D^T)_t + e^{G_L} <D, S>
+      float tot = sm.X[tid][0] + sm.X[tid + 32][0], ds = 0.f;
       for (int e = tid; e < K * V; e += 32) ds = fmaf(Sx[e], Dx[e], ds);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         tot += __shfl_xor_sync(0xffffffffu, tot, o);
         ds += __shfl_xor_sync(0xffffffffu, ds, o);
       }
-      __syncwarp();
       if (tid == 0) sm.dG[L - 1] += tot + sm.scal[0] * ds;
-    }
-    __syncthreads();
-    if (tid < 32) {  // dg_t = sum_{u >= t} dG_u (reverse running sum over the chunk)
+      __syncwarp();
+      // dg_t = sum_{u >= t} dG_u (reverse running sum over the chunk)
       float x0 = sm.dG[63 - tid], x1 = sm.dG[31 - tid];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -333,32 +407,43 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
         if (tid >= o) { x0 += y0; x1 += y1; }
       }
       x1 += __shfl_sync(0xffffffffu, x0, 31);
-      const int r0 = 63 - tid, r1 = 31 - tid;  // rows of x0, x1
+      const int r0 = 63 - tid, r1 = 31 - tid;
       if (r0 < L) a.dg[(t0 + r0) * a.hv + j] = x0;
       if (r1 < L) a.dg[(t0 + r1) * a.hv + j] = x1;
     }
-    // ---- dq = diag(e^G) dO S^T + (dattn o Gamma) K;  per value head, summed over the group later
+    // ---- dA o Gamma and dattn o Gamma in place
+    for (int e = tid; e < C * C; e += kGradThreads) {
+      const int t = e / C, s = e % C;
+      const float gm = s <= t ? gam(t, s) : 0.f;
+      sm.dA[t][s] *= gm;
+      sm.dat[t][s] *= gm;
+    }
+    // ---- dq = diag(e^G) dO S^T + (dattn o Gamma) K  (per value head; the group sum follows)
     float* dqv = a.dqv + (t0 * a.hv + j) * (int64_t)K;
     float* dkv = a.dkv + (t0 * a.hv + j) * (int64_t)K;
     const int64_t rs = (int64_t)a.hv * K;  // row stride of dqv, dkv
-    mm(L, K, V, [&](int t, int c) { return DO[t * V + c]; }, [&](int c, int i) { return Sx[c * K + i]; },
-       [&](int t, int i, float x) { dqv[t * rs + i] = sm.eG[t] * x; });
-    __syncthreads();
-    mm(L, K, L, [&](int t, int s) { return sm.dat[t][s]; }, [&](int s, int i) { return KF[s * K + i]; },
-       [&](int t, int i, float x) { dqv[t * rs + i] += x; });
-    // ---- dk = -diag(beta e^G) dB S^T + diag(beta) (dA o Gamma) K + (dA o Gamma)^T diag(beta) K
-    //          + (dattn o Gamma)^T Q + diag(e^{G_L - G}) delta D^T
-    mm(L, K, V, [&](int t, int c) { return DD[t * V + c]; }, [&](int c, int i) { return Sx[c * K + i]; },
-       [&](int t, int i, float x) { dkv[t * rs + i] = sm.ekt[t] * X[t * K + i] - sm.b[t] * sm.eG[t] * x; });
-    __syncthreads();
-    mm(L, K, L, [&](int t, int s) { return sm.dA[t][s]; }, [&](int s, int i) { return KF[s * K + i]; },
-       [&](int t, int i, float x) { dkv[t * rs + i] += sm.b[t] * x; });
-    __syncthreads();
-    mm(L, K, L, [&](int t, int s) { return sm.dA[s][t] * sm.b[s]; }, [&](int s, int i) { return KF[s * K + i]; },
-       [&](int t, int i, float x) { dkv[t * rs + i] += x; });
-    __syncthreads();
-    mm(L, K, L, [&](int t, int s) { return sm.dat[s][t]; }, [&](int s, int i) { return QF[s * K + i]; },
-       [&](int t, int i, float x) { dkv[t * rs + i] += x; });
+    mm<K, false, false>(sm, V, [&](int t, int c) { return DO[t * V + c]; },
+                        [&](int c, int i) { return Sx[c * K + i]; },
+                        [&](int t, int i, float x) { if (t < L) dqv[t * rs + i] = sm.eG[t] * x; });
+    mm<K, false, false>(sm, C, [&](int t, int s) { return sm.dat[t][s]; },
+                        [&](int s, int i) { return KF[s * K + i]; },
+                        [&](int t, int i, float x) { if (t < L) dqv[t * rs + i] += x; });
+    // ---- dk = -diag(beta e^G) dB S^T + diag(e^{G_L - G}) delta D^T + diag(beta) (dA o Gamma) K
+    //          + (dA o Gamma)^T diag(beta) K + (dattn o Gamma)^T Q
+    mm<K, false, false>(sm, V, [&](int t, int c) { return DD[t * V + c]; },
+                        [&](int c, int i) { return Sx[c * K + i]; },
+                        [&](int t, int i, float x) {
+                          if (t < L) dkv[t * rs + i] = sm.ekt[t] * XD[t * K + i] - sm.b[t] * sm.eG[t] * x;
+                        });
+    mm<K, false, false>(sm, C, [&](int t, int s) { return sm.dA[t][s]; },
+                        [&](int s, int i) { return KF[s * K + i]; },
+                        [&](int t, int i, float x) { if (t < L) dkv[t * rs + i] += sm.b[t] * x; });
+    mm<K, true, false>(sm, C, [&](int t, int s) { return sm.dA[s][t] * sm.b[s]; },
+                       [&](int s, int i) { return KF[s * K + i]; },
+                       [&](int t, int i, float x) { if (t < L) dkv[t * rs + i] += x; });
+    mm<K, true, false>(sm, C, [&](int t, int s) { return sm.dat[s][t]; },
+                       [&](int s, int i) { return QF[s * K + i]; },
+                       [&](int t, int i, float x) { if (t < L) dkv[t * rs + i] += x; });
   }
 }
 
@@ -384,12 +469,18 @@ __global__ void group_sum_kernel(BwdArgs a) {
 template <int K, int V>
 cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
   const dim3 cg((unsigned)(a.N * a.hv), (unsigned)(V / 32));
-  column_kernel<K, false><<<cg, kColThreads, 0, s>>>(a);
-  column_kernel<K, true><<<cg, kColThreads, 0, s>>>(a);
-  cudaError_t e = cudaFuncSetAttribute(chunk_grad_kernel<K, V>,
+  cudaError_t e = cudaFuncSetAttribute(column_kernel<K, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)sizeof(GradSmem));
+                                       (int)column_smem<K, false>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(column_kernel<K, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)column_smem<K, true>());
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(chunk_grad_kernel<K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(GradSmem));
   if (e != cudaSuccess) return e;
+  column_kernel<K, false><<<cg, kColThreads, column_smem<K, false>(), s>>>(a);
+  column_kernel<K, true><<<cg, kColThreads, column_smem<K, true>(), s>>>(a);
   chunk_grad_kernel<K, V><<<a.grad_ctas, kGradThreads, sizeof(GradSmem), s>>>(a);
   group_sum_kernel<<<1024, 256, 0, s>>>(a);
   return cudaGetLastError();
