@@ -53,6 +53,22 @@ __device__ __forceinline__ void st_io(void* p, int64_t i, float x, bool bf16) {
     static_cast<float*>(p)[i] = x;
 }
 
+// eight consecutive I/O elements (16-byte aligned in bf16, 32-byte in fp32) as fp32 into dst
+__device__ __forceinline__ void ld8(const void* p, int64_t i, bool bf16, float* dst) {
+  if (bf16) {
+    const uint4 x = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p) + i);
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&x);
+    const float2 f0 = __bfloat1622float2(h2[0]), f1 = __bfloat1622float2(h2[1]);
+    const float2 f2 = __bfloat1622float2(h2[2]), f3 = __bfloat1622float2(h2[3]);
+    *reinterpret_cast<float4*>(dst) = make_float4(f0.x, f0.y, f1.x, f1.y);
+    *reinterpret_cast<float4*>(dst + 4) = make_float4(f2.x, f2.y, f3.x, f3.y);
+  } else {
+    const float4* f = reinterpret_cast<const float4*>(static_cast<const float*>(p) + i);
+    *reinterpret_cast<float4*>(dst) = f[0];
+    *reinterpret_cast<float4*>(dst + 4) = f[1];
+  }
+}
+
 // first chunk slot of sequence n (slots enumerate (sequence, chunk) pairs; see slot_to_chunk)
 __device__ __forceinline__ int64_t slot_base(const int32_t* cu, int n) {
   return cu ? (int64_t)cu[n] / C + n : 0;
@@ -103,14 +119,14 @@ __global__ void __launch_bounds__(kColThreads) column_kernel(BwdArgs a) {
 #pragma unroll
     for (int i = 0; i < RPL; ++i) dst[p + 4 * i] = h[i];
     __syncthreads();  // the previous chunk's inputs have been used
-    for (int e = threadIdx.x; e < L * K; e += kColThreads) {
-      const int t = e / K, i = e % K;
-      ks[e] = ld_io(a.k, ((c0 + t) * a.hk + kh) * K + i, a.bf16);
-      if (REVERSE) qs[e] = ld_io(a.q, ((c0 + t) * a.hk + kh) * K + i, a.bf16);
+    for (int e = threadIdx.x; e < L * (K / 8); e += kColThreads) {
+      const int t = e / (K / 8), i = 8 * (e % (K / 8));
+      ld8(a.k, ((c0 + t) * a.hk + kh) * K + i, a.bf16, ks + t * K + i);
+      if (REVERSE) ld8(a.q, ((c0 + t) * a.hk + kh) * K + i, a.bf16, qs + t * K + i);
     }
-    for (int e = threadIdx.x; e < L * 32; e += kColThreads) {
-      const int t = e / 32, cc = e % 32;
-      vs[e] = ld_io(vin, ((c0 + t) * a.hv + j) * a.V + v0 + cc, a.bf16);
+    for (int e = threadIdx.x; e < L * 4; e += kColThreads) {
+      const int t = e / 4, cc = 8 * (e % 4);
+      ld8(vin, ((c0 + t) * a.hv + j) * a.V + v0 + cc, a.bf16, vs + t * 32 + cc);
     }
     for (int t = threadIdx.x; t < L; t += kColThreads) {
       gs[t] = __expf(a.g[(c0 + t) * a.hv + j]);
@@ -126,13 +142,15 @@ __global__ void __launch_bounds__(kColThreads) column_kernel(BwdArgs a) {
 #pragma unroll
         for (int i = 0; i < RPL; ++i) h[i] = fmaf(qr[4 * i], x, h[i]);
       }
-      float d0 = 0.f, d1 = 0.f;
+      float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
 #pragma unroll
-      for (int i = 0; i < RPL; i += 2) {
+      for (int i = 0; i < RPL; i += 4) {
         d0 = fmaf(kr[4 * i], h[i], d0);
         d1 = fmaf(kr[4 * i + 4], h[i + 1], d1);
+        d2 = fmaf(kr[4 * i + 8], h[i + 2], d2);
+        d3 = fmaf(kr[4 * i + 12], h[i + 3], d3);
       }
-      float d = d0 + d1;
+      float d = (d0 + d1) + (d2 + d3);
       d += __shfl_xor_sync(0xffffffffu, d, 1);
       d += __shfl_xor_sync(0xffffffffu, d, 2);
       if (REVERSE) {  // dd = k . F;  dh <- alpha (F - beta k dd)
@@ -164,12 +182,13 @@ struct GradSmem {
   float As[C][33];      // product tiles
   float Bs[32][129];
   float X[C][129];      // the triangular solves
+  float KF[C][129], QF[C][129];  // k, q of the chunk (fp32; rows past the chunk are zero)
 };
 
 // floats of one CTA's workspace slice: K S, Q S, R, delta, d_delta (then dB), dout as [C][V];
-// k, q, delta D^T as [C][K]
+// delta D^T as [C][K]
 template <int K, int V>
-__host__ __device__ constexpr int64_t grad_slice() { return 6 * (int64_t)C * V + 3 * (int64_t)C * K; }
+__host__ __device__ constexpr int64_t grad_slice() { return 6 * (int64_t)C * V + (int64_t)C * K; }
 
 // out(i, c, x) for i < C, c < N with x = sum_{y < Y} A(i, y) B(y, c) (Y a multiple of 32):
 // 32-wide slices of y are staged in shared memory; thread (ty, tx) of 16 x 32 accumulates rows
@@ -228,9 +247,9 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
   float* DL = R + C * V;     // [C][V]  delta
   float* DD = DL + C * V;    // [C][V]  d_delta, then dB
   float* DO = DD + C * V;    // [C][V]  dout (fp32)
-  float* KF = DO + C * V;    // [C][K]  k (fp32)
-  float* QF = KF + C * K;    // [C][K]  q (fp32)
-  float* XD = QF + C * K;    // [C][K]  delta D^T
+  float* XD = DO + C * V;    // [C][K]  delta D^T
+  auto KF = [&](int t, int i) -> float& { return sm.KF[t][i]; };
+  auto QF = [&](int t, int i) -> float& { return sm.QF[t][i]; };
   for (int64_t u = blockIdx.x; u < units; u += gridDim.x) {
     const int64_t slot = u / a.hv;
     const int j = (int)(u % a.hv), kh = j / (a.hv / a.hk);
@@ -270,8 +289,8 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
     for (int e = tid; e < C * K; e += kGradThreads) {
       const int t = e / K, i = e % K;
       const bool ok = t < L;
-      KF[e] = ok ? ld_io(a.k, ((t0 + t) * a.hk + kh) * K + i, a.bf16) : 0.f;
-      QF[e] = ok ? ld_io(a.q, ((t0 + t) * a.hk + kh) * K + i, a.bf16) : 0.f;
+      KF(t, i) = ok ? ld_io(a.k, ((t0 + t) * a.hk + kh) * K + i, a.bf16) : 0.f;
+      QF(t, i) = ok ? ld_io(a.q, ((t0 + t) * a.hk + kh) * K + i, a.bf16) : 0.f;
     }
     for (int e = tid; e < C * V; e += kGradThreads) {
       const int t = e / V, c = e % V;
@@ -280,16 +299,16 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
     __syncthreads();
     auto gam = [&](int t, int s) { return __expf(sm.G[t] - sm.G[s]); };  // for s <= t
     // ---- Gamma o K K^T (strictly lower), attn; K S, Q S
-    mm<C, false, true>(sm, K, [&](int t, int y) { return KF[t * K + y]; },
-                       [&](int y, int s) { return KF[s * K + y]; },
+    mm<C, false, true>(sm, K, [&](int t, int y) { return KF(t, y); },
+                       [&](int y, int s) { return KF(s, y); },
                        [&](int t, int s, float x) { sm.GKK[t][s] = (s < t && t < L) ? gam(t, s) * x : 0.f; });
-    mm<C, false, true>(sm, K, [&](int t, int y) { return QF[t * K + y]; },
-                       [&](int y, int s) { return KF[s * K + y]; },
+    mm<C, false, true>(sm, K, [&](int t, int y) { return QF(t, y); },
+                       [&](int y, int s) { return KF(s, y); },
                        [&](int t, int s, float x) { sm.At[t][s] = (s <= t && t < L) ? gam(t, s) * x : 0.f; });
-    mm<V, false, true>(sm, K, [&](int t, int y) { return KF[t * K + y]; },
+    mm<V, false, true>(sm, K, [&](int t, int y) { return KF(t, y); },
                        [&](int y, int c) { return Sx[c * K + y]; },
                        [&](int t, int c, float x) { KS[t * V + c] = x; });
-    mm<V, false, true>(sm, K, [&](int t, int y) { return QF[t * K + y]; },
+    mm<V, false, true>(sm, K, [&](int t, int y) { return QF(t, y); },
                        [&](int y, int c) { return Sx[c * K + y]; },
                        [&](int t, int c, float x) { QS[t * V + c] = x; });
     __syncthreads();
@@ -321,7 +340,7 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
     mm<V, true, false>(sm, C, [&](int t, int s) { return sm.At[s][t]; },
                        [&](int s, int c) { return DO[s * V + c]; },
                        [&](int t, int c, float x) { DD[t * V + c] = x; });
-    mm<V, false, true>(sm, K, [&](int t, int y) { return sm.ekt[t] * KF[t * K + y]; },
+    mm<V, false, true>(sm, K, [&](int t, int y) { return sm.ekt[t] * KF(t, y); },
                        [&](int y, int c) { return Dx[c * K + y]; },
                        [&](int t, int c, float x) { sm.X[t][c] = t < L ? DD[t * V + c] + x : 0.f; });
     __syncthreads();
@@ -373,7 +392,7 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
           dg += sm.dA[t][s] * sm.b[t] * sm.GKK[t][s] - sm.dA[s][t] * sm.b[s] * sm.GKK[s][t];
           dg += sm.dat[t][s] * sm.At[t][s] - sm.dat[s][t] * sm.At[s][t];
         }
-        for (int i = p; i < K; i += 8) kd = fmaf(KF[t * K + i], XD[t * K + i], kd);
+        for (int i = p; i < K; i += 8) kd = fmaf(KF(t, i), XD[t * K + i], kd);
       }
 #pragma unroll
       for (int o = 1; o < 8; o <<= 1) {
@@ -426,7 +445,7 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
                         [&](int c, int i) { return Sx[c * K + i]; },
                         [&](int t, int i, float x) { if (t < L) dqv[t * rs + i] = sm.eG[t] * x; });
     mm<K, false, false>(sm, C, [&](int t, int s) { return sm.dat[t][s]; },
-                        [&](int s, int i) { return KF[s * K + i]; },
+                        [&](int s, int i) { return KF(s, i); },
                         [&](int t, int i, float x) { if (t < L) dqv[t * rs + i] += x; });
     // ---- dk = -diag(beta e^G) dB S^T + diag(e^{G_L - G}) delta D^T + diag(beta) (dA o Gamma) K
     //          + (dA o Gamma)^T diag(beta) K + (dattn o Gamma)^T Q
@@ -436,13 +455,13 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
                           if (t < L) dkv[t * rs + i] = sm.ekt[t] * XD[t * K + i] - sm.b[t] * sm.eG[t] * x;
                         });
     mm<K, false, false>(sm, C, [&](int t, int s) { return sm.dA[t][s]; },
-                        [&](int s, int i) { return KF[s * K + i]; },
+                        [&](int s, int i) { return KF(s, i); },
                         [&](int t, int i, float x) { if (t < L) dkv[t * rs + i] += sm.b[t] * x; });
     mm<K, true, false>(sm, C, [&](int t, int s) { return sm.dA[s][t] * sm.b[s]; },
-                       [&](int s, int i) { return KF[s * K + i]; },
+                       [&](int s, int i) { return KF(s, i); },
                        [&](int t, int i, float x) { if (t < L) dkv[t * rs + i] += x; });
     mm<K, true, false>(sm, C, [&](int t, int s) { return sm.dat[s][t]; },
-                       [&](int s, int i) { return QF[s * K + i]; },
+                       [&](int s, int i) { return QF(s, i); },
                        [&](int t, int i, float x) { if (t < L) dkv[t * rs + i] += x; });
   }
 }
@@ -491,7 +510,7 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
 int64_t bwd_slots(int64_t T, int N) { return T / kChunk + N; }
 
 size_t bwd_scratch_floats(int K, int V, int ctas) {
-  return (size_t)ctas * (6 * (size_t)kChunk * V + 3 * (size_t)kChunk * K);
+  return (size_t)ctas * (6 * (size_t)kChunk * V + (size_t)kChunk * K);
 }
 
 cudaError_t backward(const BwdArgs& a, cudaStream_t s) {
