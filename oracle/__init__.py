@@ -186,6 +186,50 @@ def token_backward(q, k, v, g, beta, dout, h0=None, dh_final=None, cu_seqlens=No
     return r
 
 
+def prologue(x, conv_w, a, b, A_log, dt_bias, hk, hv, K, V, conv_state=None, cu_seqlens=None,
+             activation="none"):
+    """The layer-side steps ahead of the recurrence, in fp64 (page "Add context parallelism to
+    the Gated Delta Net", section "Implementation", layer-side bullets: a causal depthwise conv
+    over the q | k | v channels whose halo is conv_kernel_dim - 1 tokens; page "RFC(qwen35): TP
+    Phase2", section "Partition Contract": a per-request conv state of qkv_dim x
+    (conv_kernel_dim - 1) inputs).  Readings where the pages are silent: the conv output may
+    pass through SiLU (``activation``); q and k are L2-normalised per (token, head); g =
+    -exp(A_log) softplus(a + dt_bias) and beta = sigmoid(b) per value head.
+      x [T, 2 hk K + hv V] (q channels, then k, then v); conv_w [channels, W];
+      conv_state [N, channels, W - 1] (the inputs before each sequence, oldest first; None =
+      zeros); a, b [T, hv]; A_log, dt_bias [hv].
+    Returns q, k [T, hk, K], v [T, hv, V], g, beta [T, hv], new conv state [N, channels, W - 1]
+    (the last W - 1 inputs of each sequence, older state entries shifting in when a sequence is
+    shorter than W - 1)."""
+    x, conv_w, a, b, A_log, dt_bias = map(_f64, (x, conv_w, a, b, A_log, dt_bias))
+    T, Ch = x.shape
+    W = conv_w.shape[1]
+    cu = _cu(cu_seqlens, T)
+    N = len(cu) - 1
+    st = np.zeros((N, Ch, W - 1)) if conv_state is None else _f64(conv_state)
+    y = np.zeros((T, Ch))
+    new_state = np.zeros((N, Ch, W - 1))
+    for n in range(N):
+        # the sequence's inputs with the W - 1 carried ones in front: ext[s + W - 1] = x[cu[n] + s]
+        ext = np.concatenate([st[n].T, x[cu[n]:cu[n + 1]]], axis=0)
+        L = cu[n + 1] - cu[n]
+        for t in range(L):
+            y[cu[n] + t] = np.sum(ext[t:t + W] * conv_w.T, axis=0)
+        new_state[n] = ext[len(ext) - (W - 1):].T if W > 1 else new_state[n]
+    if activation == "silu":
+        y = y / (1.0 + np.exp(-y))
+    elif activation != "none":
+        raise ValueError(activation)
+    q = y[:, :hk * K].reshape(T, hk, K)
+    k = y[:, hk * K:2 * hk * K].reshape(T, hk, K)
+    v = y[:, 2 * hk * K:].reshape(T, hv, V)
+    q = q / np.sqrt(np.maximum(np.sum(q * q, -1, keepdims=True), 1e-12))
+    k = k / np.sqrt(np.maximum(np.sum(k * k, -1, keepdims=True), 1e-12))
+    g = -np.exp(A_log)[None, :] * np.logaddexp(0.0, a + dt_bias[None, :])
+    beta = 1.0 / (1.0 + np.exp(-b))
+    return q, k, v, g, beta, new_state
+
+
 def decode(q, k, v, g, beta, state, slot, nthreads=None):
     """One decode step over a pool of per-slot states ("RFC(qwen35): TP Phase2", sections
     "Execution Contract" -- decode updates only the request's own recurrent state -- and
