@@ -45,6 +45,10 @@ BWD_FLOP_PER_TOKEN = HV * (2 * (6 * C * KD * VD + 6 * C * C * KD + 3 * C * C * V
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (maximum SM clock)
 FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 BWD_STEPS = 5
+# prologue: bytes per token it must move (x read, q, k, v written in bf16; a, b read in bf16;
+# g, beta written in fp32); W = 4 taps, SiLU
+CH = 2 * HK * KD + HV * VD
+PRO_BYTES_PER_TOKEN = CH * 2 * 2 + HV * 2 * 2 + HV * 4 * 2
 # decode: requests per step, slots in the state pool, timed steps; bytes one step must move
 # (each request's fp32 state read and written once per value head, q, k, v, out, g, beta, slot)
 DEC_B, DEC_SLOTS, DEC_STEPS = 256, 256, 200
@@ -458,6 +462,32 @@ def run_ours(args, ws, rank, local):
         raise gdn.GdnError(st, "backward device status")
     del bws, bo, dout
 
+    # the prologue at the same workload: q, k, v, g, beta from projection-shaped inputs
+    gen = torch.Generator().manual_seed(200 + rank)
+    px = torch.randn(T, CH, generator=gen).to(torch.bfloat16).to(dev)
+    pw = (torch.randn(CH, 4, generator=gen) * 0.5).to(dev)
+    pab = torch.randn(2, T, HV, generator=gen).to(torch.bfloat16).to(dev)
+    pal = torch.full((HV,), -2.3, device=dev)
+    pdt = torch.zeros(HV, device=dev)
+    pp = gdn.PrologueProblem(T, 1, HK, HV, KD, VD, 4, 1, gdn.GDN_BF16)
+    po = [torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"]),
+          torch.empty_like(d["g"]), torch.empty_like(d["beta"])]
+
+    def pro_step():
+        gdn.gdn_prologue(pp, px, pw, None, pab[0], pab[1], pal, pdt, None, *po, None,
+                         stream=stream)
+
+    for _ in range(3):
+        pro_step()
+    barrier()
+    e0.record(stream)
+    for _ in range(20):
+        pro_step()
+    e1.record(stream)
+    barrier()
+    pro_ms = e0.elapsed_time(e1) / 20
+    del px, pab, po
+
     if rank != 0:
         return None
     hbm, tf, tf_sus, src = peaks()
@@ -541,6 +571,18 @@ def run_ours(args, ws, rank, local):
                          "frac": BWD_FLOP_PER_TOKEN * T / (bwd_ms / 1e3) / 1e12 / FP32_ALU_TFLOPS,
                          "peak_source": "fp32 FMA units x maximum SM clock (not measured)",
                          "algorithmic_flop_per_step": BWD_FLOP_PER_TOKEN * T,
+                         "traffic": None}},
+        "prologue": {
+            "workload": f"conv (4 taps, SiLU) + L2 norm + g, beta: T={T}, {CH} channels, "
+                        f"Hk={HK} Hv={HV} K=V={KD} bf16",
+            "ms_per_step": pro_ms, "tokens_per_s": T / (pro_ms / 1e3), "steps": 20,
+            "gpu_launches_per_step": 1,
+            "roofline": {"kernel": "prologue_kernel", "bound": "hbm",
+                         "achieved": PRO_BYTES_PER_TOKEN * T / (pro_ms / 1e3) / 1e9,
+                         "peak": hbm, "unit": "GB/s",
+                         "frac": PRO_BYTES_PER_TOKEN * T / (pro_ms / 1e3) / 1e9 / hbm,
+                         "peak_source": src,
+                         "algorithmic_bytes_per_launch": PRO_BYTES_PER_TOKEN * T,
                          "traffic": None}},
         "decode": {
             "workload": f"decode bf16 B={DEC_B} requests, pool of {DEC_SLOTS} slots, Hk={HK} "

@@ -431,6 +431,50 @@ BwdLayout bwd_layout(const gdn_problem* p) {
   return L;
 }
 
+gdn_status gdn_prologue(const gdn_prologue_problem* p, const void* x, const float* conv_w,
+                        const void* conv_state_in, const void* a, const void* b,
+                        const float* A_log, const float* dt_bias, const int32_t* cu_seqlens,
+                        void* q, void* k, void* v, float* g, float* beta, void* conv_state_out,
+                        int32_t* dev_status, cudaStream_t stream) {
+  if (!p) return GDN_ERR_INVALID_ARGUMENT;
+  if (p->total_tokens < 0 || p->total_tokens > (int64_t)INT32_MAX || p->num_seqs < 1 ||
+      p->hk < 1 || p->hv < 1 || p->k_dim < 1 || p->v_dim < 1 || p->hv % p->hk != 0)
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (p->io_dtype != GDN_BF16 && p->io_dtype != GDN_F32) return GDN_ERR_UNSUPPORTED;
+  if (p->k_dim > 128 || p->v_dim > 128 || p->conv_width < 1 || p->conv_width > 4 ||
+      (p->activation != 0 && p->activation != 1) || 2 * p->hk + p->hv > 65535)
+    return GDN_ERR_UNSUPPORTED;
+  if (!conv_w || !A_log || !dt_bias || (p->total_tokens > 0 &&
+      (!x || !a || !b || !q || !k || !v || !g || !beta)))
+    return GDN_ERR_INVALID_ARGUMENT;
+  if (!cu_seqlens && p->num_seqs != 1) return GDN_ERR_INVALID_ARGUMENT;
+  gdn::PrologueArgs pa;
+  memset(&pa, 0, sizeof(pa));
+  pa.T = p->total_tokens;
+  pa.N = p->num_seqs;
+  pa.hk = p->hk;
+  pa.hv = p->hv;
+  pa.K = p->k_dim;
+  pa.V = p->v_dim;
+  pa.W = p->conv_width;
+  pa.bf16 = p->io_dtype == GDN_BF16;
+  pa.silu = p->activation == 1;
+  pa.x = x; pa.state_in = conv_state_in; pa.a = a; pa.b = b;
+  pa.conv_w = conv_w; pa.A_log = A_log; pa.dt_bias = dt_bias; pa.cu = cu_seqlens;
+  pa.q = q; pa.k = k; pa.v = v; pa.state_out = conv_state_out; pa.g = g; pa.beta = beta;
+  pa.status = dev_status;
+  if (cu_seqlens) {
+    Args va;
+    memset(&va, 0, sizeof(va));
+    va.T = p->total_tokens;
+    va.N = p->num_seqs;
+    va.cu = cu_seqlens;
+    va.status = dev_status;
+    GDN_TRY(gdn::launch_validate_cu(va, stream));
+  }
+  return to_status(gdn::prologue(pa, stream));
+}
+
 gdn_status gdn_check_decode_problem(const gdn_decode_problem* p) {
   if (!p) return GDN_ERR_INVALID_ARGUMENT;
   if (p->batch < 0 || p->slots < 1 || p->hk < 1 || p->hv < 1 || p->k_dim < 1 || p->v_dim < 1)

@@ -90,4 +90,18 @@ int64_t bwd_slots(int64_t T, int N);
 size_t bwd_scratch_floats(int K, int V, int ctas);
 cudaError_t backward(const BwdArgs& a, cudaStream_t s);
 
+// The layer prologue (gdn_prologue).
+struct PrologueArgs {
+  int64_t T;
+  int N, hk, hv, K, V, W;
+  bool bf16, silu;
+  const void *x, *state_in, *a, *b;
+  const float *conv_w, *A_log, *dt_bias;
+  const int32_t* cu;
+  void *q, *k, *v, *state_out;
+  float *g, *beta;
+  int32_t* status;
+};
+cudaError_t prologue(const PrologueArgs& a, cudaStream_t s);
+
 }  // namespace gdn

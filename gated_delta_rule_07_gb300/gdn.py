@@ -36,7 +36,7 @@ EXPORTED = ("gdn_status_string", "gdn_check_problem", "gdn_workspace_size", "gdn
             "gdn_segment_summary_fused", "gdn_chunk_emit_fused", "gdn_last_error_string",
             "gdn_forward_static_scratch", "gdn_forward_timed", "gdn_forward_with_limits",
             "gdn_check_decode_problem", "gdn_decode_step", "gdn_backward_workspace_size",
-            "gdn_backward")
+            "gdn_backward", "gdn_prologue")
 
 
 class Problem(ctypes.Structure):
@@ -50,6 +50,13 @@ class DecodeProblem(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("slots", ctypes.c_int32), ("hk", ctypes.c_int32),
                 ("hv", ctypes.c_int32), ("k_dim", ctypes.c_int32), ("v_dim", ctypes.c_int32),
                 ("io_dtype", ctypes.c_int32)]
+
+
+class PrologueProblem(ctypes.Structure):
+    _fields_ = [("total_tokens", ctypes.c_int64), ("num_seqs", ctypes.c_int32),
+                ("hk", ctypes.c_int32), ("hv", ctypes.c_int32), ("k_dim", ctypes.c_int32),
+                ("v_dim", ctypes.c_int32), ("conv_width", ctypes.c_int32),
+                ("activation", ctypes.c_int32), ("io_dtype", ctypes.c_int32)]
 
 
 class GdnError(RuntimeError):
@@ -89,6 +96,8 @@ _lib.gdn_backward_workspace_size.restype = ctypes.c_size_t
 _lib.gdn_backward_workspace_size.argtypes = [_pp]
 _lib.gdn_backward.argtypes = [_pp, _vp, _vp, _vp, _fp, _fp, _fp, _ip, _vp, _fp, _vp, _vp, _vp,
                               _fp, _fp, _fp, _vp, ctypes.c_size_t, _vp]
+_lib.gdn_prologue.argtypes = [ctypes.POINTER(PrologueProblem), _vp, _fp, _vp, _vp, _vp, _fp, _fp,
+                              _ip, _vp, _vp, _vp, _fp, _fp, _vp, _ip, _vp]
 _dpp = ctypes.POINTER(DecodeProblem)
 _lib.gdn_check_decode_problem.argtypes = [_dpp]
 _lib.gdn_decode_step.argtypes = [_dpp, _vp, _vp, _vp, _fp, _fp, _ip, _fp, _vp, _ip, _vp]
@@ -259,6 +268,37 @@ def backward(q, k, v, g, beta, dout, h0=None, dh_final=None, cu_seqlens=None, wo
     if check_status:
         _check(gdn_device_status(workspace, True, stream), "gdn_backward (device status)")
     return dq, dk, dv, dg, dbeta, dh0
+
+
+def gdn_prologue(p, x, conv_w, conv_state_in, a, b, A_log, dt_bias, cu_seqlens, q, k, v, g,
+                 beta, conv_state_out, dev_status=None, stream=None):
+    _check(_lib.gdn_prologue(ctypes.byref(p), _ptr(x), _ptr(conv_w), _ptr(conv_state_in), _ptr(a),
+                             _ptr(b), _ptr(A_log), _ptr(dt_bias), _ptr(cu_seqlens), _ptr(q),
+                             _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(conv_state_out),
+                             _ptr(dev_status), _stream(stream)), "gdn_prologue")
+
+
+def prologue(x, conv_w, a, b, A_log, dt_bias, hk, hv, K, V, conv_state=None, cu_seqlens=None,
+             activation="none", check_status=False, stream=None):
+    """q, k, v, g, beta, new conv state from the projections (layouts of include/gdn.h)."""
+    T = x.shape[0]
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    W = conv_w.shape[1]
+    io = {torch.bfloat16: GDN_BF16, torch.float32: GDN_F32}[x.dtype]
+    p = PrologueProblem(T, N, hk, hv, K, V, W, {"none": 0, "silu": 1}[activation], io)
+    dev = x.device
+    q = torch.empty(T, hk, K, dtype=x.dtype, device=dev)
+    k = torch.empty_like(q)
+    v = torch.empty(T, hv, V, dtype=x.dtype, device=dev)
+    g = torch.empty(T, hv, dtype=torch.float32, device=dev)
+    beta = torch.empty_like(g)
+    new_state = torch.empty(N, x.shape[1], max(W - 1, 0), dtype=x.dtype, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev) if check_status else None
+    gdn_prologue(p, x, conv_w, conv_state, a, b, A_log, dt_bias, cu_seqlens, q, k, v, g, beta,
+                 new_state if W > 1 else None, st, stream)
+    if check_status:
+        _check(gdn_device_status(st, True, stream), "gdn_prologue (device status)")
+    return q, k, v, g, beta, new_state
 
 
 def make_decode_problem(B, slots, hk, hv, K, V, dtype=torch.bfloat16) -> DecodeProblem:

@@ -268,6 +268,42 @@ gdn_status gdn_backward(const gdn_problem* p, const void* q, const void* k, cons
                         void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------- */
+/* Prologue: the layer-side steps that produce q, k, v, g, beta from the projections.          */
+
+typedef struct gdn_prologue_problem {
+    int64_t total_tokens;     /* T >= 0                                                     */
+    int32_t num_seqs;         /* N >= 1                                                     */
+    int32_t hk, hv;           /* key heads, value heads (hv % hk == 0)                      */
+    int32_t k_dim, v_dim;     /* K, V in [1, 128]                                           */
+    int32_t conv_width;       /* W in [1, 4]: taps of the causal conv                       */
+    int32_t activation;       /* 0: none, 1: SiLU after the conv                            */
+    int32_t io_dtype;         /* gdn_dtype of x, the conv states, a, b, q, k, v             */
+} gdn_prologue_problem;
+
+/* The layer prologue ahead of the recurrence (page "Add context parallelism to the Gated Delta
+ * Net", section "Implementation", layer-side bullets: a causal depthwise conv over the q | k | v
+ * channels with a halo of conv_kernel_dim - 1 tokens; page "RFC(qwen35): TP Phase2", section
+ * "Partition Contract": a per-request conv state of qkv_dim x (conv_kernel_dim - 1) inputs).
+ * With Ch = 2 hk K + hv V channels (q's, then k's, then v's):
+ *     y_t[c] = sum_{i < W} conv_w[c][i] x_{t-W+1+i}[c]     (inputs before a sequence's start
+ *              come from conv_state_in[n][c][0 .. W-2], oldest first, or are 0 when it is NULL)
+ *     y -> SiLU(y) when activation = 1;  q, k = their channels / max(L2 norm, 1e-6) per head;
+ *     v = its channels;  g = -exp(A_log) softplus(a + dt_bias);  beta = sigmoid(b)
+ * (the optional SiLU, the L2 normalisation and the g, beta maps are readings: the pages name
+ * these steps without formulas).
+ *   x [T, Ch] io dtype;  conv_w [Ch, W] fp32;  conv_state_in, conv_state_out [N, Ch, W-1] io dtype
+ *   (either may be NULL; out may alias in: it receives each sequence's last W-1 inputs, older
+ *   entries shifting in when a sequence is shorter);  a, b [T, hv] io dtype;  A_log, dt_bias
+ *   [hv] fp32;  outputs q, k [T, hk, K], v [T, hv, V] io dtype, g, beta [T, hv] fp32, in the
+ *   layouts gdn_forward reads.  cu_seqlens as for gdn_forward (device-checked; dev_status
+ *   records GDN_ERR_DEVICE_INPUT).  HBM-bound elementwise kernels. */
+gdn_status gdn_prologue(const gdn_prologue_problem* p, const void* x, const float* conv_w,
+                        const void* conv_state_in, const void* a, const void* b,
+                        const float* A_log, const float* dt_bias, const int32_t* cu_seqlens,
+                        void* q, void* k, void* v, float* g, float* beta, void* conv_state_out,
+                        int32_t* dev_status, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------- */
 /* Decode: one token per request over a pool of per-slot recurrent states.                   */
 
 typedef struct gdn_decode_problem {

@@ -184,3 +184,22 @@ def test_backward_rejects_bad_arguments_before_any_launch(gdn):
     # the state and state-gradient checkpoints: 2 * 4 * K * V bytes per chunk and value head
     ws = gdn.gdn_backward_workspace_size(prob(gdn, T=65536))
     assert ws >= 2 * (65536 // 64) * 32 * 128 * 128 * 4
+
+
+def test_prologue_rejects_bad_arguments_before_any_launch(gdn):
+    fake = 1 << 20
+    L = gdn._lib
+    by = ctypes.byref
+
+    def call(**kw):
+        base = dict(T=64, N=1, hk=2, hv=4, K=64, V=64, W=4, act=0, io=0)
+        base.update(kw)
+        p = gdn.PrologueProblem(base["T"], base["N"], base["hk"], base["hv"], base["K"],
+                                base["V"], base["W"], base["act"], base["io"])
+        return L.gdn_prologue(by(p), fake, fake, None, fake, fake, fake, fake, None, fake, fake,
+                              fake, fake, fake, None, None, None)
+
+    assert call(W=5) == 2 and call(W=0) == 2 and call(act=2) == 2 and call(K=256) == 2
+    assert call(hk=3) == 1 and call(N=2) == 1 and call(T=-1) == 1 and call(io=5) == 2
+    assert L.gdn_prologue(None, fake, fake, None, fake, fake, fake, fake, None, fake, fake, fake,
+                          fake, fake, None, None, None) == 1
