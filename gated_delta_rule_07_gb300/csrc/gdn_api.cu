@@ -441,13 +441,16 @@ gdn_status gdn_prologue(const gdn_prologue_problem* p, const void* x, const floa
       p->hk < 1 || p->hv < 1 || p->k_dim < 1 || p->v_dim < 1 || p->hv % p->hk != 0)
     return GDN_ERR_INVALID_ARGUMENT;
   if (p->io_dtype != GDN_BF16 && p->io_dtype != GDN_F32) return GDN_ERR_UNSUPPORTED;
-  if (p->k_dim > 128 || p->v_dim > 128 || p->conv_width < 1 || p->conv_width > 4 ||
+  if (p->k_dim > 128 || p->v_dim > 128 || p->k_dim % 8 || p->v_dim % 8 || p->conv_width < 1 ||
+      p->conv_width > 4 ||
       (p->activation != 0 && p->activation != 1) || 2 * p->hk + p->hv > 65535)
     return GDN_ERR_UNSUPPORTED;
   if (!conv_w || !A_log || !dt_bias || (p->total_tokens > 0 &&
       (!x || !a || !b || !q || !k || !v || !g || !beta)))
     return GDN_ERR_INVALID_ARGUMENT;
   if (!cu_seqlens && p->num_seqs != 1) return GDN_ERR_INVALID_ARGUMENT;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(k) || !aligned16(v))
+    return GDN_ERR_INVALID_ARGUMENT;
   gdn::PrologueArgs pa;
   memset(&pa, 0, sizeof(pa));
   pa.T = p->total_tokens;

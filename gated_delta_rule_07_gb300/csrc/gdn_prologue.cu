@@ -25,7 +25,7 @@ namespace gdn {
 namespace {
 
 constexpr int kTB = 64;       // tokens per CTA
-constexpr int kPThreads = 128;
+constexpr int kPThreads = 512;  // 128 channels x 4 quarters of the token block
 
 __device__ __forceinline__ float ld_x(const void* p, int64_t i, bool bf16) {
   return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i])
@@ -49,10 +49,55 @@ __device__ __forceinline__ int seq_of(const int32_t* cu, int N, int64_t t) {
   return lo;
 }
 
-// grid: (token blocks, 2 hk + hv head slices); thread = channel within the slice
+constexpr int kHalo = 3;       // inputs before a block's first token that its conv can read
+constexpr int kRow = 128 + 1;  // padded row of a staged tile (floats)
+
+// eight consecutive I/O elements (16-byte aligned in bf16, 32-byte in fp32) as fp32
+__device__ __forceinline__ void ld8x(const void* p, int64_t i, bool bf16, float* dst) {
+  if (bf16) {
+    const uint4 x = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p) + i);
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const float2 f = __bfloat1622float2(h2[m]);
+      dst[2 * m] = f.x;
+      dst[2 * m + 1] = f.y;
+    }
+  } else {
+    const float4* f = reinterpret_cast<const float4*>(static_cast<const float*>(p) + i);
+    const float4 u = f[0], w = f[1];
+    dst[0] = u.x; dst[1] = u.y; dst[2] = u.z; dst[3] = u.w;
+    dst[4] = w.x; dst[5] = w.y; dst[6] = w.z; dst[7] = w.w;
+  }
+}
+__device__ __forceinline__ void st8x(void* p, int64_t i, bool bf16, const float* v) {
+  if (bf16) {
+    uint4 x;
+    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&x);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) h2[m] = __floats2bfloat162_rn(v[2 * m], v[2 * m + 1]);
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p) + i) = x;
+  } else {
+    float4* f = reinterpret_cast<float4*>(static_cast<float*>(p) + i);
+    f[0] = make_float4(v[0], v[1], v[2], v[3]);
+    f[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+}
+
+struct ProSmem {
+  float xs[kTB + kHalo][kRow];  // inputs of tokens t0 - 3 .. t1 - 1 (rows before 0 are zero);
+                                // row t + 3 then receives token t's conv output
+  float inv[kTB];
+  int64_t sb[kTB];              // start of each token's sequence
+  int seq[kTB];                 // and its index
+};
+
+// grid: (token blocks, 2 hk + hv head slices).  The block's input tile is staged in shared memory
+// with 16-byte loads, the conv reads it (or, before a sequence's start, the sequence's conv
+// state), and the outputs leave with 16-byte stores.
 __global__ void __launch_bounds__(kPThreads) prologue_kernel(PrologueArgs a) {
-  __shared__ float ys[kTB][kPThreads + 1];
-  __shared__ float inv[kTB];
+  extern __shared__ __align__(16) uint8_t praw[];
+  ProSmem& sm = *reinterpret_cast<ProSmem*>(praw);
   const int blk = blockIdx.y, tid = threadIdx.x;
   const bool is_q = blk < a.hk, is_k = !is_q && blk < 2 * a.hk;
   const int hd = is_q ? blk : is_k ? blk - a.hk : blk - 2 * a.hk;  // head within its kind
@@ -63,68 +108,94 @@ __global__ void __launch_bounds__(kPThreads) prologue_kernel(PrologueArgs a) {
   const int64_t Ch = 2LL * a.hk * a.K + (int64_t)a.hv * a.V;
   const int64_t t0 = (int64_t)blockIdx.x * kTB;
   const int64_t t1 = (t0 + kTB < a.T) ? t0 + kTB : a.T;
-  const int W = a.W;
-  if (tid < width) {
-    const int64_t c = ch + tid;
-    float w[4];
+  const int nt = (int)(t1 - t0), W = a.W, g8 = width / 8;
+  // ---- stage the tile; each token's sequence
+  for (int e = tid; e < (nt + kHalo) * g8; e += kPThreads) {
+    const int r = e / g8, c8 = 8 * (e % g8);
+    const int64_t t = t0 - kHalo + r;
+    if (t >= 0) ld8x(a.x, t * Ch + ch + c8, a.bf16, &sm.xs[r][c8]);
+    else
+#pragma unroll
+      for (int m = 0; m < 8; ++m) sm.xs[r][c8 + m] = 0.f;
+  }
+  for (int t = tid; t < nt; t += kPThreads) {
+    const int n = seq_of(a.cu, a.N, t0 + t);
+    sm.seq[t] = n;
+    sm.sb[t] = a.cu ? a.cu[n] : 0;
+  }
+  __syncthreads();
+  // ---- the conv (and SiLU), a channel per thread: the window slides through the staged tile in
+  // registers; a token whose window crosses its sequence's start reads the conv state instead
+  const int cl = tid & 127, qt = tid >> 7;  // channel, quarter of the block's tokens
+  const bool act = cl < width;
+  const int64_t c = ch + cl;
+  const int tq = 16 * qt;  // the quarter's first token; its window = tokens tq - 3 .. tq - 1
+  float w[4] = {0.f, 0.f, 0.f, 0.f}, x0 = 0.f, x1 = 0.f, x2 = 0.f;
+  if (act) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) w[i] = i < W ? a.conv_w[c * W + i] : 0.f;
-    // win[i] = x_{t - W + 1 + i} for i < W - 1 (the carried inputs), refilled at sequence starts
-    int n = seq_of(a.cu, a.N, t0);
-    int64_t sb = a.cu ? a.cu[n] : 0;
-    float win[3] = {0.f, 0.f, 0.f};
-    auto fill = [&](int64_t t) {  // the W - 1 inputs before token t of sequence n
+    x0 = sm.xs[tq][cl];
+    x1 = sm.xs[tq + 1][cl];
+    x2 = sm.xs[tq + 2][cl];
+  }
+  __syncthreads();  // every window is read before any output overwrites an input row
+  if (act) {
 #pragma unroll
-      for (int i = 0; i < 3; ++i) {
-        const int64_t s = t - (W - 1) + i;
-        float x = 0.f;
-        if (i < W - 1) {
-          if (s >= sb) x = ld_x(a.x, s * Ch + c, a.bf16);
-          else if (a.state_in) x = ld_x(a.state_in, ((int64_t)n * Ch + c) * (W - 1) + (s - sb + W - 1), a.bf16);
+    for (int jj = 0; jj < 16; ++jj) {
+      const int t = tq + jj;
+      if (t >= nt) break;
+      const float x3 = sm.xs[t + kHalo][cl];
+      float y;
+      if (t0 + t - (W - 1) >= sm.sb[t]) {  // the whole window lies in the token's sequence
+        y = W == 4 ? fmaf(w[0], x0, fmaf(w[1], x1, fmaf(w[2], x2, w[3] * x3)))
+          : W == 3 ? fmaf(w[0], x1, fmaf(w[1], x2, w[2] * x3))
+          : W == 2 ? fmaf(w[0], x2, w[1] * x3)
+                   : w[0] * x3;
+      } else {  // the window crosses the sequence's start: earlier inputs from its conv state
+        const int64_t tt = t0 + t, sb = sm.sb[t];
+        y = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (i < W) {
+            const int64_t s = tt - (W - 1) + i;  // the input this tap reads
+            const int wi = 4 - W + i;            // the window register holding it
+            float x = 0.f;
+            if (s >= sb) x = wi == 0 ? x0 : wi == 1 ? x1 : wi == 2 ? x2 : x3;
+            else if (a.state_in) x = ld_x(a.state_in, ((int64_t)sm.seq[t] * Ch + c) * (W - 1) + (s - sb + W - 1), a.bf16);
+            y = fmaf(w[i], x, y);
+          }
         }
-        win[i] = x;
       }
-    };
-    fill(t0);
-    int64_t next = (a.cu && n + 1 <= a.N) ? a.cu[n + 1] : a.T;
-    for (int64_t t = t0; t < t1; ++t) {
-      while (t >= next && n + 1 < a.N) {  // a new sequence starts at t
-        ++n;
-        sb = a.cu[n];
-        next = a.cu[n + 1];
-        fill(t);
-      }
-      const float xt = ld_x(a.x, t * Ch + c, a.bf16);
-      float y = (W == 4 ? w[3] : W == 3 ? w[2] : W == 2 ? w[1] : w[0]) * xt;
-#pragma unroll
-      for (int i = 0; i < 3; ++i)
-        if (i < W - 1) y = fmaf(w[i], win[i], y);
-      win[0] = W == 2 ? xt : win[1];  // shift the window (constant indices: registers)
-      win[1] = W == 3 ? xt : win[2];
-      win[2] = xt;
-      if (a.silu) y = y / (1.f + __expf(-y));
-      ys[t - t0][tid] = y;
+      x0 = x1;
+      x1 = x2;
+      x2 = x3;
+      if (a.silu) y = __fdividef(y, 1.f + __expf(-y));  // (the divisor is >= 1)
+      sm.xs[t + kHalo][cl] = y;
     }
   }
   __syncthreads();
-  const int nt = (int)(t1 - t0);
   if (is_q || is_k) {  // 1 / max(|y|, 1e-6) per token: a warp per token in turn
     const int warp = tid >> 5, lane = tid & 31;
     for (int t = warp; t < nt; t += kPThreads / 32) {
-      float s = 0.f;
-      for (int c = lane; c < width; c += 32) s = fmaf(ys[t][c], ys[t][c], s);
+      float s2 = 0.f;
+      for (int c = lane; c < width; c += 32) s2 = fmaf(sm.xs[t + kHalo][c], sm.xs[t + kHalo][c], s2);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) inv[t] = rsqrtf(fmaxf(s, 1e-12f));
+      for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+      if (lane == 0) sm.inv[t] = rsqrtf(fmaxf(s2, 1e-12f));
     }
     __syncthreads();
   }
-  if (tid < width) {
+  // ---- outputs, eight channels a store
+  {
     void* dst = is_q ? a.q : is_k ? a.k : a.v;
     const int heads = (is_q || is_k) ? a.hk : a.hv;
-    for (int t = 0; t < nt; ++t) {
-      const float y = (is_q || is_k) ? ys[t][tid] * inv[t] : ys[t][tid];
-      st_x(dst, ((t0 + t) * heads + hd) * (int64_t)width + tid, y, a.bf16);
+    for (int e = tid; e < nt * g8; e += kPThreads) {
+      const int t = e / g8, c8 = 8 * (e % g8);
+      const float sc = (is_q || is_k) ? sm.inv[t] : 1.f;
+      float v8[8];
+#pragma unroll
+      for (int m = 0; m < 8; ++m) v8[m] = sm.xs[t + kHalo][c8 + m] * sc;
+      st8x(dst, ((t0 + t) * heads + hd) * (int64_t)width + c8, a.bf16, v8);
     }
   }
   if (!is_q && !is_k && tid < nt) {  // g, beta of this value head
@@ -166,8 +237,11 @@ __global__ void prologue_state_kernel(PrologueArgs a) {
 
 cudaError_t prologue(const PrologueArgs& a, cudaStream_t s) {
   if (a.T > 0) {
+    cudaError_t e = cudaFuncSetAttribute(prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sizeof(ProSmem));
+    if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)((a.T + kTB - 1) / kTB), (unsigned)(2 * a.hk + a.hv));
-    prologue_kernel<<<grid, kPThreads, 0, s>>>(a);
+    prologue_kernel<<<grid, kPThreads, sizeof(ProSmem), s>>>(a);
   }
   if (a.state_out && a.W > 1) {
     const dim3 grid(64, (unsigned)a.N);

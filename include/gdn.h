@@ -274,7 +274,7 @@ typedef struct gdn_prologue_problem {
     int64_t total_tokens;     /* T >= 0                                                     */
     int32_t num_seqs;         /* N >= 1                                                     */
     int32_t hk, hv;           /* key heads, value heads (hv % hk == 0)                      */
-    int32_t k_dim, v_dim;     /* K, V in [1, 128]                                           */
+    int32_t k_dim, v_dim;     /* K, V: multiples of 8 up to 128                             */
     int32_t conv_width;       /* W in [1, 4]: taps of the causal conv                       */
     int32_t activation;       /* 0: none, 1: SiLU after the conv                            */
     int32_t io_dtype;         /* gdn_dtype of x, the conv states, a, b, q, k, v             */
@@ -295,8 +295,8 @@ typedef struct gdn_prologue_problem {
  *   (either may be NULL; out may alias in: it receives each sequence's last W-1 inputs, older
  *   entries shifting in when a sequence is shorter);  a, b [T, hv] io dtype;  A_log, dt_bias
  *   [hv] fp32;  outputs q, k [T, hk, K], v [T, hv, V] io dtype, g, beta [T, hv] fp32, in the
- *   layouts gdn_forward reads.  cu_seqlens as for gdn_forward (device-checked; dev_status
- *   records GDN_ERR_DEVICE_INPUT).  HBM-bound elementwise kernels. */
+ *   layouts gdn_forward reads.  x, q, k, v 16-byte aligned.  cu_seqlens as for gdn_forward
+ *   (device-checked; dev_status records GDN_ERR_DEVICE_INPUT).  HBM-bound elementwise kernels. */
 gdn_status gdn_prologue(const gdn_prologue_problem* p, const void* x, const float* conv_w,
                         const void* conv_state_in, const void* a, const void* b,
                         const float* A_log, const float* dt_bias, const int32_t* cu_seqlens,

@@ -200,6 +200,7 @@ def test_prologue_rejects_bad_arguments_before_any_launch(gdn):
                               fake, fake, fake, None, None, None)
 
     assert call(W=5) == 2 and call(W=0) == 2 and call(act=2) == 2 and call(K=256) == 2
+    assert call(K=60) == 2 and call(V=12) == 2
     assert call(hk=3) == 1 and call(N=2) == 1 and call(T=-1) == 1 and call(io=5) == 2
     assert L.gdn_prologue(None, fake, fake, None, fake, fake, fake, fake, None, fake, fake, fake,
                           fake, fake, None, None, None) == 1
