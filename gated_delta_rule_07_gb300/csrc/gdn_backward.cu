@@ -192,28 +192,48 @@ __host__ __device__ constexpr int64_t grad_slice() { return 6 * (int64_t)C * V +
 
 // out(i, c, x) for i < C, c < N with x = sum_{y < Y} A(i, y) B(y, c) (Y a multiple of 32):
 // 32-wide slices of y are staged in shared memory; thread (ty, tx) of 16 x 32 accumulates rows
-// ty + 16 r and columns tx + 32 m in registers.  AI / BY: the operand's contiguous index is i
-// (for A) / y (for B), so that the staging loads walk memory in order.
+// ty + 16 r and columns tx + 32 m in registers.  Each thread fetches its share of the next slice
+// into registers while the current one is multiplied, so the operands' latency is hidden.
+// AI / BY: the operand's contiguous index is i (for A) / y (for B), so that the fetches walk
+// memory in order.
 template <int N, bool AI, bool BY, typename FA, typename FB, typename FO>
 __device__ __forceinline__ void mm(GradSmem& sm, int Y, FA A, FB B, FO out) {
   constexpr int RM = C / 16, RN = N / 32;
+  constexpr int NA = C * 32 / kGradThreads, NB = 32 * N / kGradThreads;
   const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
   float acc[RM][RN];
 #pragma unroll
   for (int r = 0; r < RM; ++r)
 #pragma unroll
     for (int m = 0; m < RN; ++m) acc[r][m] = 0.f;
+  float pa[NA], pb[NB];
+  auto fetch = [&](int y0) {
+#pragma unroll
+    for (int k = 0; k < NA; ++k) {
+      const int e = tid + k * kGradThreads;
+      pa[k] = A(AI ? e % C : e / 32, y0 + (AI ? e / C : e % 32));
+    }
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+      const int e = tid + k * kGradThreads;
+      pb[k] = B(y0 + (BY ? e % 32 : e / N), BY ? e / 32 : e % N);
+    }
+  };
+  fetch(0);
   for (int y0 = 0; y0 < Y; y0 += 32) {
-    __syncthreads();
-    for (int e = tid; e < C * 32; e += kGradThreads) {
-      const int i = AI ? e % C : e / 32, yy = AI ? e / C : e % 32;
-      sm.As[i][yy] = A(i, y0 + yy);
+    __syncthreads();  // the previous slice (or product) is done with the tiles
+#pragma unroll
+    for (int k = 0; k < NA; ++k) {
+      const int e = tid + k * kGradThreads;
+      sm.As[AI ? e % C : e / 32][AI ? e / C : e % 32] = pa[k];
     }
-    for (int e = tid; e < 32 * N; e += kGradThreads) {
-      const int c = BY ? e / 32 : e % N, yy = BY ? e % 32 : e / N;
-      sm.Bs[yy][c] = B(y0 + yy, c);
+#pragma unroll
+    for (int k = 0; k < NB; ++k) {
+      const int e = tid + k * kGradThreads;
+      sm.Bs[BY ? e % 32 : e / N][BY ? e / 32 : e % N] = pb[k];
     }
     __syncthreads();
+    if (y0 + 32 < Y) fetch(y0 + 32);
 #pragma unroll 8
     for (int yy = 0; yy < 32; ++yy) {
       float av[RM], bv[RN];
