@@ -90,6 +90,7 @@ struct ProSmem {
   float inv[kTB];
   int64_t sb[kTB];              // start of each token's sequence
   int seq[kTB];                 // and its index
+  int inside[kTB];              // 1: the token's whole conv window lies in its sequence
 };
 
 // grid: (token blocks, 2 hk + hv head slices).  The block's input tile is staged in shared memory
@@ -120,8 +121,10 @@ __global__ void __launch_bounds__(kPThreads) prologue_kernel(PrologueArgs a) {
   }
   for (int t = tid; t < nt; t += kPThreads) {
     const int n = seq_of(a.cu, a.N, t0 + t);
+    const int64_t sb = a.cu ? a.cu[n] : 0;
     sm.seq[t] = n;
-    sm.sb[t] = a.cu ? a.cu[n] : 0;
+    sm.sb[t] = sb;
+    sm.inside[t] = t0 + t - (W - 1) >= sb;
   }
   __syncthreads();
   // ---- the conv (and SiLU), a channel per thread: the window slides through the staged tile in
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(kPThreads) prologue_kernel(PrologueArgs a) {
       if (t >= nt) break;
       const float x3 = sm.xs[t + kHalo][cl];
       float y;
-      if (t0 + t - (W - 1) >= sm.sb[t]) {  // the whole window lies in the token's sequence
+      if (sm.inside[t]) {  // the whole window lies in the token's sequence
         y = W == 4 ? fmaf(w[0], x0, fmaf(w[1], x1, fmaf(w[2], x2, w[3] * x3)))
           : W == 3 ? fmaf(w[0], x1, fmaf(w[1], x2, w[2] * x3))
           : W == 2 ? fmaf(w[0], x2, w[1] * x3)
