@@ -11,9 +11,10 @@
 //   y_t[c] = sum_{i < W} w[c][i] x_{t - W + 1 + i}[c], with inputs before a sequence's start taken
 //   from its conv state (oldest first) or zero.
 //
-// HBM-bound elementwise work: one CTA per (block of 64 tokens, head slice of the channels), one
-// thread per channel that slides the conv window through the block in registers; the block's
-// outputs are staged in shared memory so that q and k can be normalised per token.
+// HBM-bound elementwise work, streamed through registers: a thread owns four consecutive channels
+// of one head and walks a run of 64 tokens, its conv window held in registers and the next four
+// tokens' inputs already in flight; q and k are normalised by a shuffle reduction over the lanes
+// that hold the head.  No shared memory, no block barrier.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -23,9 +24,6 @@
 
 namespace gdn {
 namespace {
-
-constexpr int kTB = 64;       // tokens per CTA
-constexpr int kPThreads = 512;  // 128 channels x 4 quarters of the token block
 
 __device__ __forceinline__ float ld_x(const void* p, int64_t i, bool bf16) {
   return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i])
@@ -38,7 +36,7 @@ __device__ __forceinline__ void st_x(void* p, int64_t i, float x, bool bf16) {
     static_cast<float*>(p)[i] = x;
 }
 
-// sequence of token t: the largest n with cu[n] <= t (cu null: one sequence)
+// sequence of token t: the largest n < N with cu[n] <= t (cu null: one sequence)
 __device__ __forceinline__ int seq_of(const int32_t* cu, int N, int64_t t) {
   if (!cu) return 0;
   int lo = 0, hi = N - 1;
@@ -49,166 +47,227 @@ __device__ __forceinline__ int seq_of(const int32_t* cu, int N, int64_t t) {
   return lo;
 }
 
-constexpr int kHalo = 3;       // inputs before a block's first token that its conv can read
-constexpr int kRow = 128 + 1;  // padded row of a staged tile (floats)
+constexpr int kSThreads = 256;  // threads of a CTA
+constexpr int kLoadBytes = 16;  // bytes of one token a thread loads: its consecutive channels
+constexpr int kRing = 8;        // tokens in a thread's shared-memory ring (kRing - 1 in flight)
+template <typename IO>
+__host__ __device__ constexpr int cpt() { return kLoadBytes / (int)sizeof(IO); }  // channels a thread owns
 
-// eight consecutive I/O elements (16-byte aligned in bf16, 32-byte in fp32) as fp32
-__device__ __forceinline__ void ld8x(const void* p, int64_t i, bool bf16, float* dst) {
-  if (bf16) {
-    const uint4 x = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p) + i);
-    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&x);
+constexpr int kWords = kLoadBytes / 4;
+static_assert(kLoadBytes == 16, "one 16-byte copy per token and thread");
+struct Raw {  // one token's channels of a thread, as loaded
+  uint32_t u[kWords];
+};
+__device__ __forceinline__ Raw raw_load(const void* p) {
+  const uint4 v = __ldg(static_cast<const uint4*>(p));
+  Raw r;
+  r.u[0] = v.x; r.u[1] = v.y; r.u[2] = v.z; r.u[3] = v.w;
+  return r;
+}
+__device__ __forceinline__ void raw_store(void* p, const Raw& r) {
+  *static_cast<uint4*>(p) = make_uint4(r.u[0], r.u[1], r.u[2], r.u[3]);
+}
+template <typename IO>
+__device__ __forceinline__ Raw raw_at(const void* base, int64_t i) {
+  return raw_load(static_cast<const IO*>(base) + i);
+}
+// to fp32 (a bf16 is the top half of an fp32) and back
+template <typename IO>
+__device__ __forceinline__ void unpack(const Raw& r, float* f) {
 #pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const float2 f = __bfloat1622float2(h2[m]);
-      dst[2 * m] = f.x;
-      dst[2 * m + 1] = f.y;
+  for (int i = 0; i < kWords; ++i) {
+    if constexpr (sizeof(IO) == 2) {
+      f[2 * i] = __uint_as_float(r.u[i] << 16);
+      f[2 * i + 1] = __uint_as_float(r.u[i] & 0xffff0000u);
+    } else {
+      f[i] = __uint_as_float(r.u[i]);
     }
-  } else {
-    const float4* f = reinterpret_cast<const float4*>(static_cast<const float*>(p) + i);
-    const float4 u = f[0], w = f[1];
-    dst[0] = u.x; dst[1] = u.y; dst[2] = u.z; dst[3] = u.w;
-    dst[4] = w.x; dst[5] = w.y; dst[6] = w.z; dst[7] = w.w;
   }
 }
-__device__ __forceinline__ void st8x(void* p, int64_t i, bool bf16, const float* v) {
-  if (bf16) {
-    uint4 x;
-    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&x);
+template <typename IO>
+__device__ __forceinline__ Raw pack(const float* f) {
+  Raw r;
 #pragma unroll
-    for (int m = 0; m < 4; ++m) h2[m] = __floats2bfloat162_rn(v[2 * m], v[2 * m + 1]);
-    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p) + i) = x;
-  } else {
-    float4* f = reinterpret_cast<float4*>(static_cast<float*>(p) + i);
-    f[0] = make_float4(v[0], v[1], v[2], v[3]);
-    f[1] = make_float4(v[4], v[5], v[6], v[7]);
+  for (int i = 0; i < kWords; ++i) {
+    if constexpr (sizeof(IO) == 2) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      r.u[i] = *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+      r.u[i] = __float_as_uint(f[i]);
+    }
   }
+  return r;
 }
 
-struct ProSmem {
-  float xs[kTB + kHalo][kRow];  // inputs of tokens t0 - 3 .. t1 - 1 (rows before 0 are zero);
-                                // row t + 3 then receives token t's conv output
-  float inv[kTB];
-  int64_t sb[kTB];              // start of each token's sequence
-  int seq[kTB];                 // and its index
-  int inside[kTB];              // 1: the token's whole conv window lies in its sequence
+// how the channel slots of a token map onto threads: a head of width w occupies the next power
+// of two >= w / kCPT lanes (aligned), q heads then k heads then v heads
+struct SlotMap {
+  int lphk, lphv;    // lanes per q / k head, per v head
+  int qk_slots;      // 2 hk lphk
+  int slots;         // qk_slots + hv lphv
+  int cpr;           // CTAs per token run
+  int ranges;        // token ranges (the grid is ranges x cpr CTAs, all resident at once)
 };
 
-// grid: (token blocks, 2 hk + hv head slices).  The block's input tile is staged in shared memory
-// with 16-byte loads, the conv reads it (or, before a sequence's start, the sequence's conv
-// state), and the outputs leave with 16-byte stores.
-__global__ void __launch_bounds__(kPThreads) prologue_kernel(PrologueArgs a) {
-  extern __shared__ __align__(16) uint8_t praw[];
-  ProSmem& sm = *reinterpret_cast<ProSmem*>(praw);
-  const int blk = blockIdx.y, tid = threadIdx.x;
-  const bool is_q = blk < a.hk, is_k = !is_q && blk < 2 * a.hk;
-  const int hd = is_q ? blk : is_k ? blk - a.hk : blk - 2 * a.hk;  // head within its kind
-  const int width = (is_q || is_k) ? a.K : a.V;
-  const int64_t ch = is_q ? (int64_t)hd * a.K
-                   : is_k ? (int64_t)a.hk * a.K + (int64_t)hd * a.K
-                          : 2LL * a.hk * a.K + (int64_t)hd * a.V;  // first channel of the slice
-  const int64_t Ch = 2LL * a.hk * a.K + (int64_t)a.hv * a.V;
-  const int64_t t0 = (int64_t)blockIdx.x * kTB;
-  const int64_t t1 = (t0 + kTB < a.T) ? t0 + kTB : a.T;
-  const int nt = (int)(t1 - t0), W = a.W, g8 = width / 8;
-  // ---- stage the tile; each token's sequence
-  for (int e = tid; e < (nt + kHalo) * g8; e += kPThreads) {
-    const int r = e / g8, c8 = 8 * (e % g8);
-    const int64_t t = t0 - kHalo + r;
-    if (t >= 0) ld8x(a.x, t * Ch + ch + c8, a.bf16, &sm.xs[r][c8]);
-    else
-#pragma unroll
-      for (int m = 0; m < 8; ++m) sm.xs[r][c8 + m] = 0.f;
+// SiLU y sigmoid(y).  fp32 I/O: y / (1 + e^-y).  bf16 I/O: h + h tanh(h) with h = y / 2 on the
+// hardware tanh approximation (absolute error ~2.5e-4 |y|, below the bf16 rounding of the result
+// where it matters, and one special-function op instead of two)
+template <typename IO>
+__device__ __forceinline__ float silu(float y) {
+  if constexpr (sizeof(IO) == 2) {
+    const float h = 0.5f * y;
+    float th;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(th) : "f"(h));
+    return fmaf(h, th, h);
+  } else {
+    return __fdividef(y, 1.f + __expf(-y));  // (the divisor is >= 1)
   }
-  for (int t = tid; t < nt; t += kPThreads) {
-    const int n = seq_of(a.cu, a.N, t0 + t);
-    const int64_t sb = a.cu ? a.cu[n] : 0;
-    sm.seq[t] = n;
-    sm.sb[t] = sb;
-    sm.inside[t] = t0 + t - (W - 1) >= sb;
-  }
-  __syncthreads();
-  // ---- the conv (and SiLU), a channel per thread: the window slides through the staged tile in
-  // registers; a token whose window crosses its sequence's start reads the conv state instead
-  const int cl = tid & 127, qt = tid >> 7;  // channel, quarter of the block's tokens
-  const bool act = cl < width;
-  const int64_t c = ch + cl;
-  const int tq = 16 * qt;  // the quarter's first token; its window = tokens tq - 3 .. tq - 1
-  float w[4] = {0.f, 0.f, 0.f, 0.f}, x0 = 0.f, x1 = 0.f, x2 = 0.f;
-  if (act) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) w[i] = i < W ? a.conv_w[c * W + i] : 0.f;
-    x0 = sm.xs[tq][cl];
-    x1 = sm.xs[tq + 1][cl];
-    x2 = sm.xs[tq + 2][cl];
-  }
-  __syncthreads();  // every window is read before any output overwrites an input row
-  if (act) {
-#pragma unroll
-    for (int jj = 0; jj < 16; ++jj) {
-      const int t = tq + jj;
-      if (t >= nt) break;
-      const float x3 = sm.xs[t + kHalo][cl];
-      float y;
-      if (sm.inside[t]) {  // the whole window lies in the token's sequence
-        y = W == 4 ? fmaf(w[0], x0, fmaf(w[1], x1, fmaf(w[2], x2, w[3] * x3)))
-          : W == 3 ? fmaf(w[0], x1, fmaf(w[1], x2, w[2] * x3))
-          : W == 2 ? fmaf(w[0], x2, w[1] * x3)
-                   : w[0] * x3;
-      } else {  // the window crosses the sequence's start: earlier inputs from its conv state
-        const int64_t tt = t0 + t, sb = sm.sb[t];
-        y = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (i < W) {
-            const int64_t s = tt - (W - 1) + i;  // the input this tap reads
-            const int wi = 4 - W + i;            // the window register holding it
-            float x = 0.f;
-            if (s >= sb) x = wi == 0 ? x0 : wi == 1 ? x1 : wi == 2 ? x2 : x3;
-            else if (a.state_in) x = ld_x(a.state_in, ((int64_t)sm.seq[t] * Ch + c) * (W - 1) + (s - sb + W - 1), a.bf16);
-            y = fmaf(w[i], x, y);
-          }
-        }
-      }
-      x0 = x1;
-      x1 = x2;
-      x2 = x3;
-      if (a.silu) y = __fdividef(y, 1.f + __expf(-y));  // (the divisor is >= 1)
-      sm.xs[t + kHalo][cl] = y;
-    }
-  }
-  __syncthreads();
-  if (is_q || is_k) {  // 1 / max(|y|, 1e-6) per token: a warp per token in turn
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int t = warp; t < nt; t += kPThreads / 32) {
-      float s2 = 0.f;
-      for (int c = lane; c < width; c += 32) s2 = fmaf(sm.xs[t + kHalo][c], sm.xs[t + kHalo][c], s2);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-      if (lane == 0) sm.inv[t] = rsqrtf(fmaxf(s2, 1e-12f));
-    }
-    __syncthreads();
-  }
-  // ---- outputs, eight channels a store
-  {
-    void* dst = is_q ? a.q : is_k ? a.k : a.v;
-    const int heads = (is_q || is_k) ? a.hk : a.hv;
-    for (int e = tid; e < nt * g8; e += kPThreads) {
-      const int t = e / g8, c8 = 8 * (e % g8);
-      const float sc = (is_q || is_k) ? sm.inv[t] : 1.f;
-      float v8[8];
-#pragma unroll
-      for (int m = 0; m < 8; ++m) v8[m] = sm.xs[t + kHalo][c8 + m] * sc;
-      st8x(dst, ((t0 + t) * heads + hd) * (int64_t)width + c8, a.bf16, v8);
-    }
-  }
-  if (!is_q && !is_k && tid < nt) {  // g, beta of this value head
-    const int64_t t = t0 + tid;
-    const float av = ld_x(a.a, t * a.hv + hd, a.bf16), bv = ld_x(a.b, t * a.hv + hd, a.bf16);
-    const float z = av + a.dt_bias[hd];
+}
+// one 16-byte copy global -> shared of this thread's (no bytes read, zero filled, when !ok), as
+// its own commit group
+__device__ __forceinline__ void ring_copy(uint32_t dst, const void* src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(ok ? 16 : 0)
+               : "memory");
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+// g, beta of every (token, value head)
+__device__ void gate_maps(const PrologueArgs& a) {
+  const int64_t n = a.T * a.hv, stride = (int64_t)gridDim.x * kSThreads;
+  for (int64_t e = (int64_t)blockIdx.x * kSThreads + threadIdx.x; e < n; e += stride) {
+    const int h = (int)(e % a.hv);
+    const float av = ld_x(a.a, e, a.bf16), bv = ld_x(a.b, e, a.bf16);
+    const float z = av + a.dt_bias[h];
     const float sp = z > 20.f ? z : log1pf(__expf(z));  // softplus
-    a.g[t * a.hv + hd] = -__expf(a.A_log[hd]) * sp;
-    a.beta[t * a.hv + hd] = 1.f / (1.f + __expf(-bv));
+    a.g[e] = -__expf(a.A_log[h]) * sp;
+    a.beta[e] = 1.f / (1.f + __expf(-bv));
   }
+}
+
+// one input of a window read the slow way (only where the window reaches before its sequence's
+// start): token u from x inside the sequence that starts at sb, before it the sequence's conv
+// state (oldest entry first), zero past the state
+template <typename IO>
+__device__ __forceinline__ void window_input(const PrologueArgs& a, int64_t Ch, int64_t c,
+                                             int64_t u, int64_t sb, int seq, float* f) {
+  if (u >= sb && u >= 0) {
+    unpack<IO>(raw_at<IO>(a.x, u * Ch + c), f);
+    return;
+  }
+  const int W1 = a.W - 1;
+  const int64_t j = W1 - (sb - u);
+  const int64_t base = ((int64_t)seq * Ch + c) * W1 + j;
+#pragma unroll
+  for (int m = 0; m < cpt<IO>(); ++m)
+    f[m] = (a.state_in && j >= 0) ? ld_x(a.state_in, base + m * W1, a.bf16) : 0.f;
+}
+
+// grid: m.ranges x m.cpr CTAs, as many as are resident at once: CTA (range r, part p) walks the
+// tokens of range r through the channels of part p, then takes its share of the g, beta maps.
+// Taps are padded to four, y_t = w0 x_{t-3} + w1 x_{t-2} + w2 x_{t-1} + w3 x_t, summed in that fixed order.
+template <typename IO>
+__global__ void __launch_bounds__(kSThreads, 2) prologue_kernel(PrologueArgs a, SlotMap m) {
+  constexpr int kCPT = cpt<IO>();
+  const int range = (int)blockIdx.x / m.cpr;
+  const int slot = ((int)blockIdx.x % m.cpr) * kSThreads + (int)threadIdx.x;
+  // this thread's head and lanes
+  const bool qk = slot < m.qk_slots;
+  const int lph = qk ? m.lphk : m.lphv;
+  const int rel = qk ? slot : slot - m.qk_slots;
+  const int hh = rel / lph, l = rel % lph;  // head (q heads then k heads, or v head), lane
+  const int width = qk ? a.K : a.V;
+  const bool act = slot < m.slots && kCPT * l < width;
+  const int64_t Ch = 2LL * a.hk * a.K + (int64_t)a.hv * a.V;
+  const int64_t c = (qk ? (int64_t)hh * a.K : 2LL * a.hk * a.K + (int64_t)hh * a.V) + kCPT * l;
+  const int head = qk && hh >= a.hk ? hh - a.hk : hh, heads = qk ? a.hk : a.hv;
+  IO* dst = static_cast<IO*>(qk ? (hh < a.hk ? a.q : a.k) : a.v) + (int64_t)head * width + kCPT * l;
+  const int64_t drow = (int64_t)heads * width;
+  const bool warp_qk = ((slot & ~31) < m.qk_slots);  // the warp holds some q / k head
+  const int W = a.W;
+  float w[kCPT][4];
+#pragma unroll
+  for (int ch = 0; ch < kCPT; ++ch)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[ch][i] = (act && i >= 4 - W) ? a.conv_w[(c + ch) * W + i - (4 - W)] : 0.f;
+
+  const int64_t t0 = a.T * range / m.ranges, t1 = a.T * (range + 1) / m.ranges;
+  int n = seq_of(a.cu, a.N, t0);
+  int64_t s0 = a.cu ? a.cu[n] : 0, s1 = a.cu ? a.cu[n + 1] : a.T;  // the sequence's bounds
+
+  // the window ahead of the run (replaced from the conv state where a token's window reaches
+  // before its sequence's start)
+  float x3[kCPT], x2[kCPT], x1[kCPT];
+#pragma unroll
+  for (int m2 = 0; m2 < kCPT; ++m2) x3[m2] = x2[m2] = x1[m2] = 0.f;
+  if (act && t0 >= 3) {
+    unpack<IO>(raw_at<IO>(a.x, (t0 - 3) * Ch + c), x3);
+    unpack<IO>(raw_at<IO>(a.x, (t0 - 2) * Ch + c), x2);
+    unpack<IO>(raw_at<IO>(a.x, (t0 - 1) * Ch + c), x1);
+  }
+  // the thread's ring of inputs in flight: slot r of thread i at ring[r][i]
+  extern __shared__ __align__(16) uint4 ring[];
+  const uint32_t ring0 = (uint32_t)__cvta_generic_to_shared(ring + threadIdx.x);
+  const IO* xc = static_cast<const IO*>(a.x) + c;
+#pragma unroll
+  for (int r = 0; r < kRing - 1; ++r) {
+    const int64_t t = t0 + r;
+    ring_copy(ring0 + r * kSThreads * 16, xc + (act && t < t1 ? t * Ch : 0), act && t < t1);
+  }
+  int rs = 0;  // the ring slot of token t
+  for (int64_t t = t0; t < t1; ++t) {
+    {  // token t + kRing - 1 into the slot that token t - 1 used; then token t has landed
+      const int64_t tn = t + kRing - 1;
+      const int sn = rs == 0 ? kRing - 1 : rs - 1;
+      ring_copy(ring0 + sn * kSThreads * 16, xc + (act && tn < t1 ? tn * Ch : 0), act && tn < t1);
+      asm volatile("cp.async.wait_group %0;\n" ::"n"(kRing - 1) : "memory");
+    }
+    while (n < a.N - 1 && t >= s1) {  // (uniform: every thread of the CTA walks the same tokens)
+      ++n;
+      s0 = s1;
+      s1 = a.cu[n + 1];
+    }
+    if (t - 3 < s0 && act) {  // the window reaches before the sequence's start
+      window_input<IO>(a, Ch, c, t - 3, s0, n, x3);
+      window_input<IO>(a, Ch, c, t - 2, s0, n, x2);
+      window_input<IO>(a, Ch, c, t - 1, s0, n, x1);
+    }
+    float x0[kCPT], o[kCPT];
+    {
+      const uint4 v = ring[rs * kSThreads + threadIdx.x];
+      Raw r;
+      r.u[0] = v.x; r.u[1] = v.y; r.u[2] = v.z; r.u[3] = v.w;
+      unpack<IO>(r, x0);
+    }
+    rs = rs == kRing - 1 ? 0 : rs + 1;
+    float s2 = 0.f;
+#pragma unroll
+    for (int ch = 0; ch < kCPT; ++ch) {
+      float y = fmaf(w[ch][0], x3[ch], fmaf(w[ch][1], x2[ch], fmaf(w[ch][2], x1[ch], w[ch][3] * x0[ch])));
+      if (a.silu) y = silu<IO>(y);
+      o[ch] = y;
+      s2 = fmaf(y, y, s2);
+      x3[ch] = x2[ch];
+      x2[ch] = x1[ch];
+      x1[ch] = x0[ch];
+    }
+    if (warp_qk) {  // 1 / max(|y|, 1e-6) over the head's lanes (aligned groups of lphk)
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float other = __shfl_xor_sync(0xffffffffu, s2, off);
+        if (off < m.lphk) s2 += other;
+      }
+      if (qk) {
+        const float inv = rsqrtf(fmaxf(s2, 1e-12f));
+#pragma unroll
+        for (int ch = 0; ch < kCPT; ++ch) o[ch] *= inv;
+      }
+    }
+    if (act) raw_store(dst + t * drow, pack<IO>(o));
+  }
+  asm volatile("cp.async.wait_all;\n" ::: "memory");
+  gate_maps(a);
 }
 
 // new conv state: the last W - 1 inputs of each sequence; when a sequence is shorter, the older
@@ -240,11 +299,33 @@ __global__ void prologue_state_kernel(PrologueArgs a) {
 
 cudaError_t prologue(const PrologueArgs& a, cudaStream_t s) {
   if (a.T > 0) {
-    cudaError_t e = cudaFuncSetAttribute(prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sizeof(ProSmem));
+    auto pow2 = [](int x) { int p = 1; while (p < x) p <<= 1; return p; };
+    SlotMap m;
+    const int cp = kLoadBytes / (a.bf16 ? 2 : 4);
+    m.lphk = pow2(a.K / cp);
+    m.lphv = pow2(a.V / cp);
+    m.qk_slots = 2 * a.hk * m.lphk;
+    m.slots = m.qk_slots + a.hv * m.lphv;
+    m.cpr = (m.slots + kSThreads - 1) / kSThreads;
+    const int smem = kRing * kSThreads * 16;
+    const auto kern = a.bf16 ? prologue_kernel<__nv_bfloat16> : prologue_kernel<float>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    int dev = 0, sms = 0, per_sm = 0;
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSThreads, smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)((a.T + kTB - 1) / kTB), (unsigned)(2 * a.hk + a.hv));
-    prologue_kernel<<<grid, kPThreads, sizeof(ProSmem), s>>>(a);
+    // one wave: the token ranges split the resident CTAs between them (at least 16 tokens each)
+    const int64_t resident = (int64_t)(per_sm > 0 ? per_sm : 1) * sms;
+    int64_t ranges = resident / m.cpr;
+    if (ranges > (a.T + 15) / 16) ranges = (a.T + 15) / 16;
+    m.ranges = (int)(ranges > 1 ? ranges : 1);
+    const int64_t ctas = (int64_t)m.ranges * m.cpr;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    if (a.bf16)
+      prologue_kernel<__nv_bfloat16><<<(unsigned)ctas, kSThreads, smem, s>>>(a, m);
+    else
+      prologue_kernel<float><<<(unsigned)ctas, kSThreads, smem, s>>>(a, m);
   }
   if (a.state_out && a.W > 1) {
     const dim3 grid(64, (unsigned)a.N);
