@@ -39,7 +39,6 @@ namespace gdn {
 namespace {
 
 constexpr int C = kChunk;  // 64
-constexpr int kColThreads = 128;   // 32 state columns per CTA, 4 lanes per column
 constexpr int kGradThreads = 512;
 
 __device__ __forceinline__ float ld_io(const void* p, int64_t i, bool bf16) {
@@ -76,30 +75,62 @@ __device__ __forceinline__ int64_t slot_base(const int32_t* cu, int n) {
 
 // ------------------------------------------------------------------ column recurrences
 
-// Shared memory of one column CTA: a chunk of k (and, reversed, q) as fp32 rows, the CTA's 32
-// columns of v (or dout), g and beta.
-template <int K, bool REVERSE>
-constexpr size_t column_smem() {
-  return sizeof(float) * ((size_t)C * K * (REVERSE ? 2 : 1) + (size_t)C * 32 + 2 * C);
+constexpr int kPhases = 8;   // threads per state column; each holds K / 8 contiguous rows
+constexpr int kColBlock = 16;  // state columns per CTA
+constexpr int kColThreads = kColBlock * kPhases;
+constexpr int kStage = 32;   // tokens staged in shared memory at a time (half a chunk)
+
+// A staged key (or query) row: the K values in kPhases segments of K / kPhases, each followed
+// by 4 floats of padding, so that the eight phases' 16-byte reads of one row hit eight
+// different groups of four banks.
+template <int K>
+__host__ __device__ constexpr int row_stride() { return K + 4 * kPhases; }
+
+// Shared memory of one column CTA: kStage rows of k (and, reversed, q), the CTA's columns of v
+// (or dout), exp(g) and beta.
+template <int K>
+__host__ __device__ constexpr size_t column_smem() {
+  return sizeof(float) * ((size_t)2 * kStage * row_stride<K>() + (size_t)kStage * kColBlock + 2 * kStage);
 }
 
-// One CTA: sequence n, value head j, 32 state columns; thread (column, row phase p) holds rows
-// p, p + 4, p + 8, ... of its column (the four phases of a column then read four banks of a
-// staged key row).  Each chunk's inputs are staged in shared memory first.  Forward: stores the
-// state entering every chunk as states[slot][j][v][i] (a state column contiguous).  Reverse:
-// stores the gradient of the state leaving every chunk in the same layout, and dh0.
+// kStage tokens [c0 + s0, c0 + s0 + n) of chunk inputs into shared memory (fp32, padded rows)
 template <int K, bool REVERSE>
-__global__ void __launch_bounds__(kColThreads) column_kernel(BwdArgs a) {
-  constexpr int RPL = K / 4;
-  extern __shared__ __align__(16) float csm[];
-  float* ks = csm;                                 // [C][K]
-  float* qs = ks + C * K;                          // [C][K] (reverse)
-  float* vs = qs + (REVERSE ? C * K : 0);          // [C][32]
-  float* gs = vs + C * 32;                         // [C]
-  float* bs = gs + C;                              // [C]
+__device__ __forceinline__ void stage_tokens(const BwdArgs& a, int64_t t0, int n, int j, int kh,
+                                             int v0, float* ks, float* qs, float* vs, float* gs,
+                                             float* bs) {
+  constexpr int RPL = K / kPhases, RS = row_stride<K>();
+  const void* vin = REVERSE ? a.dout : a.v;
+  for (int e = threadIdx.x; e < n * (K / 8); e += kColThreads) {
+    const int t = e / (K / 8), i = 8 * (e % (K / 8));
+    const int o = t * RS + (i / RPL) * (RPL + 4) + i % RPL;  // 8 | RPL: one segment
+    ld8(a.k, ((t0 + t) * a.hk + kh) * K + i, a.bf16, ks + o);
+    if (REVERSE) ld8(a.q, ((t0 + t) * a.hk + kh) * K + i, a.bf16, qs + o);
+  }
+  for (int e = threadIdx.x; e < n * (kColBlock / 8); e += kColThreads) {
+    const int t = e / (kColBlock / 8), cc = 8 * (e % (kColBlock / 8));
+    ld8(vin, ((t0 + t) * a.hv + j) * a.V + v0 + cc, a.bf16, vs + t * kColBlock + cc);
+  }
+  for (int t = threadIdx.x; t < n; t += kColThreads) {
+    gs[t] = __expf(a.g[(t0 + t) * a.hv + j]);
+    bs[t] = a.beta[(t0 + t) * a.hv + j];
+  }
+}
+
+// One direction of one CTA: sequence n, value head j, kColBlock state columns; thread (column,
+// phase p) holds rows [p RPL, (p + 1) RPL) of its column.  Forward: stores the state entering
+// every chunk as states[slot][j][v][i] (a state column contiguous).  Reverse: stores the gradient
+// of the state leaving every chunk in the same layout, and dh0.
+template <int K, bool REVERSE>
+__device__ __forceinline__ void column_run(const BwdArgs& a, float* csm) {
+  constexpr int RPL = K / kPhases, RS = row_stride<K>();
+  float* ks = csm;                        // [kStage][RS]
+  float* qs = ks + kStage * RS;           // [kStage][RS] (reverse)
+  float* vs = qs + kStage * RS;           // [kStage][kColBlock]
+  float* gs = vs + kStage * kColBlock;    // [kStage]
+  float* bs = gs + kStage;                // [kStage]
   const int nj = blockIdx.x, n = nj / a.hv, j = nj % a.hv, kh = j / (a.hv / a.hk);
-  const int col = threadIdx.x >> 2, p = threadIdx.x & 3;
-  const int v0 = blockIdx.y * 32, v = v0 + col;
+  const int col = threadIdx.x / kPhases, p = threadIdx.x % kPhases;
+  const int v0 = blockIdx.y * kColBlock, v = v0 + col;
   int64_t t0, t1;
   if (!seq_bounds(a.cu, n, a.T, a.status, t0, t1)) return;
   const int64_t KV = (int64_t)K * a.V;
@@ -107,68 +138,85 @@ __global__ void __launch_bounds__(kColThreads) column_kernel(BwdArgs a) {
   const float* init = REVERSE ? a.dh_final : a.h0;
 #pragma unroll
   for (int i = 0; i < RPL; ++i)
-    h[i] = init ? init[((int64_t)n * a.hv + j) * KV + (int64_t)(p + 4 * i) * a.V + v] : 0.f;
+    h[i] = init ? init[((int64_t)n * a.hv + j) * KV + (int64_t)(p * RPL + i) * a.V + v] : 0.f;
   float* store = REVERSE ? a.dstates : a.states;
-  const void* vin = REVERSE ? a.dout : a.v;
   const int64_t nc = (t1 - t0 + C - 1) / C, sb = slot_base(a.cu, n);
+  const int ko = p * (RPL + 4);  // this phase's segment of a staged row
   for (int64_t ci = 0; ci < nc; ++ci) {
     const int64_t c = REVERSE ? nc - 1 - ci : ci;
     const int64_t c0 = t0 + c * C;
     const int L = (int)((t1 - c0) < C ? (t1 - c0) : C);
-    float* dst = store + (((sb + c) * a.hv + j) * a.V + v) * K;
+    float4* dst = reinterpret_cast<float4*>(store + (((sb + c) * a.hv + j) * a.V + v) * K + p * RPL);
 #pragma unroll
-    for (int i = 0; i < RPL; ++i) dst[p + 4 * i] = h[i];
-    __syncthreads();  // the previous chunk's inputs have been used
-    for (int e = threadIdx.x; e < L * (K / 8); e += kColThreads) {
-      const int t = e / (K / 8), i = 8 * (e % (K / 8));
-      ld8(a.k, ((c0 + t) * a.hk + kh) * K + i, a.bf16, ks + t * K + i);
-      if (REVERSE) ld8(a.q, ((c0 + t) * a.hk + kh) * K + i, a.bf16, qs + t * K + i);
-    }
-    for (int e = threadIdx.x; e < L * 4; e += kColThreads) {
-      const int t = e / 4, cc = 8 * (e % 4);
-      ld8(vin, ((c0 + t) * a.hv + j) * a.V + v0 + cc, a.bf16, vs + t * 32 + cc);
-    }
-    for (int t = threadIdx.x; t < L; t += kColThreads) {
-      gs[t] = __expf(a.g[(c0 + t) * a.hv + j]);
-      bs[t] = a.beta[(c0 + t) * a.hv + j];
-    }
-    __syncthreads();
-    for (int s = 0; s < L; ++s) {
-      const int t = REVERSE ? L - 1 - s : s;
-      const float alpha = gs[t], beta = bs[t], x = vs[t * 32 + col];
-      const float* kr = ks + t * K + p;
-      if (REVERSE) {  // F = dh + q dout^T
-        const float* qr = qs + t * K + p;
+    for (int i = 0; i < RPL / 4; ++i) dst[i] = make_float4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+    const int nb = (L + kStage - 1) / kStage;
+    for (int bi = 0; bi < nb; ++bi) {
+      const int b = REVERSE ? nb - 1 - bi : bi;
+      const int bn = (L - b * kStage) < kStage ? (L - b * kStage) : kStage;
+      __syncthreads();  // the previous block's inputs have been used
+      stage_tokens<K, REVERSE>(a, c0 + b * kStage, bn, j, kh, v0, ks, qs, vs, gs, bs);
+      __syncthreads();
+      for (int s = 0; s < bn; ++s) {
+        const int t = REVERSE ? bn - 1 - s : s;
+        const float alpha = gs[t], beta = bs[t], x = vs[t * kColBlock + col];
+        float kv[RPL];
+        const float4* kr = reinterpret_cast<const float4*>(ks + t * RS + ko);
 #pragma unroll
-        for (int i = 0; i < RPL; ++i) h[i] = fmaf(qr[4 * i], x, h[i]);
-      }
-      float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+        for (int i = 0; i < RPL / 4; ++i) {
+          const float4 f = kr[i];
+          kv[4 * i] = f.x; kv[4 * i + 1] = f.y; kv[4 * i + 2] = f.z; kv[4 * i + 3] = f.w;
+        }
+        if (REVERSE) {  // F = dh + q dout^T
+          const float4* qr = reinterpret_cast<const float4*>(qs + t * RS + ko);
 #pragma unroll
-      for (int i = 0; i < RPL; i += 4) {
-        d0 = fmaf(kr[4 * i], h[i], d0);
-        d1 = fmaf(kr[4 * i + 4], h[i + 1], d1);
-        d2 = fmaf(kr[4 * i + 8], h[i + 2], d2);
-        d3 = fmaf(kr[4 * i + 12], h[i + 3], d3);
-      }
-      float d = (d0 + d1) + (d2 + d3);
-      d += __shfl_xor_sync(0xffffffffu, d, 1);
-      d += __shfl_xor_sync(0xffffffffu, d, 2);
-      if (REVERSE) {  // dd = k . F;  dh <- alpha (F - beta k dd)
-        const float bd = beta * d;
+          for (int i = 0; i < RPL / 4; ++i) {
+            const float4 f = qr[i];
+            h[4 * i] = fmaf(f.x, x, h[4 * i]);
+            h[4 * i + 1] = fmaf(f.y, x, h[4 * i + 1]);
+            h[4 * i + 2] = fmaf(f.z, x, h[4 * i + 2]);
+            h[4 * i + 3] = fmaf(f.w, x, h[4 * i + 3]);
+          }
+        }
+        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
 #pragma unroll
-        for (int i = 0; i < RPL; ++i) h[i] = alpha * fmaf(-kr[4 * i], bd, h[i]);
-      } else {  // delta = beta (v - alpha k . h);  h <- alpha h + k delta
-        const float dl = beta * (x - alpha * d);
+        for (int i = 0; i < RPL; i += 4) {
+          d0 = fmaf(kv[i], h[i], d0);
+          d1 = fmaf(kv[i + 1], h[i + 1], d1);
+          d2 = fmaf(kv[i + 2], h[i + 2], d2);
+          d3 = fmaf(kv[i + 3], h[i + 3], d3);
+        }
+        float d = (d0 + d1) + (d2 + d3);
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        d += __shfl_xor_sync(0xffffffffu, d, 4);
+        if (REVERSE) {  // dd = k . F;  dh <- alpha (F - beta k dd)
+          const float bd = beta * d;
 #pragma unroll
-        for (int i = 0; i < RPL; ++i) h[i] = fmaf(kr[4 * i], dl, alpha * h[i]);
+          for (int i = 0; i < RPL; ++i) h[i] = alpha * fmaf(-kv[i], bd, h[i]);
+        } else {  // delta = beta (v - alpha k . h);  h <- alpha h + k delta
+          const float dl = beta * (x - alpha * d);
+#pragma unroll
+          for (int i = 0; i < RPL; ++i) h[i] = fmaf(kv[i], dl, alpha * h[i]);
+        }
       }
     }
   }
   if (REVERSE && a.dh0) {
 #pragma unroll
     for (int i = 0; i < RPL; ++i)
-      a.dh0[((int64_t)n * a.hv + j) * KV + (int64_t)(p + 4 * i) * a.V + v] = h[i];
+      a.dh0[((int64_t)n * a.hv + j) * KV + (int64_t)(p * RPL + i) * a.V + v] = h[i];
   }
+}
+
+// grid (N hv, V / kColBlock, 2): z = 0 the forward recurrence, z = 1 the reverse one; the two
+// directions are independent and share the SMs.
+template <int K>
+__global__ void __launch_bounds__(kColThreads) column_kernel(BwdArgs a) {
+  extern __shared__ __align__(16) float csm[];
+  if (blockIdx.z == 0)
+    column_run<K, false>(a, csm);
+  else
+    column_run<K, true>(a, csm);
 }
 
 // ------------------------------------------------------------------ per-chunk gradients
@@ -507,19 +555,14 @@ __global__ void group_sum_kernel(BwdArgs a) {
 
 template <int K, int V>
 cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
-  const dim3 cg((unsigned)(a.N * a.hv), (unsigned)(V / 32));
-  cudaError_t e = cudaFuncSetAttribute(column_kernel<K, false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)column_smem<K, false>());
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(column_kernel<K, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)column_smem<K, true>());
+  const dim3 cg((unsigned)(a.N * a.hv), (unsigned)(V / kColBlock), 2);
+  cudaError_t e = cudaFuncSetAttribute(column_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)column_smem<K>());
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(chunk_grad_kernel<K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sizeof(GradSmem));
   if (e != cudaSuccess) return e;
-  column_kernel<K, false><<<cg, kColThreads, column_smem<K, false>(), s>>>(a);
-  column_kernel<K, true><<<cg, kColThreads, column_smem<K, true>(), s>>>(a);
+  column_kernel<K><<<cg, kColThreads, column_smem<K>(), s>>>(a);
   chunk_grad_kernel<K, V><<<a.grad_ctas, kGradThreads, sizeof(GradSmem), s>>>(a);
   group_sum_kernel<<<1024, 256, 0, s>>>(a);
   return cudaGetLastError();

@@ -165,15 +165,16 @@ __device__ __forceinline__ void window_input(const PrologueArgs& a, int64_t Ch, 
 
 // grid: m.ranges x m.cpr CTAs, as many as are resident at once: CTA (range r, part p) walks the
 // tokens of range r through the channels of part p, then takes its share of the g, beta maps.
-// Taps are padded to four, y_t = w0 x_{t-3} + w1 x_{t-2} + w2 x_{t-1} + w3 x_t, summed in that fixed order.
-template <typename IO>
+// Taps are padded to four, y_t = w0 x_{t-3} + w1 x_{t-2} + w2 x_{t-1} + w3 x_t, summed in that
+// fixed order.  LPHK = m.lphk (lanes per q / k head), fixed at compile time for the norms.
+template <typename IO, int LPHK>
 __global__ void __launch_bounds__(kSThreads, 2) prologue_kernel(PrologueArgs a, SlotMap m) {
   constexpr int kCPT = cpt<IO>();
   const int range = (int)blockIdx.x / m.cpr;
   const int slot = ((int)blockIdx.x % m.cpr) * kSThreads + (int)threadIdx.x;
   // this thread's head and lanes
   const bool qk = slot < m.qk_slots;
-  const int lph = qk ? m.lphk : m.lphv;
+  const int lph = qk ? LPHK : m.lphv;
   const int rel = qk ? slot : slot - m.qk_slots;
   const int hh = rel / lph, l = rel % lph;  // head (q heads then k heads, or v head), lane
   const int width = qk ? a.K : a.V;
@@ -181,7 +182,6 @@ __global__ void __launch_bounds__(kSThreads, 2) prologue_kernel(PrologueArgs a, 
   const int64_t Ch = 2LL * a.hk * a.K + (int64_t)a.hv * a.V;
   const int64_t c = (qk ? (int64_t)hh * a.K : 2LL * a.hk * a.K + (int64_t)hh * a.V) + kCPT * l;
   const int head = qk && hh >= a.hk ? hh - a.hk : hh, heads = qk ? a.hk : a.hv;
-  IO* dst = static_cast<IO*>(qk ? (hh < a.hk ? a.q : a.k) : a.v) + (int64_t)head * width + kCPT * l;
   const int64_t drow = (int64_t)heads * width;
   const bool warp_qk = ((slot & ~31) < m.qk_slots);  // the warp holds some q / k head
   const int W = a.W;
@@ -192,82 +192,125 @@ __global__ void __launch_bounds__(kSThreads, 2) prologue_kernel(PrologueArgs a, 
     for (int i = 0; i < 4; ++i)
       w[ch][i] = (act && i >= 4 - W) ? a.conv_w[(c + ch) * W + i - (4 - W)] : 0.f;
 
-  const int64_t t0 = a.T * range / m.ranges, t1 = a.T * (range + 1) / m.ranges;
+  // token indices fit in 32 bits (the API caps the token count at INT32_MAX)
+  const int t0 = (int)(a.T * range / m.ranges), t1 = (int)(a.T * (range + 1) / m.ranges);
   int n = seq_of(a.cu, a.N, t0);
-  int64_t s0 = a.cu ? a.cu[n] : 0, s1 = a.cu ? a.cu[n + 1] : a.T;  // the sequence's bounds
+  int s0 = a.cu ? a.cu[n] : 0, s1 = a.cu ? a.cu[n + 1] : (int)a.T;  // the sequence's bounds
 
-  // the window ahead of the run (replaced from the conv state where a token's window reaches
-  // before its sequence's start)
-  float x3[kCPT], x2[kCPT], x1[kCPT];
+  // window slots: token t0 + i lives in slot i mod 4; slots 1, 2, 3 start with the three tokens
+  // ahead of the range (replaced from the conv state where a window reaches before its
+  // sequence's start)
+  float xw[4][kCPT];
 #pragma unroll
-  for (int m2 = 0; m2 < kCPT; ++m2) x3[m2] = x2[m2] = x1[m2] = 0.f;
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int ch = 0; ch < kCPT; ++ch) xw[i][ch] = 0.f;
   if (act && t0 >= 3) {
-    unpack<IO>(raw_at<IO>(a.x, (t0 - 3) * Ch + c), x3);
-    unpack<IO>(raw_at<IO>(a.x, (t0 - 2) * Ch + c), x2);
-    unpack<IO>(raw_at<IO>(a.x, (t0 - 1) * Ch + c), x1);
+    unpack<IO>(raw_at<IO>(a.x, (t0 - 3) * Ch + c), xw[1]);
+    unpack<IO>(raw_at<IO>(a.x, (t0 - 2) * Ch + c), xw[2]);
+    unpack<IO>(raw_at<IO>(a.x, (t0 - 1) * Ch + c), xw[3]);
   }
-  // the thread's ring of inputs in flight: slot r of thread i at ring[r][i]
+  // the thread's ring of inputs in flight: token t0 + i in slot i mod kRing, at ring[slot][thread]
   extern __shared__ __align__(16) uint4 ring[];
   const uint32_t ring0 = (uint32_t)__cvta_generic_to_shared(ring + threadIdx.x);
   const IO* xc = static_cast<const IO*>(a.x) + c;
 #pragma unroll
   for (int r = 0; r < kRing - 1; ++r) {
-    const int64_t t = t0 + r;
-    ring_copy(ring0 + r * kSThreads * 16, xc + (act && t < t1 ? t * Ch : 0), act && t < t1);
+    const bool ok = act && t0 + r < t1;
+    ring_copy(ring0 + r * kSThreads * 16, ok ? xc + (int64_t)(t0 + r) * Ch : xc, ok);
   }
-  int rs = 0;  // the ring slot of token t
-  for (int64_t t = t0; t < t1; ++t) {
-    {  // token t + kRing - 1 into the slot that token t - 1 used; then token t has landed
-      const int64_t tn = t + kRing - 1;
-      const int sn = rs == 0 ? kRing - 1 : rs - 1;
-      ring_copy(ring0 + sn * kSThreads * 16, xc + (act && tn < t1 ? tn * Ch : 0), act && tn < t1);
-      asm volatile("cp.async.wait_group %0;\n" ::"n"(kRing - 1) : "memory");
-    }
-    while (n < a.N - 1 && t >= s1) {  // (uniform: every thread of the CTA walks the same tokens)
-      ++n;
-      s0 = s1;
-      s1 = a.cu[n + 1];
-    }
-    if (t - 3 < s0 && act) {  // the window reaches before the sequence's start
-      window_input<IO>(a, Ch, c, t - 3, s0, n, x3);
-      window_input<IO>(a, Ch, c, t - 2, s0, n, x2);
-      window_input<IO>(a, Ch, c, t - 1, s0, n, x1);
-    }
-    float x0[kCPT], o[kCPT];
-    {
-      const uint4 v = ring[rs * kSThreads + threadIdx.x];
-      Raw r;
-      r.u[0] = v.x; r.u[1] = v.y; r.u[2] = v.z; r.u[3] = v.w;
-      unpack<IO>(r, x0);
-    }
-    rs = rs == kRing - 1 ? 0 : rs + 1;
-    float s2 = 0.f;
+  const IO* xn = xc + (int64_t)(t0 + kRing - 1) * Ch;  // the next token to copy
+  IO* dp = static_cast<IO*>(qk ? (hh < a.hk ? a.q : a.k) : a.v) + (int64_t)head * width +
+           kCPT * l + t0 * drow;
+  static_assert(kRing % 4 == 0, "ring slots advance four tokens at a time");
+  for (int tb = t0; tb < t1; tb += 4) {
+    const int rb = (tb - t0) % kRing;
 #pragma unroll
-    for (int ch = 0; ch < kCPT; ++ch) {
-      float y = fmaf(w[ch][0], x3[ch], fmaf(w[ch][1], x2[ch], fmaf(w[ch][2], x1[ch], w[ch][3] * x0[ch])));
-      if (a.silu) y = silu<IO>(y);
-      o[ch] = y;
-      s2 = fmaf(y, y, s2);
-      x3[ch] = x2[ch];
-      x2[ch] = x1[ch];
-      x1[ch] = x0[ch];
-    }
-    if (warp_qk) {  // 1 / max(|y|, 1e-6) over the head's lanes (aligned groups of lphk)
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float other = __shfl_xor_sync(0xffffffffu, s2, off);
-        if (off < m.lphk) s2 += other;
+    for (int J = 0; J < 4; ++J) {
+      const int t = tb + J;
+      if (t >= t1) break;
+      {  // token t + kRing - 1 into the slot that token t - 1 used; then token t has landed
+        const bool ok = act && t + kRing - 1 < t1;
+        ring_copy(ring0 + ((rb + J + kRing - 1) % kRing) * kSThreads * 16, ok ? xn : xc, ok);
+        xn += Ch;
+        asm volatile("cp.async.wait_group %0;\n" ::"n"(kRing - 1) : "memory");
       }
-      if (qk) {
-        const float inv = rsqrtf(fmaxf(s2, 1e-12f));
-#pragma unroll
-        for (int ch = 0; ch < kCPT; ++ch) o[ch] *= inv;
+      if (t >= s1 || t - 3 < s0) {  // (uniform: every thread of the CTA walks the same tokens)
+        while (n < a.N - 1 && t >= s1) {
+          ++n;
+          s0 = s1;
+          s1 = a.cu[n + 1];
+        }
+        if (t - 3 < s0 && act) {  // the window reaches before the sequence's start
+          window_input<IO>(a, Ch, c, t - 3, s0, n, xw[(J + 1) & 3]);
+          window_input<IO>(a, Ch, c, t - 2, s0, n, xw[(J + 2) & 3]);
+          window_input<IO>(a, Ch, c, t - 1, s0, n, xw[(J + 3) & 3]);
+        }
       }
+      {
+        const uint4 v = ring[(rb + J) * kSThreads + threadIdx.x];
+        Raw r;
+        r.u[0] = v.x; r.u[1] = v.y; r.u[2] = v.z; r.u[3] = v.w;
+        unpack<IO>(r, xw[J]);
+      }
+      float o[kCPT], s2 = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < kCPT; ++ch) {
+        float y = fmaf(w[ch][0], xw[(J + 1) & 3][ch],
+                       fmaf(w[ch][1], xw[(J + 2) & 3][ch],
+                            fmaf(w[ch][2], xw[(J + 3) & 3][ch], w[ch][3] * xw[J][ch])));
+        if (a.silu) y = silu<IO>(y);
+        o[ch] = y;
+        s2 = fmaf(y, y, s2);
+      }
+      if (warp_qk) {  // 1 / max(|y|, 1e-6) over the head's lanes (aligned groups of LPHK)
+#pragma unroll
+        for (int off = 1; off < LPHK; off <<= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, off);
+        if (qk) {
+          const float inv = rsqrtf(fmaxf(s2, 1e-12f));
+#pragma unroll
+          for (int ch = 0; ch < kCPT; ++ch) o[ch] *= inv;
+        }
+      }
+      if (act) raw_store(dp, pack<IO>(o));
+      dp += drow;
     }
-    if (act) raw_store(dst + t * drow, pack<IO>(o));
   }
   asm volatile("cp.async.wait_all;\n" ::: "memory");
   gate_maps(a);
+}
+
+template <typename IO, int LPHK>
+cudaError_t launch_prologue(const PrologueArgs& a, SlotMap m, cudaStream_t s) {
+  const int smem = kRing * kSThreads * 16;
+  const auto kern = prologue_kernel<IO, LPHK>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int dev = 0, sms = 0, per_sm = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSThreads, smem);
+  if (e != cudaSuccess) return e;
+  // one wave: the token ranges split the resident CTAs between them (at least 16 tokens each)
+  const int64_t resident = (int64_t)(per_sm > 0 ? per_sm : 1) * sms;
+  int64_t ranges = resident / m.cpr;
+  if (ranges > (a.T + 15) / 16) ranges = (a.T + 15) / 16;
+  m.ranges = (int)(ranges > 1 ? ranges : 1);
+  const int64_t ctas = (int64_t)m.ranges * m.cpr;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  kern<<<(unsigned)ctas, kSThreads, smem, s>>>(a, m);
+  return cudaGetLastError();
+}
+
+template <typename IO>
+cudaError_t launch_prologue_io(const PrologueArgs& a, const SlotMap& m, cudaStream_t s) {
+  switch (m.lphk) {
+    case 1: return launch_prologue<IO, 1>(a, m, s);
+    case 2: return launch_prologue<IO, 2>(a, m, s);
+    case 4: return launch_prologue<IO, 4>(a, m, s);
+    case 8: return launch_prologue<IO, 8>(a, m, s);
+    case 16: return launch_prologue<IO, 16>(a, m, s);
+    default: return launch_prologue<IO, 32>(a, m, s);
+  }
 }
 
 // new conv state: the last W - 1 inputs of each sequence; when a sequence is shorter, the older
@@ -307,25 +350,9 @@ cudaError_t prologue(const PrologueArgs& a, cudaStream_t s) {
     m.qk_slots = 2 * a.hk * m.lphk;
     m.slots = m.qk_slots + a.hv * m.lphv;
     m.cpr = (m.slots + kSThreads - 1) / kSThreads;
-    const int smem = kRing * kSThreads * 16;
-    const auto kern = a.bf16 ? prologue_kernel<__nv_bfloat16> : prologue_kernel<float>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    int dev = 0, sms = 0, per_sm = 0;
-    if (e == cudaSuccess) e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSThreads, smem);
+    cudaError_t e = a.bf16 ? launch_prologue_io<__nv_bfloat16>(a, m, s)
+                           : launch_prologue_io<float>(a, m, s);
     if (e != cudaSuccess) return e;
-    // one wave: the token ranges split the resident CTAs between them (at least 16 tokens each)
-    const int64_t resident = (int64_t)(per_sm > 0 ? per_sm : 1) * sms;
-    int64_t ranges = resident / m.cpr;
-    if (ranges > (a.T + 15) / 16) ranges = (a.T + 15) / 16;
-    m.ranges = (int)(ranges > 1 ? ranges : 1);
-    const int64_t ctas = (int64_t)m.ranges * m.cpr;
-    if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    if (a.bf16)
-      prologue_kernel<__nv_bfloat16><<<(unsigned)ctas, kSThreads, smem, s>>>(a, m);
-    else
-      prologue_kernel<float><<<(unsigned)ctas, kSThreads, smem, s>>>(a, m);
   }
   if (a.state_out && a.W > 1) {
     const dim3 grid(64, (unsigned)a.N);
