@@ -87,32 +87,96 @@ template <int K>
 __host__ __device__ constexpr int row_stride() { return K + 4 * kPhases; }
 
 // Shared memory of one column CTA: kStage rows of k (and, reversed, q), the CTA's columns of v
-// (or dout), exp(g) and beta.
+// (or dout), exp(g), beta, the scale factors of the scaled state and two block scalars.
 template <int K>
 __host__ __device__ constexpr size_t column_smem() {
-  return sizeof(float) * ((size_t)2 * kStage * row_stride<K>() + (size_t)kStage * kColBlock + 2 * kStage);
+  return sizeof(float) * ((size_t)2 * kStage * row_stride<K>() + (size_t)kStage * kColBlock + 4 * kStage + 4);
 }
 
-// kStage tokens [c0 + s0, c0 + s0 + n) of chunk inputs into shared memory (fp32, padded rows)
+// The scaled state.  Within a staged block the recurrences carry h~ with h = A h~, A the product
+// of the decays exp(g) met so far in the block, so that a token's update is one multiply-add per
+// element:
+//   forward, token t (A' = A exp(g_t)):  delta = beta (v - A' k.h~),  h~ += k delta / A'
+//   reverse, token t (B the decays of the block's later tokens):  F~ = h~ + q dout / B,
+//            h~ = F~ - beta k (k.F~)
+// and h = A h~ again at the block's end.  A comes from a warp prefix sum P of g: A'_t = e^{P_t},
+// B_t = e^{P_end - P_t}.  A block whose partial sums leave [-27, 27] (factors beyond ~5e11) takes
+// the unscaled recurrence instead.
+struct ColStage {
+  float *ks, *qs, *vs, *gs, *bs, *sc, *iv, *blk;  // blk[0]: 1 = scaled; blk[1]: e^{P_end}
+};
+
+// kStage tokens [t0, t0 + n) of chunk inputs into shared memory (fp32, padded rows); warp 0
+// also forms the block's scale factors
 template <int K, bool REVERSE>
 __device__ __forceinline__ void stage_tokens(const BwdArgs& a, int64_t t0, int n, int j, int kh,
-                                             int v0, float* ks, float* qs, float* vs, float* gs,
-                                             float* bs) {
+                                             int v0, ColStage st) {
   constexpr int RPL = K / kPhases, RS = row_stride<K>();
   const void* vin = REVERSE ? a.dout : a.v;
+  if (threadIdx.x < 32) {
+    const int t = threadIdx.x;
+    const float g = t < n ? a.g[(t0 + t) * a.hv + j] : 0.f;
+    if (t < n) {
+      st.gs[t] = __expf(g);
+      st.bs[t] = a.beta[(t0 + t) * a.hv + j];
+    }
+    float P = g;  // inclusive prefix sum of g over the block
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, P, o);
+      if (t >= o) P += y;
+    }
+    const float Pn = __shfl_sync(0xffffffffu, P, n - 1);
+    const bool ok = __all_sync(0xffffffffu, fabsf(P) <= 27.f);
+    if (t < n) {
+      if (REVERSE) {
+        st.iv[t] = __expf(P - Pn);  // 1 / B before token t
+      } else {
+        st.sc[t] = __expf(P);       // A'
+        st.iv[t] = __expf(-P);      // 1 / A'
+      }
+    }
+    if (t == 0) {
+      st.blk[0] = ok ? 1.f : 0.f;
+      st.blk[1] = __expf(Pn);
+    }
+  }
   for (int e = threadIdx.x; e < n * (K / 8); e += kColThreads) {
     const int t = e / (K / 8), i = 8 * (e % (K / 8));
     const int o = t * RS + (i / RPL) * (RPL + 4) + i % RPL;  // 8 | RPL: one segment
-    ld8(a.k, ((t0 + t) * a.hk + kh) * K + i, a.bf16, ks + o);
-    if (REVERSE) ld8(a.q, ((t0 + t) * a.hk + kh) * K + i, a.bf16, qs + o);
+    ld8(a.k, ((t0 + t) * a.hk + kh) * K + i, a.bf16, st.ks + o);
+    if (REVERSE) ld8(a.q, ((t0 + t) * a.hk + kh) * K + i, a.bf16, st.qs + o);
   }
   for (int e = threadIdx.x; e < n * (kColBlock / 8); e += kColThreads) {
     const int t = e / (kColBlock / 8), cc = 8 * (e % (kColBlock / 8));
-    ld8(vin, ((t0 + t) * a.hv + j) * a.V + v0 + cc, a.bf16, vs + t * kColBlock + cc);
+    ld8(vin, ((t0 + t) * a.hv + j) * a.V + v0 + cc, a.bf16, st.vs + t * kColBlock + cc);
   }
-  for (int t = threadIdx.x; t < n; t += kColThreads) {
-    gs[t] = __expf(a.g[(t0 + t) * a.hv + j]);
-    bs[t] = a.beta[(t0 + t) * a.hv + j];
+}
+
+// the dot product of a staged row segment with the thread's rows, summed over the column's
+// phases
+template <int RPL>
+__device__ __forceinline__ float col_dot(const float* kv, const float* h) {
+  float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+  for (int i = 0; i < RPL; i += 4) {
+    d0 = fmaf(kv[i], h[i], d0);
+    d1 = fmaf(kv[i + 1], h[i + 1], d1);
+    d2 = fmaf(kv[i + 2], h[i + 2], d2);
+    d3 = fmaf(kv[i + 3], h[i + 3], d3);
+  }
+  float d = (d0 + d1) + (d2 + d3);
+  d += __shfl_xor_sync(0xffffffffu, d, 1);
+  d += __shfl_xor_sync(0xffffffffu, d, 2);
+  d += __shfl_xor_sync(0xffffffffu, d, 4);
+  return d;
+}
+template <int RPL>
+__device__ __forceinline__ void ld_seg(const float* src, float* dst) {
+#pragma unroll
+  for (int i = 0; i < RPL / 4; ++i) {
+    const float4 f = reinterpret_cast<const float4*>(src)[i];
+    dst[4 * i] = f.x; dst[4 * i + 1] = f.y; dst[4 * i + 2] = f.z; dst[4 * i + 3] = f.w;
   }
 }
 
@@ -123,11 +187,15 @@ __device__ __forceinline__ void stage_tokens(const BwdArgs& a, int64_t t0, int n
 template <int K, bool REVERSE>
 __device__ __forceinline__ void column_run(const BwdArgs& a, float* csm) {
   constexpr int RPL = K / kPhases, RS = row_stride<K>();
-  float* ks = csm;                        // [kStage][RS]
-  float* qs = ks + kStage * RS;           // [kStage][RS] (reverse)
-  float* vs = qs + kStage * RS;           // [kStage][kColBlock]
-  float* gs = vs + kStage * kColBlock;    // [kStage]
-  float* bs = gs + kStage;                // [kStage]
+  ColStage st;
+  st.ks = csm;                         // [kStage][RS]
+  st.qs = st.ks + kStage * RS;         // [kStage][RS] (reverse)
+  st.vs = st.qs + kStage * RS;         // [kStage][kColBlock]
+  st.gs = st.vs + kStage * kColBlock;  // [kStage] exp(g)
+  st.bs = st.gs + kStage;              // [kStage] beta
+  st.sc = st.bs + kStage;              // [kStage] A' (forward)
+  st.iv = st.sc + kStage;              // [kStage] 1 / A' (forward), 1 / B (reverse)
+  st.blk = st.iv + kStage;             // [2]
   const int nj = blockIdx.x, n = nj / a.hv, j = nj % a.hv, kh = j / (a.hv / a.hk);
   const int col = threadIdx.x / kPhases, p = threadIdx.x % kPhases;
   const int v0 = blockIdx.y * kColBlock, v = v0 + col;
@@ -154,49 +222,53 @@ __device__ __forceinline__ void column_run(const BwdArgs& a, float* csm) {
       const int b = REVERSE ? nb - 1 - bi : bi;
       const int bn = (L - b * kStage) < kStage ? (L - b * kStage) : kStage;
       __syncthreads();  // the previous block's inputs have been used
-      stage_tokens<K, REVERSE>(a, c0 + b * kStage, bn, j, kh, v0, ks, qs, vs, gs, bs);
+      stage_tokens<K, REVERSE>(a, c0 + b * kStage, bn, j, kh, v0, st);
       __syncthreads();
-      for (int s = 0; s < bn; ++s) {
-        const int t = REVERSE ? bn - 1 - s : s;
-        const float alpha = gs[t], beta = bs[t], x = vs[t * kColBlock + col];
-        float kv[RPL];
-        const float4* kr = reinterpret_cast<const float4*>(ks + t * RS + ko);
+      if (st.blk[0] != 0.f) {  // the scaled state
+#pragma unroll 2
+        for (int s = 0; s < bn; ++s) {
+          const int t = REVERSE ? bn - 1 - s : s;
+          const float beta = st.bs[t], x = st.vs[t * kColBlock + col], ivt = st.iv[t];
+          float kv[RPL];
+          ld_seg<RPL>(st.ks + t * RS + ko, kv);
+          if (REVERSE) {  // F~ = h~ + q dout / B;  h~ <- F~ - beta k (k . F~)
+            float qv[RPL];
+            ld_seg<RPL>(st.qs + t * RS + ko, qv);
+            const float xs = x * ivt;
 #pragma unroll
-        for (int i = 0; i < RPL / 4; ++i) {
-          const float4 f = kr[i];
-          kv[4 * i] = f.x; kv[4 * i + 1] = f.y; kv[4 * i + 2] = f.z; kv[4 * i + 3] = f.w;
-        }
-        if (REVERSE) {  // F = dh + q dout^T
-          const float4* qr = reinterpret_cast<const float4*>(qs + t * RS + ko);
+            for (int i = 0; i < RPL; ++i) h[i] = fmaf(qv[i], xs, h[i]);
+            const float bd = beta * col_dot<RPL>(kv, h);
 #pragma unroll
-          for (int i = 0; i < RPL / 4; ++i) {
-            const float4 f = qr[i];
-            h[4 * i] = fmaf(f.x, x, h[4 * i]);
-            h[4 * i + 1] = fmaf(f.y, x, h[4 * i + 1]);
-            h[4 * i + 2] = fmaf(f.z, x, h[4 * i + 2]);
-            h[4 * i + 3] = fmaf(f.w, x, h[4 * i + 3]);
+            for (int i = 0; i < RPL; ++i) h[i] = fmaf(-kv[i], bd, h[i]);
+          } else {  // delta = beta (v - A' k . h~);  h~ += k delta / A'
+            const float d = col_dot<RPL>(kv, h);
+            const float f = beta * fmaf(-st.sc[t], d, x) * ivt;
+#pragma unroll
+            for (int i = 0; i < RPL; ++i) h[i] = fmaf(kv[i], f, h[i]);
           }
         }
-        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+        const float mult = st.blk[1];
 #pragma unroll
-        for (int i = 0; i < RPL; i += 4) {
-          d0 = fmaf(kv[i], h[i], d0);
-          d1 = fmaf(kv[i + 1], h[i + 1], d1);
-          d2 = fmaf(kv[i + 2], h[i + 2], d2);
-          d3 = fmaf(kv[i + 3], h[i + 3], d3);
-        }
-        float d = (d0 + d1) + (d2 + d3);
-        d += __shfl_xor_sync(0xffffffffu, d, 1);
-        d += __shfl_xor_sync(0xffffffffu, d, 2);
-        d += __shfl_xor_sync(0xffffffffu, d, 4);
-        if (REVERSE) {  // dd = k . F;  dh <- alpha (F - beta k dd)
-          const float bd = beta * d;
+        for (int i = 0; i < RPL; ++i) h[i] *= mult;
+      } else {  // the plain recurrence
+        for (int s = 0; s < bn; ++s) {
+          const int t = REVERSE ? bn - 1 - s : s;
+          const float alpha = st.gs[t], beta = st.bs[t], x = st.vs[t * kColBlock + col];
+          float kv[RPL];
+          ld_seg<RPL>(st.ks + t * RS + ko, kv);
+          if (REVERSE) {  // F = dh + q dout^T;  dd = k . F;  dh <- alpha (F - beta k dd)
+            float qv[RPL];
+            ld_seg<RPL>(st.qs + t * RS + ko, qv);
 #pragma unroll
-          for (int i = 0; i < RPL; ++i) h[i] = alpha * fmaf(-kv[i], bd, h[i]);
-        } else {  // delta = beta (v - alpha k . h);  h <- alpha h + k delta
-          const float dl = beta * (x - alpha * d);
+            for (int i = 0; i < RPL; ++i) h[i] = fmaf(qv[i], x, h[i]);
+            const float bd = beta * col_dot<RPL>(kv, h);
 #pragma unroll
-          for (int i = 0; i < RPL; ++i) h[i] = fmaf(kv[i], dl, alpha * h[i]);
+            for (int i = 0; i < RPL; ++i) h[i] = alpha * fmaf(-kv[i], bd, h[i]);
+          } else {  // delta = beta (v - alpha k . h);  h <- alpha h + k delta
+            const float dl = beta * (x - alpha * col_dot<RPL>(kv, h));
+#pragma unroll
+            for (int i = 0; i < RPL; ++i) h[i] = fmaf(kv[i], dl, alpha * h[i]);
+          }
         }
       }
     }
@@ -211,7 +283,7 @@ __device__ __forceinline__ void column_run(const BwdArgs& a, float* csm) {
 // grid (N hv, V / kColBlock, 2): z = 0 the forward recurrence, z = 1 the reverse one; the two
 // directions are independent and share the SMs.
 template <int K>
-__global__ void __launch_bounds__(kColThreads) column_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(kColThreads, 4) column_kernel(BwdArgs a) {
   extern __shared__ __align__(16) float csm[];
   if (blockIdx.z == 0)
     column_run<K, false>(a, csm);
@@ -227,8 +299,8 @@ struct GradSmem {
   float dA[C][C + 1], dat[C][C + 1];
   float G[C], eG[C], ekt[C], b[C], dG[C];
   float scal[4];
-  float As[C][33];      // product tiles
-  float Bs[32][129];
+  float As[C][36];      // product tiles (row strides of 4 and 8 banks mod 32: the tensor-core
+  float Bs[32][136];    // fragments read them without bank conflicts)
   float X[C][129];      // the triangular solves
   float KF[C][129], QF[C][129];  // k, q of the chunk (fp32; rows past the chunk are zero)
 };
@@ -238,22 +310,42 @@ struct GradSmem {
 template <int K, int V>
 __host__ __device__ constexpr int64_t grad_slice() { return 6 * (int64_t)C * V + (int64_t)C * K; }
 
-// out(i, c, x) for i < C, c < N with x = sum_{y < Y} A(i, y) B(y, c) (Y a multiple of 32):
-// 32-wide slices of y are staged in shared memory; thread (ty, tx) of 16 x 32 accumulates rows
-// ty + 16 r and columns tx + 32 m in registers.  Each thread fetches its share of the next slice
-// into registers while the current one is multiplied, so the operands' latency is hidden.
-// AI / BY: the operand's contiguous index is i (for A) / y (for B), so that the fetches walk
-// memory in order.
-template <int N, bool AI, bool BY, typename FA, typename FB, typename FO>
+// TF32 operand (round to nearest, ties away) and one warp-level tensor-core product
+// D(16 x 8) += A(16 x 8) B(8 x 8) with fp32 accumulation
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;\n" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// out(i, c, x) for i < C, c < N with x = sum_{y < Y} A(i, y) B(y, c) (Y a multiple of 32), on
+// the tensor cores: 32-wide slices of y are staged in shared memory (each thread fetches its
+// share of the next slice into registers while the current one is multiplied); warp w owns rows
+// 16 (w mod 4) .. + 16 and N / 4 columns from (w / 4) N / 4, as N / 32 tiles of 16 x 8.
+// TF3: each operand is split into a TF32 head and a TF32 remainder and three products are
+// summed (head x remainder, remainder x head, head x head), which keeps fp32 accuracy; without
+// it the operands are rounded to TF32 once.  AI / BY: the operand's contiguous index is i (for
+// A) / y (for B), so that the fetches walk memory in order.
+template <int N, bool AI, bool BY, bool TF3, typename FA, typename FB, typename FO>
 __device__ __forceinline__ void mm(GradSmem& sm, int Y, FA A, FB B, FO out) {
-  constexpr int RM = C / 16, RN = N / 32;
+  constexpr int NT = N / 32;  // 16 x 8 tiles of a warp
   constexpr int NA = C * 32 / kGradThreads, NB = 32 * N / kGradThreads;
-  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
-  float acc[RM][RN];
+  static_assert(kGradThreads == 512 && C == 64, "16 warps over a 64-row output");
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int grp = lane >> 2, tig = lane & 3;
+  const int r0 = 16 * (warp & 3) + grp, c0 = (warp >> 2) * (N / 4) + grp;
+  float acc[NT][4];
 #pragma unroll
-  for (int r = 0; r < RM; ++r)
+  for (int m = 0; m < NT; ++m)
 #pragma unroll
-    for (int m = 0; m < RN; ++m) acc[r][m] = 0.f;
+    for (int q = 0; q < 4; ++q) acc[m][q] = 0.f;
   float pa[NA], pb[NB];
   auto fetch = [&](int y0) {
 #pragma unroll
@@ -282,31 +374,49 @@ __device__ __forceinline__ void mm(GradSmem& sm, int Y, FA A, FB B, FO out) {
     }
     __syncthreads();
     if (y0 + 32 < Y) fetch(y0 + 32);
-#pragma unroll 8
-    for (int yy = 0; yy < 32; ++yy) {
-      float av[RM], bv[RN];
 #pragma unroll
-      for (int r = 0; r < RM; ++r) av[r] = sm.As[ty + 16 * r][yy];
+    for (int k8 = 0; k8 < 32; k8 += 8) {
+      const float af[4] = {sm.As[r0][k8 + tig], sm.As[r0 + 8][k8 + tig], sm.As[r0][k8 + tig + 4],
+                           sm.As[r0 + 8][k8 + tig + 4]};
+      uint32_t ah[4], al[4];
 #pragma unroll
-      for (int m = 0; m < RN; ++m) bv[m] = sm.Bs[yy][tx + 32 * m];
+      for (int q = 0; q < 4; ++q) {
+        ah[q] = to_tf32(af[q]);
+        if (TF3) al[q] = to_tf32(af[q] - __uint_as_float(ah[q]));
+      }
 #pragma unroll
-      for (int r = 0; r < RM; ++r)
+      for (int m = 0; m < NT; ++m) {
+        const float bf[2] = {sm.Bs[k8 + tig][c0 + 8 * m], sm.Bs[k8 + tig + 4][c0 + 8 * m]};
+        uint32_t bh[2], bl[2];
 #pragma unroll
-        for (int m = 0; m < RN; ++m) acc[r][m] = fmaf(av[r], bv[m], acc[r][m]);
+        for (int q = 0; q < 2; ++q) {
+          bh[q] = to_tf32(bf[q]);
+          if (TF3) bl[q] = to_tf32(bf[q] - __uint_as_float(bh[q]));
+        }
+        if (TF3) {
+          mma_tf32(acc[m], al, bh);
+          mma_tf32(acc[m], ah, bl);
+        }
+        mma_tf32(acc[m], ah, bh);
+      }
     }
   }
+  const int cc = (warp >> 2) * (N / 4) + 2 * tig;
 #pragma unroll
-  for (int r = 0; r < RM; ++r)
-#pragma unroll
-    for (int m = 0; m < RN; ++m) out(ty + 16 * r, tx + 32 * m, acc[r][m]);
+  for (int m = 0; m < NT; ++m) {
+    out(r0, cc + 8 * m, acc[m][0]);
+    out(r0, cc + 8 * m + 1, acc[m][1]);
+    out(r0 + 8, cc + 8 * m, acc[m][2]);
+    out(r0 + 8, cc + 8 * m + 1, acc[m][3]);
+  }
 }
 
 // One CTA per (chunk slot, value head); grid-stride over the units.
-template <int K, int V>
+template <int K, int V, bool TF3>
 __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
   extern __shared__ __align__(16) uint8_t smraw[];
   GradSmem& sm = *reinterpret_cast<GradSmem*>(smraw);
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int64_t nslots = a.nslots, units = nslots * a.hv;
   float* ws = a.scratch + (int64_t)blockIdx.x * grad_slice<K, V>();
   float* KS = ws;            // [C][V]  K S
@@ -367,16 +477,16 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
     __syncthreads();
     auto gam = [&](int t, int s) { return __expf(sm.G[t] - sm.G[s]); };  // for s <= t
     // ---- Gamma o K K^T (strictly lower), attn; K S, Q S
-    mm<C, false, true>(sm, K, [&](int t, int y) { return KF(t, y); },
+    mm<C, false, true, TF3>(sm, K, [&](int t, int y) { return KF(t, y); },
                        [&](int y, int s) { return KF(s, y); },
                        [&](int t, int s, float x) { sm.GKK[t][s] = (s < t && t < L) ? gam(t, s) * x : 0.f; });
-    mm<C, false, true>(sm, K, [&](int t, int y) { return QF(t, y); },
+    mm<C, false, true, TF3>(sm, K, [&](int t, int y) { return QF(t, y); },
                        [&](int y, int s) { return KF(s, y); },
                        [&](int t, int s, float x) { sm.At[t][s] = (s <= t && t < L) ? gam(t, s) * x : 0.f; });
-    mm<V, false, true>(sm, K, [&](int t, int y) { return KF(t, y); },
+    mm<V, false, true, TF3>(sm, K, [&](int t, int y) { return KF(t, y); },
                        [&](int y, int c) { return Sx[c * K + y]; },
                        [&](int t, int c, float x) { KS[t * V + c] = x; });
-    mm<V, false, true>(sm, K, [&](int t, int y) { return QF(t, y); },
+    mm<V, false, true, TF3>(sm, K, [&](int t, int y) { return QF(t, y); },
                        [&](int y, int c) { return Sx[c * K + y]; },
                        [&](int t, int c, float x) { QS[t * V + c] = x; });
     __syncthreads();
@@ -405,10 +515,10 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
     for (int e = tid; e < C * V; e += kGradThreads) DL[e] = sm.X[e / V][e % V];
     __syncthreads();
     // ---- d_delta = attn^T dO + Kt D
-    mm<V, true, false>(sm, C, [&](int t, int s) { return sm.At[s][t]; },
+    mm<V, true, false, TF3>(sm, C, [&](int t, int s) { return sm.At[s][t]; },
                        [&](int s, int c) { return DO[s * V + c]; },
                        [&](int t, int c, float x) { DD[t * V + c] = x; });
-    mm<V, false, true>(sm, K, [&](int t, int y) { return sm.ekt[t] * KF(t, y); },
+    mm<V, false, true, TF3>(sm, K, [&](int t, int y) { return sm.ekt[t] * KF(t, y); },
                        [&](int y, int c) { return Dx[c * K + y]; },
                        [&](int t, int c, float x) { sm.X[t][c] = t < L ? DD[t * V + c] + x : 0.f; });
     __syncthreads();
@@ -434,14 +544,14 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
     }
     __syncthreads();
     // ---- dA = -(dB delta^T) o strictly lower, dattn = (dO delta^T) o lower
-    mm<C, false, true>(sm, V, [&](int t, int c) { return DD[t * V + c]; },
+    mm<C, false, true, TF3>(sm, V, [&](int t, int c) { return DD[t * V + c]; },
                        [&](int c, int s) { return DL[s * V + c]; },
                        [&](int t, int s, float x) { sm.dA[t][s] = (s < t && t < L) ? -x : 0.f; });
-    mm<C, false, true>(sm, V, [&](int t, int c) { return DO[t * V + c]; },
+    mm<C, false, true, TF3>(sm, V, [&](int t, int c) { return DO[t * V + c]; },
                        [&](int c, int s) { return DL[s * V + c]; },
                        [&](int t, int s, float x) { sm.dat[t][s] = (s <= t && t < L) ? x : 0.f; });
     // ---- delta D^T
-    mm<K, false, false>(sm, V, [&](int t, int c) { return DL[t * V + c]; },
+    mm<K, false, false, TF3>(sm, V, [&](int t, int c) { return DL[t * V + c]; },
                         [&](int c, int i) { return Dx[c * K + i]; },
                         [&](int t, int i, float x) { XD[t * K + i] = x; });
     __syncthreads();
@@ -509,26 +619,26 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
     float* dqv = a.dqv + (t0 * a.hv + j) * (int64_t)K;
     float* dkv = a.dkv + (t0 * a.hv + j) * (int64_t)K;
     const int64_t rs = (int64_t)a.hv * K;  // row stride of dqv, dkv
-    mm<K, false, false>(sm, V, [&](int t, int c) { return DO[t * V + c]; },
+    mm<K, false, false, TF3>(sm, V, [&](int t, int c) { return DO[t * V + c]; },
                         [&](int c, int i) { return Sx[c * K + i]; },
                         [&](int t, int i, float x) { if (t < L) dqv[t * rs + i] = sm.eG[t] * x; });
-    mm<K, false, false>(sm, C, [&](int t, int s) { return sm.dat[t][s]; },
+    mm<K, false, false, TF3>(sm, C, [&](int t, int s) { return sm.dat[t][s]; },
                         [&](int s, int i) { return KF(s, i); },
                         [&](int t, int i, float x) { if (t < L) dqv[t * rs + i] += x; });
     // ---- dk = -diag(beta e^G) dB S^T + diag(e^{G_L - G}) delta D^T + diag(beta) (dA o Gamma) K
     //          + (dA o Gamma)^T diag(beta) K + (dattn o Gamma)^T Q
-    mm<K, false, false>(sm, V, [&](int t, int c) { return DD[t * V + c]; },
+    mm<K, false, false, TF3>(sm, V, [&](int t, int c) { return DD[t * V + c]; },
                         [&](int c, int i) { return Sx[c * K + i]; },
                         [&](int t, int i, float x) {
                           if (t < L) dkv[t * rs + i] = sm.ekt[t] * XD[t * K + i] - sm.b[t] * sm.eG[t] * x;
                         });
-    mm<K, false, false>(sm, C, [&](int t, int s) { return sm.dA[t][s]; },
+    mm<K, false, false, TF3>(sm, C, [&](int t, int s) { return sm.dA[t][s]; },
                         [&](int s, int i) { return KF(s, i); },
                         [&](int t, int i, float x) { if (t < L) dkv[t * rs + i] += sm.b[t] * x; });
-    mm<K, true, false>(sm, C, [&](int t, int s) { return sm.dA[s][t] * sm.b[s]; },
+    mm<K, true, false, TF3>(sm, C, [&](int t, int s) { return sm.dA[s][t] * sm.b[s]; },
                        [&](int s, int i) { return KF(s, i); },
                        [&](int t, int i, float x) { if (t < L) dkv[t * rs + i] += x; });
-    mm<K, true, false>(sm, C, [&](int t, int s) { return sm.dat[s][t]; },
+    mm<K, true, false, TF3>(sm, C, [&](int t, int s) { return sm.dat[s][t]; },
                        [&](int s, int i) { return QF(s, i); },
                        [&](int t, int i, float x) { if (t < L) dkv[t * rs + i] += x; });
   }
@@ -559,11 +669,17 @@ cudaError_t launch_all(const BwdArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(column_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)column_smem<K>());
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(chunk_grad_kernel<K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(chunk_grad_kernel<K, V, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(GradSmem));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(chunk_grad_kernel<K, V, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)sizeof(GradSmem));
   if (e != cudaSuccess) return e;
   column_kernel<K><<<cg, kColThreads, column_smem<K>(), s>>>(a);
-  chunk_grad_kernel<K, V><<<a.grad_ctas, kGradThreads, sizeof(GradSmem), s>>>(a);
+  if (a.bf16)  // TF32 products (their error is far below the bf16 rounding of the results)
+    chunk_grad_kernel<K, V, false><<<a.grad_ctas, kGradThreads, sizeof(GradSmem), s>>>(a);
+  else  // split-TF32 products: fp32 accuracy
+    chunk_grad_kernel<K, V, true><<<a.grad_ctas, kGradThreads, sizeof(GradSmem), s>>>(a);
   group_sum_kernel<<<1024, 256, 0, s>>>(a);
   return cudaGetLastError();
 }
