@@ -564,7 +564,7 @@ def run_ours(args, ws, rank, local):
             "workload": f"long-context bf16 T={T} Hk={HK} Hv={HV} K=V={KD}: gradients of q, k, "
                         "v, g, beta, h0 for a random dout",
             "ms_per_step": bwd_ms, "tokens_per_s": T / (bwd_ms / 1e3), "steps": BWD_STEPS,
-            "gpu_launches_per_step": 4,
+            "gpu_launches_per_step": 3,
             "roofline": {"bound": "alu", "unit": "TFLOP/s",
                          "achieved": BWD_FLOP_PER_TOKEN * T / (bwd_ms / 1e3) / 1e12,
                          "peak": FP32_ALU_TFLOPS,

@@ -41,10 +41,6 @@ namespace {
 constexpr int C = kChunk;  // 64
 constexpr int kGradThreads = 512;
 
-__device__ __forceinline__ float ld_io(const void* p, int64_t i, bool bf16) {
-  return bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i])
-              : static_cast<const float*>(p)[i];
-}
 __device__ __forceinline__ void st_io(void* p, int64_t i, float x, bool bf16) {
   if (bf16)
     static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(x);
@@ -301,7 +297,9 @@ struct GradSmem {
   float scal[4];
   float As[C][36];      // product tiles (row strides of 4 and 8 banks mod 32: the tensor-core
   float Bs[32][136];    // fragments read them without bank conflicts)
-  float X[C][129];      // the triangular solves
+  float X[C][129];      // d_delta (the back solve's right-hand side)
+  float Tm[C][C + 1];   // T = (I + A)^-1, unit lower triangular
+  float red[16];        // per-warp partial sums
   float KF[C][129], QF[C][129];  // k, q of the chunk (fp32; rows past the chunk are zero)
 };
 
@@ -464,15 +462,27 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
       sm.b[tid + 32] = tid + 32 < L ? a.beta[(t0 + tid + 32) * a.hv + j] : 0.f;
       if (tid == 0) sm.scal[0] = __expf(GL);
     }
-    for (int e = tid; e < C * K; e += kGradThreads) {
-      const int t = e / K, i = e % K;
-      const bool ok = t < L;
-      KF(t, i) = ok ? ld_io(a.k, ((t0 + t) * a.hk + kh) * K + i, a.bf16) : 0.f;
-      QF(t, i) = ok ? ld_io(a.q, ((t0 + t) * a.hk + kh) * K + i, a.bf16) : 0.f;
+    for (int e8 = tid; e8 < C * K / 8; e8 += kGradThreads) {  // eight elements a load
+      const int t = 8 * e8 / K, i = 8 * e8 % K;
+      float k8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, q8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (t < L) {
+        ld8(a.k, ((t0 + t) * a.hk + kh) * K + i, a.bf16, k8);
+        ld8(a.q, ((t0 + t) * a.hk + kh) * K + i, a.bf16, q8);
+      }
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        KF(t, i + m) = k8[m];
+        QF(t, i + m) = q8[m];
+      }
     }
-    for (int e = tid; e < C * V; e += kGradThreads) {
-      const int t = e / V, c = e % V;
-      DO[e] = t < L ? ld_io(a.dout, ((t0 + t) * a.hv + j) * V + c, a.bf16) : 0.f;
+    for (int e8 = tid; e8 < C * V / 8; e8 += kGradThreads) {
+      const int e = 8 * e8, t = e / V, c = e % V;
+      if (t < L) {
+        ld8(a.dout, ((t0 + t) * a.hv + j) * V + c, a.bf16, DO + e);
+      } else {
+        reinterpret_cast<float4*>(DO + e)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        reinterpret_cast<float4*>(DO + e)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
     __syncthreads();
     auto gam = [&](int t, int s) { return __expf(sm.G[t] - sm.G[s]); };  // for s <= t
@@ -490,29 +500,33 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
                        [&](int y, int c) { return Sx[c * K + y]; },
                        [&](int t, int c, float x) { QS[t * V + c] = x; });
     __syncthreads();
-    // ---- R = V - e^G K S;  delta = (I + A)^-1 diag(beta) R by forward substitution in shared
-    // memory: four threads per column split each row's sum
-    for (int e = tid; e < C * V; e += kGradThreads) {
-      const int t = e / V, c = e % V;
-      const float r = t < L ? ld_io(a.v, ((t0 + t) * a.hv + j) * V + c, a.bf16) - sm.eG[t] * KS[e] : 0.f;
-      R[e] = r;
-      sm.X[t][c] = sm.b[t] * r;
+    // ---- R = V - e^G K S;  T = (I + A)^-1 by forward substitution on the identity in shared
+    // memory (eight threads per column split each row's sum); delta = T diag(beta) R
+    for (int e8 = tid; e8 < C * V / 8; e8 += kGradThreads) {
+      const int e = 8 * e8, t = e / V, c = e % V;
+      float v8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (t < L) ld8(a.v, ((t0 + t) * a.hv + j) * V + c, a.bf16, v8);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) R[e + m] = t < L ? v8[m] - sm.eG[t] * KS[e + m] : 0.f;
     }
-    __syncthreads();
     {
-      const int c = tid >> 2, p = tid & 3;
-      for (int t = 1; t < L; ++t) {
+      const int c = tid >> 3, p = tid & 7;  // column c of T (the 512 threads cover C = 64)
+      for (int t = p; t < C; t += 8) sm.Tm[t][c] = t == c ? 1.f : 0.f;
+      __syncwarp();
+      for (int t = 1; t < L; ++t) {  // T[t][c] = -beta_t sum_{c <= s < t} GKK[t][s] T[s][c]
         float x = 0.f;
-        if (c < V)
-          for (int s = p; s < t; s += 4) x = fmaf(sm.b[t] * sm.GKK[t][s], sm.X[s][c], x);
+        for (int s = c + p; s < t; s += 8) x = fmaf(sm.GKK[t][s], sm.Tm[s][c], x);
         x += __shfl_xor_sync(0xffffffffu, x, 1);
         x += __shfl_xor_sync(0xffffffffu, x, 2);
-        if (c < V && p == 0) sm.X[t][c] -= x;
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        if (p == 0 && t > c) sm.Tm[t][c] = -sm.b[t] * x;
         __syncwarp();
       }
     }
     __syncthreads();
-    for (int e = tid; e < C * V; e += kGradThreads) DL[e] = sm.X[e / V][e % V];
+    mm<V, false, false, TF3>(sm, C, [&](int t, int s) { return sm.Tm[t][s]; },
+                             [&](int s, int c) { return sm.b[s] * R[s * V + c]; },
+                             [&](int t, int c, float x) { DL[t * V + c] = x; });
     __syncthreads();
     // ---- d_delta = attn^T dO + Kt D
     mm<V, true, false, TF3>(sm, C, [&](int t, int s) { return sm.At[s][t]; },
@@ -522,26 +536,13 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
                        [&](int y, int c) { return Dx[c * K + y]; },
                        [&](int t, int c, float x) { sm.X[t][c] = t < L ? DD[t * V + c] + x : 0.f; });
     __syncthreads();
-    // ---- dB = (I + A)^-T d_delta by back substitution
-    {
-      const int c = tid >> 2, p = tid & 3;
-      for (int t = L - 2; t >= 0; --t) {
-        float x = 0.f;
-        if (c < V)
-          for (int s = t + 1 + p; s < L; s += 4) x = fmaf(sm.b[s] * sm.GKK[s][t], sm.X[s][c], x);
-        x += __shfl_xor_sync(0xffffffffu, x, 1);
-        x += __shfl_xor_sync(0xffffffffu, x, 2);
-        if (c < V && p == 0) sm.X[t][c] -= x;
-        __syncwarp();
-      }
-    }
-    __syncthreads();
-    for (int e = tid; e < C * V; e += kGradThreads) {
-      const int t = e / V, c = e % V;
-      const float x = sm.X[t][c];
-      DD[e] = x;
-      if (t < L) st_io(a.dv, ((t0 + t) * a.hv + j) * V + c, sm.b[t] * x, a.bf16);
-    }
+    // ---- dB = T^T d_delta
+    mm<V, true, false, TF3>(sm, C, [&](int t, int s) { return sm.Tm[s][t]; },
+                            [&](int s, int c) { return sm.X[s][c]; },
+                            [&](int t, int c, float x) {
+                              DD[t * V + c] = x;
+                              if (t < L) st_io(a.dv, ((t0 + t) * a.hv + j) * V + c, sm.b[t] * x, a.bf16);
+                            });
     __syncthreads();
     // ---- dA = -(dB delta^T) o strictly lower, dattn = (dO delta^T) o lower
     mm<C, false, true, TF3>(sm, V, [&](int t, int c) { return DD[t * V + c]; },
@@ -586,9 +587,20 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
       }
     }
     __syncthreads();
+    {  // <S, D> over the whole CTA
+      float ds = 0.f;
+      for (int e = 4 * tid; e < K * V; e += 4 * kGradThreads) {
+        const float4 x = *reinterpret_cast<const float4*>(Sx + e);
+        const float4 y = *reinterpret_cast<const float4*>(Dx + e);
+        ds = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, ds))));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ds += __shfl_xor_sync(0xffffffffu, ds, o);
+      if ((tid & 31) == 0) sm.red[tid >> 5] = ds;
+    }
+    __syncthreads();
     if (tid < 32) {  // dG_L += sum_t Kt_t . (delta D^T)_t + e^{G_L} <D, S>
-      float tot = sm.X[tid][0] + sm.X[tid + 32][0], ds = 0.f;
-      for (int e = tid; e < K * V; e += 32) ds = fmaf(Sx[e], Dx[e], ds);
+      float tot = sm.X[tid][0] + sm.X[tid + 32][0], ds = tid < kGradThreads / 32 ? sm.red[tid] : 0.f;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         tot += __shfl_xor_sync(0xffffffffu, tot, o);
