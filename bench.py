@@ -583,7 +583,8 @@ def run_ours(args, ws, rank, local):
                          "frac": PRO_BYTES_PER_TOKEN * T / (pro_ms / 1e3) / 1e9 / hbm,
                          "peak_source": src,
                          "algorithmic_bytes_per_launch": PRO_BYTES_PER_TOKEN * T,
-                         "traffic": None}},
+                         "traffic": (None if stored_traffic("prologue") is None
+                                     else stored_traffic("prologue") * T)}},
         "decode": {
             "workload": f"decode bf16 B={DEC_B} requests, pool of {DEC_SLOTS} slots, Hk={HK} "
                         f"Hv={HV} K=V={KD}; fp32 state pool "
