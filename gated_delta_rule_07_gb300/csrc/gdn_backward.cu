@@ -71,10 +71,12 @@ __device__ __forceinline__ int64_t slot_base(const int32_t* cu, int n) {
 
 // ------------------------------------------------------------------ column recurrences
 
-constexpr int kPhases = 8;   // threads per state column; each holds K / 8 contiguous rows
+constexpr int kPhases = 8;   // threads per state column; each holds K / kPhases contiguous rows
 constexpr int kColBlock = 16;  // state columns per CTA
 constexpr int kColThreads = kColBlock * kPhases;
 constexpr int kStage = 32;   // tokens staged in shared memory at a time (half a chunk)
+constexpr int kColMinBlocks = 4;  // CTAs per SM the registers must allow (512 CTAs: ~3.4 per SM)
+static_assert(kStage <= 32 && kColThreads >= 32 && kColBlock % 8 == 0, "one warp scans a block");
 
 // A staged key (or query) row: the K values in kPhases segments of K / kPhases, each followed
 // by 4 floats of padding, so that the eight phases' 16-byte reads of one row hit eight
@@ -137,11 +139,21 @@ __device__ __forceinline__ void stage_tokens(const BwdArgs& a, int64_t t0, int n
       st.blk[1] = __expf(Pn);
     }
   }
+  static_assert(RPL % 4 == 0, "whole 16-byte pieces per segment");
   for (int e = threadIdx.x; e < n * (K / 8); e += kColThreads) {
     const int t = e / (K / 8), i = 8 * (e % (K / 8));
-    const int o = t * RS + (i / RPL) * (RPL + 4) + i % RPL;  // 8 | RPL: one segment
-    ld8(a.k, ((t0 + t) * a.hk + kh) * K + i, a.bf16, st.ks + o);
-    if (REVERSE) ld8(a.q, ((t0 + t) * a.hk + kh) * K + i, a.bf16, st.qs + o);
+    // the eight values land in one segment (RPL >= 8) or in two consecutive ones (RPL = 4)
+    const int o0 = t * RS + (i / RPL) * (RPL + 4) + i % RPL;
+    const int o1 = t * RS + ((i + 4) / RPL) * (RPL + 4) + (i + 4) % RPL;
+    float x[8];
+    ld8(a.k, ((t0 + t) * a.hk + kh) * K + i, a.bf16, x);
+    *reinterpret_cast<float4*>(st.ks + o0) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4*>(st.ks + o1) = make_float4(x[4], x[5], x[6], x[7]);
+    if (REVERSE) {
+      ld8(a.q, ((t0 + t) * a.hk + kh) * K + i, a.bf16, x);
+      *reinterpret_cast<float4*>(st.qs + o0) = make_float4(x[0], x[1], x[2], x[3]);
+      *reinterpret_cast<float4*>(st.qs + o1) = make_float4(x[4], x[5], x[6], x[7]);
+    }
   }
   for (int e = threadIdx.x; e < n * (kColBlock / 8); e += kColThreads) {
     const int t = e / (kColBlock / 8), cc = 8 * (e % (kColBlock / 8));
@@ -162,9 +174,8 @@ __device__ __forceinline__ float col_dot(const float* kv, const float* h) {
     d3 = fmaf(kv[i + 3], h[i + 3], d3);
   }
   float d = (d0 + d1) + (d2 + d3);
-  d += __shfl_xor_sync(0xffffffffu, d, 1);
-  d += __shfl_xor_sync(0xffffffffu, d, 2);
-  d += __shfl_xor_sync(0xffffffffu, d, 4);
+#pragma unroll
+  for (int o = 1; o < kPhases; o <<= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
   return d;
 }
 template <int RPL>
@@ -279,7 +290,7 @@ __device__ __forceinline__ void column_run(const BwdArgs& a, float* csm) {
 // grid (N hv, V / kColBlock, 2): z = 0 the forward recurrence, z = 1 the reverse one; the two
 // directions are independent and share the SMs.
 template <int K>
-__global__ void __launch_bounds__(kColThreads, 4) column_kernel(BwdArgs a) {
+__global__ void __launch_bounds__(kColThreads, kColMinBlocks) column_kernel(BwdArgs a) {
   extern __shared__ __align__(16) float csm[];
   if (blockIdx.z == 0)
     column_run<K, false>(a, csm);
