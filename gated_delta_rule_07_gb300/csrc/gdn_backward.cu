@@ -71,16 +71,16 @@ __device__ __forceinline__ int64_t slot_base(const int32_t* cu, int n) {
 
 // ------------------------------------------------------------------ column recurrences
 
-constexpr int kPhases = 8;   // threads per state column; each holds K / kPhases contiguous rows
-constexpr int kColBlock = 16;  // state columns per CTA
+constexpr int kPhases = 16;  // threads per state column; each holds K / kPhases contiguous rows
+constexpr int kColBlock = 8;  // state columns per CTA
 constexpr int kColThreads = kColBlock * kPhases;
-constexpr int kStage = 32;   // tokens staged in shared memory at a time (half a chunk)
-constexpr int kColMinBlocks = 4;  // CTAs per SM the registers must allow (512 CTAs: ~3.4 per SM)
+constexpr int kStage = 16;   // tokens staged in shared memory at a time (a quarter chunk)
+constexpr int kColMinBlocks = 7;  // CTAs per SM the registers must allow (1024 CTAs: ~6.7 per SM)
 static_assert(kStage <= 32 && kColThreads >= 32 && kColBlock % 8 == 0, "one warp scans a block");
 
 // A staged key (or query) row: the K values in kPhases segments of K / kPhases, each followed
-// by 4 floats of padding, so that the eight phases' 16-byte reads of one row hit eight
-// different groups of four banks.
+// by 4 floats of padding, so that the phases' 16-byte reads of one row spread over the banks
+// (at most two reads to a group of four banks).
 template <int K>
 __host__ __device__ constexpr int row_stride() { return K + 4 * kPhases; }
 
@@ -511,8 +511,8 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
                        [&](int y, int c) { return Sx[c * K + y]; },
                        [&](int t, int c, float x) { QS[t * V + c] = x; });
     __syncthreads();
-    // ---- R = V - e^G K S;  T = (I + A)^-1 by forward substitution on the identity in shared
-    // memory (eight threads per column split each row's sum); delta = T diag(beta) R
+    // ---- R = V - e^G K S;  T = (I + A)^-1 in shared memory (blockwise: the diagonal blocks by
+    // substitution, the rest from them); delta = T diag(beta) R
     for (int e8 = tid; e8 < C * V / 8; e8 += kGradThreads) {
       const int e = 8 * e8, t = e / V, c = e % V;
       float v8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -520,11 +520,11 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
 #pragma unroll
       for (int m = 0; m < 8; ++m) R[e + m] = t < L ? v8[m] - sm.eG[t] * KS[e + m] : 0.f;
     }
-    {
-      const int c = tid >> 3, p = tid & 7;  // column c of T (the 512 threads cover C = 64)
+    {  // the four 16 x 16 diagonal blocks of T by substitution, eight threads per column
+      const int c = tid >> 3, p = tid & 7, c0 = c & ~15;  // (a warp's four columns share a block)
       for (int t = p; t < C; t += 8) sm.Tm[t][c] = t == c ? 1.f : 0.f;
       __syncwarp();
-      for (int t = 1; t < L; ++t) {  // T[t][c] = -beta_t sum_{c <= s < t} GKK[t][s] T[s][c]
+      for (int t = c0 + 1; t < c0 + 16; ++t) {  // T[t][c] = -beta_t sum_{c <= s < t} GKK[t][s] T[s][c]
         float x = 0.f;
         for (int s = c + p; s < t; s += 8) x = fmaf(sm.GKK[t][s], sm.Tm[s][c], x);
         x += __shfl_xor_sync(0xffffffffu, x, 1);
@@ -532,6 +532,28 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
         x += __shfl_xor_sync(0xffffffffu, x, 4);
         if (p == 0 && t > c) sm.Tm[t][c] = -sm.b[t] * x;
         __syncwarp();
+      }
+    }
+    // the blocks below the diagonal, one band at a time (block (i, j) needs the bands nearer the
+    // diagonal): T_ij = -T_ii sum_{j <= k < i} A_ik T_kj with A = diag(beta) GKK; the sums go
+    // through sm.X (free until d_delta)
+    float* Pb = &sm.X[0][0];  // [3][16][16]
+    for (int d = 1; d < 4; ++d) {
+      __syncthreads();
+      for (int e = tid; e < (4 - d) * 256; e += kGradThreads) {
+        const int j = e >> 8, i = j + d, r = (e >> 4) & 15, cc = e & 15;
+        const int row = 16 * i + r;
+        float x = 0.f;
+        for (int s = 16 * j; s < 16 * i; ++s) x = fmaf(sm.GKK[row][s], sm.Tm[s][16 * j + cc], x);
+        Pb[e] = sm.b[row] * x;
+      }
+      __syncthreads();
+      for (int e = tid; e < (4 - d) * 256; e += kGradThreads) {
+        const int j = e >> 8, i = j + d, r = (e >> 4) & 15, cc = e & 15;
+        float x = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) x = fmaf(sm.Tm[16 * i + r][16 * i + m], Pb[(j << 8) + (m << 4) + cc], x);
+        sm.Tm[16 * i + r][16 * j + cc] = -x;
       }
     }
     __syncthreads();
