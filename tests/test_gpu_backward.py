@@ -113,6 +113,22 @@ def test_backward_long_bf16_65536(gdn):
           "long bf16 T=65536")
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16], ids=["fp32", "bf16"])
+def test_backward_strong_decay_blocks(gdn, dtype):
+    """Stretches of strong decay (g = -3 and -8 per token) mixed with the usual recipe: the state
+    recurrences carry a scaled state h = A h~ within each staged block and fall back to the plain
+    recurrence where the block's summed decay leaves the range of the scale factors; this case
+    takes both paths (and decays that underflow to zero within a chunk)."""
+    lengths = (300, 150)
+    inp = inputs.custom(sum(lengths), 2, 4, 128, 128, dtype, h0_std=0.05, seed=31, lengths=lengths)
+    inp.g[40:90] = -3.0      # a block sum of -48: the plain recurrence
+    inp.g[200:216, 1] = -8.0  # one value head only
+    inp.g[330:345] = -0.5     # sums near the range's edge
+    dout, dhf = cotangents(inp, seed=32)
+    check(run(gdn, inp, dout, dhf), reference(inp, dout, dhf), dtype == torch.bfloat16,
+          f"strong decay {dtype}")
+
+
 def test_backward_empty_stream_passes_the_state_gradient(gdn):
     q = torch.zeros(0, 2, 64, device="cuda")
     v = torch.zeros(0, 4, 64, device="cuda")
