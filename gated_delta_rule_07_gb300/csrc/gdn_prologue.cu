@@ -213,13 +213,15 @@ __global__ void __launch_bounds__(kSThreads, 2) prologue_kernel(PrologueArgs a, 
   // the thread's ring of inputs in flight: token t0 + i in slot i mod kRing, at ring[slot][thread]
   extern __shared__ __align__(16) uint4 ring[];
   const uint32_t ring0 = (uint32_t)__cvta_generic_to_shared(ring + threadIdx.x);
-  const IO* xc = static_cast<const IO*>(a.x) + c;
+  // (a copy that reads nothing still names x's first element, an address inside the tensor)
+  const IO* x0 = static_cast<const IO*>(a.x);
+  const IO* xc = x0 + c;
 #pragma unroll
   for (int r = 0; r < kRing - 1; ++r) {
     const bool ok = act && t0 + r < t1;
-    ring_copy(ring0 + r * kSThreads * 16, ok ? xc + (int64_t)(t0 + r) * Ch : xc, ok);
+    ring_copy(ring0 + r * kSThreads * 16, ok ? xc + (int64_t)(t0 + r) * Ch : x0, ok);
   }
-  const IO* xn = xc + (int64_t)(t0 + kRing - 1) * Ch;  // the next token to copy
+  const IO* xn = xc + (int64_t)(t0 + kRing - 1) * Ch;  // the next token to copy (used when in range)
   IO* dp = static_cast<IO*>(qk ? (hh < a.hk ? a.q : a.k) : a.v) + (int64_t)head * width +
            kCPT * l + t0 * drow;
   static_assert(kRing % 4 == 0, "ring slots advance four tokens at a time");
@@ -231,7 +233,7 @@ __global__ void __launch_bounds__(kSThreads, 2) prologue_kernel(PrologueArgs a, 
       if (t >= t1) break;
       {  // token t + kRing - 1 into the slot that token t - 1 used; then token t has landed
         const bool ok = act && t + kRing - 1 < t1;
-        ring_copy(ring0 + ((rb + J + kRing - 1) % kRing) * kSThreads * 16, ok ? xn : xc, ok);
+        ring_copy(ring0 + ((rb + J + kRing - 1) % kRing) * kSThreads * 16, ok ? xn : x0, ok);
         xn += Ch;
         asm volatile("cp.async.wait_group %0;\n" ::"n"(kRing - 1) : "memory");
       }

@@ -68,6 +68,15 @@ def test_prologue_matches_oracle(gdn, dtype, W, act):
     compare(gdn, args, 2, 4, 128, 64, act, f"{dtype} W={W} {act}")
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32], ids=["bf16", "fp32"])
+def test_prologue_uneven_head_widths(gdn, dtype):
+    """Head widths that do not fill a power of two of lanes (K = 96, V = 40: a thread's lanes
+    are padded out to the next power of two per head, and the padding lanes neither load nor
+    store), one key head, three value heads, sequences of 0, 1, 2, 3 and 77 tokens."""
+    args = case(1, 3, 96, 40, 4, (3, 0, 77, 1, 2), dtype, seed=5)
+    compare(gdn, args, 1, 3, 96, 40, "silu", f"uneven heads {dtype}")
+
+
 def test_prologue_headline_geometry_bf16(gdn):
     """Hk = 16, Hv = 32, K = V = 128 (8192 channels), 8192 tokens in three sequences."""
     args = case(16, 32, 128, 128, 4, (3000, 64, 5128), torch.bfloat16, seed=9)
