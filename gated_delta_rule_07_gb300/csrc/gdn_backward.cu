@@ -25,9 +25,10 @@
 // S and D at every chunk boundary come from two column-parallel token recurrences (a state
 // column only meets its own value column): the forward one stores each chunk's entering state,
 // the reverse one (dh_prev = alpha (F - beta k (k^T F)), F = dh + q dout^T) each chunk's
-// leaving gradient and, at the sequence start, dh0.  Everything is fp32 arithmetic on CUDA
-// cores; the per-chunk work runs as one CTA per (chunk, value head) that walks through the
-// products above with its intermediates in a per-CTA slice of the workspace.
+// leaving gradient and, at the sequence start, dh0; both run in one launch, on fp32 CUDA cores.
+// The per-chunk work runs as one CTA per (chunk, value head) that walks through the products
+// above on the tensor cores (warp-level TF32 products with fp32 accumulation), with T = (I + A)^-1
+// formed once in shared memory and its intermediates in a per-CTA slice of the workspace.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>

@@ -259,8 +259,11 @@ size_t gdn_backward_workspace_size(const gdn_problem* p);
  *   dh0         [N, hv, K, V] fp32, or NULL to skip
  *   workspace   ws_bytes >= gdn_backward_workspace_size(p), 16-byte aligned; its first 4 bytes
  *               are the status word (reset by this call)
- * segments_per_seq is not used.  All arithmetic is fp32 on CUDA cores.  Tails, padding, cu_seqlens
- * checks and errors as for gdn_forward.  Returns GDN_OK once the work is enqueued. */
+ * segments_per_seq is not used.  The state recurrences and the triangular factors are fp32
+ * arithmetic on CUDA cores; the per-chunk products run on the tensor cores with fp32
+ * accumulation, their operands rounded to TF32 for bf16 I/O and split into two TF32 parts
+ * (fp32 accuracy) for fp32 I/O.  Tails, padding, cu_seqlens checks and errors as for
+ * gdn_forward.  Returns GDN_OK once the work is enqueued. */
 gdn_status gdn_backward(const gdn_problem* p, const void* q, const void* k, const void* v,
                         const float* g, const float* beta, const float* h0,
                         const int32_t* cu_seqlens, const void* dout, const float* dh_final,
