@@ -307,8 +307,9 @@ struct GradSmem {
   float dA[C][C + 1], dat[C][C + 1];
   float G[C], eG[C], ekt[C], b[C], dG[C];
   float scal[4];
-  float As[C][36];      // product tiles (row strides of 4 and 8 banks mod 32: the tensor-core
-  float Bs[32][136];    // fragments read them without bank conflicts)
+  float As[2 * C][36];  // product tiles (row strides of 4 and 8 banks mod 32: the tensor-core
+  float Bs[32][136];    // fragments read them without bank conflicts); As holds 128 rows when
+                        // two products that share B run as one
   float X[C][129];      // d_delta (the back solve's right-hand side)
   float Tm[C][C + 1];   // T = (I + A)^-1, unit lower triangular
   float red[16];        // per-warp partial sums
@@ -335,22 +336,25 @@ __device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, const uint
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// out(i, c, x) for i < C, c < N with x = sum_{y < Y} A(i, y) B(y, c) (Y a multiple of 32), on
+// out(i, c, x) for i < M, c < N with x = sum_{y < Y} A(i, y) B(y, c) (Y a multiple of 32), on
 // the tensor cores: 32-wide slices of y are staged in shared memory (each thread fetches its
-// share of the next slice into registers while the current one is multiplied); warp w owns rows
-// 16 (w mod 4) .. + 16 and N / 4 columns from (w / 4) N / 4, as N / 32 tiles of 16 x 8.
+// share of the next slice into registers while the current one is multiplied).  M = 64, or 128
+// for two 64-row products that share B (rows 64.. the second).  Warp w owns 16 rows from
+// 16 (w mod M/16) and N M / 256 columns, as 16 x 8 tiles.
 // TF3: each operand is split into a TF32 head and a TF32 remainder and three products are
 // summed (head x remainder, remainder x head, head x head), which keeps fp32 accuracy; without
 // it the operands are rounded to TF32 once.  AI / BY: the operand's contiguous index is i (for
 // A) / y (for B), so that the fetches walk memory in order.
-template <int N, bool AI, bool BY, bool TF3, typename FA, typename FB, typename FO>
+template <int M, int N, bool AI, bool BY, bool TF3, typename FA, typename FB, typename FO>
 __device__ __forceinline__ void mm(GradSmem& sm, int Y, FA A, FB B, FO out) {
-  constexpr int NT = N / 32;  // 16 x 8 tiles of a warp
-  constexpr int NA = C * 32 / kGradThreads, NB = 32 * N / kGradThreads;
-  static_assert(kGradThreads == 512 && C == 64, "16 warps over a 64-row output");
+  constexpr int MB = M / 16;                // row blocks
+  constexpr int NC = N * M / 256;           // columns of a warp
+  constexpr int NT = NC / 8;                // its 16 x 8 tiles
+  constexpr int NA = M * 32 / kGradThreads, NB = 32 * N / kGradThreads;
+  static_assert(kGradThreads == 512 && (M == 64 || M == 128) && NT >= 1, "16 warps over M rows");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int grp = lane >> 2, tig = lane & 3;
-  const int r0 = 16 * (warp & 3) + grp, c0 = (warp >> 2) * (N / 4) + grp;
+  const int r0 = 16 * (warp % MB) + grp, c0 = (warp / MB) * NC + grp;
   float acc[NT][4];
 #pragma unroll
   for (int m = 0; m < NT; ++m)
@@ -361,7 +365,7 @@ __device__ __forceinline__ void mm(GradSmem& sm, int Y, FA A, FB B, FO out) {
 #pragma unroll
     for (int k = 0; k < NA; ++k) {
       const int e = tid + k * kGradThreads;
-      pa[k] = A(AI ? e % C : e / 32, y0 + (AI ? e / C : e % 32));
+      pa[k] = A(AI ? e % M : e / 32, y0 + (AI ? e / M : e % 32));
     }
 #pragma unroll
     for (int k = 0; k < NB; ++k) {
@@ -375,7 +379,7 @@ __device__ __forceinline__ void mm(GradSmem& sm, int Y, FA A, FB B, FO out) {
 #pragma unroll
     for (int k = 0; k < NA; ++k) {
       const int e = tid + k * kGradThreads;
-      sm.As[AI ? e % C : e / 32][AI ? e / C : e % 32] = pa[k];
+      sm.As[AI ? e % M : e / 32][AI ? e / M : e % 32] = pa[k];
     }
 #pragma unroll
     for (int k = 0; k < NB; ++k) {
@@ -411,7 +415,7 @@ __device__ __forceinline__ void mm(GradSmem& sm, int Y, FA A, FB B, FO out) {
       }
     }
   }
-  const int cc = (warp >> 2) * (N / 4) + 2 * tig;
+  const int cc = (warp / MB) * NC + 2 * tig;
 #pragma unroll
   for (int m = 0; m < NT; ++m) {
     out(r0, cc + 8 * m, acc[m][0]);
@@ -499,16 +503,17 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
     __syncthreads();
     auto gam = [&](int t, int s) { return __expf(sm.G[t] - sm.G[s]); };  // for s <= t
     // ---- Gamma o K K^T (strictly lower), attn; K S, Q S
-    mm<C, false, true, TF3>(sm, K, [&](int t, int y) { return KF(t, y); },
-                       [&](int y, int s) { return KF(s, y); },
-                       [&](int t, int s, float x) { sm.GKK[t][s] = (s < t && t < L) ? gam(t, s) * x : 0.f; });
-    mm<C, false, true, TF3>(sm, K, [&](int t, int y) { return QF(t, y); },
-                       [&](int y, int s) { return KF(s, y); },
-                       [&](int t, int s, float x) { sm.At[t][s] = (s <= t && t < L) ? gam(t, s) * x : 0.f; });
-    mm<V, false, true, TF3>(sm, K, [&](int t, int y) { return KF(t, y); },
+    mm<2 * C, C, false, true, TF3>(  // rows 0-63: K K^T, rows 64-127: Q K^T (they share K^T)
+        sm, K, [&](int t, int y) { return t < C ? KF(t, y) : QF(t - C, y); },
+        [&](int y, int s) { return KF(s, y); },
+        [&](int t, int s, float x) {
+          if (t < C) sm.GKK[t][s] = (s < t && t < L) ? gam(t, s) * x : 0.f;
+          else sm.At[t - C][s] = (s <= t - C && t - C < L) ? gam(t - C, s) * x : 0.f;
+        });
+    mm<C, V, false, true, TF3>(sm, K, [&](int t, int y) { return KF(t, y); },
                        [&](int y, int c) { return Sx[c * K + y]; },
                        [&](int t, int c, float x) { KS[t * V + c] = x; });
-    mm<V, false, true, TF3>(sm, K, [&](int t, int y) { return QF(t, y); },
+    mm<C, V, false, true, TF3>(sm, K, [&](int t, int y) { return QF(t, y); },
                        [&](int y, int c) { return Sx[c * K + y]; },
                        [&](int t, int c, float x) { QS[t * V + c] = x; });
     __syncthreads();
@@ -558,20 +563,20 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
       }
     }
     __syncthreads();
-    mm<V, false, false, TF3>(sm, C, [&](int t, int s) { return sm.Tm[t][s]; },
+    mm<C, V, false, false, TF3>(sm, C, [&](int t, int s) { return sm.Tm[t][s]; },
                              [&](int s, int c) { return sm.b[s] * R[s * V + c]; },
                              [&](int t, int c, float x) { DL[t * V + c] = x; });
     __syncthreads();
     // ---- d_delta = attn^T dO + Kt D
-    mm<V, true, false, TF3>(sm, C, [&](int t, int s) { return sm.At[s][t]; },
+    mm<C, V, true, false, TF3>(sm, C, [&](int t, int s) { return sm.At[s][t]; },
                        [&](int s, int c) { return DO[s * V + c]; },
                        [&](int t, int c, float x) { DD[t * V + c] = x; });
-    mm<V, false, true, TF3>(sm, K, [&](int t, int y) { return sm.ekt[t] * KF(t, y); },
+    mm<C, V, false, true, TF3>(sm, K, [&](int t, int y) { return sm.ekt[t] * KF(t, y); },
                        [&](int y, int c) { return Dx[c * K + y]; },
                        [&](int t, int c, float x) { sm.X[t][c] = t < L ? DD[t * V + c] + x : 0.f; });
     __syncthreads();
     // ---- dB = T^T d_delta
-    mm<V, true, false, TF3>(sm, C, [&](int t, int s) { return sm.Tm[s][t]; },
+    mm<C, V, true, false, TF3>(sm, C, [&](int t, int s) { return sm.Tm[s][t]; },
                             [&](int s, int c) { return sm.X[s][c]; },
                             [&](int t, int c, float x) {
                               DD[t * V + c] = x;
@@ -579,14 +584,15 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
                             });
     __syncthreads();
     // ---- dA = -(dB delta^T) o strictly lower, dattn = (dO delta^T) o lower
-    mm<C, false, true, TF3>(sm, V, [&](int t, int c) { return DD[t * V + c]; },
-                       [&](int c, int s) { return DL[s * V + c]; },
-                       [&](int t, int s, float x) { sm.dA[t][s] = (s < t && t < L) ? -x : 0.f; });
-    mm<C, false, true, TF3>(sm, V, [&](int t, int c) { return DO[t * V + c]; },
-                       [&](int c, int s) { return DL[s * V + c]; },
-                       [&](int t, int s, float x) { sm.dat[t][s] = (s <= t && t < L) ? x : 0.f; });
+    mm<2 * C, C, false, true, TF3>(  // rows 0-63: dB delta^T, rows 64-127: dO delta^T
+        sm, V, [&](int t, int c) { return t < C ? DD[t * V + c] : DO[(t - C) * V + c]; },
+        [&](int c, int s) { return DL[s * V + c]; },
+        [&](int t, int s, float x) {
+          if (t < C) sm.dA[t][s] = (s < t && t < L) ? -x : 0.f;
+          else sm.dat[t - C][s] = (s <= t - C && t - C < L) ? x : 0.f;
+        });
     // ---- delta D^T
-    mm<K, false, false, TF3>(sm, V, [&](int t, int c) { return DL[t * V + c]; },
+    mm<C, K, false, false, TF3>(sm, V, [&](int t, int c) { return DL[t * V + c]; },
                         [&](int c, int i) { return Dx[c * K + i]; },
                         [&](int t, int i, float x) { XD[t * K + i] = x; });
     __syncthreads();
@@ -665,26 +671,26 @@ __global__ void __launch_bounds__(kGradThreads) chunk_grad_kernel(BwdArgs a) {
     float* dqv = a.dqv + (t0 * a.hv + j) * (int64_t)K;
     float* dkv = a.dkv + (t0 * a.hv + j) * (int64_t)K;
     const int64_t rs = (int64_t)a.hv * K;  // row stride of dqv, dkv
-    mm<K, false, false, TF3>(sm, V, [&](int t, int c) { return DO[t * V + c]; },
+    mm<C, K, false, false, TF3>(sm, V, [&](int t, int c) { return DO[t * V + c]; },
                         [&](int c, int i) { return Sx[c * K + i]; },
                         [&](int t, int i, float x) { if (t < L) dqv[t * rs + i] = sm.eG[t] * x; });
-    mm<K, false, false, TF3>(sm, C, [&](int t, int s) { return sm.dat[t][s]; },
+    mm<C, K, false, false, TF3>(sm, C, [&](int t, int s) { return sm.dat[t][s]; },
                         [&](int s, int i) { return KF(s, i); },
                         [&](int t, int i, float x) { if (t < L) dqv[t * rs + i] += x; });
     // ---- dk = -diag(beta e^G) dB S^T + diag(e^{G_L - G}) delta D^T + diag(beta) (dA o Gamma) K
     //          + (dA o Gamma)^T diag(beta) K + (dattn o Gamma)^T Q
-    mm<K, false, false, TF3>(sm, V, [&](int t, int c) { return DD[t * V + c]; },
+    mm<C, K, false, false, TF3>(sm, V, [&](int t, int c) { return DD[t * V + c]; },
                         [&](int c, int i) { return Sx[c * K + i]; },
                         [&](int t, int i, float x) {
                           if (t < L) dkv[t * rs + i] = sm.ekt[t] * XD[t * K + i] - sm.b[t] * sm.eG[t] * x;
                         });
-    mm<K, false, false, TF3>(sm, C, [&](int t, int s) { return sm.dA[t][s]; },
+    mm<C, K, false, false, TF3>(sm, C, [&](int t, int s) { return sm.dA[t][s]; },
                         [&](int s, int i) { return KF(s, i); },
                         [&](int t, int i, float x) { if (t < L) dkv[t * rs + i] += sm.b[t] * x; });
-    mm<K, true, false, TF3>(sm, C, [&](int t, int s) { return sm.dA[s][t] * sm.b[s]; },
+    mm<C, K, true, false, TF3>(sm, C, [&](int t, int s) { return sm.dA[s][t] * sm.b[s]; },
                        [&](int s, int i) { return KF(s, i); },
                        [&](int t, int i, float x) { if (t < L) dkv[t * rs + i] += x; });
-    mm<K, true, false, TF3>(sm, C, [&](int t, int s) { return sm.dat[s][t]; },
+    mm<C, K, true, false, TF3>(sm, C, [&](int t, int s) { return sm.dat[s][t]; },
                        [&](int s, int i) { return QF(s, i); },
                        [&](int t, int i, float x) { if (t < L) dkv[t * rs + i] += x; });
   }
