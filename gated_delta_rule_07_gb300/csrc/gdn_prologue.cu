@@ -100,12 +100,12 @@ __device__ __forceinline__ Raw pack(const float* f) {
 }
 
 // how the channel slots of a token map onto threads: a head of width w occupies the next power
-// of two >= w / kCPT lanes (aligned), q heads then k heads then v heads
+// of two >= w / cpt<IO>() lanes (aligned), q heads then k heads then v heads
 struct SlotMap {
   int lphk, lphv;    // lanes per q / k head, per v head
   int qk_slots;      // 2 hk lphk
   int slots;         // qk_slots + hv lphv
-  int cpr;           // CTAs per token run
+  int cpr;           // CTAs per token range (each a slice of the channel slots)
   int ranges;        // token ranges (the grid is ranges x cpr CTAs, all resident at once)
 };
 
