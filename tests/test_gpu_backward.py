@@ -71,7 +71,7 @@ def check(got, ref, bf16, case):
 
 
 @pytest.mark.parametrize("T,lengths", [(64, None), (64 * 3 + 21, None), (None, (120, 1, 257)),
-                                       (None, (64, 128))])
+                                       (None, (64, 128)), (None, (0, 70, 0, 5))])
 def test_backward_fp32_small(gdn, T, lengths):
     if lengths is not None:
         T = sum(lengths)
@@ -94,6 +94,14 @@ def test_backward_prefill_bf16_4096(gdn):
     dout, dhf = cotangents(inp, seed=11)
     check(run(gdn, inp, dout, dhf, cu=False), reference(inp, dout, dhf, cu=False), True,
           "prefill bf16 T=4096")
+
+
+def test_backward_empty_sequences_bf16(gdn):
+    """Empty sequences among packed ones: their dh0 is dh_final, and they take no chunk."""
+    inp = inputs.custom(0, 2, 4, 128, 128, torch.bfloat16, h0_std=0.02, seed=41,
+                        lengths=(0, 65, 0, 0, 130))
+    dout, dhf = cotangents(inp, seed=42)
+    check(run(gdn, inp, dout, dhf), reference(inp, dout, dhf), True, "empty sequences bf16")
 
 
 def test_backward_varlen_bf16(gdn):
