@@ -37,9 +37,10 @@ BYTES_PER_TOKEN = HK * KD * 2 * 2 + HV * VD * 2 * 2 + HV * 4 * 2
 # what each phase-1 kernel must read per token: k, v, g, beta (U half); k, g, beta (M half)
 SUM_U_BYTES_PER_TOKEN = HK * KD * 2 + HV * VD * 2 + HV * 4 * 2
 SUM_M_BYTES_PER_TOKEN = HK * KD * 2 + HV * 4 * 2
-# backward (fp32 CUDA-core arithmetic): FLOPs per token of what it computes -- per chunk and
-# value head 6 CKV + 6 C^2 K + 3 C^2 V products and two C x C triangular solves over V columns,
-# per token and value head the two state-column recurrences (2 KV + 3 KV multiply-adds)
+# backward (state recurrences and triangular factors on fp32 CUDA cores, products on TF32 tensor
+# cores): FLOPs per token of what it computes -- per chunk and value head 6 CKV + 6 C^2 K +
+# 3 C^2 V products and two C x C triangular solves over V columns, per token and value head the
+# two state-column recurrences (2 KV + 3 KV multiply-adds)
 BWD_FLOP_PER_TOKEN = HV * (2 * (6 * C * KD * VD + 6 * C * C * KD + 3 * C * C * VD
                                  + C * (C - 1) * VD) / C + 2 * 5 * KD * VD)
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (maximum SM clock)
