@@ -338,7 +338,8 @@ __device__ __forceinline__ void mma_tf32(float* d, const uint32_t* a, const uint
 
 // out(i, c, x) for i < M, c < N with x = sum_{y < Y} A(i, y) B(y, c) (Y a multiple of 32), on
 // the tensor cores: 32-wide slices of y are staged in shared memory (each thread fetches its
-// share of the next slice into registers while the current one is multiplied).  M = 64, or 128
+// share of the next slice into registers, from before the barrier that precedes the current
+// slice's multiply until after it).  M = 64, or 128
 // for two 64-row products that share B (rows 64.. the second).  Warp w owns 16 rows from
 // 16 (w mod M/16) and N M / 256 columns, as 16 x 8 tiles.
 // TF3: each operand is split into a TF32 head and a TF32 remainder and three products are
@@ -386,8 +387,8 @@ __device__ __forceinline__ void mm(GradSmem& sm, int Y, FA A, FB B, FO out) {
       const int e = tid + k * kGradThreads;
       sm.Bs[BY ? e % 32 : e / N][BY ? e / 32 : e % N] = pb[k];
     }
+    if (y0 + 32 < Y) fetch(y0 + 32);  // (reads the operands' sources, not the tiles)
     __syncthreads();
-    if (y0 + 32 < Y) fetch(y0 + 32);
 #pragma unroll
     for (int k8 = 0; k8 < 32; k8 += 8) {
       const float af[4] = {sm.As[r0][k8 + tig], sm.As[r0 + 8][k8 + tig], sm.As[r0][k8 + tig + 4],
